@@ -1,0 +1,54 @@
+"""Plant mistakes in a copy of the oracle (on the CPU) and check that the pins
+catch every one of them: a pin suite that passes a broken oracle proves
+nothing.  Each mutant is built from oracle.c with one textual change."""
+import os
+import shutil
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_CHECKS
+
+MUTATIONS = {
+    "half_exponent_bias": ("ldexp((double)(1024 + f), e - 25)", "ldexp((double)(1024 + f), e - 24)"),
+    "q4k_low_nibble_from_high": ("q[64 * c + l] = qs[32 * c + l] & 15;", "q[64 * c + l] = qs[32 * c + l] >> 4;"),
+    "q4k_scale_index": ("sc[j] = s[j] & 63;", "sc[j] = s[j + 4] & 63;"),
+    "q4k_high_scale_bits": ("sc[j] = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);", "sc[j] = (s[j + 4] & 15) | ((s[j] >> 6) << 4);"),
+    "q6k_qh_shift": ("o[l + 32] = (L[l + 32] & 15) | (((H[l] >> 2) & 3) << 4);", "o[l + 32] = (L[l + 32] & 15) | (((H[l] >> 4) & 3) << 4);"),
+    "q6k_pack_halves": ("uint8_t *L = ql + 64 * h;\n        uint8_t *H", "uint8_t *L = ql + 32 * h;\n        uint8_t *H"),
+    "q8k_round_half_even": ("float r = roundf(xb[i] / db);", "float r = rintf(xb[i] / db);"),
+    "q8k_scale_128": ("float db = amax / 127.0f;", "float db = amax / 128.0f;"),
+    "q8k_bsum_offbyone": ("sb[g] = (int16_t)s;", "sb[g] = (int16_t)(s + (g == 3));"),
+    "q8k_amax_signed": ("float a = fabsf(xb[i]);", "float a = xb[i];"),
+    "gemm_q4k_drop_dmin": ("(d * (double)dot - dmin * (double)corr)", "(d * (double)dot - 0.0 * (double)corr)"),
+    "gemm_q4k_bsum_pair": ("corr += (int64_t)mn[j] * (bs[2 * j] + bs[2 * j + 1]);", "corr += (int64_t)mn[j] * (bs[j] + bs[j + 8]);"),
+    "gemm_q4k_subblock_width": ("for (int i = 32 * j; i < 32 * j + 32; ++i)", "for (int i = 32 * j; i < 32 * j + 31; ++i)"),
+    "gemm_q6k_offset_31": ("dot += (int64_t)sc[j] * (I - 32 * (int64_t)bs[j]);", "dot += (int64_t)sc[j] * (I - 31 * (int64_t)bs[j]);"),
+    "gemm_q6k_transposed_x": ("const int8_t *xq = qs + m * K + b * 256;\n                const int16_t *bs = bsums + m * (K / 16) + b * 16;\n                int64_t dot = 0;\n", "const int8_t *xq = qs + m * K + b * 256 + (b > 0 ? -256 : 0);\n                const int16_t *bs = bsums + m * (K / 16) + b * 16;\n                int64_t dot = 0;\n"),
+    "gemm_absc_signed": ("absc[r * N + n] += fabs(cb);\n            }\n        }\n    }\n    free(own);\n}\n\nvoid oracle_gemm_q6k", "absc[r * N + n] += cb;\n            }\n        }\n    }\n    free(own);\n}\n\nvoid oracle_gemm_q6k"),
+    "brute_dmin_sign": ("w[i] = d * sc[i / 32] * q[i] - dmin * mn[i / 32];", "w[i] = d * sc[i / 32] * q[i] + dmin * mn[i / 32];"),
+}
+
+
+def _fails(orc):
+    failed = []
+    for check in ALL_CHECKS:
+        try:
+            check(orc)
+        except AssertionError:
+            failed.append(check.__name__)
+    return failed
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutant_is_caught(name, tmp_path):
+    src = open(oracle.SRC).read()
+    old, new = MUTATIONS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique/present"
+    mdir = tmp_path / "mut"
+    mdir.mkdir()
+    shutil.copy(os.path.join(oracle.HERE, "oracle.h"), mdir / "oracle.h")
+    (mdir / "oracle.c").write_text(src.replace(old, new))
+    lib = oracle.build(str(mdir / "oracle.c"), str(mdir / "liboracle_mut.so"), force=True)
+    failed = _fails(oracle.Oracle(lib))
+    assert failed, f"no pin catches mutation {name}"
