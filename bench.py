@@ -1,0 +1,356 @@
+#!/usr/bin/env python
+"""Benchmark of the k-quant prefill matmul on one GB300 (or N replicas).
+
+One step = the whole hot path on one batch: quantize fp32 activations to Q8_K
+(qgemm_quantize_q8k), then the Q4_K x Q8_K GEMM (qgemm_q4k: operand
+preparation + the tcgen05 tile GEMM).  Default workload: Q4_K, M = 512 tokens,
+K = 2048, N = 11008 (FFN up-projection shape), X ~ N(0,1) with 1% of the
+columns scaled x8; synthetic, seeded (synth.py).
+
+Metric: effective TOPS = 2*M*N*K / step time (the whole job over all ranks);
+weight GB/s and the tile GEMM's roofline fraction are reported beside it.
+
+Timing: W untimed warm-up steps, then exactly K steps, each bracketed by CUDA
+events on the launching stream, with L2 flushed before every step (a 256 MiB
+write, outside the events); barrier + synchronize on both sides; the slowest
+rank's mean is the step time.  The GEMM kernel alone is timed with events the
+library records around its launch (qgemm_set_profile_events).
+
+--impl reference times the CPU oracle (the parity authority) on bounded
+samples of the same workload on the host cores: the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "k-quant GEMM effective TOPS and weight GB/s vs roofline at prefill M"
+UNIT = "TOPS"
+DEFAULT_WORKLOAD = synth.C1.name
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one tile-GEMM launch, from
+# the ncu capture summarised under profiles/ (None until measured, and reset
+# to None whenever the kernel changes).
+NCU_TRAFFIC_BYTES = {}
+
+
+def workloads():
+    return {w.name: w for w in synth.CONFIGS}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return None
+        win = [s for t, s in self.samples if t0 <= t <= t1]
+        widened = False
+        if len(win) < 3:
+            win = [s for t, s in self.samples if t0 - 2.0 <= t <= t1 + 0.2]
+            widened = True
+        if not win:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, smax = [], []
+        for s in win:
+            try:
+                sm.append(float(s[1]))
+                smax.append(float(s[2]))
+            except (ValueError, IndexError):
+                continue
+            for i, n in enumerate(names):
+                if len(s) > 5 + i and s[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if widened:
+            out["window"] = "timed region plus the 2 s of warm-up before it (timed region shorter than 3 samples)"
+        return out
+
+
+def gpu_id_for_smi(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(wl, rows, x=None, w=None):
+    """Time the CPU oracle (quantize + GEMM) on `rows` token rows; returns (seconds, ops)."""
+    import oracle
+    orc = oracle.get()
+    w = wl.weights() if w is None else w
+    x = wl.x() if x is None else x
+    xs = np.ascontiguousarray(x[:rows])
+    t = time.perf_counter()
+    qs, d, bs = orc.quantize_q8k(xs)
+    orc.gemm(wl.wtype, w, wl.K, qs, d, bs)
+    dt = time.perf_counter() - t
+    return dt, 2.0 * rows * wl.N * wl.K
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    wl = workloads()[args.workload]
+    w, x = wl.weights(), wl.x()
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(wl, rows, x, w)
+    ts, ops = [], 0.0
+    for _ in range(args.steps):
+        dt, ops = oracle_sample(wl, rows, x, w)
+        ts.append(dt)
+    mean = sum(ts) / len(ts)
+    value = ops / mean / 1e12
+    sample = f"{rows} of {wl.M} token rows per step (quantize + GEMM over all N={wl.N}, K={wl.K})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(wl):
+    return {"workload": wl.name, "weights": "Q4_K" if wl.wtype == 4 else "Q6_K", "M": wl.M, "K": wl.K,
+            "N": wl.N, "x": f"{wl.sigma}*N(0,1)" + (", 1% columns x8" if wl.outlier_frac else ""),
+            "l2": "flushed before every step (256 MiB write outside the timed events)"}
+
+
+# ------------------------------------------------------------------ GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads()))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=256, help="token rows in the CPU-baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=2, help="token rows per reference-arm step")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    import torch.distributed as dist
+    import block_quantized_matmul_quantize_gb300 as qg
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    wl = workloads()[args.workload]
+    assert wl.wtype == 4 or wl.wtype == 6
+    M, N, K = wl.M, wl.N, wl.K
+    w_host, x_host = wl.weights(), wl.x()
+    dev = torch.device("cuda", local)
+    w = torch.from_numpy(w_host).to(dev)
+    if wl.wtype == 6:
+        w = qg.qgemm_q6k_prepack(w, N, K)
+    x = torch.from_numpy(x_host).to(dev)
+    q = qg.Q8K.empty(M, K, dev)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(qg.qgemm_workspace_bytes(M, N, K), 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def gemm():
+        if wl.wtype == 4:
+            qg.qgemm_q4k(w, N, K, q, y=y, workspace=ws)
+        else:
+            qg.qgemm_q6k(w, N, K, q, y=y, workspace=ws)
+
+    def step():
+        qg.qgemm_quantize_q8k(x, out=q)
+        gemm()
+
+    sampler = ClockSampler(gpu_id_for_smi(local))
+    # warm-up, then about half a second more so that clocks settle
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    t_end = time.time() + 0.5
+    while time.time() < t_end:
+        for _ in range(20):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+
+    K_steps = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    gb = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    ga = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    for e in gb + ga:      # create the events (torch creates them lazily on first record)
+        e.record()
+    torch.cuda.synchronize()
+
+    c0 = qg.qgemm_get_counters()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K_steps):
+        flush.zero_()
+        qg.qgemm_set_profile_events(gb[i], ga[i])
+        ev_s[i].record(stream)
+        step()
+        ev_e[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t1 = time.time()
+    qg.qgemm_set_profile_events(None, None)
+    c1 = qg.qgemm_get_counters()
+    sampler.stop()
+
+    step_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(K_steps)]
+    gemm_ms = [gb[i].elapsed_time(ga[i]) for i in range(K_steps)]
+    mean_ms = sum(step_ms) / K_steps
+    gemm_mean_ms = sum(gemm_ms) / K_steps
+    if world > 1:
+        t = torch.tensor([mean_ms, gemm_mean_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_ms, gemm_mean_ms = float(t[0]), float(t[1])
+
+    ops = 2.0 * M * N * K
+    value = world * ops / (mean_ms * 1e-3) / 1e12
+    launches = sum(c1[k] - c0[k] for k in ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small"))
+
+    # ---- end to end through the public API with host buffers
+    x_pin = torch.from_numpy(x_host).pin_memory()
+    y_pin = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    for _ in range(3):
+        x.copy_(x_pin, non_blocking=True)
+        step()
+        y_pin.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    for i in range(K_steps):
+        flush.zero_()
+        e_s[i].record(stream)
+        x.copy_(x_pin, non_blocking=True)
+        step()
+        y_pin.copy_(y, non_blocking=True)
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = sum(e_s[i].elapsed_time(e_e[i]) for i in range(K_steps)) / K_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    e2e_value = world * ops / (e2e_ms * 1e-3) / 1e12
+
+    bits, site = qg.qgemm_get_device_status()
+
+    if rank == 0:
+        peaks, peak_src = measured_peaks()
+        peak = float(peaks["bf16_tflops"])
+        achieved = ops / (gemm_mean_ms * 1e-3) / 1e12
+        wbytes = N * (K // 256) * wl.block_bytes
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K_steps,
+            "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": config_of(wl),
+            "weight_gbs": wbytes / (gemm_mean_ms * 1e-3) / 1e9,
+            "kernels_us": {"step": mean_ms * 1e3, "tile_gemm": gemm_mean_ms * 1e3,
+                           "quantize_and_prep": (mean_ms - gemm_mean_ms) * 1e3},
+            "roofline": {"kernel": "gemm_tc_kernel (tile GEMM)", "bound": "tensor", "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{peak_src} bf16_tflops (burst; fp16 has the bf16 rate)",
+                         "traffic": NCU_TRAFFIC_BYTES.get(wl.name)},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.nbytes),
+                    "d2h_bytes_per_step": int(M * N * 4)},
+            "gpu_launches": int(launches),
+            "clocks": sampler.summary(t0, t1),
+            "device_status": bits,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            rows = min(args.cpu_rows, M)
+            dt, cops = oracle_sample(wl, rows, x_host, w_host)
+            line["cpu_baseline"] = {"value": cops / dt / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                    "sample": f"{rows} of {M} token rows (quantize + GEMM over all N), "
+                                              f"{dt:.1f} s"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

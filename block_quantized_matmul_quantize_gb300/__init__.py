@@ -1,0 +1,204 @@
+"""Python binding of the k-quant prefill matmul library (libqgemm.so).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in include/qgemm.h.  PyTorch provides device
+memory and the current stream.  The functions carry the C names.
+
+There is no CPU fallback: if the library has not been built, or a call fails,
+a QgemmError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+import torch
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libqgemm.so")
+
+QGEMM_OK, QGEMM_EINVAL, QGEMM_EALIGN, QGEMM_EUNSUPPORTED, QGEMM_ECUDA, QGEMM_EDEVICE = range(6)
+QGEMM_DEV_TIMEOUT, QGEMM_DEV_Q4K_RANGE, QGEMM_DEV_Q6K_SCALE = 0x1, 0x2, 0x4
+QGEMM_OPT_SMALL_M_MAX, QGEMM_OPT_FORCE_BM, QGEMM_OPT_FORCE_SPLITS = 0, 1, 2
+
+Q4K_BLOCK_BYTES = 144
+Q6K_BLOCK_BYTES = 210
+
+
+class QgemmError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"qgemm error {code}: {msg}")
+        self.code = code
+
+
+class _Counters(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in
+                ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small", "q6k_prepack", "split_k")]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise QgemmError(QGEMM_ECUDA, f"{LIB_PATH} not found: build it first "
+                             "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, sz, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+        sig = {
+            "qgemm_version": ([], i32),
+            "qgemm_last_error": ([], ctypes.c_char_p),
+            "qgemm_quantize_q8k": ([vp, i64, i64, i64, vp, vp, vp, vp], i32),
+            "qgemm_workspace_bytes": ([i64, i64, i64], sz),
+            "qgemm_q4k": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
+            "qgemm_q6k_packed_bytes": ([i64, i64], sz),
+            "qgemm_q6k_prepack": ([vp, i64, i64, i64, vp, vp], i32),
+            "qgemm_q6k": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
+            "qgemm_get_counters": ([ctypes.POINTER(_Counters)], i32),
+            "qgemm_reset_counters": ([], i32),
+            "qgemm_get_device_status": ([ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)], i32),
+            "qgemm_set_option": ([i32, i64], i32),
+            "qgemm_get_option": ([i32], i64),
+            "qgemm_set_profile_events": ([vp, vp], i32),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != QGEMM_OK:
+        raise QgemmError(rc, lib().qgemm_last_error().decode())
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+@dataclasses.dataclass
+class Q8K:
+    """Q8_K activations as three device planes (row stride K, K/256, K/16)."""
+    qs: torch.Tensor      # int8  [M, K]
+    d: torch.Tensor       # fp32  [M, K/256]
+    bsums: torch.Tensor   # int16 [M, K/16]
+
+    @property
+    def M(self) -> int:
+        return self.qs.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.qs.shape[1]
+
+    @staticmethod
+    def empty(M: int, K: int, device="cuda") -> "Q8K":
+        return Q8K(torch.empty((M, K), dtype=torch.int8, device=device),
+                   torch.empty((M, K // 256), dtype=torch.float32, device=device),
+                   torch.empty((M, K // 16), dtype=torch.int16, device=device))
+
+
+def qgemm_version() -> int:
+    return lib().qgemm_version()
+
+
+def qgemm_quantize_q8k(x: torch.Tensor, out: Q8K | None = None, stream=None) -> Q8K:
+    """fp32 [M, K] (row stride x.stride(0)) -> Q8K planes."""
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if out is None:
+        out = Q8K.empty(M, K, x.device)
+    _check(lib().qgemm_quantize_q8k(_ptr(x), M, K, x.stride(0), _ptr(out.qs), _ptr(out.d), _ptr(out.bsums),
+                                    _stream(stream)))
+    return out
+
+
+def qgemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().qgemm_workspace_bytes(M, N, K))
+
+
+def _workspace(M, N, K, workspace, device):
+    need = qgemm_workspace_bytes(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return workspace
+
+
+def qgemm_q4k(w: torch.Tensor, N: int, K: int, x: Q8K, y: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y[M, N] = X_q8k @ W_q4k^T.  w: uint8 [N, ldw] device tensor of Q4_K blocks."""
+    assert w.dtype == torch.uint8 and w.dim() == 2 and w.stride(1) == 1
+    M = x.M
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
+    workspace = _workspace(M, N, K, workspace, x.qs.device)
+    _check(lib().qgemm_q4k(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
+                           y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return y
+
+
+def qgemm_q6k_packed_bytes(N: int, K: int) -> int:
+    return int(lib().qgemm_q6k_packed_bytes(N, K))
+
+
+def qgemm_q6k_prepack(w_aos: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """Q6_K blocks (uint8 [N, ldw]) -> the padded layout qgemm_q6k reads."""
+    assert w_aos.dtype == torch.uint8 and w_aos.dim() == 2 and w_aos.stride(1) == 1
+    if out is None:
+        out = torch.empty(qgemm_q6k_packed_bytes(N, K), dtype=torch.uint8, device=w_aos.device)
+    _check(lib().qgemm_q6k_prepack(_ptr(w_aos), N, K, w_aos.stride(0), _ptr(out), _stream(stream)))
+    return out
+
+
+def qgemm_q6k(w_packed: torch.Tensor, N: int, K: int, x: Q8K, y: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    M = x.M
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
+    workspace = _workspace(M, N, K, workspace, x.qs.device)
+    _check(lib().qgemm_q6k(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y), y.stride(0),
+                           _ptr(workspace), workspace.numel(), _stream(stream)))
+    return y
+
+
+def qgemm_get_counters() -> dict:
+    c = _Counters()
+    _check(lib().qgemm_get_counters(ctypes.byref(c)))
+    return {n: int(getattr(c, n)) for n, _ in _Counters._fields_}
+
+
+def qgemm_reset_counters() -> None:
+    _check(lib().qgemm_reset_counters())
+
+
+def qgemm_get_device_status() -> tuple[int, int]:
+    bits, site = ctypes.c_uint32(0), ctypes.c_uint32(0)
+    _check(lib().qgemm_get_device_status(ctypes.byref(bits), ctypes.byref(site)))
+    return int(bits.value), int(site.value)
+
+
+def qgemm_set_option(option: int, value: int) -> None:
+    _check(lib().qgemm_set_option(option, value))
+
+
+def qgemm_get_option(option: int) -> int:
+    return int(lib().qgemm_get_option(option))
+
+
+def qgemm_set_profile_events(before=None, after=None) -> None:
+    """torch.cuda.Event objects (already created, e.g. recorded once) or None."""
+    def h(ev):
+        return None if ev is None else ctypes.c_void_p(ev.cuda_event)
+    _check(lib().qgemm_set_profile_events(h(before), h(after)))

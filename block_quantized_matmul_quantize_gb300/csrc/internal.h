@@ -1,0 +1,58 @@
+// internal.h -- declarations shared by the CUDA translation units of the
+// library (not installed, not part of the C ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+
+namespace qg {
+
+// Device status bits (the word lives in qgemm_api.cu; kernels get its address).
+enum : uint32_t {
+    ST_TIMEOUT = 1u << 0,       // an mbarrier wait gave up (pipeline broken)
+    ST_Q4K_RANGE = 1u << 1,     // Q4_K block with |dmin/d| too large for the fp16 correction operand
+    ST_Q6K_SCALE = 1u << 2,     // Q6_K sub-scale with |sc| > 64 (fp16 operand not exact)
+};
+// The status lives in two words: [0] = OR of the bits above, [1] = 1 + the
+// site id of the first wait that timed out (0 = none).
+
+constexpr uint64_t QG_WAIT_NS = 2000000000ull;  // 2 s of wall time per wait
+constexpr uint32_t QG_WAIT_ITERS = 1u << 28;    // and at most this many polls
+
+constexpr int Q4K_BLOCK = 144;
+constexpr int Q6K_BLOCK = 210;
+constexpr int Q6K_PACKED = 224;                 // 210 B + 14 B of zero padding (16-B aligned)
+
+// ---- kernels' host launchers (each returns cudaError_t of the launch) ----
+cudaError_t launch_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d,
+                                int16_t* bsums, cudaStream_t s);
+
+// Q8_K planes -> tensor-core operand planes in the workspace:
+//   xh  [M][K] fp16 (the int8 values), xbs [M][K/16] fp16 (bsums),
+//   dxT [nb][Mp] fp32 (d transposed, Mp = M rounded up to 4, tail zeroed).
+cudaError_t launch_xprep(const int8_t* qs, const float* d, const int16_t* bsums, int64_t M, int64_t K,
+                         __half* xh, __half* xbs, float* dxT, int64_t Mp, cudaStream_t s);
+
+struct TcLaunch {
+    int wtype;            // 4 or 6
+    int bm;               // tokens per CTA: 16, 32, 64, 128
+    int64_t M, N, K;
+    int splits;           // K splits (>1 -> Y accumulated with atomics, pre-zeroed)
+    float* y;
+    int64_t ldy;
+    uint32_t* status;
+    const CUtensorMap* tm_w;    // raw weight blocks, 2D uint8
+    const CUtensorMap* tm_xh;   // fp16 [M][K], box {64, bm}, 128B swizzle
+    const CUtensorMap* tm_xbs;  // fp16 [M][K/16], box {16, bm}, 32B swizzle (Q4_K only)
+    const CUtensorMap* tm_dx;   // fp32 [nb][Mp], box {bm, 1}
+};
+size_t tc_smem_bytes(int wtype, int bm);
+cudaError_t tc_prepare(int wtype, int bm);   // sets the dynamic smem attribute (per device)
+cudaError_t launch_gemm_tc(const TcLaunch& a, cudaStream_t s);
+
+cudaError_t launch_q6k_prepack(const uint8_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* out,
+                               cudaStream_t s);
+
+}  // namespace qg

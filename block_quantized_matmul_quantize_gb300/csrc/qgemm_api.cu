@@ -1,0 +1,365 @@
+// qgemm_api.cu -- the C ABI (include/qgemm.h): argument validation, path
+// selection, TMA descriptor set-up, counters, options and device status.
+// Host code only, apart from the device status word.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "qgemm.h"
+
+namespace {
+
+// ------------------------------------------------------------ errors
+thread_local char g_err[256] = {0};
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+void clear_err() { g_err[0] = 0; }
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(QGEMM_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ------------------------------------------------------------ global state
+std::atomic<uint64_t> g_cnt[8];
+enum { C_QUANT, C_XPREP, C_Q4K_TC, C_Q6K_TC, C_Q4K_SMALL, C_Q6K_SMALL, C_PREPACK, C_SPLITK };
+std::atomic<int64_t> g_opt[3] = {{0}, {0}, {0}};
+std::atomic<cudaEvent_t> g_ev_before{nullptr}, g_ev_after{nullptr};
+
+}  // namespace
+
+// Device status: [0] = bits, [1] = 1 + site of the first timed-out wait.
+__device__ uint32_t g_qgemm_status[2];
+
+namespace {
+
+constexpr int MAX_DEV = 64;
+struct DevState {
+    bool init = false;
+    cudaError_t init_err = cudaSuccess;
+    uint32_t* status = nullptr;
+    int sm_count = 0;
+};
+std::mutex g_mtx;
+DevState g_dev[MAX_DEV];
+
+int device_state(DevState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= MAX_DEV) return fail(QGEMM_EUNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_mtx);
+    DevState& st = g_dev[dev];
+    if (!st.init) {
+        st.init = true;
+        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status), g_qgemm_status);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        for (int wt : {4, 6})
+            for (int bm : {16, 32, 64, 128})
+                if (e == cudaSuccess) e = qg::tc_prepare(wt, bm);
+        st.init_err = e;
+    }
+    if (st.init_err != cudaSuccess) return cuda_fail(st.init_err, "device set-up");
+    *out = &st;
+    return QGEMM_OK;
+}
+
+// ------------------------------------------------------------ TMA descriptors
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// 2D tiled map: `inner` elements per row (contiguous), `outer` rows,
+// `row_bytes` between rows, box {box_inner, box_outer}; out of range -> zeros.
+int make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+             uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(QGEMM_ECUDA, "cuTensorMapEncodeTiled not available from the driver");
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QGEMM_ECUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return QGEMM_OK;
+}
+
+// ------------------------------------------------------------ validation
+int check_q8k(const int8_t* xqs, const float* xd, const int16_t* xbsums) {
+    if (!xqs || !xd || !xbsums) return fail(QGEMM_EINVAL, "null Q8_K plane");
+    if (!aligned(xqs, 16) || !aligned(xd, 16) || !aligned(xbsums, 16))
+        return fail(QGEMM_EALIGN, "Q8_K planes must be 16-byte aligned");
+    return QGEMM_OK;
+}
+int check_mk(int64_t M, int64_t K) {
+    if (M < 0) return fail(QGEMM_EINVAL, "M must be >= 0 (got %lld)", static_cast<long long>(M));
+    if (K < 256 || K % 256 != 0)
+        return fail(QGEMM_EINVAL, "K must be a positive multiple of 256 (got %lld)", static_cast<long long>(K));
+    if (M >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+        return fail(QGEMM_EUNSUPPORTED, "M and K must be below 2^31");
+    return QGEMM_OK;
+}
+
+struct Plan {
+    int bm;
+    int splits;
+};
+
+Plan plan_tc(int64_t M, int64_t N, int64_t K, int sm_count) {
+    Plan p{};
+    const int64_t fbm = g_opt[QGEMM_OPT_FORCE_BM].load();
+    if (fbm == 16 || fbm == 32 || fbm == 64 || fbm == 128)
+        p.bm = static_cast<int>(fbm);
+    else
+        p.bm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+    const int64_t nb = K / 256;
+    const int64_t fs = g_opt[QGEMM_OPT_FORCE_SPLITS].load();
+    if (fs > 0) {
+        p.splits = static_cast<int>(fs > nb ? nb : fs);
+    } else {
+        const int64_t tiles = ((N + 127) / 128) * ((M + p.bm - 1) / p.bm);
+        int64_t s = 1;
+        if (tiles < sm_count) s = (sm_count + tiles - 1) / tiles;
+        int64_t smax = nb / 2 > 0 ? nb / 2 : 1;  // keep >= 2 superblocks per split
+        if (s > smax) s = smax;
+        p.splits = static_cast<int>(s);
+    }
+    return p;
+}
+
+int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs, const float* xd,
+           const int16_t* xbsums, int64_t M, float* y, int64_t ldy, void* ws, size_t ws_bytes,
+           cudaStream_t stream) {
+    DevState* ds = nullptr;
+    int rc = device_state(&ds);
+    if (rc) return rc;
+    const size_t need = qgemm_workspace_bytes(M, N, K);
+    if (!ws || ws_bytes < need)
+        return fail(QGEMM_EINVAL, "workspace of %zu bytes needed (got %zu)", need, ws ? ws_bytes : size_t(0));
+    if (!aligned(ws, 256)) return fail(QGEMM_EALIGN, "workspace must be 256-byte aligned");
+
+    const Plan pl = plan_tc(M, N, K, ds->sm_count);
+    const int64_t nb = K / 256;
+    const int64_t Mp = (M + 3) / 4 * 4;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    __half* xh = reinterpret_cast<__half*>(base);
+    __half* xbs = reinterpret_cast<__half*>(base + align256(size_t(M) * K * 2));
+    float* dxT = reinterpret_cast<float*>(base + align256(size_t(M) * K * 2) + align256(size_t(M) * (K / 16) * 2));
+
+    cudaError_t e = qg::launch_xprep(xqs, xd, xbsums, M, K, xh, xbs, dxT, Mp, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "operand preparation launch");
+    g_cnt[C_XPREP]++;
+
+    CUtensorMap tm_w, tm_xh, tm_xbs, tm_dx;
+    const int blk = wtype == 4 ? qg::Q4K_BLOCK : qg::Q6K_PACKED;
+    if ((rc = make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, uint64_t(nb) * blk, N, ldw, blk, 128,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return rc;
+    if ((rc = make_map(&tm_xh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, K, M, uint64_t(K) * 2, 64, pl.bm,
+                       CU_TENSOR_MAP_SWIZZLE_128B)))
+        return rc;
+    if ((rc = make_map(&tm_xbs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xbs, K / 16, M, uint64_t(K / 16) * 2, 16, pl.bm,
+                       CU_TENSOR_MAP_SWIZZLE_32B)))
+        return rc;
+    if ((rc = make_map(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dxT, Mp, nb, uint64_t(Mp) * 4, pl.bm, 1,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return rc;
+
+    if (pl.splits > 1) {
+        e = cudaMemset2DAsync(y, size_t(ldy) * 4, 0, size_t(N) * 4, size_t(M), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "zeroing Y for split-K");
+    }
+    qg::TcLaunch a{};
+    a.wtype = wtype;
+    a.bm = pl.bm;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.splits = pl.splits;
+    a.y = y;
+    a.ldy = ldy;
+    a.status = ds->status;
+    a.tm_w = &tm_w;
+    a.tm_xh = &tm_xh;
+    a.tm_xbs = wtype == 4 ? &tm_xbs : nullptr;
+    a.tm_dx = &tm_dx;
+    cudaEvent_t evb = g_ev_before.load(), eva = g_ev_after.load();
+    if (evb) cudaEventRecord(evb, stream);
+    e = qg::launch_gemm_tc(a, stream);
+    if (eva) cudaEventRecord(eva, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tile GEMM launch");
+    g_cnt[wtype == 4 ? C_Q4K_TC : C_Q6K_TC]++;
+    if (pl.splits > 1) g_cnt[C_SPLITK]++;
+    return QGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qgemm_version(void) { return 100; }
+
+const char* qgemm_last_error(void) { return g_err; }
+
+int qgemm_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d, int16_t* bsums,
+                       qgemm_stream_t stream) {
+    clear_err();
+    int rc = check_mk(M, K);
+    if (rc) return rc;
+    if (M == 0) return QGEMM_OK;
+    if (!x) return fail(QGEMM_EINVAL, "x is null");
+    if (ldx < K) return fail(QGEMM_EINVAL, "ldx (%lld) < K (%lld)", (long long)ldx, (long long)K);
+    if (!aligned(x, 16) || ldx % 4 != 0) return fail(QGEMM_EALIGN, "x must be 16-byte aligned with ldx % 4 == 0");
+    if ((rc = check_q8k(qs, d, bsums))) return rc;
+    cudaError_t e = qg::launch_quantize_q8k(x, M, K, ldx, qs, d, bsums, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    g_cnt[C_QUANT]++;
+    return QGEMM_OK;
+}
+
+size_t qgemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    (void)N;
+    if (M <= 0 || K <= 0 || K % 256) return 0;
+    const int64_t nb = K / 256, Mp = (M + 3) / 4 * 4;
+    return align256(size_t(M) * K * 2) + align256(size_t(M) * (K / 16) * 2) + align256(size_t(nb) * Mp * 4);
+}
+
+static int gemm_common_checks(const void* w, int64_t N, int64_t K, const int8_t* xqs, const float* xd,
+                              const int16_t* xbsums, int64_t M, float* y, int64_t ldy) {
+    int rc = check_mk(M, K);
+    if (rc) return rc;
+    if (N < 1) return fail(QGEMM_EINVAL, "N must be >= 1 (got %lld)", (long long)N);
+    if (N >= (int64_t(1) << 31)) return fail(QGEMM_EUNSUPPORTED, "N must be below 2^31");
+    if (M == 0) return QGEMM_OK;
+    if (!w) return fail(QGEMM_EINVAL, "weights pointer is null");
+    if (!aligned(w, 16)) return fail(QGEMM_EALIGN, "weights must be 16-byte aligned");
+    if ((rc = check_q8k(xqs, xd, xbsums))) return rc;
+    if (!y) return fail(QGEMM_EINVAL, "y is null");
+    if (ldy < N) return fail(QGEMM_EINVAL, "ldy (%lld) < N (%lld)", (long long)ldy, (long long)N);
+    if (!aligned(y, 4)) return fail(QGEMM_EALIGN, "y must be 4-byte aligned");
+    return QGEMM_OK;
+}
+
+int qgemm_q4k(const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs, const float* xd,
+              const int16_t* xbsums, int64_t M, float* y, int64_t ldy, void* workspace, size_t workspace_bytes,
+              qgemm_stream_t stream) {
+    clear_err();
+    int rc = gemm_common_checks(w, N, K, xqs, xd, xbsums, M, y, ldy);
+    if (rc || M == 0) return rc;
+    if (ldw < (K / 256) * qg::Q4K_BLOCK) return fail(QGEMM_EINVAL, "ldw smaller than a row of Q4_K blocks");
+    if (ldw % 16 != 0) return fail(QGEMM_EALIGN, "ldw must be a multiple of 16 bytes");
+    return run_tc(4, w, N, K, ldw, xqs, xd, xbsums, M, y, ldy, workspace, workspace_bytes,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t qgemm_q6k_packed_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % 256) return 0;
+    return size_t(N) * size_t(K / 256) * qg::Q6K_PACKED;
+}
+
+int qgemm_q6k_prepack(const void* w_aos, int64_t N, int64_t K, int64_t ldw, void* w_packed, qgemm_stream_t stream) {
+    clear_err();
+    if (N < 1) return fail(QGEMM_EINVAL, "N must be >= 1");
+    if (K < 256 || K % 256) return fail(QGEMM_EINVAL, "K must be a positive multiple of 256");
+    if (!w_aos || !w_packed) return fail(QGEMM_EINVAL, "null pointer");
+    if (ldw < (K / 256) * qg::Q6K_BLOCK) return fail(QGEMM_EINVAL, "ldw smaller than a row of Q6_K blocks");
+    if (!aligned(w_packed, 16)) return fail(QGEMM_EALIGN, "w_packed must be 16-byte aligned");
+    cudaError_t e = qg::launch_q6k_prepack(static_cast<const uint8_t*>(w_aos), N, K, ldw,
+                                           static_cast<uint8_t*>(w_packed), reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "prepack launch");
+    g_cnt[C_PREPACK]++;
+    return QGEMM_OK;
+}
+
+int qgemm_q6k(const void* w_packed, int64_t N, int64_t K, const int8_t* xqs, const float* xd,
+              const int16_t* xbsums, int64_t M, float* y, int64_t ldy, void* workspace, size_t workspace_bytes,
+              qgemm_stream_t stream) {
+    clear_err();
+    int rc = gemm_common_checks(w_packed, N, K, xqs, xd, xbsums, M, y, ldy);
+    if (rc || M == 0) return rc;
+    return run_tc(6, w_packed, N, K, (K / 256) * qg::Q6K_PACKED, xqs, xd, xbsums, M, y, ldy, workspace,
+                  workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int qgemm_get_counters(qgemm_counters* out) {
+    if (!out) return fail(QGEMM_EINVAL, "null counters pointer");
+    out->quantize = g_cnt[C_QUANT];
+    out->xprep = g_cnt[C_XPREP];
+    out->q4k_tc = g_cnt[C_Q4K_TC];
+    out->q6k_tc = g_cnt[C_Q6K_TC];
+    out->q4k_small = g_cnt[C_Q4K_SMALL];
+    out->q6k_small = g_cnt[C_Q6K_SMALL];
+    out->q6k_prepack = g_cnt[C_PREPACK];
+    out->split_k = g_cnt[C_SPLITK];
+    return QGEMM_OK;
+}
+
+int qgemm_reset_counters(void) {
+    for (auto& c : g_cnt) c = 0;
+    return QGEMM_OK;
+}
+
+int qgemm_get_device_status(uint32_t* bits, uint32_t* site) {
+    clear_err();
+    DevState* ds = nullptr;
+    int rc = device_state(&ds);
+    if (rc) return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    uint32_t h[2] = {0, 0};
+    e = cudaMemcpyFromSymbol(h, g_qgemm_status, sizeof(h));
+    if (e != cudaSuccess) return cuda_fail(e, "reading device status");
+    const uint32_t z[2] = {0, 0};
+    e = cudaMemcpyToSymbol(g_qgemm_status, z, sizeof(z));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing device status");
+    if (bits) *bits = h[0];
+    if (site) *site = h[1];
+    return QGEMM_OK;
+}
+
+int qgemm_set_option(int option, int64_t value) {
+    clear_err();
+    if (option < 0 || option > 2) return fail(QGEMM_EINVAL, "unknown option %d", option);
+    if (value < 0) return fail(QGEMM_EINVAL, "option values are >= 0");
+    if (option == QGEMM_OPT_FORCE_BM && value != 0 && value != 16 && value != 32 && value != 64 && value != 128)
+        return fail(QGEMM_EINVAL, "FORCE_BM must be 0, 16, 32, 64 or 128");
+    g_opt[option] = value;
+    return QGEMM_OK;
+}
+
+int64_t qgemm_get_option(int option) {
+    if (option < 0 || option > 2) return -1;
+    return g_opt[option].load();
+}
+
+int qgemm_set_profile_events(qgemm_event_t before, qgemm_event_t after) {
+    g_ev_before = reinterpret_cast<cudaEvent_t>(before);
+    g_ev_after = reinterpret_cast<cudaEvent_t>(after);
+    return QGEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,171 @@
+// quantize.cu -- fp32 activations -> Q8_K, plus the small HBM-bound helper
+// kernels around the GEMM (operand preparation, Q6_K repacking).
+//
+// Q8_K, as the library defines it (the block the pages call "BlockQ8_K,
+// 292 B / 256 elements", vllm.cpp PR #3036, commit 4): per 256-element chunk
+// of a row, d = amax/127 (fp32), q = round-half-away-from-zero(x/d) clamped to
+// +-127, and 16 int16 sums of each 16 consecutive q.  amax = 0 gives d = 0 and
+// all-zero q and sums.  Stored as three planes (qs [M][K] int8, d [M][K/256]
+// fp32, bsums [M][K/16] int16) so that every plane row is 16-byte aligned.
+//
+// Numerics: x/d and amax/127 are IEEE fp32 divisions, correctly rounded (the
+// library is built without fast-math; -prec-div=true), and roundf rounds
+// halves away from zero, so the int8 values, scales and sums are bit-exact
+// with any IEEE implementation of the same definition.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace qg {
+
+namespace {
+
+constexpr int QWARPS = 8;  // chunks (warps) per block
+
+// One warp per 256-element chunk: each lane owns 8 consecutive elements
+// (two 16-byte loads), so one chunk is one coalesced 1 KiB read.
+__global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* __restrict__ x, int64_t M,
+                                                                  int64_t K, int64_t ldx, int8_t* __restrict__ qs,
+                                                                  float* __restrict__ dout,
+                                                                  int16_t* __restrict__ bsums) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nb = K >> 8;
+    const int64_t chunk = static_cast<int64_t>(blockIdx.x) * QWARPS + (threadIdx.x >> 5);
+    if (chunk >= M * nb) return;
+    const int64_t m = chunk / nb;
+    const int64_t b = chunk - m * nb;
+
+    const float4* src = reinterpret_cast<const float4*>(x + m * ldx + b * 256) + lane * 2;
+    const float4 v0 = __ldcs(src);
+    const float4 v1 = __ldcs(src + 1);
+    float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+
+    int q[8];
+    float d = 0.0f;
+    if (amax == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = 0;
+    } else {
+        d = amax / 127.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float r = roundf(v[i] / d);
+            r = fminf(fmaxf(r, -127.0f), 127.0f);
+            q[i] = static_cast<int>(r);
+        }
+    }
+    uint2 packed;
+    packed.x = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) | (static_cast<uint32_t>(q[3] & 0xff) << 24);
+    packed.y = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) | (static_cast<uint32_t>(q[7] & 0xff) << 24);
+    *reinterpret_cast<uint2*>(qs + m * K + b * 256 + lane * 8) = packed;
+
+    int s = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+    s += __shfl_xor_sync(0xffffffffu, s, 1);  // lanes 2g, 2g+1 hold group g's 16 values
+    if ((lane & 1) == 0) bsums[m * (K >> 4) + b * 16 + (lane >> 1)] = static_cast<int16_t>(s);
+    if (lane == 0) dout[m * nb + b] = d;
+}
+
+// Q8_K -> fp16 operand planes.  Every int8 value and every bsum (|bsum| <=
+// 16*127) is an integer of at most 11 significant bits, so fp16 holds it exactly.
+__global__ void xprep_kernel(const int8_t* __restrict__ qs, const float* __restrict__ d,
+                             const int16_t* __restrict__ bsums, int64_t M, int64_t K, __half* __restrict__ xh,
+                             __half* __restrict__ xbs, float* __restrict__ dxT, int64_t Mp) {
+    const int64_t nb = K >> 8;
+    const int64_t n16 = M * (K >> 4);                 // 16-element groups of qs (= number of bsums)
+    const int64_t ndx = nb * Mp;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16 + ndx; i += stride) {
+        if (i < n16) {
+            const int4 raw = __ldcs(reinterpret_cast<const int4*>(qs) + i);
+            const int w[4] = {raw.x, raw.y, raw.z, raw.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int lo = static_cast<int8_t>((w[j] >> (16 * h)) & 0xff);
+                    const int hi = static_cast<int8_t>((w[j] >> (16 * h + 8)) & 0xff);
+                    const __half2 p = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+                    o[2 * j + h] = *reinterpret_cast<const uint32_t*>(&p);
+                }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(xh) + 2 * i;
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            xbs[i] = __int2half_rn(bsums[i]);
+        } else {
+            const int64_t j = i - n16;
+            const int64_t b = j / Mp;
+            const int64_t m = j - b * Mp;
+            dxT[j] = (m < M) ? d[m * nb + b] : 0.0f;
+        }
+    }
+}
+
+// Q6_K 210-byte blocks -> 224-byte blocks (same bytes, 14 zero bytes after),
+// so that every block and every row starts on a 16-byte boundary.
+__global__ void q6k_prepack_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t nb, int64_t ldw,
+                                   uint8_t* __restrict__ out) {
+    const int64_t total = N * nb * (Q6K_PACKED / 16);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int64_t blk = i / (Q6K_PACKED / 16);
+        const int part = static_cast<int>(i - blk * (Q6K_PACKED / 16));
+        const int64_t n = blk / nb;
+        const int64_t b = blk - n * nb;
+        const uint8_t* src = w + n * ldw + b * Q6K_BLOCK;
+        uint8_t v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int off = part * 16 + j;
+            v[j] = off < Q6K_BLOCK ? src[off] : 0;
+        }
+        uint4 o;
+        o.x = v[0] | (v[1] << 8) | (v[2] << 16) | (static_cast<uint32_t>(v[3]) << 24);
+        o.y = v[4] | (v[5] << 8) | (v[6] << 16) | (static_cast<uint32_t>(v[7]) << 24);
+        o.z = v[8] | (v[9] << 8) | (v[10] << 16) | (static_cast<uint32_t>(v[11]) << 24);
+        o.w = v[12] | (v[13] << 8) | (v[14] << 16) | (static_cast<uint32_t>(v[15]) << 24);
+        reinterpret_cast<uint4*>(out)[i] = o;
+    }
+}
+
+int grid_for(int64_t work, int threads) {
+    int64_t g = (work + threads - 1) / threads;
+    const int64_t cap = 152 * 16;
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    return static_cast<int>(g);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d,
+                                int16_t* bsums, cudaStream_t s) {
+    const int64_t chunks = M * (K >> 8);
+    const int64_t blocks = (chunks + QWARPS - 1) / QWARPS;
+    quantize_q8k_kernel<<<static_cast<unsigned>(blocks), QWARPS * 32, 0, s>>>(x, M, K, ldx, qs, d, bsums);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_xprep(const int8_t* qs, const float* d, const int16_t* bsums, int64_t M, int64_t K,
+                         __half* xh, __half* xbs, float* dxT, int64_t Mp, cudaStream_t s) {
+    const int64_t work = M * (K >> 4) + (K >> 8) * Mp;
+    xprep_kernel<<<grid_for(work, 256), 256, 0, s>>>(qs, d, bsums, M, K, xh, xbs, dxT, Mp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q6k_prepack(const uint8_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* out,
+                               cudaStream_t s) {
+    const int64_t nb = K >> 8;
+    const int64_t work = N * nb * (Q6K_PACKED / 16);
+    q6k_prepack_kernel<<<grid_for(work, 256), 256, 0, s>>>(w, N, nb, ldw, out);
+    return cudaGetLastError();
+}
+
+}  // namespace qg

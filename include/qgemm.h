@@ -1,0 +1,173 @@
+/*
+ * qgemm.h -- C ABI of the k-quant prefill matmul library for GB300 (sm_103a).
+ *
+ * The operation is the quantized prefill GEMM of llama.cpp-style models:
+ * weights stored as Q4_K or Q6_K blocks multiply activations quantized on the
+ * fly to Q8_K, giving an fp32 output.  The pages this library follows study
+ * it as "KQuantGemmKWmmaQ4K/Q6K" ("perf(KERNEL-QUANT-CIQ-GEMM-ROCM):
+ * cooperative-tile WMMA kernels -- Shared rejected, BigTile accepted",
+ * vllm.cpp PR #3036) and as llama.cpp's mul_mat_q ("cuda: branch-free PTQ1_0
+ * MMQ tile loader and full Ampere tile table", llama.cpp PR #214).
+ *
+ * Block formats (field meaning; the byte packing is the GGUF one):
+ *   Q4_K, 144 B / 256 weights: fp16 d, fp16 dmin, 12 bytes holding eight
+ *         6-bit sub-scales sc_j and eight 6-bit sub-mins m_j, 128 bytes of
+ *         4-bit quants; sub-block j = weights 32j..32j+31;
+ *         w = d*sc_j*q - dmin*m_j.
+ *   Q6_K, 210 B / 256 weights: ql[128] (low 4 bits), qh[64] (high 2 bits),
+ *         int8 scales[16] (sub-block j = weights 16j..16j+15), fp16 d;
+ *         w = d*sc_j*(q - 32).
+ *   Q8_K, 256 activations: fp32 d = amax/127, int8 q = round-half-away(x/d)
+ *         clamped to +-127, int16 bsums[16] = sums of each 16 q (the
+ *         "BlockQ8_K (292B/256 elements)" of PR #3036, commit 4).  Here kept
+ *         as three planes: qs [M][K] int8, d [M][K/256] fp32, bsums [M][K/16]
+ *         int16, each contiguous with row stride K, K/256, K/16 elements.
+ *
+ * Conventions (all calls):
+ *   - Device pointers are caller-owned; the library never allocates or frees
+ *     device memory.  Scratch ("workspace") is passed in, sized by a query
+ *     function -- the caller-owned-scratch convention of the pages
+ *     (hip_linear_attention_prefill_scratch_bytes, hip-ep PR #627).
+ *   - Calls enqueue work on `stream` and return; they do not synchronize.
+ *   - Argument errors are reported synchronously and nothing is launched
+ *     (a nonzero status, so the caller can fall back: "the launcher returns
+ *     nonzero and the runtime falls back", hip-ep PR #627).  Unsupported
+ *     shapes are declined, never computed wrongly.  qgemm_last_error()
+ *     gives a one-line reason (thread-local).
+ *   - Y is fully overwritten (beta = 0).
+ *   - The library keeps process-global launch counters and options (not
+ *     synchronized between threads that change options concurrently).
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QGEMM_API __attribute__((visibility("default")))
+#else
+#define QGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qgemm_stream_t; /* = cudaStream_t; NULL = legacy default stream */
+typedef struct CUevent_st *qgemm_event_t;   /* = cudaEvent_t */
+
+typedef enum {
+    QGEMM_OK = 0,
+    QGEMM_EINVAL = 1,       /* bad size, null pointer, too-small workspace   */
+    QGEMM_EALIGN = 2,       /* pointer or stride not aligned as required     */
+    QGEMM_EUNSUPPORTED = 3, /* shape outside what the kernels handle         */
+    QGEMM_ECUDA = 4,        /* a CUDA launch or runtime call failed          */
+    QGEMM_EDEVICE = 5       /* device-side check failed (see status)         */
+} qgemm_status;
+
+/* Library version, major*10000 + minor*100 + patch. */
+QGEMM_API int qgemm_version(void);
+
+/* One-line description of the last failure in this thread ("" if none). */
+QGEMM_API const char *qgemm_last_error(void);
+
+/* ------------------------------------------------------------- Q8_K ----
+ * qgemm_quantize_q8k: fp32 activations -> Q8_K planes (step "quantize the
+ * activations" that precedes the GEMM; PR #3036 commit 5, EnsureQuantScratch).
+ *   x      device, fp32 [M][ldx] row-major, 16-B aligned, ldx % 4 == 0,
+ *          ldx >= K; values must be finite.
+ *   M      rows (tokens), M >= 0 (M == 0: nothing to do, QGEMM_OK).
+ *   K      columns, K >= 256 and K % 256 == 0.
+ *   qs     device, int8 [M][K], 16-B aligned.
+ *   d      device, fp32 [M][K/256], 16-B aligned.
+ *   bsums  device, int16 [M][K/16], 16-B aligned.
+ * Bit-exact with the IEEE definition: d = amax/127 (fp32), q = roundf(x/d)
+ * clamped to +-127, amax == 0 -> d = 0, q = 0, bsums = 0.
+ * Errors: EINVAL (sizes, null), EALIGN, ECUDA (launch). */
+QGEMM_API int qgemm_quantize_q8k(const float *x, int64_t M, int64_t K, int64_t ldx, int8_t *qs, float *d,
+                       int16_t *bsums, qgemm_stream_t stream);
+
+/* ------------------------------------------------------------- GEMM ----
+ * Workspace bytes the GEMM calls need for M tokens and depth K (holds the
+ * fp16 tensor-core operand copy of the Q8_K activations).  0 when the small-M
+ * path runs.  The workspace must be 256-B aligned. */
+QGEMM_API size_t qgemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* qgemm_q4k: Y[M][N] = X_q8k[M][K] * W_q4k[N][K]^T.
+ *   w      device, N rows of K/256 Q4_K blocks (144 B each), row stride ldw
+ *          bytes; 16-B aligned; ldw % 16 == 0; ldw >= (K/256)*144.
+ *   N      weight rows, N >= 1.     K: K >= 256, K % 256 == 0.
+ *   xqs, xd, xbsums   the Q8_K planes of M tokens (as qgemm_quantize_q8k
+ *          writes them).   M >= 0 (0: nothing to do).
+ *   y      device, fp32 [M][ldy], ldy >= N, 4-B aligned.  Overwritten.
+ *   workspace, workspace_bytes   device scratch >= qgemm_workspace_bytes.
+ * Accuracy: |Y - Y_exact| <= 2e-5 * sum_b |c_b| + 1e-6 per element, c_b the
+ * contribution of superblock b (fp32 accumulation of exact integer partials).
+ * Value range: |dmin/d| <= 1000 per block (else device status
+ * QGEMM_DEV_Q4K_RANGE is set and Y is not to be trusted).
+ * Errors: EINVAL, EALIGN, EUNSUPPORTED (M, N >= 2^31), ECUDA. */
+QGEMM_API int qgemm_q4k(const void *w, int64_t N, int64_t K, int64_t ldw, const int8_t *xqs, const float *xd,
+              const int16_t *xbsums, int64_t M, float *y, int64_t ldy, void *workspace,
+              size_t workspace_bytes, qgemm_stream_t stream);
+
+/* Q6_K weights are used in a repacked form: each 210-B block padded to 224 B
+ * (16-B aligned blocks and rows for TMA).  Repack once, e.g. at model load;
+ * the repack is not part of the GEMM.
+ *   w_aos  device, N rows of K/256 Q6_K blocks (210 B), row stride ldw >=
+ *          (K/256)*210 bytes, no alignment requirement.
+ *   w_packed device, qgemm_q6k_packed_bytes(N, K) bytes, 16-B aligned. */
+QGEMM_API size_t qgemm_q6k_packed_bytes(int64_t N, int64_t K);
+QGEMM_API int qgemm_q6k_prepack(const void *w_aos, int64_t N, int64_t K, int64_t ldw, void *w_packed,
+                      qgemm_stream_t stream);
+
+/* qgemm_q6k: as qgemm_q4k, with Q6_K weights repacked by qgemm_q6k_prepack.
+ * Value range: sub-scales |sc| <= 64 (else device status QGEMM_DEV_Q6K_SCALE). */
+QGEMM_API int qgemm_q6k(const void *w_packed, int64_t N, int64_t K, const int8_t *xqs, const float *xd,
+              const int16_t *xbsums, int64_t M, float *y, int64_t ldy, void *workspace,
+              size_t workspace_bytes, qgemm_stream_t stream);
+
+/* ------------------------------------------------------ diagnostics ----
+ * Launch counters per path (proof of which kernel ran: the per-variant
+ * dispatch counters of PR #3036, commit 4). */
+typedef struct {
+    uint64_t quantize;     /* qgemm_quantize_q8k launches           */
+    uint64_t xprep;        /* operand-preparation launches         */
+    uint64_t q4k_tc;       /* Q4_K tensor-core tile GEMM launches   */
+    uint64_t q6k_tc;       /* Q6_K tensor-core tile GEMM launches   */
+    uint64_t q4k_small;    /* Q4_K small-M streaming launches       */
+    uint64_t q6k_small;    /* Q6_K small-M streaming launches       */
+    uint64_t q6k_prepack;  /* Q6_K repack launches                  */
+    uint64_t split_k;      /* GEMM launches that used split-K       */
+} qgemm_counters;
+QGEMM_API int qgemm_get_counters(qgemm_counters *out);
+QGEMM_API int qgemm_reset_counters(void);
+
+/* Device status word of the current device.  Bits: */
+#define QGEMM_DEV_TIMEOUT 0x1u   /* a pipeline wait gave up (bounded waits) */
+#define QGEMM_DEV_Q4K_RANGE 0x2u /* a Q4_K block had |dmin/d| > 1000        */
+#define QGEMM_DEV_Q6K_SCALE 0x4u /* a Q6_K sub-scale had |sc| > 64          */
+/* Synchronizes the device, returns the status bits in *bits and the site of
+ * the first timed-out wait (0 = none) in *site (may be NULL), then clears
+ * both.  QGEMM_ECUDA if the device is unusable. */
+QGEMM_API int qgemm_get_device_status(uint32_t *bits, uint32_t *site);
+
+/* ----------------------------------------------------------- options ----
+ * Process-global knobs, mainly for tests and tuning. */
+typedef enum {
+    QGEMM_OPT_SMALL_M_MAX = 0,  /* M <= this uses the small-M path (default 0 = off) */
+    QGEMM_OPT_FORCE_BM = 1,     /* tokens per CTA for the tile path: 0 = auto, 16/32/64/128 */
+    QGEMM_OPT_FORCE_SPLITS = 2  /* split-K factor: 0 = auto, else 1..K/256       */
+} qgemm_option;
+QGEMM_API int qgemm_set_option(int option, int64_t value);
+QGEMM_API int64_t qgemm_get_option(int option);
+
+/* Profiling hook: if set (non-NULL), every GEMM call records `before` on its
+ * stream just before the main GEMM kernel and `after` just after it, so a
+ * caller can time that kernel alone.  Pass NULLs to disable. */
+QGEMM_API int qgemm_set_profile_events(qgemm_event_t before, qgemm_event_t after);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QGEMM_H */

@@ -1,0 +1,116 @@
+"""The C-ABI library builds, loads and exports every symbol include/qgemm.h
+declares; host-side validation rejects bad arguments before touching the GPU.
+No compute calls: these run without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_quantized_matmul_quantize_gb300 as qg
+from block_quantized_matmul_quantize_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemm.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    qbuild.build()
+    return qg.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qgemm_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for need in ("qgemm_quantize_q8k", "qgemm_q4k", "qgemm_q6k", "qgemm_q6k_prepack",
+                 "qgemm_workspace_bytes", "qgemm_get_counters", "qgemm_get_device_status"):
+        assert need in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_no_oracle_symbols_in_library(L):
+    # the product library shares no code with the CPU oracle
+    for n in ("oracle_gemm_q4k", "oracle_quantize_q8k", "oracle_q4k_fields"):
+        with pytest.raises(AttributeError):
+            getattr(L, n)
+
+
+def test_version(L):
+    assert L.qgemm_version() >= 100
+
+
+FAKE = ctypes.c_void_p(0x100000)      # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p(0x100004)
+
+
+def test_quantize_validation(L):
+    assert L.qgemm_quantize_q8k(FAKE, 1, 100, 100, FAKE, FAKE, FAKE, None) == qg.QGEMM_EINVAL
+    assert b"multiple of 256" in L.qgemm_last_error()
+    assert L.qgemm_quantize_q8k(FAKE, -1, 256, 256, FAKE, FAKE, FAKE, None) == qg.QGEMM_EINVAL
+    assert L.qgemm_quantize_q8k(FAKE, 0, 256, 256, FAKE, FAKE, FAKE, None) == qg.QGEMM_OK   # empty
+    assert L.qgemm_quantize_q8k(None, 2, 256, 256, FAKE, FAKE, FAKE, None) == qg.QGEMM_EINVAL
+    assert L.qgemm_quantize_q8k(FAKE, 2, 256, 128, FAKE, FAKE, FAKE, None) == qg.QGEMM_EINVAL
+    assert L.qgemm_quantize_q8k(MISALIGNED, 2, 256, 256, FAKE, FAKE, FAKE, None) == qg.QGEMM_EALIGN
+    assert L.qgemm_quantize_q8k(FAKE, 2, 256, 258, FAKE, FAKE, FAKE, None) == qg.QGEMM_EALIGN
+    assert L.qgemm_quantize_q8k(FAKE, 2, 256, 256, MISALIGNED, FAKE, FAKE, None) == qg.QGEMM_EALIGN
+    assert L.qgemm_quantize_q8k(FAKE, 2, 256, 256, None, FAKE, FAKE, None) == qg.QGEMM_EINVAL
+
+
+def test_gemm_validation(L):
+    ws = FAKE
+    args = lambda **kw: dict(dict(w=FAKE, N=128, K=512, ldw=288, qs=FAKE, d=FAKE, bs=FAKE, M=4, y=FAKE,
+                                  ldy=128), **kw)
+
+    def q4k(a):
+        return L.qgemm_q4k(a["w"], a["N"], a["K"], a["ldw"], a["qs"], a["d"], a["bs"], a["M"], a["y"],
+                           a["ldy"], ws, 1 << 20, None)
+    assert q4k(args(K=300)) == qg.QGEMM_EINVAL
+    assert q4k(args(N=0)) == qg.QGEMM_EINVAL
+    assert q4k(args(M=0)) == qg.QGEMM_OK                    # empty: nothing launched
+    assert q4k(args(ldw=287)) == qg.QGEMM_EINVAL           # shorter than a row of blocks
+    assert q4k(args(ldw=296)) == qg.QGEMM_EALIGN           # not a multiple of 16
+    assert q4k(args(w=MISALIGNED)) == qg.QGEMM_EALIGN
+    assert q4k(args(w=None)) == qg.QGEMM_EINVAL
+    assert q4k(args(qs=MISALIGNED)) == qg.QGEMM_EALIGN
+    assert q4k(args(y=None)) == qg.QGEMM_EINVAL
+    assert q4k(args(ldy=100)) == qg.QGEMM_EINVAL
+    assert q4k(args(N=1 << 31)) == qg.QGEMM_EUNSUPPORTED
+    assert L.qgemm_q6k(FAKE, 128, 384, FAKE, FAKE, FAKE, 4, FAKE, 128, ws, 1 << 20, None) == qg.QGEMM_EINVAL
+    assert L.qgemm_q6k_prepack(FAKE, 0, 256, 210, FAKE, None) == qg.QGEMM_EINVAL
+    assert L.qgemm_q6k_prepack(FAKE, 4, 256, 200, FAKE, None) == qg.QGEMM_EINVAL
+    assert L.qgemm_q6k_prepack(FAKE, 4, 256, 210, MISALIGNED, None) == qg.QGEMM_EALIGN
+
+
+def test_size_queries(L):
+    assert L.qgemm_workspace_bytes(0, 8, 256) == 0
+    assert L.qgemm_workspace_bytes(4, 8, 300) == 0
+    M, K = 5, 512
+    # xh fp16 5*512*2 = 5120; bsums fp16 5*32*2 = 320 -> 512; d^T fp32 2*8*4 = 64 -> 256
+    expect = 5120 + 512 + 256
+    assert L.qgemm_workspace_bytes(M, 8, K) == expect
+    assert L.qgemm_q6k_packed_bytes(3, 512) == 3 * 2 * 224
+    assert L.qgemm_q6k_packed_bytes(3, 100) == 0
+
+
+def test_options_and_counters(L):
+    assert L.qgemm_set_option(1, 48) == qg.QGEMM_EINVAL
+    assert L.qgemm_set_option(7, 0) == qg.QGEMM_EINVAL
+    assert L.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 64) == qg.QGEMM_OK
+    assert L.qgemm_get_option(qg.QGEMM_OPT_FORCE_BM) == 64
+    assert L.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0) == qg.QGEMM_OK
+    assert L.qgemm_get_option(99) == -1
+    L.qgemm_reset_counters()
+    c = qg._Counters()
+    assert L.qgemm_get_counters(ctypes.byref(c)) == 0
+    assert c.q4k_tc == 0 and c.quantize == 0
+    assert L.qgemm_get_counters(None) == qg.QGEMM_EINVAL

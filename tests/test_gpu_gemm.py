@@ -1,0 +1,202 @@
+"""Q4_K / Q6_K x Q8_K GEMM on the GPU vs the CPU oracle.
+
+Tolerance (per element): |Y_gpu - Y_oracle| <= 2e-5 * sum_b |c_b| + 1e-6, with
+c_b the oracle's fp64 per-superblock contribution.  The Q8_K operand the GEMM
+consumes is the GPU quantizer's, first checked bit-exact against the oracle's.
+
+Coverage: the benchmark workloads (full output where the oracle finishes in
+seconds, seeded row samples plus every tail row at the large sizes), ragged
+M / N edges around every tile size, every tile width and split-K factor,
+degenerate blocks (d = 0, dmin = 0, all-zero quants, extreme sub-scales),
+guard canaries around Y, the launch counters and the device status word.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import block_quantized_matmul_quantize_gb300 as qg
+from gpu_common import (assert_q8k_equal, device_status_clean, ensure_built, gpu_gemm, gpu_quantize,
+                        q8k_numpy, to_dev)
+from parity_util import assert_gemm_close, oracle_gemm, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_SPLITS, 0)
+    yield
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_SPLITS, 0)
+
+
+def weights(wtype, N, K, seed):
+    return (synth.gen_q4k if wtype == 4 else synth.gen_q6k)(N, K, seed)
+
+
+def check(wtype, w, K, x, rows=None, what=""):
+    q = gpu_quantize(x)
+    q8 = q8k_numpy(q)
+    assert_q8k_equal(q8, oracle.get().quantize_q8k(x), what)
+    y = gpu_gemm(wtype, w, K, q)
+    yr, absc = oracle_gemm(wtype, w, K, *q8, rows=rows)
+    ysel = y if rows is None else y[rows]
+    return assert_gemm_close(ysel, yr, absc, what)
+
+
+RAGGED = [(1, 128, 256), (2, 136, 512), (3, 1, 256), (5, 200, 768), (7, 128, 1024), (8, 256, 512),
+          (9, 130, 512), (15, 128, 256), (16, 128, 512), (17, 300, 512), (31, 129, 256), (33, 128, 768),
+          (63, 256, 512), (64, 128, 512), (65, 136, 512), (80, 128, 1024), (127, 128, 256),
+          (128, 256, 512), (129, 130, 768), (200, 384, 512), (257, 256, 1024)]
+
+
+@pytest.mark.parametrize("wtype", [4, 6])
+@pytest.mark.parametrize("M,N,K", RAGGED)
+def test_ragged_shapes(wtype, M, N, K):
+    w = weights(wtype, N, K, 31 + M * 7 + N)
+    x = synth.gen_x(M, K, 17 + M, outlier_frac=0.01)
+    check(wtype, w, K, x, what=f"Q{wtype}_K M{M} N{N} K{K}")
+
+
+@pytest.mark.parametrize("wtype", [4, 6])
+@pytest.mark.parametrize("bm", [16, 32, 64, 128])
+@pytest.mark.parametrize("splits", [1, 2, 3, 8])
+def test_every_tile_and_split(wtype, bm, splits):
+    M, N, K = 100, 300, 2048
+    w = weights(wtype, N, K, 5)
+    x = synth.gen_x(M, K, 6)
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, bm)
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_SPLITS, splits)
+    try:
+        qg.qgemm_reset_counters()
+        check(wtype, w, K, x, what=f"bm{bm} splits{splits}")
+        c = qg.qgemm_get_counters()
+        assert c["q4k_tc" if wtype == 4 else "q6k_tc"] == 1
+        assert c["split_k"] == (1 if splits > 1 else 0)
+    finally:
+        qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
+        qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_SPLITS, 0)
+
+
+@pytest.mark.parametrize("wl", [synth.C0, synth.C1, synth.C2], ids=lambda w: w.name)
+def test_workload_full(wl):
+    check(wl.wtype, wl.weights(), wl.K, wl.x(), what=wl.name)
+
+
+@pytest.mark.parametrize("wl", [synth.C3] + [synth.sweep(m) for m in synth.SWEEP_M],
+                         ids=lambda w: w.name)
+def test_workload_sampled(wl):
+    rows = None if wl.M <= 64 else sample_rows(wl.M, 48, seed=wl.M)
+    check(wl.wtype, wl.weights(), wl.K, wl.x(), rows=rows, what=wl.name)
+
+
+def _q4k_blocks(orc, N, nb, rng, d_bits=None, dmin_bits=None, q_zero=False):
+    rows = []
+    for n in range(N):
+        blks = []
+        for b in range(nb):
+            db = int(rng.integers(0x0C00, 0x1400)) if d_bits is None else d_bits
+            mb = int(rng.integers(0x0C00, 0x1400)) if dmin_bits is None else dmin_bits
+            q = np.zeros(256, int) if q_zero else rng.integers(0, 16, 256)
+            blks.append(orc.q4k_pack(db, mb, rng.integers(0, 64, 8), rng.integers(0, 64, 8), q))
+        rows.append(np.concatenate(blks))
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("case", ["d_zero", "dmin_zero", "both_zero", "q_zero", "max_fields"])
+def test_q4k_degenerate_blocks(case):
+    orc = oracle.get()
+    rng = np.random.default_rng(3)
+    N, K, M = 130, 512, 20
+    if case == "d_zero":
+        w = _q4k_blocks(orc, N, 2, rng, d_bits=0)
+    elif case == "dmin_zero":
+        w = _q4k_blocks(orc, N, 2, rng, dmin_bits=0)
+    elif case == "both_zero":
+        w = _q4k_blocks(orc, N, 2, rng, d_bits=0, dmin_bits=0)
+    elif case == "q_zero":
+        w = _q4k_blocks(orc, N, 2, rng, q_zero=True)
+    else:
+        blk = orc.q4k_pack(0x3C00, 0x3C00, np.full(8, 63), np.full(8, 63), np.full(256, 15))
+        w = np.tile(blk, (N, 2))
+    x = synth.gen_x(M, K, 8)
+    x[3] = 0.0                                        # an all-zero token row
+    x[4, :256] = 127.0                                # saturated superblock
+    check(4, w, K, x, what=case)
+    device_status_clean()
+
+
+def test_q6k_scale_edges():
+    orc = oracle.get()
+    rng = np.random.default_rng(4)
+    N, K, M = 136, 512, 33
+    rows = []
+    for n in range(N):
+        sc = rng.choice([-64, -63, 64, 63, 0, 1, -1, 32, -32], 16)
+        blks = [orc.q6k_pack(0x3C00 if n % 3 else 0, sc, rng.integers(0, 64, 256)) for _ in range(2)]
+        rows.append(np.concatenate(blks))
+    w = np.stack(rows)
+    check(6, w, K, synth.gen_x(M, K, 9), what="q6k sc=+-64")
+    device_status_clean()
+
+
+def test_out_of_range_blocks_are_flagged():
+    orc = oracle.get()
+    rng = np.random.default_rng(5)
+    # Q4_K: d tiny, dmin large -> |dmin/d| > 1000
+    blk = orc.q4k_pack(0x0001, 0x3C00, rng.integers(0, 64, 8), rng.integers(1, 64, 8), rng.integers(0, 16, 256))
+    w = np.tile(blk, (128, 1))
+    q = gpu_quantize(synth.gen_x(16, 256, 1))
+    gpu_gemm(4, w, 256, q)
+    bits, _ = qg.qgemm_get_device_status()
+    assert bits & qg.QGEMM_DEV_Q4K_RANGE
+    # Q6_K: sub-scale -100
+    blk6 = orc.q6k_pack(0x3C00, np.full(16, -100), rng.integers(0, 64, 256))
+    gpu_gemm(6, np.tile(blk6, (128, 1)), 256, q)
+    bits, _ = qg.qgemm_get_device_status()
+    assert bits & qg.QGEMM_DEV_Q6K_SCALE
+    device_status_clean()
+
+
+@pytest.mark.parametrize("wtype", [4, 6])
+def test_output_canaries_and_row_stride(wtype):
+    M, N, K = 70, 200, 768
+    w = weights(wtype, N, K, 12)
+    x = synth.gen_x(M, K, 13)
+    q = gpu_quantize(x)
+    ldy = N + 24
+    sentinel = -1234.5
+    big = torch.full((M + 2, ldy), sentinel, dtype=torch.float32, device="cuda")
+    y = big[1:M + 1, :N]
+    gpu_gemm(wtype, w, K, q, y=y)
+    b = big.cpu().numpy()
+    assert np.all(b[0] == sentinel) and np.all(b[M + 1] == sentinel), "rows outside Y touched"
+    assert np.all(b[1:M + 1, N:] == sentinel), "padding columns touched"
+    yr, absc = oracle_gemm(wtype, w, K, *q8k_numpy(q))
+    assert_gemm_close(b[1:M + 1, :N], yr, absc, "strided Y")
+
+
+def test_empty_m_is_a_noop():
+    w = to_dev(weights(4, 128, 256, 1))
+    q = qg.Q8K.empty(0, 256)
+    y = torch.empty((0, 128), dtype=torch.float32, device="cuda")
+    qg.qgemm_reset_counters()
+    qg.qgemm_q4k(w, 128, 256, q, y=y)
+    assert qg.qgemm_get_counters()["q4k_tc"] == 0
+
+
+def test_bad_workspace_is_rejected():
+    w = to_dev(weights(4, 128, 512, 1))
+    q = gpu_quantize(synth.gen_x(8, 512, 2))
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(qg.QgemmError) as ei:
+        qg.qgemm_q4k(w, 128, 512, q, workspace=small)
+    assert ei.value.code == qg.QGEMM_EINVAL
+
+
+def test_device_status_clean_at_end():
+    device_status_clean()
