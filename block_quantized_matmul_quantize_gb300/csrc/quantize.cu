@@ -4,9 +4,10 @@
 // Q8_K, as the library defines it (the block the pages call "BlockQ8_K,
 // 292 B / 256 elements", vllm.cpp PR #3036, commit 4): per 256-element chunk
 // of a row, d = amax/127 (fp32), q = round-half-away-from-zero(x/d) clamped to
-// +-127, and 16 int16 sums of each 16 consecutive q.  amax = 0 gives d = 0 and
-// all-zero q and sums.  Stored as three planes (qs [M][K] int8, d [M][K/256]
-// fp32, bsums [M][K/16] int16) so that every plane row is 16-byte aligned.
+// +-127, and 16 int16 sums of each 16 consecutive q.  d = 0 (amax = 0, or
+// amax/127 underflowing to zero) gives all-zero q and sums.  Stored as three
+// planes (qs [M][K] int8, d [M][K/256] fp32, bsums [M][K/16] int16) so that
+// every plane row is 16-byte aligned.
 //
 // Numerics: x/d and amax/127 are IEEE fp32 divisions, correctly rounded (the
 // library is built without fast-math; -prec-div=true), and roundf rounds
@@ -47,12 +48,12 @@ __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* 
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
 
     int q[8];
-    float d = 0.0f;
-    if (amax == 0.0f) {
+    const float d = amax / 127.0f;
+    if (d == 0.0f) {
+        // amax == 0, or amax/127 underflows to zero: the chunk quantizes to zero
 #pragma unroll
         for (int i = 0; i < 8; ++i) q[i] = 0;
     } else {
-        d = amax / 127.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             float r = roundf(v[i] / d);

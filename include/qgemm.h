@@ -83,7 +83,8 @@ QGEMM_API const char *qgemm_last_error(void);
  *   d      device, fp32 [M][K/256], 16-B aligned.
  *   bsums  device, int16 [M][K/16], 16-B aligned.
  * Bit-exact with the IEEE definition: d = amax/127 (fp32), q = roundf(x/d)
- * clamped to +-127, amax == 0 -> d = 0, q = 0, bsums = 0.
+ * clamped to +-127; d == 0 (amax == 0, or amax/127 underflowing to zero)
+ * -> q = 0, bsums = 0.
  * Errors: EINVAL (sizes, null), EALIGN, ECUDA (launch). */
 QGEMM_API int qgemm_quantize_q8k(const float *x, int64_t M, int64_t K, int64_t ldx, int8_t *qs, float *d,
                        int16_t *bsums, qgemm_stream_t stream);

@@ -165,9 +165,11 @@ void oracle_dequant_q6k(const uint8_t *blk, double w[256])
 /* ---------------------------------------------------------------- Q8_K --
  * Per 256-element chunk of a row:
  *   amax = max |x_i| (fp32, exact);
- *   amax == 0  ->  d = 0, every q = 0, every bsum = 0;
- *   otherwise  d = amax / 127 (fp32, correctly rounded division) and
- *              q_i = clamp(roundf(x_i / d), -127, 127), x_i / d again a
+ *   d = amax / 127 (fp32, correctly rounded division);
+ *   d == 0 (amax == 0, or amax/127 underflowing to zero) -> every q = 0,
+ *              every bsum = 0 (the pages leave this case open; x/0 has no
+ *              value, so the chunk is taken as all zeros);
+ *   otherwise  q_i = clamp(roundf(x_i / d), -127, 127), x_i / d again a
  *              correctly rounded fp32 division and roundf rounding halves
  *              away from zero;
  *   bsums[g] = sum of q_{16g .. 16g+15}.
@@ -187,13 +189,15 @@ void oracle_quantize_q8k(const float *x, int64_t M, int64_t K, int64_t ldx,
                 if (a > amax)
                     amax = a;
             }
-            if (amax == 0.0f) {
+            float db = amax / 127.0f;
+            if (db == 0.0f) {
+                /* amax == 0, or amax so small that amax/127 underflows to
+                 * zero: x/d is undefined, the chunk quantizes to zero. */
                 d[m * nb + b] = 0.0f;
                 memset(qb, 0, 256);
                 memset(sb, 0, 16 * sizeof(int16_t));
                 continue;
             }
-            float db = amax / 127.0f;
             d[m * nb + b] = db;
             for (int i = 0; i < 256; ++i) {
                 float r = roundf(xb[i] / db);
