@@ -191,6 +191,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=256, help="token rows in the CPU-baseline sample")
     ap.add_argument("--ref-rows", type=int, default=2, help="token rows per reference-arm step")
+    ap.add_argument("--settle", type=float, default=0.5,
+                    help="seconds of extra untimed steps after warm-up (clock settling); 0 = none")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -243,7 +245,7 @@ def main():
         flush.zero_()
         step()
     torch.cuda.synchronize()
-    t_end = time.time() + 0.5
+    t_end = time.time() + args.settle
     while time.time() < t_end:
         for _ in range(20):
             flush.zero_()
