@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
             "qgemm_quantize_q8k": ([vp, i64, i64, i64, vp, vp, vp, vp], i32),
             "qgemm_workspace_bytes": ([i64, i64, i64], sz),
             "qgemm_q4k": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
+            "qgemm_q4k_noalloc": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp], i32),
             "qgemm_q6k_packed_bytes": ([i64, i64], sz),
             "qgemm_q6k_prepack": ([vp, i64, i64, i64, vp, vp], i32),
             "qgemm_q6k": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
@@ -145,6 +146,19 @@ def qgemm_q4k(w: torch.Tensor, N: int, K: int, x: Q8K, y: torch.Tensor | None = 
     workspace = _workspace(M, N, K, workspace, x.qs.device)
     _check(lib().qgemm_q4k(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
                            y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return y
+
+
+def qgemm_q4k_noalloc(w: torch.Tensor, N: int, K: int, x: Q8K, y: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """qgemm_q4k without a workspace: the library's built-in device scratch is
+    used (for callers that cannot allocate; see include/qgemm.h)."""
+    assert w.dtype == torch.uint8 and w.dim() == 2 and w.stride(1) == 1
+    M = x.M
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
+    _check(lib().qgemm_q4k_noalloc(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
+                                   y.stride(0), _stream(stream)))
     return y
 
 

@@ -52,6 +52,9 @@ size_t tc_smem_bytes(int wtype, int bm);
 cudaError_t tc_prepare(int wtype, int bm);   // sets the dynamic smem attribute (per device)
 cudaError_t launch_gemm_tc(const TcLaunch& a, cudaStream_t s);
 
+// Record a one-line message for qgemm_last_error() and return `code`.
+int set_last_error(int code, const char* msg);
+
 cudaError_t launch_q6k_prepack(const uint8_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* out,
                                cudaStream_t s);
 

@@ -219,6 +219,10 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
 
 }  // namespace
 
+namespace qg {
+int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace qg
+
 extern "C" {
 
 int qgemm_version(void) { return 100; }

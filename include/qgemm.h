@@ -128,6 +128,34 @@ QGEMM_API int qgemm_q6k(const void *w_packed, int64_t N, int64_t K, const int8_t
               const int16_t *xbsums, int64_t M, float *y, int64_t ldy, void *workspace,
               size_t workspace_bytes, qgemm_stream_t stream);
 
+/* -------------------------------------------- allocation-free Q4_K GEMM ----
+ * The pages have no counterpart to this call; it serves callers that cannot
+ * allocate device memory where they call the GEMM (for example a plugin
+ * inside a host framework that owns all device memory and gives the plugin
+ * no allocator, or code where cudaMalloc is not allowed, such as a host
+ * callback, or not acceptable on a latency-critical path).
+ *
+ * qgemm_q4k_noalloc computes exactly what qgemm_q4k computes (same
+ * arguments minus the workspace) but takes its scratch from a fixed array of
+ * QGEMM_NOALLOC_SCRATCH_BYTES bytes that the library keeps in device memory
+ * (one per GPU that loads the library, held until the process exits).  It
+ * allocates nothing.
+ *   - Size limit: qgemm_workspace_bytes(M, N, K) must not exceed
+ *     QGEMM_NOALLOC_SCRATCH_BYTES (16 MiB: M*K up to about 7.8 million, e.g.
+ *     M = 512 at K = 11008 or M = 2048 at K = 3584); larger calls return
+ *     QGEMM_EUNSUPPORTED with a message and launch nothing.
+ *   - The first call on each device looks up the scratch array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that
+ *     first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents; every byte the GEMM reads is rewritten by the same call, so
+ *     nothing needs clearing.  Calls that overlap on the GPU (e.g. on two
+ *     streams at once) race on the array: serialize them. */
+#define QGEMM_NOALLOC_SCRATCH_BYTES (16u << 20)
+QGEMM_API int qgemm_q4k_noalloc(const void *w, int64_t N, int64_t K, int64_t ldw, const int8_t *xqs,
+                                const float *xd, const int16_t *xbsums, int64_t M, float *y, int64_t ldy,
+                                qgemm_stream_t stream);
+
 /* ------------------------------------------------------ diagnostics ----
  * Launch counters per path (proof of which kernel ran: the per-variant
  * dispatch counters of PR #3036, commit 4). */
