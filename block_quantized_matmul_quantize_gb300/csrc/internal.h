@@ -40,6 +40,7 @@ struct TcLaunch {
     int bm;               // tokens per CTA: 16, 32, 64, 128
     int64_t M, N, K;
     int splits;           // K splits (>1 -> Y accumulated with atomics, pre-zeroed)
+    int sm_count;         // persistent grid: min(work items, SMs)
     float* y;
     int64_t ldy;
     uint32_t* status;

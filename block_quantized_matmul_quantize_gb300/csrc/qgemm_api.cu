@@ -200,6 +200,7 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
     a.N = N;
     a.K = K;
     a.splits = pl.splits;
+    a.sm_count = ds->sm_count;
     a.y = y;
     a.ldy = ldy;
     a.status = ds->status;
