@@ -41,16 +41,22 @@
 //     the activation stream fed.
 //
 // TMEM columns: [0, 2*BM) two fp32 accumulators (superblock t uses t & 1);
-// [256, 512) eight 32-column K64 stages of the weight operand.
+// [256, 512) four 64-column K128 stages of the weight operand.
+//
+// The MMA-issuing thread is the critical path: the tensor pipe queues only a
+// couple of MMAs, so every barrier wait, commit and bit of loop bookkeeping
+// between MMAs idles it (measured on GB300: 4 MMAs per K64 handshake kept it
+// ~35% busy; doubling the MMAs per handshake added the work at full rate).
+// Hence K128 handshakes (8 MMAs each) and a non-blocking look-ahead probe of
+// the next step's barriers issued between the MMAs of the current one.
 //
 // Warp roles (16 warps, persistent CTAs looping over (n-tile, m-tile, split)
 // work items with token tiles varying fastest):
-//   warp 0      TMA producers: lane c (0..3) loads activation K64 chunk c of
-//               every superblock (one issuing thread alone cannot keep the
-//               activation stream fed; four can)
+//   warps 0, 3  TMA producers of the activation stages (K128 or K256 per
+//               stage, one barrier each), alternating stage by stage
 //   warp 1      TMEM owner + MMA issuer (one thread)
-//   warp 2      TMA producer: raw weight blocks (+ L2 prefetch ahead)
-//   warp 3      TMA producer: per-superblock side data (bsums, dx)
+//   warp 2      TMA producer: raw weight blocks (+ L2 prefetch ahead) and the
+//               per-superblock side data (bsums, dx)
 //   warps 4-7   unpack: thread = weight row; branch-free expand of each K64
 //               chunk into registers, tcgen05.st into TMEM
 //   warps 8-15  epilogue: warp w reads TMEM lanes 32*(w%4).. and half of the
@@ -68,7 +74,7 @@ namespace {
 constexpr int BN = 128;        // weight rows per CTA = MMA M
 constexpr int NWARPS = 16;
 constexpr int NTHREADS = NWARPS * 32;
-constexpr int A_STAGES = 8;    // weight-operand K64 stages in TMEM (32 columns each)
+constexpr int A_STAGES = 4;    // weight-operand K128 stages in TMEM (64 columns each)
 constexpr int A_TMEM_COL = 256;
 constexpr int KCH = 64;        // K elements per stage
 constexpr int SB_SLOTS = 3;    // per-superblock side-data slots
@@ -103,7 +109,14 @@ template <int WT, int BM>
 struct Layout {
     static constexpr int RAW_SLOTS = 3;
     static constexpr bool CORR = WTraits<WT>::CORR;
-    static constexpr int B_STAGE = BM * 128;
+    // An activation stage carries SCH K64 boxes that complete on one barrier:
+    // a whole superblock for BM <= 64, half of one for BM = 128.  (Measured on
+    // GB300: a TMA ring handing over 16 KB per barrier phase delivers about a
+    // third of what the same ring moves in 32 KB or 64 KB phases.)
+    static constexpr int SCH = BM >= 128 ? 2 : 4;
+    static constexpr int SPS = 4 / SCH;                  // stages per superblock
+    static constexpr int BOX = BM * 128;                 // one K64 box: BM rows x 128 B
+    static constexpr int B_STAGE = SCH * BOX;
     static constexpr int RAW = BN * WTraits<WT>::RAW_BLOCK;
     // per-superblock side slot
     static constexpr int SB_ACORR = 0;                                       // 2 slabs x 128 rows x 32 B
@@ -116,7 +129,7 @@ struct Layout {
     static constexpr int OFF_SB = OFF_RAW + align_up(RAW_SLOTS * RAW, 1024);
     static constexpr int OFF_B = OFF_SB + SB_SLOTS * SB;
     static constexpr int RESERVE = 1024 /* base alignment */ + 512 /* barriers, misc */;
-    static constexpr int B_STAGES = cmin(12, (SMEM_LIMIT - RESERVE - OFF_B) / B_STAGE) & ~3;
+    static constexpr int B_STAGES = cmin(12, (SMEM_LIMIT - RESERVE - OFF_B) / B_STAGE) & ~1;
     static constexpr int OFF_BAR = OFF_B + B_STAGES * B_STAGE;
     static constexpr int NBAR = 2 * RAW_SLOTS + 2 * A_STAGES + 2 * B_STAGES + 2 * SB_SLOTS + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -280,61 +293,47 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         fence_mbar_init();
     }
     if (warp == W_PROD_X && lane == 0) tma_prefetch_desc(&tm_xh);
-    if (warp == W_PROD_X2 && lane == 0) {
+    if (warp == W_PROD_W && lane == 0) {
+        tma_prefetch_desc(&tm_w);
         tma_prefetch_desc(&tm_dx);
         if (L::CORR) tma_prefetch_desc(&tm_xbs);
     }
-    if (warp == W_PROD_W && lane == 0) tma_prefetch_desc(&tm_w);
     if (warp == W_MMA) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == W_PROD_X) {
+    if (warp == W_PROD_X || warp == W_PROD_X2) {
         // ------------------------------------------------ activation producers
-        // lane c loads K64 chunk c of every superblock; B_STAGES is a multiple
-        // of 4, so every stage is always filled by the same lane.
-        if (lane < 4) {
-            const int c = lane;
-            int t = 0;
-            bool ok = true;
-            for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
-                int n0, m0, kb0, kb1;
-                work_of(wi, n0, m0, kb0, kb1);
-                for (int i = kb0; i < kb1; ++i, ++t) {
-                    const int b = sb_at(i, kb0, kb1, n0);
-                    const int g = 4 * t + c;
-                    const int s = g % BS;
-                    ok = mbar_wait(&b_empty[s], ((g / BS) & 1) ^ 1, abort_flag, status, 2);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(&b_full[s], BM * 128);
-                    tma_load_2d(&tm_xh, &b_full[s], b_stage(s), b * 256 + KCH * c, m0);
-                }
-            }
-        }
-    } else if (warp == W_PROD_X2) {
-        // ------------------------------------------------ side-data producer
+        // Stage g (running over all stages of this CTA) is filled by warp 0 for
+        // even g and warp 3 for odd g; B_STAGES is even, so every stage always
+        // has the same producer.
         if (lane == 0) {
-            int t = 0;
+            const int par = (warp == W_PROD_X) ? 0 : 1;
+            int g = 0;
             bool ok = true;
             for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
                 int n0, m0, kb0, kb1;
                 work_of(wi, n0, m0, kb0, kb1);
-                for (int i = kb0; i < kb1; ++i, ++t) {
+                for (int i = kb0; i < kb1 && ok; ++i) {
                     const int b = sb_at(i, kb0, kb1, n0);
-                    const int p = t % SBN;
-                    ok = mbar_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1, abort_flag, status, 1);
-                    if (!ok) break;
-                    uint8_t* sb = sb_slot(p);
-                    mbar_arrive_expect_tx(&sb_full[p], (L::CORR ? BM * 32 : 0) + BM * 4);
-                    if (L::CORR) tma_load_2d(&tm_xbs, &sb_full[p], sb + L::SB_BCORR, b * 16, m0);
-                    tma_load_2d(&tm_dx, &sb_full[p], sb + L::SB_DX, m0, b);
+                    for (int h = 0; h < L::SPS; ++h, ++g) {
+                        if ((g & 1) != par) continue;
+                        const int s = g % BS;
+                        ok = mbar_wait(&b_empty[s], ((g / BS) & 1) ^ 1, abort_flag, status, 2);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(&b_full[s], L::B_STAGE);
+#pragma unroll
+                        for (int q = 0; q < L::SCH; ++q)
+                            tma_load_2d(&tm_xh, &b_full[s], b_stage(s) + q * L::BOX, b * 256 + KCH * (h * L::SCH + q),
+                                        m0);
+                    }
                 }
             }
         }
     } else if (warp == W_PROD_W) {
-        // ------------------------------------------------ weight producer
+        // ------------------------------------------------ weight + side-data producer
         if (lane == 0) {
             int t = 0;
             bool ok = true;
@@ -361,6 +360,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (!ok) break;
                     mbar_arrive_expect_tx(&raw_full[r], L::RAW);
                     tma_load_2d(&tm_w, &raw_full[r], raw_slot(r), b * WTraits<WT>::RAW_BLOCK, n0);
+                    const int p = t % SBN;
+                    ok = mbar_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1, abort_flag, status, 1);
+                    if (!ok) break;
+                    uint8_t* sb = sb_slot(p);
+                    mbar_arrive_expect_tx(&sb_full[p], (L::CORR ? BM * 32 : 0) + BM * 4);
+                    if (L::CORR) tma_load_2d(&tm_xbs, &sb_full[p], sb + L::SB_BCORR, b * 16, m0);
+                    tma_load_2d(&tm_dx, &sb_full[p], sb + L::SB_DX, m0, b);
                 }
             }
         }
@@ -372,6 +378,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint64_t bdesc0 = smem_desc(smem_u32(b_stage(0)), 16, 1024, SWZ_128B);
             int t = 0;
             int sa = 0, pa = 0, sx = 0, px = 0;   // running stage index and phase of the A and B rings
+            bool ahead = false;                   // next step's barriers already seen complete
             bool ok = true;
             for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
                 int n0, m0, kb0, kb1;
@@ -380,24 +387,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int buf = t & 1;
                     ok = mbar_wait(&acc_empty[buf], ((t >> 1) & 1) ^ 1, abort_flag, status, 4);
                     if (!ok) break;
-                    tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BM;
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        ok = mbar_wait(&b_full[sx], px, abort_flag, status, 5) &&
-                             mbar_wait(&a_full[sa], pa, abort_flag, status, 12);
-                        if (!ok) break;
+                    for (int h = 0; h < 2; ++h) {   // K128 steps: chunks 2h, 2h+1
+                        const bool new_b = ((2 * h) % L::SCH) == 0;
+                        if (!ahead) {
+                            ok = (!new_b || mbar_wait(&b_full[sx], px, abort_flag, status, 5)) &&
+                                 mbar_wait(&a_full[sa], pa, abort_flag, status, 12);
+                            if (!ok) break;
+                        }
                         tc_fence_after();
-                        const uint32_t a0 = tmem_base + A_TMEM_COL + 32 * sa;
-                        const uint64_t bd = bdesc0 + static_cast<uint64_t>((sx * L::B_STAGE) >> 4);
-                        mma_f16_ta(d_tmem, a0, bd, IDESC, c != 0);
+                        const uint32_t a0 = tmem_base + A_TMEM_COL + 64 * sa;
+                        const int q0 = (2 * h) % L::SCH;
+                        const uint64_t bd = bdesc0 + static_cast<uint64_t>((sx * L::B_STAGE + q0 * L::BOX) >> 4);
+                        mma_f16_ta(d_tmem, a0, bd, IDESC, h != 0);
                         mma_f16_ta(d_tmem, a0 + 8, bd + 2, IDESC, 1u);
                         mma_f16_ta(d_tmem, a0 + 16, bd + 4, IDESC, 1u);
                         mma_f16_ta(d_tmem, a0 + 24, bd + 6, IDESC, 1u);
+                        // look ahead while these run: are the next step's stages in?
+                        {
+                            const int na = (sa + 1 == A_STAGES) ? 0 : sa + 1;
+                            const uint32_t npa = (sa + 1 == A_STAGES) ? pa ^ 1 : pa;
+                            const bool last_b = (q0 + 2 == L::SCH);       // this step ends the B stage
+                            const int nx = last_b ? ((sx + 1 == BS) ? 0 : sx + 1) : sx;
+                            const uint32_t npx = (last_b && sx + 1 == BS) ? px ^ 1 : px;
+                            const bool next_new_b = ((2 * (h ^ 1)) % L::SCH) == 0;
+                            ahead = mbar_test_wait(&a_full[na], npa) &&
+                                    (!next_new_b || mbar_test_wait(&b_full[nx], npx));
+                        }
+                        const uint64_t bd1 = bd + (L::BOX >> 4);
+                        mma_f16_ta(d_tmem, a0 + 32, bd1, IDESC, 1u);
+                        mma_f16_ta(d_tmem, a0 + 40, bd1 + 2, IDESC, 1u);
+                        mma_f16_ta(d_tmem, a0 + 48, bd1 + 4, IDESC, 1u);
+                        mma_f16_ta(d_tmem, a0 + 56, bd1 + 6, IDESC, 1u);
                         mma_commit(&a_empty[sa]);
-                        mma_commit(&b_empty[sx]);
                         if (++sa == A_STAGES) sa = 0, pa ^= 1;
-                        if (++sx == BS) sx = 0, px ^= 1;
+                        if (q0 + 2 == L::SCH) {
+                            mma_commit(&b_empty[sx]);
+                            if (++sx == BS) sx = 0, px ^= 1;
+                        }
                     }
                     if (!ok) break;
                     if (L::CORR) {
@@ -475,7 +503,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
-                        const int g = 4 * t + c;
+                        const int g = 2 * t + (c >> 1);   // K128 step
                         const int s = g % A_STAGES;
                         const int sl = main_on ? static_cast<int>((((c < 2) ? sc03 : sc47) >> (16 * (c & 1))) & 0xff) : 0;
                         const int sh = main_on ? static_cast<int>((((c < 2) ? sc03 : sc47) >> (16 * (c & 1) + 8)) & 0xff) : 0;
@@ -485,14 +513,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const uint32_t cH = h2dup(__int2half_rn(-64 * sh));
                         uint32_t v[32];
                         unpack_q4k_chunk(blk, c, scL, cL, scH, cH, v);
-                        ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
-                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                        tc_fence_after();
-                        tmem_st_32x32b_x32(lane_base + 32 * s, v);
+                        if ((c & 1) == 0) {
+                            ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
+                            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                            tc_fence_after();
+                        }
+                        tmem_st_32x32b_x32(lane_base + 64 * s + 32 * (c & 1), v);
                         tmem_st_wait();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&a_full[s]);
+                        if (c & 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&a_full[s]);
+                        }
                     }
                     if (!ok) break;
                 } else {
@@ -515,7 +547,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
-                        const int g = 4 * t + c;
+                        const int g = 2 * t + (c >> 1);   // K128 step
                         const int s = g % A_STAGES;
                         // the chunk's four sub-block scales: bytes 4c..4c+3 of the scale array
                         const uint32_t scw = c == 0 ? sw[0] : c == 1 ? sw[1] : c == 2 ? sw[2] : sw[3];
@@ -525,14 +557,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             s4[q] = h2dup(__int2half_rn(static_cast<int8_t>((scw >> (8 * q)) & 0xff)));
                         uint32_t v[32];
                         unpack_q6k_chunk(blk, c, s4, v);
-                        ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
-                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                        tc_fence_after();
-                        tmem_st_32x32b_x32(lane_base + 32 * s, v);
+                        if ((c & 1) == 0) {
+                            ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
+                            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                            tc_fence_after();
+                        }
+                        tmem_st_32x32b_x32(lane_base + 64 * s + 32 * (c & 1), v);
                         tmem_st_wait();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&a_full[s]);
+                        if (c & 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&a_full[s]);
+                        }
                     }
                     if (!ok) break;
                 }
