@@ -43,18 +43,22 @@
 // TMEM columns: [0, 2*BM) two fp32 accumulators (superblock t uses t & 1);
 // [256, 512) four 64-column K128 stages of the weight operand.
 //
-// The MMA-issuing thread is the critical path: the tensor pipe queues only a
-// couple of MMAs, so every barrier wait, commit and bit of loop bookkeeping
-// between MMAs idles it (measured on GB300: 4 MMAs per K64 handshake kept it
-// ~35% busy; doubling the MMAs per handshake added the work at full rate).
-// Hence K128 handshakes (8 MMAs each) and a non-blocking look-ahead probe of
-// the next step's barriers issued between the MMAs of the current one.
+// MMA issue is the critical path.  On GB300 a tcgen05.mma (M128 N128 K16)
+// holds its issuing thread for ~55 of the ~64 cycles it runs, and the pipe
+// keeps only about one more queued, so the barrier waits, commits and loop
+// bookkeeping of a single issuing thread leave the tensor pipe idle between
+// MMAs (measured: ~35% busy with 4 MMAs per handshake).  Two issuing threads
+// in different warps, each owning one of the two accumulators (even / odd
+// superblocks), hide each other's bookkeeping; per thread the handshakes are
+// K128 (8 MMAs) with a non-blocking look-ahead probe of the next step's
+// barriers between the MMAs of the current one.
 //
 // Warp roles (16 warps, persistent CTAs looping over (n-tile, m-tile, split)
 // work items with token tiles varying fastest):
-//   warps 0, 3  TMA producers of the activation stages (K128 or K256 per
-//               stage, one barrier each), alternating stage by stage
-//   warp 1      TMEM owner + MMA issuer (one thread)
+//   warp 0      TMA producer of the activation stages (K128 or K256 per stage,
+//               one barrier each)
+//   warps 1, 3  MMA issuers (one thread each): even / odd superblocks; warp 1
+//               also owns the TMEM allocation
 //   warp 2      TMA producer: raw weight blocks (+ L2 prefetch ahead) and the
 //               per-superblock side data (bsums, dx)
 //   warps 4-7   unpack: thread = weight row; branch-free expand of each K64
@@ -85,7 +89,7 @@ constexpr int SMEM_LIMIT = 232448;
 constexpr int W_PROD_X = 0;
 constexpr int W_MMA = 1;
 constexpr int W_PROD_W = 2;
-constexpr int W_PROD_X2 = 3;
+constexpr int W_MMA2 = 3;
 constexpr int W_UNPACK0 = 4;
 constexpr int W_EPI0 = 8;
 
@@ -223,6 +227,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr int R = L::RAW_SLOTS;
     constexpr int BS = L::B_STAGES;
     constexpr int SBN = SB_SLOTS;
+    // With two-box stages and as many activation stages as weight-operand
+    // stages, every K128 step consumes exactly one stage of each ring, so one
+    // commit (on a_empty) releases both and the activation producers wait on it.
+    constexpr bool MERGED_RELEASE = (L::SCH == 2) && (BS == A_STAGES);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -283,7 +291,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int p = 0; p < SBN; ++p) {
             mbar_init(&sb_full[p], 1 + 4);
-            mbar_init(&sb_empty[p], (L::CORR ? 1 : 0) + 8);
+            mbar_init(&sb_empty[p], 8);   // the epilogue warps, after acc_full covered the MMAs reading it
         }
         for (int p = 0; p < 2; ++p) {
             mbar_init(&acc_full[p], 1);
@@ -304,14 +312,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == W_PROD_X || warp == W_PROD_X2) {
-        // ------------------------------------------------ activation producers
-        // Stage g (running over all stages of this CTA) is filled by warp 0 for
-        // even g and warp 3 for odd g; B_STAGES is even, so every stage always
-        // has the same producer.
+    if (warp == W_PROD_X) {
+        // ------------------------------------------------ activation producer
         if (lane == 0) {
-            const int par = (warp == W_PROD_X) ? 0 : 1;
-            int g = 0;
+            int g = 0;   // running stage counter
             bool ok = true;
             for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
                 int n0, m0, kb0, kb1;
@@ -319,9 +323,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int i = kb0; i < kb1 && ok; ++i) {
                     const int b = sb_at(i, kb0, kb1, n0);
                     for (int h = 0; h < L::SPS; ++h, ++g) {
-                        if ((g & 1) != par) continue;
                         const int s = g % BS;
-                        ok = mbar_wait(&b_empty[s], ((g / BS) & 1) ^ 1, abort_flag, status, 2);
+                        ok = mbar_wait(MERGED_RELEASE ? &a_empty[s] : &b_empty[s], ((g / BS) & 1) ^ 1, abort_flag,
+                                       status, 2);
                         if (!ok) break;
                         mbar_arrive_expect_tx(&b_full[s], L::B_STAGE);
 #pragma unroll
@@ -370,77 +374,109 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-    } else if (warp == W_MMA) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp == W_MMA || warp == W_MMA2) {
+        // ------------------------------------------------ MMA issuers
+        // Thread `par` takes the superblocks t with t % 2 == par, i.e. always
+        // accumulator `par`, A stages 2*par and 2*par+1 and (two-box stages)
+        // the same two activation stages.  Per superblock: two K128 steps of 8
+        // MMAs (+2 correction MMAs for Q4_K) and up to four commits; readiness
+        // of the next step, the side slot and the next accumulator is probed
+        // without blocking between the MMAs of the current step.
         if (lane == 0) {
+            const int par = (warp == W_MMA) ? 0 : 1;
             constexpr uint32_t IDESC = idesc_f16_f32(BN, BM);
-            // descriptor of activation stage 0; stage s, K-step kk adds (s*B_STAGE + 32*kk) >> 4
+            // descriptor of activation stage 0; stage s, box q, K-step kk adds (s*B_STAGE + q*BOX + 32*kk) >> 4
             const uint64_t bdesc0 = smem_desc(smem_u32(b_stage(0)), 16, 1024, SWZ_128B);
+            // correction operands of side slot 0; slot p adds (p * SB) >> 4
+            const uint32_t sb0 = smem_u32(sb_slot(0));
+            const uint64_t acorr0 = smem_desc(sb0 + L::SB_ACORR, 16, 256, SWZ_32B);
+            const uint64_t bcorr0 = smem_desc(sb0 + L::SB_BCORR, 16, 256, SWZ_32B);
+            const uint32_t d_tmem = tmem_base + par * BM;
+            // stage index and phase parity of K128 step j of superblock t, in each ring
+            auto a_at = [&](int t, int j, int& s, uint32_t& ph) {
+                const int g = 2 * t + j;
+                s = g % A_STAGES;
+                ph = static_cast<uint32_t>(g / A_STAGES) & 1u;
+            };
+            auto b_at = [&](int t, int j, int& s, uint32_t& ph) {
+                const int g = t * L::SPS + (2 * j) / L::SCH;
+                s = g % BS;
+                ph = static_cast<uint32_t>(g / BS) & 1u;
+            };
             int t = 0;
-            int sa = 0, pa = 0, sx = 0, px = 0;   // running stage index and phase of the A and B rings
-            bool ahead = false;                   // next step's barriers already seen complete
+            bool step_ok = false;   // next step's A (and B) stage seen complete
+            bool acc_ok = false;    // next superblock's accumulator seen free
             bool ok = true;
             for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
                 int n0, m0, kb0, kb1;
                 work_of(wi, n0, m0, kb0, kb1);
                 for (int b = kb0; b < kb1 && ok; ++b, ++t) {
-                    const int buf = t & 1;
-                    ok = mbar_wait(&acc_empty[buf], ((t >> 1) & 1) ^ 1, abort_flag, status, 4);
-                    if (!ok) break;
-                    const uint32_t d_tmem = tmem_base + buf * BM;
-#pragma unroll 1
+                    if ((t & 1) != par) continue;
+                    const int p = t % SBN;
+                    if (!acc_ok) {
+                        ok = mbar_wait(&acc_empty[par], ((t >> 1) & 1) ^ 1, abort_flag, status, 4);
+                        if (!ok) break;
+                    }
+                    bool sb_ok = !L::CORR;
+#pragma unroll
                     for (int h = 0; h < 2; ++h) {   // K128 steps: chunks 2h, 2h+1
-                        const bool new_b = ((2 * h) % L::SCH) == 0;
-                        if (!ahead) {
-                            ok = (!new_b || mbar_wait(&b_full[sx], px, abort_flag, status, 5)) &&
-                                 mbar_wait(&a_full[sa], pa, abort_flag, status, 12);
+                        const int q0 = (2 * h) % L::SCH;   // first box of the step in its B stage
+                        int sa, sx;
+                        uint32_t pa, px;
+                        a_at(t, h, sa, pa);
+                        b_at(t, h, sx, px);
+                        if (!step_ok) {
+                            ok = mbar_wait(&a_full[sa], pa, abort_flag, status, 12);
+                            if (ok && q0 == 0) ok = mbar_wait(&b_full[sx], px, abort_flag, status, 5);
                             if (!ok) break;
                         }
                         tc_fence_after();
                         const uint32_t a0 = tmem_base + A_TMEM_COL + 64 * sa;
-                        const int q0 = (2 * h) % L::SCH;
                         const uint64_t bd = bdesc0 + static_cast<uint64_t>((sx * L::B_STAGE + q0 * L::BOX) >> 4);
                         mma_f16_ta(d_tmem, a0, bd, IDESC, h != 0);
                         mma_f16_ta(d_tmem, a0 + 8, bd + 2, IDESC, 1u);
                         mma_f16_ta(d_tmem, a0 + 16, bd + 4, IDESC, 1u);
                         mma_f16_ta(d_tmem, a0 + 24, bd + 6, IDESC, 1u);
-                        // look ahead while these run: are the next step's stages in?
+                        // probes, while these run: this thread's next step is step 1 of
+                        // superblock t, or step 0 of superblock t + 2
+                        const bool last_b = (q0 + 2 == L::SCH);   // this step ends its B stage
                         {
-                            const int na = (sa + 1 == A_STAGES) ? 0 : sa + 1;
-                            const uint32_t npa = (sa + 1 == A_STAGES) ? pa ^ 1 : pa;
-                            const bool last_b = (q0 + 2 == L::SCH);       // this step ends the B stage
-                            const int nx = last_b ? ((sx + 1 == BS) ? 0 : sx + 1) : sx;
-                            const uint32_t npx = (last_b && sx + 1 == BS) ? px ^ 1 : px;
-                            const bool next_new_b = ((2 * (h ^ 1)) % L::SCH) == 0;
-                            ahead = mbar_test_wait(&a_full[na], npa) &&
-                                    (!next_new_b || mbar_test_wait(&b_full[nx], npx));
+                            const int nt = h == 0 ? t : t + 2, nh = h ^ 1;
+                            int na, nx;
+                            uint32_t npa, npx;
+                            a_at(nt, nh, na, npa);
+                            b_at(nt, nh, nx, npx);
+                            const bool ta = mbar_test_wait(&a_full[na], npa);
+                            const bool tb = ((2 * nh) % L::SCH != 0) || mbar_test_wait(&b_full[nx], npx);
+                            if (h == 0) {
+                                if (L::CORR) sb_ok = mbar_test_wait(&sb_full[p], (t / SBN) & 1);
+                            } else {
+                                acc_ok = mbar_test_wait(&acc_empty[par], (((t + 2) >> 1) & 1) ^ 1);
+                            }
+                            step_ok = ta && tb;
                         }
                         const uint64_t bd1 = bd + (L::BOX >> 4);
                         mma_f16_ta(d_tmem, a0 + 32, bd1, IDESC, 1u);
                         mma_f16_ta(d_tmem, a0 + 40, bd1 + 2, IDESC, 1u);
                         mma_f16_ta(d_tmem, a0 + 48, bd1 + 4, IDESC, 1u);
                         mma_f16_ta(d_tmem, a0 + 56, bd1 + 6, IDESC, 1u);
+                        // frees the A stage (and, with MERGED_RELEASE, the B stage of this step)
                         mma_commit(&a_empty[sa]);
-                        if (++sa == A_STAGES) sa = 0, pa ^= 1;
-                        if (q0 + 2 == L::SCH) {
-                            mma_commit(&b_empty[sx]);
-                            if (++sx == BS) sx = 0, px ^= 1;
-                        }
+                        if (last_b && !MERGED_RELEASE) mma_commit(&b_empty[sx]);
                     }
                     if (!ok) break;
                     if (L::CORR) {
-                        const int p = t % SBN;
-                        ok = mbar_wait(&sb_full[p], (t / SBN) & 1, abort_flag, status, 6);
-                        if (!ok) break;
+                        if (!sb_ok) {
+                            ok = mbar_wait(&sb_full[p], (t / SBN) & 1, abort_flag, status, 6);
+                            if (!ok) break;
+                        }
                         tc_fence_after();
-                        const uint32_t sb = smem_u32(sb_slot(p));
-                        const uint64_t bdesc = smem_desc(sb + L::SB_BCORR, 16, 256, SWZ_32B);
-                        mma_f16(d_tmem, smem_desc(sb + L::SB_ACORR, 16, 256, SWZ_32B), bdesc, IDESC, 1u);
-                        mma_f16(d_tmem, smem_desc(sb + L::SB_ACORR + BN * 32, 16, 256, SWZ_32B), bdesc, IDESC,
-                                1u);
-                        mma_commit(&sb_empty[p]);
+                        const uint64_t po = static_cast<uint64_t>((p * L::SB) >> 4);
+                        mma_f16(d_tmem, acorr0 + po, bcorr0 + po, IDESC, 1u);
+                        mma_f16(d_tmem, acorr0 + po + ((BN * 32) >> 4), bcorr0 + po, IDESC, 1u);
                     }
-                    mma_commit(&acc_full[buf]);
+                    // completion of everything so far: the epilogue then also frees side slot p
+                    mma_commit(&acc_full[par]);
                 }
             }
         }
@@ -501,30 +537,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&sb_full[p]);
                     }
+                    // K128 steps: the second chunk is expanded while the first one's
+                    // tcgen05.st is in flight, one wait::st and one a_full per step
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        const int g = 2 * t + (c >> 1);   // K128 step
+                    for (int j = 0; j < 2; ++j) {
+                        const int g = 2 * t + j;
                         const int s = g % A_STAGES;
-                        const int sl = main_on ? static_cast<int>((((c < 2) ? sc03 : sc47) >> (16 * (c & 1))) & 0xff) : 0;
-                        const int sh = main_on ? static_cast<int>((((c < 2) ? sc03 : sc47) >> (16 * (c & 1) + 8)) & 0xff) : 0;
-                        const uint32_t scL = h2dup(__int2half_rn(sl));
-                        const uint32_t cL = h2dup(__int2half_rn(-1024 * sl));
-                        const uint32_t scH = h2dup(__float2half_rn(static_cast<float>(sh) * 0.0625f));
-                        const uint32_t cH = h2dup(__int2half_rn(-64 * sh));
-                        uint32_t v[32];
-                        unpack_q4k_chunk(blk, c, scL, cL, scH, cH, v);
-                        if ((c & 1) == 0) {
-                            ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
-                            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                            tc_fence_after();
+                        // sub-block scales of chunks 2j (bytes 0, 1) and 2j+1 (bytes 2, 3)
+                        const uint32_t scw = main_on ? (j == 0 ? sc03 : sc47) : 0u;
+                        uint32_t v0[32], v1[32];
+                        {
+                            const int sl = static_cast<int>(scw & 0xff), sh = static_cast<int>((scw >> 8) & 0xff);
+                            unpack_q4k_chunk(blk, 2 * j, h2dup(__int2half_rn(sl)), h2dup(__int2half_rn(-1024 * sl)),
+                                             h2dup(__float2half_rn(static_cast<float>(sh) * 0.0625f)),
+                                             h2dup(__int2half_rn(-64 * sh)), v0);
                         }
-                        tmem_st_32x32b_x32(lane_base + 64 * s + 32 * (c & 1), v);
+                        ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
+                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                        tc_fence_after();
+                        tmem_st_32x32b_x32(lane_base + 64 * s, v0);
+                        {
+                            const int sl = static_cast<int>((scw >> 16) & 0xff), sh = static_cast<int>(scw >> 24);
+                            unpack_q4k_chunk(blk, 2 * j + 1, h2dup(__int2half_rn(sl)), h2dup(__int2half_rn(-1024 * sl)),
+                                             h2dup(__float2half_rn(static_cast<float>(sh) * 0.0625f)),
+                                             h2dup(__int2half_rn(-64 * sh)), v1);
+                        }
+                        tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
                         tmem_st_wait();
-                        if (c & 1) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&a_full[s]);
-                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&a_full[s]);
                     }
                     if (!ok) break;
                 } else {
@@ -545,30 +587,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&sb_full[p]);
                     }
+                    // K128 steps, as for Q4_K
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        const int g = 2 * t + (c >> 1);   // K128 step
+                    for (int j = 0; j < 2; ++j) {
+                        const int g = 2 * t + j;
                         const int s = g % A_STAGES;
                         // the chunk's four sub-block scales: bytes 4c..4c+3 of the scale array
-                        const uint32_t scw = c == 0 ? sw[0] : c == 1 ? sw[1] : c == 2 ? sw[2] : sw[3];
-                        uint32_t s4[4];
+                        auto scales = [&](uint32_t scw, uint32_t (&s4)[4]) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            s4[q] = h2dup(__int2half_rn(static_cast<int8_t>((scw >> (8 * q)) & 0xff)));
-                        uint32_t v[32];
-                        unpack_q6k_chunk(blk, c, s4, v);
-                        if ((c & 1) == 0) {
-                            ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
-                            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                            tc_fence_after();
+                            for (int q = 0; q < 4; ++q)
+                                s4[q] = h2dup(__int2half_rn(static_cast<int8_t>((scw >> (8 * q)) & 0xff)));
+                        };
+                        uint32_t v0[32], v1[32];
+                        {
+                            uint32_t s4[4];
+                            scales(j == 0 ? sw[0] : sw[2], s4);
+                            unpack_q6k_chunk(blk, 2 * j, s4, v0);
                         }
-                        tmem_st_32x32b_x32(lane_base + 64 * s + 32 * (c & 1), v);
+                        ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
+                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                        tc_fence_after();
+                        tmem_st_32x32b_x32(lane_base + 64 * s, v0);
+                        {
+                            uint32_t s4[4];
+                            scales(j == 0 ? sw[1] : sw[3], s4);
+                            unpack_q6k_chunk(blk, 2 * j + 1, s4, v1);
+                        }
+                        tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
                         tmem_st_wait();
-                        if (c & 1) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&a_full[s]);
-                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&a_full[s]);
                     }
                     if (!ok) break;
                 }
