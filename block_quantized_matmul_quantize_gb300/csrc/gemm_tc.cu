@@ -162,6 +162,18 @@ __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
+// a[0..3] += (S[0..3] * e) * dx[0..3], two columns per packed fp32 instruction
+__device__ __forceinline__ void fold4(float* a, const uint32_t* S, float2 ee, float4 dx) {
+    const float2 lo = __ffma2_rn(__fmul2_rn(make_float2(__uint_as_float(S[0]), __uint_as_float(S[1])), ee),
+                                 make_float2(dx.x, dx.y), make_float2(a[0], a[1]));
+    const float2 hi = __ffma2_rn(__fmul2_rn(make_float2(__uint_as_float(S[2]), __uint_as_float(S[3])), ee),
+                                 make_float2(dx.z, dx.w), make_float2(a[2], a[3]));
+    a[0] = lo.x;
+    a[1] = lo.y;
+    a[2] = hi.x;
+    a[3] = hi.y;
+}
+
 __device__ __forceinline__ uint32_t h2dup(__half h) {
     const uint32_t u = __half_as_ushort(h);
     return u | (u << 16);
@@ -486,6 +498,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + A_TMEM_COL;
+        // A K128 step's a_full is signalled only after the next chunk has been
+        // expanded, so the wait for its tcgen05.st to land overlaps that work;
+        // it is signalled at once before any wait that might block.
+        int pend = -1;   // A stage whose a_full is still to be signalled
+        auto signal = [&]() {
+            if (pend >= 0) {
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[pend]);
+                pend = -1;
+            }
+        };
         int t = 0;
         bool ok = true;
         for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
@@ -493,6 +518,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             work_of(wi, n0, m0, kb0, kb1);
             for (int b = kb0; b < kb1; ++b, ++t) {
                 const int r = t % R;
+                if (!mbar_test_wait(&raw_full[r], (t / R) & 1)) signal();
                 ok = mbar_wait(&raw_full[r], (t / R) & 1, abort_flag, status, 7);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 const uint8_t* blk = raw_slot(r) + row * WTraits<WT>::RAW_BLOCK;
@@ -521,6 +547,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             a1[j] = h2dup(h1);
                             a2[j] = h2dup(h2);
                         }
+                        if (!mbar_test_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1)) signal();
                         ok = mbar_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1, abort_flag, status, 8);
                         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                         uint8_t* sb = sb_slot(p);
@@ -552,6 +579,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                              h2dup(__float2half_rn(static_cast<float>(sh) * 0.0625f)),
                                              h2dup(__int2half_rn(-64 * sh)), v0);
                         }
+                        signal();
                         ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
                         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                         tc_fence_after();
@@ -563,10 +591,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                              h2dup(__int2half_rn(-64 * sh)), v1);
                         }
                         tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
-                        tmem_st_wait();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&a_full[s]);
+                        pend = s;
                     }
                     if (!ok) break;
                 } else {
@@ -581,6 +606,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (grp == 0) {
                         if (bad) atomicOr(status, ST_Q6K_SCALE);
                         const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
+                        if (!mbar_test_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1)) signal();
                         ok = mbar_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1, abort_flag, status, 8);
                         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                         reinterpret_cast<float*>(sb_slot(p) + L::SB_E)[row] = d;
@@ -604,6 +630,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             scales(j == 0 ? sw[0] : sw[2], s4);
                             unpack_q6k_chunk(blk, 2 * j, s4, v0);
                         }
+                        signal();
                         ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
                         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                         tc_fence_after();
@@ -614,10 +641,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             unpack_q6k_chunk(blk, 2 * j + 1, s4, v1);
                         }
                         tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
-                        tmem_st_wait();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&a_full[s]);
+                        pend = s;
                     }
                     if (!ok) break;
                 }
@@ -625,6 +649,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (lane == 0) mbar_arrive(&raw_empty[r]);
             }
         }
+        signal();
     } else if (warp >= W_EPI0) {
         // ------------------------------------------------ epilogue
         constexpr int CPT = L::CPT;
@@ -650,22 +675,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc_fence_after();
                 const uint8_t* sb = sb_slot(p);
                 const float e = reinterpret_cast<const float*>(sb + L::SB_E)[row];
+                const float2 ee = make_float2(e, e);
                 const float4* dx4 = reinterpret_cast<const float4*>(sb + L::SB_DX) + col0 / 4;
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + buf * BM + col0;
                 if constexpr (CPT >= 16) {
+                    // two 16-column loads in flight per wait
+                    constexpr int PAIR = CPT >= 32 ? 2 : 1;
 #pragma unroll
-                    for (int ch = 0; ch < CPT / 16; ++ch) {
-                        uint32_t v[16];
-                        tmem_ld_32x32b_x16(taddr + 16 * ch, v);
+                    for (int ch = 0; ch < CPT / 16; ch += PAIR) {
+                        uint32_t v[PAIR][16];
+#pragma unroll
+                        for (int u = 0; u < PAIR; ++u) tmem_ld_32x32b_x16(taddr + 16 * (ch + u), v[u]);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const float4 dxv = dx4[4 * ch + q4];
-                            float* a = acc + 16 * ch + 4 * q4;
-                            a[0] = fmaf(__uint_as_float(v[4 * q4 + 0]) * e, dxv.x, a[0]);
-                            a[1] = fmaf(__uint_as_float(v[4 * q4 + 1]) * e, dxv.y, a[1]);
-                            a[2] = fmaf(__uint_as_float(v[4 * q4 + 2]) * e, dxv.z, a[2]);
-                            a[3] = fmaf(__uint_as_float(v[4 * q4 + 3]) * e, dxv.w, a[3]);
+                        for (int u = 0; u < PAIR; ++u) {
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                fold4(acc + 16 * (ch + u) + 4 * q4, v[u] + 4 * q4, ee, dx4[4 * (ch + u) + q4]);
                         }
                     }
                 } else {
@@ -673,14 +699,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tmem_ld_32x32b_x8(taddr, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q4 = 0; q4 < 2; ++q4) {
-                        const float4 dxv = dx4[q4];
-                        float* a = acc + 4 * q4;
-                        a[0] = fmaf(__uint_as_float(v[4 * q4 + 0]) * e, dxv.x, a[0]);
-                        a[1] = fmaf(__uint_as_float(v[4 * q4 + 1]) * e, dxv.y, a[1]);
-                        a[2] = fmaf(__uint_as_float(v[4 * q4 + 2]) * e, dxv.z, a[2]);
-                        a[3] = fmaf(__uint_as_float(v[4 * q4 + 3]) * e, dxv.w, a[3]);
-                    }
+                    for (int q4 = 0; q4 < 2; ++q4) fold4(acc + 4 * q4, v + 4 * q4, ee, dx4[q4]);
                 }
                 tc_fence_before();
                 __syncwarp();
