@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(PKG_DIR, "libqgemm.so")
 QGEMM_OK, QGEMM_EINVAL, QGEMM_EALIGN, QGEMM_EUNSUPPORTED, QGEMM_ECUDA, QGEMM_EDEVICE = range(6)
 QGEMM_DEV_TIMEOUT, QGEMM_DEV_Q4K_RANGE, QGEMM_DEV_Q6K_SCALE = 0x1, 0x2, 0x4
 QGEMM_OPT_SMALL_M_MAX, QGEMM_OPT_FORCE_BM, QGEMM_OPT_FORCE_SPLITS = 0, 1, 2
+QGEMM_SMALL_M_DEFAULT = 8   # the library's default for QGEMM_OPT_SMALL_M_MAX
 
 Q4K_BLOCK_BYTES = 144
 Q6K_BLOCK_BYTES = 210

@@ -53,6 +53,25 @@ size_t tc_smem_bytes(int wtype, int bm);
 cudaError_t tc_prepare(int wtype, int bm);   // sets the dynamic smem attribute (per device)
 cudaError_t launch_gemm_tc(const TcLaunch& a, cudaStream_t s);
 
+// Small-M streaming path (smallm.cu): M <= SMALL_M_LIMIT tokens, reads the
+// Q8_K planes directly (no workspace).
+constexpr int SMALL_M_LIMIT = 8;
+struct SmallLaunch {
+    int wtype;            // 4 or 6 (Q6_K: the 224-B repacked blocks)
+    int64_t M, N, K;
+    const void* w;
+    int64_t ldw;          // bytes between weight rows (multiple of 16)
+    const int8_t* xqs;
+    const float* xd;
+    const int16_t* xbs;
+    float* y;
+    int64_t ldy;
+    int sm_count;
+    uint32_t* status;
+};
+bool small_supported(int wtype, int64_t M, int64_t K);
+cudaError_t launch_small(const SmallLaunch& a, cudaStream_t s);
+
 // Record a one-line message for qgemm_last_error() and return `code`.
 int set_last_error(int code, const char* msg);
 

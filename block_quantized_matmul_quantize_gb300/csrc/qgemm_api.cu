@@ -33,7 +33,9 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // ------------------------------------------------------------ global state
 std::atomic<uint64_t> g_cnt[8];
 enum { C_QUANT, C_XPREP, C_Q4K_TC, C_Q6K_TC, C_Q4K_SMALL, C_Q6K_SMALL, C_PREPACK, C_SPLITK };
-std::atomic<int64_t> g_opt[3] = {{0}, {0}, {0}};
+// SMALL_M_MAX defaults to the measured crossover: the streaming kernel wins up
+// to 8 tokens at K = N = 5120 and at K = 4096, N = 14336.
+std::atomic<int64_t> g_opt[3] = {{qg::SMALL_M_LIMIT}, {0}, {0}};
 std::atomic<cudaEvent_t> g_ev_before{nullptr}, g_ev_after{nullptr};
 
 }  // namespace
@@ -218,6 +220,41 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
     return QGEMM_OK;
 }
 
+// Small-M path: the Q8_K planes are read directly; no workspace, one launch.
+int run_small(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs, const float* xd,
+              const int16_t* xbsums, int64_t M, float* y, int64_t ldy, cudaStream_t stream) {
+    DevState* ds = nullptr;
+    int rc = device_state(&ds);
+    if (rc) return rc;
+    qg::SmallLaunch a{};
+    a.wtype = wtype;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.w = w;
+    a.ldw = ldw;
+    a.xqs = xqs;
+    a.xd = xd;
+    a.xbs = xbsums;
+    a.y = y;
+    a.ldy = ldy;
+    a.sm_count = ds->sm_count;
+    a.status = ds->status;
+    cudaEvent_t evb = g_ev_before.load(), eva = g_ev_after.load();
+    if (evb) cudaEventRecord(evb, stream);
+    cudaError_t e = qg::launch_small(a, stream);
+    if (eva) cudaEventRecord(eva, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "small-M launch");
+    g_cnt[wtype == 4 ? C_Q4K_SMALL : C_Q6K_SMALL]++;
+    return QGEMM_OK;
+}
+
+// Path choice by token count (the pages' column-count routing): the
+// streaming kernel up to QGEMM_OPT_SMALL_M_MAX tokens, the tile GEMM above.
+bool use_small(int wtype, int64_t M, int64_t K) {
+    return M <= g_opt[QGEMM_OPT_SMALL_M_MAX].load() && qg::small_supported(wtype, M, K);
+}
+
 }  // namespace
 
 namespace qg {
@@ -277,6 +314,8 @@ int qgemm_q4k(const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xq
     if (rc || M == 0) return rc;
     if (ldw < (K / 256) * qg::Q4K_BLOCK) return fail(QGEMM_EINVAL, "ldw smaller than a row of Q4_K blocks");
     if (ldw % 16 != 0) return fail(QGEMM_EALIGN, "ldw must be a multiple of 16 bytes");
+    if (use_small(4, M, K))
+        return run_small(4, w, N, K, ldw, xqs, xd, xbsums, M, y, ldy, reinterpret_cast<cudaStream_t>(stream));
     return run_tc(4, w, N, K, ldw, xqs, xd, xbsums, M, y, ldy, workspace, workspace_bytes,
                   reinterpret_cast<cudaStream_t>(stream));
 }
@@ -306,8 +345,11 @@ int qgemm_q6k(const void* w_packed, int64_t N, int64_t K, const int8_t* xqs, con
     clear_err();
     int rc = gemm_common_checks(w_packed, N, K, xqs, xd, xbsums, M, y, ldy);
     if (rc || M == 0) return rc;
-    return run_tc(6, w_packed, N, K, (K / 256) * qg::Q6K_PACKED, xqs, xd, xbsums, M, y, ldy, workspace,
-                  workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+    const int64_t ldw = (K / 256) * qg::Q6K_PACKED;
+    if (use_small(6, M, K))
+        return run_small(6, w_packed, N, K, ldw, xqs, xd, xbsums, M, y, ldy, reinterpret_cast<cudaStream_t>(stream));
+    return run_tc(6, w_packed, N, K, ldw, xqs, xd, xbsums, M, y, ldy, workspace, workspace_bytes,
+                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 int qgemm_get_counters(qgemm_counters* out) {
@@ -352,6 +394,8 @@ int qgemm_set_option(int option, int64_t value) {
     if (value < 0) return fail(QGEMM_EINVAL, "option values are >= 0");
     if (option == QGEMM_OPT_FORCE_BM && value != 0 && value != 16 && value != 32 && value != 64 && value != 128)
         return fail(QGEMM_EINVAL, "FORCE_BM must be 0, 16, 32, 64 or 128");
+    if (option == QGEMM_OPT_SMALL_M_MAX && value > qg::SMALL_M_LIMIT)
+        return fail(QGEMM_EINVAL, "SMALL_M_MAX must be 0..%d", qg::SMALL_M_LIMIT);
     g_opt[option] = value;
     return QGEMM_OK;
 }

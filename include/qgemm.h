@@ -184,7 +184,7 @@ QGEMM_API int qgemm_get_device_status(uint32_t *bits, uint32_t *site);
 /* ----------------------------------------------------------- options ----
  * Process-global knobs, mainly for tests and tuning. */
 typedef enum {
-    QGEMM_OPT_SMALL_M_MAX = 0,  /* M <= this uses the small-M path (default 0 = off) */
+    QGEMM_OPT_SMALL_M_MAX = 0,  /* M <= this uses the small-M path: 0 = off, at most 8 (default 8) */
     QGEMM_OPT_FORCE_BM = 1,     /* tokens per CTA for the tile path: 0 = auto, 16/32/64/128 */
     QGEMM_OPT_FORCE_SPLITS = 2  /* split-K factor: 0 = auto, else 1..K/256       */
 } qgemm_option;

@@ -103,6 +103,10 @@ def test_size_queries(L):
 
 
 def test_options_and_counters(L):
+    assert L.qgemm_get_option(qg.QGEMM_OPT_SMALL_M_MAX) == qg.QGEMM_SMALL_M_DEFAULT == 8
+    assert L.qgemm_set_option(qg.QGEMM_OPT_SMALL_M_MAX, 9) == qg.QGEMM_EINVAL
+    assert L.qgemm_set_option(qg.QGEMM_OPT_SMALL_M_MAX, 0) == qg.QGEMM_OK
+    assert L.qgemm_set_option(qg.QGEMM_OPT_SMALL_M_MAX, 8) == qg.QGEMM_OK
     assert L.qgemm_set_option(1, 48) == qg.QGEMM_EINVAL
     assert L.qgemm_set_option(7, 0) == qg.QGEMM_EINVAL
     assert L.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 64) == qg.QGEMM_OK

@@ -26,10 +26,15 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
+    # the tile GEMM for every M here (the streaming path for M <= 8 has its
+    # own tests in test_gpu_smallm.py)
     ensure_built()
+    small = qg.qgemm_get_option(qg.QGEMM_OPT_SMALL_M_MAX)
+    qg.qgemm_set_option(qg.QGEMM_OPT_SMALL_M_MAX, 0)
     qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
     qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_SPLITS, 0)
     yield
+    qg.qgemm_set_option(qg.QGEMM_OPT_SMALL_M_MAX, small)
     qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
     qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_SPLITS, 0)
 
