@@ -3,9 +3,10 @@
 
 One step = the whole hot path on one batch: quantize fp32 activations to Q8_K
 (qgemm_quantize_q8k), then the Q4_K x Q8_K GEMM (qgemm_q4k: operand
-preparation + the tcgen05 tile GEMM).  Default workload: Q4_K, M = 512 tokens,
-K = 2048, N = 11008 (FFN up-projection shape), X ~ N(0,1) with 1% of the
-columns scaled x8; synthetic, seeded (synth.py).
+preparation + the tcgen05 tile GEMM, or for M <= 8 the small-M streaming
+kernel).  Default workload: Q4_K, M = 512 tokens, K = 2048, N = 11008 (FFN
+up-projection shape), X ~ N(0,1) with 1% of the columns scaled x8;
+synthetic, seeded (synth.py).
 
 Metric: effective TOPS = 2*M*N*K / step time (the whole job over all ranks);
 weight GB/s and the tile GEMM's roofline fraction are reported beside it.
@@ -42,10 +43,12 @@ METRIC = "k-quant GEMM effective TOPS and weight GB/s vs roofline at prefill M"
 UNIT = "TOPS"
 DEFAULT_WORKLOAD = synth.C1.name
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one tile-GEMM launch, from
-# the ncu capture summarised under profiles/ (None until measured, and reset
-# to None whenever the kernel changes).
-NCU_TRAFFIC_BYTES = {}
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
+# kernel, from the ncu capture summarised under profiles/ (absent until
+# measured, and removed whenever the kernel changes).
+NCU_TRAFFIC_BYTES = {
+    "q4k_m512_k2048_n11008_outliers": 15_023_616,   # gemm_tc_kernel<4,128>, commit 306144a
+}
 
 
 def workloads():
@@ -189,7 +192,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads()))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=256, help="token rows in the CPU-baseline sample")
+    ap.add_argument("--cpu-rows", type=int, default=512, help="token rows in the CPU-baseline sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline runs until this much time")
     ap.add_argument("--ref-rows", type=int, default=2, help="token rows per reference-arm step")
     ap.add_argument("--settle", type=float, default=0.5,
                     help="seconds of extra untimed steps after warm-up (clock settling); 0 = none")
@@ -322,20 +326,30 @@ def main():
 
     if rank == 0:
         peaks, peak_src = measured_peaks()
-        peak = float(peaks["bf16_tflops"])
-        achieved = ops / (gemm_mean_ms * 1e-3) / 1e12
         wbytes = N * (K // 256) * wl.block_bytes
+        small = (c1["q4k_small"] + c1["q6k_small"]) > (c0["q4k_small"] + c0["q6k_small"])
+        if small:
+            # the streaming kernel is bound by the weight bytes it reads once
+            achieved = wbytes / (gemm_mean_ms * 1e-3) / 1e9
+            roof = {"kernel": "smallm_kernel (small-M streaming)", "bound": "hbm", "achieved": achieved,
+                    "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                    "frac": achieved / float(peaks["hbm_gbs"]),
+                    "peak_source": f"{peak_src} hbm_gbs", "traffic": NCU_TRAFFIC_BYTES.get(wl.name)}
+        else:
+            peak = float(peaks["bf16_tflops"])
+            achieved = ops / (gemm_mean_ms * 1e-3) / 1e12
+            roof = {"kernel": "gemm_tc_kernel (tile GEMM)", "bound": "tensor", "achieved": achieved,
+                    "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                    "peak_source": f"{peak_src} bf16_tflops (burst; fp16 has the bf16 rate)",
+                    "traffic": NCU_TRAFFIC_BYTES.get(wl.name)}
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K_steps,
             "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": config_of(wl),
             "weight_gbs": wbytes / (gemm_mean_ms * 1e-3) / 1e9,
-            "kernels_us": {"step": mean_ms * 1e3, "tile_gemm": gemm_mean_ms * 1e3,
+            "kernels_us": {"step": mean_ms * 1e3, "gemm": gemm_mean_ms * 1e3,
                            "quantize_and_prep": (mean_ms - gemm_mean_ms) * 1e3},
-            "roofline": {"kernel": "gemm_tc_kernel (tile GEMM)", "bound": "tensor", "achieved": achieved,
-                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_source": f"{peak_src} bf16_tflops (burst; fp16 has the bf16 rate)",
-                         "traffic": NCU_TRAFFIC_BYTES.get(wl.name)},
+            "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.nbytes),
                     "d2h_bytes_per_step": int(M * N * 4)},
             "gpu_launches": int(launches),
@@ -343,11 +357,17 @@ def main():
             "device_status": bits,
         }
         if not args.no_cpu_baseline and world == 1:
+            # the oracle on `cpu_rows` token rows, repeated until about 10 s of CPU work
             rows = min(args.cpu_rows, M)
-            dt, cops = oracle_sample(wl, rows, x_host, w_host)
-            line["cpu_baseline"] = {"value": cops / dt / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                    "sample": f"{rows} of {M} token rows (quantize + GEMM over all N), "
-                                              f"{dt:.1f} s"}
+            runs, total, cops = 0, 0.0, 0.0
+            while total < args.cpu_seconds and runs < 1000:
+                dt, cops = oracle_sample(wl, rows, x_host, w_host)
+                total += dt
+                runs += 1
+            line["cpu_baseline"] = {"value": runs * cops / total / 1e12, "unit": UNIT, "cores": 1,
+                                    "kind": "oracle",
+                                    "sample": f"{rows} of {M} token rows (quantize + GEMM over all N) x {runs} "
+                                              f"runs, {total:.1f} s"}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
