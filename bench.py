@@ -14,8 +14,11 @@ weight GB/s and the tile GEMM's roofline fraction are reported beside it.
 Timing: W untimed warm-up steps, then exactly K steps, each bracketed by CUDA
 events on the launching stream, with L2 flushed before every step (a 256 MiB
 write, outside the events); barrier + synchronize on both sides; the slowest
-rank's mean is the step time.  The GEMM kernel alone is timed with events the
-library records around its launch (qgemm_set_profile_events).
+rank's mean is the step time.  A step is replayed as one CUDA graph captured
+from the API calls (--no-graph: the eager calls), which removes the host-side
+gaps between its kernels.  The same K steps then run once more as eager calls,
+with the GEMM kernel alone timed by events the library records around its
+launch (qgemm_set_profile_events).
 
 --impl reference times the CPU oracle (the parity authority) on bounded
 samples of the same workload on the host cores: the reference arm.
@@ -195,6 +198,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=512, help="token rows in the CPU-baseline sample")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline runs until this much time")
     ap.add_argument("--ref-rows", type=int, default=2, help="token rows per reference-arm step")
+    ap.add_argument("--no-graph", action="store_true", help="time the eager API calls instead of a graph replay")
     ap.add_argument("--settle", type=float, default=0.5,
                     help="seconds of extra untimed steps after warm-up (clock settling); 0 = none")
     args = ap.parse_args()
@@ -256,25 +260,55 @@ def main():
             step()
         torch.cuda.synchronize()
 
+    # The step's launches (quantize, operand preparation, GEMM) captured once as
+    # a CUDA graph: the same kernels with the same arguments, replayed without
+    # the host-side gaps between them.
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+
     K_steps = args.steps
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    ex_s = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    ex_e = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
     gb = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
     ga = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
     for e in gb + ga:      # create the events (torch creates them lazily on first record)
         e.record()
     torch.cuda.synchronize()
 
-    c0 = qg.qgemm_get_counters()
     barrier()
     torch.cuda.synchronize()
     t0 = time.time()
+    # timed steps (graph replay, or the eager calls with --no-graph)
+    for i in range(K_steps):
+        flush.zero_()
+        ev_s[i].record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+        ev_e[i].record(stream)
+    torch.cuda.synchronize()
+    # the same steps through the eager API calls, with the GEMM launch timed alone
+    c0 = qg.qgemm_get_counters()
     for i in range(K_steps):
         flush.zero_()
         qg.qgemm_set_profile_events(gb[i], ga[i])
-        ev_s[i].record(stream)
+        ex_s[i].record(stream)
         step()
-        ev_e[i].record(stream)
+        ex_e[i].record(stream)
     torch.cuda.synchronize()
     barrier()
     t1 = time.time()
@@ -283,17 +317,21 @@ def main():
     sampler.stop()
 
     step_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(K_steps)]
+    eager_ms = [ex_s[i].elapsed_time(ex_e[i]) for i in range(K_steps)]
     gemm_ms = [gb[i].elapsed_time(ga[i]) for i in range(K_steps)]
     mean_ms = sum(step_ms) / K_steps
+    eager_mean_ms = sum(eager_ms) / K_steps
     gemm_mean_ms = sum(gemm_ms) / K_steps
     if world > 1:
-        t = torch.tensor([mean_ms, gemm_mean_ms], dtype=torch.float64, device=dev)
+        t = torch.tensor([mean_ms, gemm_mean_ms, eager_mean_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_ms, gemm_mean_ms = float(t[0]), float(t[1])
+        mean_ms, gemm_mean_ms, eager_mean_ms = float(t[0]), float(t[1]), float(t[2])
 
     ops = 2.0 * M * N * K
     value = world * ops / (mean_ms * 1e-3) / 1e12
-    launches = sum(c1[k] - c0[k] for k in ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small"))
+    # library kernels per step, counted on the eager pass; the graph replays the same ones
+    per_step = sum(c1[k] - c0[k] for k in ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small"))
+    launches = per_step  # == K_steps x kernels per step, the count in each of the two timed loops
 
     # ---- end to end through the public API with host buffers
     x_pin = torch.from_numpy(x_host).pin_memory()
@@ -347,8 +385,10 @@ def main():
             "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": config_of(wl),
             "weight_gbs": wbytes / (gemm_mean_ms * 1e-3) / 1e9,
-            "kernels_us": {"step": mean_ms * 1e3, "gemm": gemm_mean_ms * 1e3,
-                           "quantize_and_prep": (mean_ms - gemm_mean_ms) * 1e3},
+            "kernels_us": {"step": mean_ms * 1e3, "step_eager_calls": eager_mean_ms * 1e3,
+                           "gemm": gemm_mean_ms * 1e3, "quantize_prep_and_gaps": (mean_ms - gemm_mean_ms) * 1e3},
+            "launch": "one CUDA graph per step (captured from the API calls)" if graph is not None
+                      else "eager API calls",
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.nbytes),
                     "d2h_bytes_per_step": int(M * N * 4)},
