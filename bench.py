@@ -2,11 +2,11 @@
 """Benchmark of the k-quant prefill matmul on one GB300 (or N replicas).
 
 One step = the whole hot path on one batch: quantize fp32 activations to Q8_K
-(qgemm_quantize_q8k), then the Q4_K x Q8_K GEMM (qgemm_q4k: operand
-preparation + the tcgen05 tile GEMM, or for M <= 8 the small-M streaming
-kernel).  Default workload: Q4_K, M = 512 tokens, K = 2048, N = 11008 (FFN
-up-projection shape), X ~ N(0,1) with 1% of the columns scaled x8;
-synthetic, seeded (synth.py).
+(qgemm_quantize_q8k_prep, which also writes the tile GEMM's fp16 operand
+planes), then the Q4_K x Q8_K GEMM (qgemm_q4k_prepared: the tcgen05 tile
+GEMM, or for M <= 8 the small-M streaming kernel).  Default workload: Q4_K,
+M = 512 tokens, K = 2048, N = 11008 (FFN up-projection shape), X ~ N(0,1)
+with 1% of the columns scaled x8; synthetic, seeded (synth.py).
 
 Metric: effective TOPS = 2*M*N*K / step time (the whole job over all ranks);
 weight GB/s and the tile GEMM's roofline fraction are reported beside it.
@@ -237,15 +237,13 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def gemm():
-        if wl.wtype == 4:
-            qg.qgemm_q4k(w, N, K, q, y=y, workspace=ws)
-        else:
-            qg.qgemm_q6k(w, N, K, q, y=y, workspace=ws)
-
     def step():
-        qg.qgemm_quantize_q8k(x, out=q)
-        gemm()
+        # quantize, writing the GEMM's operand planes in the same launch, then multiply
+        qg.qgemm_quantize_q8k_prep(x, ws, out=q)
+        if wl.wtype == 4:
+            qg.qgemm_q4k_prepared(w, N, K, q, ws, y=y)
+        else:
+            qg.qgemm_q6k_prepared(w, N, K, q, ws, y=y)
 
     sampler = ClockSampler(gpu_id_for_smi(local))
     # warm-up, then about half a second more so that clocks settle

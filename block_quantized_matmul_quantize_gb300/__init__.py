@@ -60,6 +60,9 @@ def lib() -> ctypes.CDLL:
             "qgemm_q6k_packed_bytes": ([i64, i64], sz),
             "qgemm_q6k_prepack": ([vp, i64, i64, i64, vp, vp], i32),
             "qgemm_q6k": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
+            "qgemm_quantize_q8k_prep": ([vp, i64, i64, i64, vp, vp, vp, vp, sz, vp], i32),
+            "qgemm_q4k_prepared": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
+            "qgemm_q6k_prepared": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
             "qgemm_get_counters": ([ctypes.POINTER(_Counters)], i32),
             "qgemm_reset_counters": ([], i32),
             "qgemm_get_device_status": ([ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)], i32),
@@ -185,6 +188,42 @@ def qgemm_q6k(w_packed: torch.Tensor, N: int, K: int, x: Q8K, y: torch.Tensor | 
     workspace = _workspace(M, N, K, workspace, x.qs.device)
     _check(lib().qgemm_q6k(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y), y.stride(0),
                            _ptr(workspace), workspace.numel(), _stream(stream)))
+    return y
+
+
+def qgemm_quantize_q8k_prep(x: torch.Tensor, workspace: torch.Tensor, out: Q8K | None = None,
+                            stream=None) -> Q8K:
+    """qgemm_quantize_q8k that also fills `workspace` with the tile GEMM's
+    operand planes, for qgemm_q4k_prepared / qgemm_q6k_prepared."""
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if out is None:
+        out = Q8K.empty(M, K, x.device)
+    _check(lib().qgemm_quantize_q8k_prep(_ptr(x), M, K, x.stride(0), _ptr(out.qs), _ptr(out.d), _ptr(out.bsums),
+                                         _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def qgemm_q4k_prepared(w: torch.Tensor, N: int, K: int, x: Q8K, workspace: torch.Tensor,
+                       y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """qgemm_q4k with a workspace filled by qgemm_quantize_q8k_prep from `x`."""
+    assert w.dtype == torch.uint8 and w.dim() == 2 and w.stride(1) == 1
+    M = x.M
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
+    _check(lib().qgemm_q4k_prepared(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
+                                    y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return y
+
+
+def qgemm_q6k_prepared(w_packed: torch.Tensor, N: int, K: int, x: Q8K, workspace: torch.Tensor,
+                       y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """qgemm_q6k with a workspace filled by qgemm_quantize_q8k_prep from `x`."""
+    M = x.M
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
+    _check(lib().qgemm_q6k_prepared(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
+                                    y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
 

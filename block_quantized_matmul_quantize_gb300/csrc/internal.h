@@ -26,8 +26,11 @@ constexpr int Q6K_BLOCK = 210;
 constexpr int Q6K_PACKED = 224;                 // 210 B + 14 B of zero padding (16-B aligned)
 
 // ---- kernels' host launchers (each returns cudaError_t of the launch) ----
+// With xh != nullptr the same launch also writes the tile GEMM's operand
+// planes (as launch_xprep would from its output).
 cudaError_t launch_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d,
-                                int16_t* bsums, cudaStream_t s);
+                                int16_t* bsums, cudaStream_t s, __half* xh = nullptr, __half* xbs = nullptr,
+                                float* dxT = nullptr, int64_t Mp = 0);
 
 // Q8_K planes -> tensor-core operand planes in the workspace:
 //   xh  [M][K] fp16 (the int8 values), xbs [M][K/16] fp16 (bsums),

@@ -153,9 +153,26 @@ Plan plan_tc(int64_t M, int64_t N, int64_t K, int sm_count) {
     return p;
 }
 
+// The tile GEMM's operand planes inside a workspace of qgemm_workspace_bytes(M, N, K).
+struct WsPlanes {
+    __half* xh;
+    __half* xbs;
+    float* dxT;
+    int64_t Mp;
+};
+WsPlanes ws_planes(void* ws, int64_t M, int64_t K) {
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    WsPlanes p{};
+    p.Mp = (M + 3) / 4 * 4;
+    p.xh = reinterpret_cast<__half*>(base);
+    p.xbs = reinterpret_cast<__half*>(base + align256(size_t(M) * K * 2));
+    p.dxT = reinterpret_cast<float*>(base + align256(size_t(M) * K * 2) + align256(size_t(M) * (K / 16) * 2));
+    return p;
+}
+
 int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs, const float* xd,
            const int16_t* xbsums, int64_t M, float* y, int64_t ldy, void* ws, size_t ws_bytes,
-           cudaStream_t stream) {
+           cudaStream_t stream, bool prepared) {
     DevState* ds = nullptr;
     int rc = device_state(&ds);
     if (rc) return rc;
@@ -166,15 +183,19 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
 
     const Plan pl = plan_tc(M, N, K, ds->sm_count);
     const int64_t nb = K / 256;
-    const int64_t Mp = (M + 3) / 4 * 4;
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    __half* xh = reinterpret_cast<__half*>(base);
-    __half* xbs = reinterpret_cast<__half*>(base + align256(size_t(M) * K * 2));
-    float* dxT = reinterpret_cast<float*>(base + align256(size_t(M) * K * 2) + align256(size_t(M) * (K / 16) * 2));
+    const WsPlanes wp = ws_planes(ws, M, K);
+    const int64_t Mp = wp.Mp;
+    __half* xh = wp.xh;
+    __half* xbs = wp.xbs;
+    float* dxT = wp.dxT;
 
-    cudaError_t e = qg::launch_xprep(xqs, xd, xbsums, M, K, xh, xbs, dxT, Mp, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "operand preparation launch");
-    g_cnt[C_XPREP]++;
+    cudaError_t e = cudaSuccess;
+    if (!prepared) {
+        // (a prepared workspace already holds these planes: qgemm_quantize_q8k_prep)
+        e = qg::launch_xprep(xqs, xd, xbsums, M, K, xh, xbs, dxT, Mp, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "operand preparation launch");
+        g_cnt[C_XPREP]++;
+    }
 
     CUtensorMap tm_w, tm_xh, tm_xbs, tm_dx;
     const int blk = wtype == 4 ? qg::Q4K_BLOCK : qg::Q6K_PACKED;
@@ -317,7 +338,7 @@ int qgemm_q4k(const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xq
     if (use_small(4, M, K))
         return run_small(4, w, N, K, ldw, xqs, xd, xbsums, M, y, ldy, reinterpret_cast<cudaStream_t>(stream));
     return run_tc(4, w, N, K, ldw, xqs, xd, xbsums, M, y, ldy, workspace, workspace_bytes,
-                  reinterpret_cast<cudaStream_t>(stream));
+                  reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 size_t qgemm_q6k_packed_bytes(int64_t N, int64_t K) {
@@ -349,7 +370,57 @@ int qgemm_q6k(const void* w_packed, int64_t N, int64_t K, const int8_t* xqs, con
     if (use_small(6, M, K))
         return run_small(6, w_packed, N, K, ldw, xqs, xd, xbsums, M, y, ldy, reinterpret_cast<cudaStream_t>(stream));
     return run_tc(6, w_packed, N, K, ldw, xqs, xd, xbsums, M, y, ldy, workspace, workspace_bytes,
-                  reinterpret_cast<cudaStream_t>(stream));
+                  reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+int qgemm_quantize_q8k_prep(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d,
+                            int16_t* bsums, void* workspace, size_t workspace_bytes, qgemm_stream_t stream) {
+    clear_err();
+    int rc = check_mk(M, K);
+    if (rc) return rc;
+    if (M == 0) return QGEMM_OK;
+    if (!x) return fail(QGEMM_EINVAL, "x is null");
+    if (ldx < K) return fail(QGEMM_EINVAL, "ldx (%lld) < K (%lld)", (long long)ldx, (long long)K);
+    if (!aligned(x, 16) || ldx % 4 != 0) return fail(QGEMM_EALIGN, "x must be 16-byte aligned with ldx % 4 == 0");
+    if ((rc = check_q8k(qs, d, bsums))) return rc;
+    const size_t need = qgemm_workspace_bytes(M, 1, K);
+    if (!workspace || workspace_bytes < need)
+        return fail(QGEMM_EINVAL, "workspace of %zu bytes needed (got %zu)", need,
+                    workspace ? workspace_bytes : size_t(0));
+    if (!aligned(workspace, 256)) return fail(QGEMM_EALIGN, "workspace must be 256-byte aligned");
+    const WsPlanes wp = ws_planes(workspace, M, K);
+    cudaError_t e = qg::launch_quantize_q8k(x, M, K, ldx, qs, d, bsums, reinterpret_cast<cudaStream_t>(stream), wp.xh,
+                                            wp.xbs, wp.dxT, wp.Mp);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    g_cnt[C_QUANT]++;
+    return QGEMM_OK;
+}
+
+int qgemm_q4k_prepared(const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs, const float* xd,
+                       const int16_t* xbsums, int64_t M, float* y, int64_t ldy, const void* workspace,
+                       size_t workspace_bytes, qgemm_stream_t stream) {
+    clear_err();
+    int rc = gemm_common_checks(w, N, K, xqs, xd, xbsums, M, y, ldy);
+    if (rc || M == 0) return rc;
+    if (ldw < (K / 256) * qg::Q4K_BLOCK) return fail(QGEMM_EINVAL, "ldw smaller than a row of Q4_K blocks");
+    if (ldw % 16 != 0) return fail(QGEMM_EALIGN, "ldw must be a multiple of 16 bytes");
+    if (use_small(4, M, K))
+        return run_small(4, w, N, K, ldw, xqs, xd, xbsums, M, y, ldy, reinterpret_cast<cudaStream_t>(stream));
+    return run_tc(4, w, N, K, ldw, xqs, xd, xbsums, M, y, ldy, const_cast<void*>(workspace), workspace_bytes,
+                  reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+int qgemm_q6k_prepared(const void* w_packed, int64_t N, int64_t K, const int8_t* xqs, const float* xd,
+                       const int16_t* xbsums, int64_t M, float* y, int64_t ldy, const void* workspace,
+                       size_t workspace_bytes, qgemm_stream_t stream) {
+    clear_err();
+    int rc = gemm_common_checks(w_packed, N, K, xqs, xd, xbsums, M, y, ldy);
+    if (rc || M == 0) return rc;
+    const int64_t ldw = (K / 256) * qg::Q6K_PACKED;
+    if (use_small(6, M, K))
+        return run_small(6, w_packed, N, K, ldw, xqs, xd, xbsums, M, y, ldy, reinterpret_cast<cudaStream_t>(stream));
+    return run_tc(6, w_packed, N, K, ldw, xqs, xd, xbsums, M, y, ldy, const_cast<void*>(workspace), workspace_bytes,
+                  reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 int qgemm_get_counters(qgemm_counters* out) {

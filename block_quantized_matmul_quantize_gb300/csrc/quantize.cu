@@ -23,12 +23,22 @@ namespace {
 
 constexpr int QWARPS = 8;  // chunks (warps) per block
 
+// The tile GEMM's operand planes (see xprep_kernel), written by the
+// quantizer itself when asked to ("prepared workspace").
+struct PrepOut {
+    __half* xh;    // [M][K] fp16
+    __half* xbs;   // [M][K/16] fp16
+    float* dxT;    // [K/256][Mp] fp32, rows m >= M zero
+    int64_t Mp;
+};
+
 // One warp per 256-element chunk: each lane owns 8 consecutive elements
 // (two 16-byte loads), so one chunk is one coalesced 1 KiB read.
+template <bool PREP>
 __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* __restrict__ x, int64_t M,
                                                                   int64_t K, int64_t ldx, int8_t* __restrict__ qs,
                                                                   float* __restrict__ dout,
-                                                                  int16_t* __restrict__ bsums) {
+                                                                  int16_t* __restrict__ bsums, PrepOut prep) {
     const int lane = threadIdx.x & 31;
     const int64_t nb = K >> 8;
     const int64_t chunk = static_cast<int64_t>(blockIdx.x) * QWARPS + (threadIdx.x >> 5);
@@ -70,6 +80,19 @@ __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* 
     s += __shfl_xor_sync(0xffffffffu, s, 1);  // lanes 2g, 2g+1 hold group g's 16 values
     if ((lane & 1) == 0) bsums[m * (K >> 4) + b * 16 + (lane >> 1)] = static_cast<int16_t>(s);
     if (lane == 0) dout[m * nb + b] = d;
+    if constexpr (PREP) {
+        // the same values as fp16 (integers of at most 11 significant bits: exact)
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half2 p2 = __halves2half2(__int2half_rn(q[2 * j]), __int2half_rn(q[2 * j + 1]));
+            o[j] = *reinterpret_cast<const uint32_t*>(&p2);
+        }
+        *reinterpret_cast<uint4*>(prep.xh + m * K + b * 256 + lane * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+        if ((lane & 1) == 0) prep.xbs[m * (K >> 4) + b * 16 + (lane >> 1)] = __int2half_rn(s);
+        if (lane == 0) prep.dxT[b * prep.Mp + m] = d;
+        if (m == M - 1 && lane >= 1 && lane < 4 && m + lane < prep.Mp) prep.dxT[b * prep.Mp + m + lane] = 0.0f;
+    }
 }
 
 // Q8_K -> fp16 operand planes.  Every int8 value and every bsum (|bsum| <=
@@ -147,10 +170,16 @@ int grid_for(int64_t work, int threads) {
 }  // namespace
 
 cudaError_t launch_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d,
-                                int16_t* bsums, cudaStream_t s) {
+                                int16_t* bsums, cudaStream_t s, __half* xh, __half* xbs, float* dxT, int64_t Mp) {
     const int64_t chunks = M * (K >> 8);
     const int64_t blocks = (chunks + QWARPS - 1) / QWARPS;
-    quantize_q8k_kernel<<<static_cast<unsigned>(blocks), QWARPS * 32, 0, s>>>(x, M, K, ldx, qs, d, bsums);
+    const PrepOut prep{xh, xbs, dxT, Mp};
+    if (xh)
+        quantize_q8k_kernel<true><<<static_cast<unsigned>(blocks), QWARPS * 32, 0, s>>>(x, M, K, ldx, qs, d, bsums,
+                                                                                      prep);
+    else
+        quantize_q8k_kernel<false><<<static_cast<unsigned>(blocks), QWARPS * 32, 0, s>>>(x, M, K, ldx, qs, d,
+                                                                                       bsums, prep);
     return cudaGetLastError();
 }
 

@@ -128,6 +128,34 @@ QGEMM_API int qgemm_q6k(const void *w_packed, int64_t N, int64_t K, const int8_t
               const int16_t *xbsums, int64_t M, float *y, int64_t ldy, void *workspace,
               size_t workspace_bytes, qgemm_stream_t stream);
 
+/* ------------------------------------------------ prepared workspace ----
+ * A step that quantizes and then multiplies can skip one launch: the
+ * quantizer writes the tile GEMM's fp16 operand planes into the GEMM's
+ * workspace in the same pass (the pages' "fuse the quantize into the GEMM
+ * producer" direction; the pages have no such call).
+ *
+ * qgemm_quantize_q8k_prep: exactly qgemm_quantize_q8k (same Q8_K planes,
+ * bit-exact), and in the same launch it fills `workspace` (>=
+ * qgemm_workspace_bytes(M, N, K) bytes for any N, 256-B aligned) with the
+ * operand planes derived from those Q8_K values.
+ *
+ * qgemm_q4k_prepared / qgemm_q6k_prepared: exactly qgemm_q4k / qgemm_q6k,
+ * except that the workspace must be one that qgemm_quantize_q8k_prep filled
+ * from these same Q8_K planes (same M, K; neither changed since), and it is
+ * only read.  For M <= QGEMM_OPT_SMALL_M_MAX the workspace is not used at
+ * all (the small-M path reads the planes).  Passing any other workspace
+ * gives undefined Y (the library cannot tell).
+ * Errors: as the calls they mirror. */
+QGEMM_API int qgemm_quantize_q8k_prep(const float *x, int64_t M, int64_t K, int64_t ldx, int8_t *qs, float *d,
+                                      int16_t *bsums, void *workspace, size_t workspace_bytes,
+                                      qgemm_stream_t stream);
+QGEMM_API int qgemm_q4k_prepared(const void *w, int64_t N, int64_t K, int64_t ldw, const int8_t *xqs,
+                                 const float *xd, const int16_t *xbsums, int64_t M, float *y, int64_t ldy,
+                                 const void *workspace, size_t workspace_bytes, qgemm_stream_t stream);
+QGEMM_API int qgemm_q6k_prepared(const void *w_packed, int64_t N, int64_t K, const int8_t *xqs, const float *xd,
+                                 const int16_t *xbsums, int64_t M, float *y, int64_t ldy, const void *workspace,
+                                 size_t workspace_bytes, qgemm_stream_t stream);
+
 /* -------------------------------------------- allocation-free Q4_K GEMM ----
  * The pages have no counterpart to this call; it serves callers that cannot
  * allocate device memory where they call the GEMM (for example a plugin

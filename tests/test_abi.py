@@ -66,6 +66,26 @@ def test_quantize_validation(L):
     assert L.qgemm_quantize_q8k(FAKE, 2, 256, 256, None, FAKE, FAKE, None) == qg.QGEMM_EINVAL
 
 
+def test_prepared_validation(L):
+    # quantize + prepare: the quantizer's checks, then the workspace's
+    P = L.qgemm_quantize_q8k_prep
+    assert P(FAKE, 1, 100, 100, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == qg.QGEMM_EINVAL
+    assert P(FAKE, 0, 256, 256, FAKE, FAKE, FAKE, None, 0, None) == qg.QGEMM_OK       # empty
+    assert P(MISALIGNED, 2, 256, 256, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == qg.QGEMM_EALIGN
+    need = L.qgemm_workspace_bytes(2, 1, 256)
+    assert P(FAKE, 2, 256, 256, FAKE, FAKE, FAKE, None, need, None) == qg.QGEMM_EINVAL
+    assert P(FAKE, 2, 256, 256, FAKE, FAKE, FAKE, FAKE, need - 1, None) == qg.QGEMM_EINVAL
+    assert P(FAKE, 2, 256, 256, FAKE, FAKE, FAKE, ctypes.c_void_p(0x100010), need, None) == qg.QGEMM_EALIGN
+    # the prepared GEMMs share the plain ones' argument checks
+    G = L.qgemm_q4k_prepared
+    assert G(FAKE, 128, 300, 288, FAKE, FAKE, FAKE, 4, FAKE, 128, FAKE, 1 << 20, None) == qg.QGEMM_EINVAL
+    assert G(FAKE, 128, 512, 296, FAKE, FAKE, FAKE, 4, FAKE, 128, FAKE, 1 << 20, None) == qg.QGEMM_EALIGN
+    assert G(FAKE, 128, 512, 288, FAKE, FAKE, FAKE, 0, FAKE, 128, FAKE, 1 << 20, None) == qg.QGEMM_OK
+    H = L.qgemm_q6k_prepared
+    assert H(FAKE, 128, 384, FAKE, FAKE, FAKE, 4, FAKE, 128, FAKE, 1 << 20, None) == qg.QGEMM_EINVAL
+    assert H(FAKE, 128, 512, FAKE, FAKE, FAKE, 4, None, 128, FAKE, 1 << 20, None) == qg.QGEMM_EINVAL
+
+
 def test_gemm_validation(L):
     ws = FAKE
     args = lambda **kw: dict(dict(w=FAKE, N=128, K=512, ldw=288, qs=FAKE, d=FAKE, bs=FAKE, M=4, y=FAKE,
