@@ -49,9 +49,7 @@ DEFAULT_WORKLOAD = synth.C1.name
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
 # kernel, from the ncu capture summarised under profiles/ (absent until
 # measured, and removed whenever the kernel changes).
-NCU_TRAFFIC_BYTES = {
-    "q4k_m512_k2048_n11008_outliers": 15_023_616,   # gemm_tc_kernel<4,128>, commit 306144a
-}
+NCU_TRAFFIC_BYTES = {}
 
 
 def workloads():

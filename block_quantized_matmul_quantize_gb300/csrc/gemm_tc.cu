@@ -135,7 +135,7 @@ struct Layout {
     static constexpr int RESERVE = 1024 /* base alignment */ + 512 /* barriers, misc */;
     static constexpr int B_STAGES = cmin(12, (SMEM_LIMIT - RESERVE - OFF_B) / B_STAGE) & ~1;
     static constexpr int OFF_BAR = OFF_B + B_STAGES * B_STAGE;
-    static constexpr int NBAR = 2 * RAW_SLOTS + 2 * A_STAGES + 2 * B_STAGES + 2 * SB_SLOTS + 4;
+    static constexpr int NBAR = 2 * RAW_SLOTS + 2 * A_STAGES + 2 * B_STAGES + 2 * SB_SLOTS + 4 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int TOTAL = OFF_MISC + 16 + 1024;
     static constexpr int CPT = BM / 2;                   // token columns per epilogue thread
@@ -233,8 +233,8 @@ template <int WT, int BM>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
                    const __grid_constant__ CUtensorMap tm_xbs, const __grid_constant__ CUtensorMap tm_dx,
-                   float* __restrict__ y, int64_t ldy, int M, int N, int nb, int splits, int n_tiles,
-                   int m_tiles, uint32_t* __restrict__ status) {
+                   float* __restrict__ y, int64_t ldy, int M, int N, int nb, const TcWork wk,
+                   uint32_t* __restrict__ status) {
     using L = Layout<WT, BM>;
     constexpr int R = L::RAW_SLOTS;
     constexpr int BS = L::B_STAGES;
@@ -257,27 +257,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t* sb_empty = sb_full + SBN;
     uint64_t* acc_full = sb_empty + SBN;
     uint64_t* acc_empty = acc_full + 2;
+    uint64_t* epi_bar = acc_empty + 2;   // the 8 epilogue warps, for cut tiles
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_work = n_tiles * m_tiles * splits;
+    const int num_work = wk.items;
 
     auto b_stage = [&](int s) { return smem + L::OFF_B + s * L::B_STAGE; };
     auto raw_slot = [&](int r) { return smem + L::OFF_RAW + r * L::RAW; };
     auto sb_slot = [&](int p) { return smem + L::OFF_SB + p * L::SB; };
     // work item -> (n0, m0, kb0, kb1); token tiles vary fastest, so the CTAs
     // running at the same time share weight tiles (one DRAM read, L2 hits after)
+    // (cut tiles: cut = index among the cut tiles, part = its K part; -1 for whole tiles)
+    auto work_cut = [&](int wi, int& n0, int& m0, int& kb0, int& kb1, int& cut, int& part) {
+        int tile;
+        if (wi < wk.full_items) {
+            tile = wi;
+            cut = -1;
+            part = 0;
+            kb0 = 0;
+            kb1 = nb;
+        } else {
+            const int j = wi - wk.full_items;
+            cut = j / wk.parts;
+            part = j - cut * wk.parts;
+            tile = wk.full_items + cut;
+            kb0 = static_cast<int>(static_cast<int64_t>(nb) * part / wk.parts);
+            kb1 = static_cast<int>(static_cast<int64_t>(nb) * (part + 1) / wk.parts);
+        }
+        n0 = (tile / wk.m_tiles) * BN;
+        m0 = (tile % wk.m_tiles) * BM;
+    };
     auto work_of = [&](int wi, int& n0, int& m0, int& kb0, int& kb1) {
-        const int mt = wi % m_tiles;
-        const int rest = wi / m_tiles;
-        const int nt = rest % n_tiles;
-        const int sp = rest / n_tiles;
-        n0 = nt * BN;
-        m0 = mt * BM;
-        kb0 = static_cast<int>(static_cast<int64_t>(nb) * sp / splits);
-        kb1 = static_cast<int>(static_cast<int64_t>(nb) * (sp + 1) / splits);
+        int cut, part;
+        work_cut(wi, n0, m0, kb0, kb1, cut, part);
     };
     // The i-th superblock a work item visits: its K range rotated by the weight-
     // tile index, so that the CTAs sharing a token tile at the same time read
@@ -309,6 +325,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&acc_full[p], 1);
             mbar_init(&acc_empty[p], 8);
         }
+        mbar_init(epi_bar, 8);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -658,10 +675,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int row = 32 * quad + lane;
         const int col0 = half * CPT;
         int t = 0;
+        uint32_t epi_phase = 0;
         bool ok = true;
         for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
-            int n0, m0, kb0, kb1;
-            work_of(wi, n0, m0, kb0, kb1);
+            int n0, m0, kb0, kb1, cut, part;
+            work_cut(wi, n0, m0, kb0, kb1, cut, part);
             float acc[CPT];
 #pragma unroll
             for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
@@ -709,18 +727,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             if (!ok) break;
+            if (cut >= 0) {
+                // a part of a cut tile: publish the partial tile, and the part
+                // that completes the tile adds all parts (ascending) into acc
+                // (a part is stored column by column, element (row, col) at col*128 + row,
+                // so that each warp-wide store or load is one contiguous 128-B line)
+                float* mine = wk.partials + (static_cast<int64_t>(cut) * wk.parts + part) * (BN * BM) +
+                              col0 * BN + row;
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) __stcg(mine + j * BN, acc[j]);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(epi_bar);
+                ok = mbar_wait(epi_bar, epi_phase, abort_flag, status, 13);   // every warp's partial is out
+                epi_phase ^= 1u;
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                if (warp == W_EPI0 && lane == 0) {
+                    __threadfence();
+                    *last_flag = (atomicAdd(&wk.counters[cut], 1) == wk.parts - 1);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(epi_bar);
+                ok = mbar_wait(epi_bar, epi_phase, abort_flag, status, 14);   // the flag is set
+                epi_phase ^= 1u;
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                if (!*last_flag) continue;
+                // all parts, this one included, from memory in ascending order
+                __threadfence();
+                const float* base = wk.partials + static_cast<int64_t>(cut) * wk.parts * (BN * BM) + col0 * BN + row;
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) acc[j] = __ldcg(base + j * BN);
+                for (int p2 = 1; p2 < wk.parts; ++p2) {
+#pragma unroll
+                    for (int j = 0; j < CPT; ++j) acc[j] += __ldcg(base + p2 * (BN * BM) + j * BN);
+                }
+                if (warp == W_EPI0 && lane == 0) wk.counters[cut] = 0;   // ready for the next call
+            }
             const int n = n0 + row;
             if (!*abort_flag && n < N) {
 #pragma unroll
                 for (int j = 0; j < CPT; ++j) {
                     const int m = m0 + col0 + j;
-                    if (m < M) {
-                        float* dst = y + static_cast<int64_t>(m) * ldy + n;
-                        if (splits > 1)
-                            atomicAdd(dst, acc[j]);
-                        else
-                            *dst = acc[j];
-                    }
+                    if (m < M) y[static_cast<int64_t>(m) * ldy + n] = acc[j];
                 }
             }
         }
@@ -738,13 +786,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <int WT, int BM>
 cudaError_t launch_t(const TcLaunch& a, cudaStream_t s) {
     using L = Layout<WT, BM>;
-    const int n_tiles = static_cast<int>((a.N + BN - 1) / BN);
-    const int m_tiles = static_cast<int>((a.M + BM - 1) / BM);
-    const int64_t work = static_cast<int64_t>(n_tiles) * m_tiles * a.splits;
-    const int grid = static_cast<int>(work < a.sm_count ? work : a.sm_count);
+    const int grid = a.work.items < a.sm_count ? a.work.items : a.sm_count;
     gemm_tc_kernel<WT, BM><<<grid, NTHREADS, L::TOTAL, s>>>(
         *a.tm_w, *a.tm_xh, a.tm_xbs ? *a.tm_xbs : *a.tm_xh, *a.tm_dx, a.y, a.ldy, static_cast<int>(a.M),
-        static_cast<int>(a.N), static_cast<int>(a.K / 256), a.splits, n_tiles, m_tiles, a.status);
+        static_cast<int>(a.N), static_cast<int>(a.K / 256), a.work, a.status);
     return cudaGetLastError();
 }
 

@@ -27,22 +27,40 @@ constexpr int Q6K_PACKED = 224;                 // 210 B + 14 B of zero padding 
 
 // ---- kernels' host launchers (each returns cudaError_t of the launch) ----
 // With xh != nullptr the same launch also writes the tile GEMM's operand
-// planes (as launch_xprep would from its output).
+// planes (as launch_xprep would from its output) and zeroes the split-tile
+// counters (TC_MAX_CUT_TILES ints).
 cudaError_t launch_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d,
                                 int16_t* bsums, cudaStream_t s, __half* xh = nullptr, __half* xbs = nullptr,
-                                float* dxT = nullptr, int64_t Mp = 0);
+                                float* dxT = nullptr, int64_t Mp = 0, int* counters = nullptr);
 
 // Q8_K planes -> tensor-core operand planes in the workspace:
 //   xh  [M][K] fp16 (the int8 values), xbs [M][K/16] fp16 (bsums),
 //   dxT [nb][Mp] fp32 (d transposed, Mp = M rounded up to 4, tail zeroed).
 cudaError_t launch_xprep(const int8_t* qs, const float* d, const int16_t* bsums, int64_t M, int64_t K,
-                         __half* xh, __half* xbs, float* dxT, int64_t Mp, cudaStream_t s);
+                         __half* xh, __half* xbs, float* dxT, int64_t Mp, int* counters, cudaStream_t s);
+
+// Work items of the tile GEMM: the first `full_items` tiles (token tiles
+// varying fastest) whole, then each remaining tile cut into `parts` K ranges.
+// A cut tile's parts write fp32 partial tiles to `partials` (slot = (tile -
+// full_items) * parts + part, 128 x bm floats each) and bump `counters[tile -
+// full_items]`; the part that finds all others done adds the parts in
+// ascending part order and stores Y (and resets the counter).  No atomics on
+// Y, and the result does not depend on which part finishes last.
+struct TcWork {
+    int n_tiles, m_tiles;
+    int full_items;       // whole tiles
+    int parts;            // K parts of each remaining tile (1: none)
+    int items;            // full_items + (tiles - full_items) * parts
+    float* partials;
+    int* counters;
+};
+constexpr int TC_MAX_CUT_TILES = 1024;   // counters in a workspace
 
 struct TcLaunch {
     int wtype;            // 4 or 6
     int bm;               // tokens per CTA: 16, 32, 64, 128
     int64_t M, N, K;
-    int splits;           // K splits (>1 -> Y accumulated with atomics, pre-zeroed)
+    TcWork work;
     int sm_count;         // persistent grid: min(work items, SMs)
     float* y;
     int64_t ldy;

@@ -128,9 +128,16 @@ int check_mk(int64_t M, int64_t K) {
 
 struct Plan {
     int bm;
-    int splits;
+    qg::TcWork work;   // without its pointers
 };
 
+// Tile width from M; the work list from the tile count and the SM count.
+// With fewer tiles than SMs every tile is cut into K parts so that the parts
+// fill the SMs (a part is still a whole 128-row x BM-token tile over a K
+// range: the pages' BigTile lesson that a tile must be shared is kept).
+// With more tiles than SMs the tiles stay whole: measured on GB300, cutting
+// only the last partial round (e.g. 40 of 344 tiles into 3 parts) cost more
+// in partial-tile traffic and fix-up than the idle SMs it filled.
 Plan plan_tc(int64_t M, int64_t N, int64_t K, int sm_count) {
     Plan p{};
     const int64_t fbm = g_opt[QGEMM_OPT_FORCE_BM].load();
@@ -139,26 +146,62 @@ Plan plan_tc(int64_t M, int64_t N, int64_t K, int sm_count) {
     else
         p.bm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
     const int64_t nb = K / 256;
+    qg::TcWork& w = p.work;
+    w.n_tiles = static_cast<int>((N + 127) / 128);
+    w.m_tiles = static_cast<int>((M + p.bm - 1) / p.bm);
+    const int64_t T = static_cast<int64_t>(w.n_tiles) * w.m_tiles;
+    const int64_t maxparts = nb / 2 > 1 ? (nb / 2 < 8 ? nb / 2 : 8) : 1;   // >= 2 superblocks per part
+    int64_t parts = 1, full = T;
     const int64_t fs = g_opt[QGEMM_OPT_FORCE_SPLITS].load();
     if (fs > 0) {
-        p.splits = static_cast<int>(fs > nb ? nb : fs);
+        parts = fs < nb ? fs : nb;
+        full = parts > 1 ? 0 : T;
     } else {
-        const int64_t tiles = ((N + 127) / 128) * ((M + p.bm - 1) / p.bm);
-        int64_t s = 1;
-        if (tiles < sm_count) s = (sm_count + tiles - 1) / tiles;
-        int64_t smax = nb / 2 > 0 ? nb / 2 : 1;  // keep >= 2 superblocks per split
-        if (s > smax) s = smax;
-        p.splits = static_cast<int>(s);
+        const int64_t G = sm_count > 0 ? sm_count : 1;
+        if (T < G) {
+            parts = G / T;
+            if (parts > maxparts) parts = maxparts;
+            full = parts > 1 ? 0 : T;
+        }
     }
+    if (T - full > qg::TC_MAX_CUT_TILES) parts = 1, full = T;   // counters are finite
+    if (parts <= 1) parts = 1, full = T;
+    w.full_items = static_cast<int>(full);
+    w.parts = static_cast<int>(parts);
+    w.items = static_cast<int>(full + (T - full) * parts);
     return p;
 }
 
-// The tile GEMM's operand planes inside a workspace of qgemm_workspace_bytes(M, N, K).
+size_t plane_bytes(int64_t M, int64_t K) {
+    const int64_t nb = K / 256, Mp = (M + 3) / 4 * 4;
+    return align256(size_t(M) * K * 2) + align256(size_t(M) * (K / 16) * 2) + align256(size_t(nb) * Mp * 4);
+}
+constexpr size_t COUNTER_BYTES = qg::TC_MAX_CUT_TILES * sizeof(int);
+
+size_t partial_bytes(const Plan& p) {
+    const int64_t cut = static_cast<int64_t>(p.work.n_tiles) * p.work.m_tiles - p.work.full_items;
+    return cut > 0 ? size_t(cut) * p.work.parts * 128 * p.bm * sizeof(float) : 0;
+}
+
+// SM count for sizing the workspace: the current device's, else a bound.
+int sizing_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) ==
+                                                   cudaSuccess && n > 0)
+        return n;
+    cudaGetLastError();   // (no device: clear the sticky-free error state)
+    return 160;
+}
+
+// The workspace of the tile GEMM: the operand planes, the cut-tile counters,
+// then the partial tiles of the cut tiles.
 struct WsPlanes {
     __half* xh;
     __half* xbs;
     float* dxT;
     int64_t Mp;
+    int* counters;
+    float* partials;
 };
 WsPlanes ws_planes(void* ws, int64_t M, int64_t K) {
     uint8_t* base = static_cast<uint8_t*>(ws);
@@ -167,6 +210,8 @@ WsPlanes ws_planes(void* ws, int64_t M, int64_t K) {
     p.xh = reinterpret_cast<__half*>(base);
     p.xbs = reinterpret_cast<__half*>(base + align256(size_t(M) * K * 2));
     p.dxT = reinterpret_cast<float*>(base + align256(size_t(M) * K * 2) + align256(size_t(M) * (K / 16) * 2));
+    p.counters = reinterpret_cast<int*>(base + plane_bytes(M, K));
+    p.partials = reinterpret_cast<float*>(base + plane_bytes(M, K) + COUNTER_BYTES);
     return p;
 }
 
@@ -192,7 +237,7 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
     cudaError_t e = cudaSuccess;
     if (!prepared) {
         // (a prepared workspace already holds these planes: qgemm_quantize_q8k_prep)
-        e = qg::launch_xprep(xqs, xd, xbsums, M, K, xh, xbs, dxT, Mp, stream);
+        e = qg::launch_xprep(xqs, xd, xbsums, M, K, xh, xbs, dxT, Mp, wp.counters, stream);
         if (e != cudaSuccess) return cuda_fail(e, "operand preparation launch");
         g_cnt[C_XPREP]++;
     }
@@ -212,17 +257,15 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
                        CU_TENSOR_MAP_SWIZZLE_NONE)))
         return rc;
 
-    if (pl.splits > 1) {
-        e = cudaMemset2DAsync(y, size_t(ldy) * 4, 0, size_t(N) * 4, size_t(M), stream);
-        if (e != cudaSuccess) return cuda_fail(e, "zeroing Y for split-K");
-    }
     qg::TcLaunch a{};
     a.wtype = wtype;
     a.bm = pl.bm;
     a.M = M;
     a.N = N;
     a.K = K;
-    a.splits = pl.splits;
+    a.work = pl.work;
+    a.work.counters = wp.counters;
+    a.work.partials = wp.partials;
     a.sm_count = ds->sm_count;
     a.y = y;
     a.ldy = ldy;
@@ -237,7 +280,7 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
     if (eva) cudaEventRecord(eva, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tile GEMM launch");
     g_cnt[wtype == 4 ? C_Q4K_TC : C_Q6K_TC]++;
-    if (pl.splits > 1) g_cnt[C_SPLITK]++;
+    if (pl.work.parts > 1) g_cnt[C_SPLITK]++;
     return QGEMM_OK;
 }
 
@@ -305,10 +348,10 @@ int qgemm_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t
 }
 
 size_t qgemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    (void)N;
     if (M <= 0 || K <= 0 || K % 256) return 0;
-    const int64_t nb = K / 256, Mp = (M + 3) / 4 * 4;
-    return align256(size_t(M) * K * 2) + align256(size_t(M) * (K / 16) * 2) + align256(size_t(nb) * Mp * 4);
+    const size_t base = plane_bytes(M, K) + COUNTER_BYTES;
+    if (N <= 0) return base;
+    return base + partial_bytes(plan_tc(M, N, K, sizing_sm_count()));
 }
 
 static int gemm_common_checks(const void* w, int64_t N, int64_t K, const int8_t* xqs, const float* xd,
@@ -383,14 +426,14 @@ int qgemm_quantize_q8k_prep(const float* x, int64_t M, int64_t K, int64_t ldx, i
     if (ldx < K) return fail(QGEMM_EINVAL, "ldx (%lld) < K (%lld)", (long long)ldx, (long long)K);
     if (!aligned(x, 16) || ldx % 4 != 0) return fail(QGEMM_EALIGN, "x must be 16-byte aligned with ldx % 4 == 0");
     if ((rc = check_q8k(qs, d, bsums))) return rc;
-    const size_t need = qgemm_workspace_bytes(M, 1, K);
+    const size_t need = plane_bytes(M, K) + COUNTER_BYTES;   // the planes and counters it writes
     if (!workspace || workspace_bytes < need)
         return fail(QGEMM_EINVAL, "workspace of %zu bytes needed (got %zu)", need,
                     workspace ? workspace_bytes : size_t(0));
     if (!aligned(workspace, 256)) return fail(QGEMM_EALIGN, "workspace must be 256-byte aligned");
     const WsPlanes wp = ws_planes(workspace, M, K);
     cudaError_t e = qg::launch_quantize_q8k(x, M, K, ldx, qs, d, bsums, reinterpret_cast<cudaStream_t>(stream), wp.xh,
-                                            wp.xbs, wp.dxT, wp.Mp);
+                                            wp.xbs, wp.dxT, wp.Mp, wp.counters);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     g_cnt[C_QUANT]++;
     return QGEMM_OK;

@@ -30,6 +30,7 @@ struct PrepOut {
     __half* xbs;   // [M][K/16] fp16
     float* dxT;    // [K/256][Mp] fp32, rows m >= M zero
     int64_t Mp;
+    int* counters; // TC_MAX_CUT_TILES split-tile counters, zeroed
 };
 
 // One warp per 256-element chunk: each lane owns 8 consecutive elements
@@ -92,6 +93,8 @@ __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* 
         if ((lane & 1) == 0) prep.xbs[m * (K >> 4) + b * 16 + (lane >> 1)] = __int2half_rn(s);
         if (lane == 0) prep.dxT[b * prep.Mp + m] = d;
         if (m == M - 1 && lane >= 1 && lane < 4 && m + lane < prep.Mp) prep.dxT[b * prep.Mp + m + lane] = 0.0f;
+        if (blockIdx.x == 0)
+            for (int i = threadIdx.x; i < TC_MAX_CUT_TILES; i += blockDim.x) prep.counters[i] = 0;
     }
 }
 
@@ -99,7 +102,10 @@ __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* 
 // 16*127) is an integer of at most 11 significant bits, so fp16 holds it exactly.
 __global__ void xprep_kernel(const int8_t* __restrict__ qs, const float* __restrict__ d,
                              const int16_t* __restrict__ bsums, int64_t M, int64_t K, __half* __restrict__ xh,
-                             __half* __restrict__ xbs, float* __restrict__ dxT, int64_t Mp) {
+                             __half* __restrict__ xbs, float* __restrict__ dxT, int64_t Mp,
+                             int* __restrict__ counters) {
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < TC_MAX_CUT_TILES; i += blockDim.x) counters[i] = 0;
     const int64_t nb = K >> 8;
     const int64_t n16 = M * (K >> 4);                 // 16-element groups of qs (= number of bsums)
     const int64_t ndx = nb * Mp;
@@ -170,10 +176,11 @@ int grid_for(int64_t work, int threads) {
 }  // namespace
 
 cudaError_t launch_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d,
-                                int16_t* bsums, cudaStream_t s, __half* xh, __half* xbs, float* dxT, int64_t Mp) {
+                                int16_t* bsums, cudaStream_t s, __half* xh, __half* xbs, float* dxT, int64_t Mp,
+                                int* counters) {
     const int64_t chunks = M * (K >> 8);
     const int64_t blocks = (chunks + QWARPS - 1) / QWARPS;
-    const PrepOut prep{xh, xbs, dxT, Mp};
+    const PrepOut prep{xh, xbs, dxT, Mp, counters};
     if (xh)
         quantize_q8k_kernel<true><<<static_cast<unsigned>(blocks), QWARPS * 32, 0, s>>>(x, M, K, ldx, qs, d, bsums,
                                                                                       prep);
@@ -184,9 +191,9 @@ cudaError_t launch_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ld
 }
 
 cudaError_t launch_xprep(const int8_t* qs, const float* d, const int16_t* bsums, int64_t M, int64_t K,
-                         __half* xh, __half* xbs, float* dxT, int64_t Mp, cudaStream_t s) {
+                         __half* xh, __half* xbs, float* dxT, int64_t Mp, int* counters, cudaStream_t s) {
     const int64_t work = M * (K >> 4) + (K >> 8) * Mp;
-    xprep_kernel<<<grid_for(work, 256), 256, 0, s>>>(qs, d, bsums, M, K, xh, xbs, dxT, Mp);
+    xprep_kernel<<<grid_for(work, 256), 256, 0, s>>>(qs, d, bsums, M, K, xh, xbs, dxT, Mp, counters);
     return cudaGetLastError();
 }
 
