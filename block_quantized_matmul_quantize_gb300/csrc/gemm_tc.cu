@@ -180,9 +180,16 @@ __device__ __forceinline__ uint32_t h2dup(__half h) {
 }
 
 // ---------------------------------------------------------------- unpack
-// Q4_K: expand K64 chunk c of one 144-byte block into the 64 fp16 values
-// sc_j*q in K order, two per 32-bit word: words 0..15 from the low nibbles
-// (sub-block 2c), words 16..31 from the high nibbles (sub-block 2c+1).
+// Both expanders write the K positions of every aligned group of 4 in the
+// order 0, 2, 1, 3 (fp16 pair (w[4k], w[4k+2]), then (w[4k+1], w[4k+3])):
+// two weights two bytes apart sit in one 32-bit word with no byte permute.
+// The activation operand (xh) is written in the same order, so the MMA's
+// dot products are unchanged; groups of 4 never straddle a 16-value group,
+// so the bsums are unchanged too.
+//
+// Q4_K: expand K64 chunk c of one 144-byte block into 64 fp16 values sc_j*q:
+// words 0..15 from the low nibbles (sub-block 2c), words 16..31 from the high
+// nibbles (sub-block 2c+1).
 __device__ __forceinline__ void unpack_q4k_chunk(const uint8_t* blk, int c, uint32_t scL, uint32_t cL,
                                                  uint32_t scH, uint32_t cH, uint32_t (&o)[32]) {
     const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
@@ -190,17 +197,19 @@ __device__ __forceinline__ void unpack_q4k_chunk(const uint8_t* blk, int c, uint
     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
     constexpr uint32_t MAGIC = 0x64006400u;  // fp16 1024 in both halves
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        // bytes 2j, 2j+1 of the chunk hold weights 2j, 2j+1 (low) and 32+2j, 33+2j (high)
-        const uint32_t p = prmt(w[j >> 1], (j & 1) ? 0x4342u : 0x4140u);
-        o[j] = hfma2u((p & 0x000F000Fu) | MAGIC, scL, cL);        // (1024+q)*sc - 1024*sc
-        o[16 + j] = hfma2u((p & 0x00F000F0u) | MAGIC, scH, cH);   // (1024+16q)*sc/16 - 64*sc
+    for (int k = 0; k < 8; ++k) {
+        // bytes 4k..4k+3 hold weights 4k..4k+3 (low nibbles) and 32+4k.. (high nibbles)
+        const uint32_t wk = w[k], sk = w[k] >> 8;
+        o[2 * k] = hfma2u((wk & 0x000F000Fu) | MAGIC, scL, cL);           // (1024+q)*sc - 1024*sc
+        o[2 * k + 1] = hfma2u((sk & 0x000F000Fu) | MAGIC, scL, cL);
+        o[16 + 2 * k] = hfma2u((wk & 0x00F000F0u) | MAGIC, scH, cH);      // (1024+16q)*sc/16 - 64*sc
+        o[17 + 2 * k] = hfma2u((sk & 0x00F000F0u) | MAGIC, scH, cH);
     }
 }
 
 // Q6_K: K64 chunk c = weights 64c..64c+63 of a 224-byte packed block, as
-// fp16 (q-32)*sc in K order.  Half h = c/2; low nibbles for c even, high for
-// c odd; qh bits 2*part for part = 2*(c&1) + (first / second 32 weights).
+// fp16 (q-32)*sc.  Half h = c/2; low nibbles for c even, high for c odd; qh
+// bits 4*(c&1) + 2*pp for the first (pp = 0) and second (pp = 1) 32 weights.
 __device__ __forceinline__ void unpack_q6k_chunk(const uint8_t* blk, int c, const uint32_t (&s4)[4],
                                                  uint32_t (&o)[32]) {
     const int h = c >> 1, hn = c & 1;
@@ -214,18 +223,19 @@ __device__ __forceinline__ void unpack_q6k_chunk(const uint8_t* blk, int c, cons
     constexpr uint32_t MAGIC = 0x64006400u;
     constexpr uint32_t OFF = 0x64206420u;  // fp16 1056 = 1024 + 32 in both halves
     const int nsh = 4 * hn;                 // low or high nibble
-    const int sh0 = 4 * hn;                 // qh bit offset of part 2*hn (first 32 weights)
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        // word j = weights 2j, 2j+1 of the chunk; pp = which 32, l = index in it
-        const int pp = j >> 4, l = 2 * (j & 15);
-        const uint32_t sel = ((l >> 1) & 1) ? 0x4342u : 0x4140u;
-        const uint32_t pl = prmt(Lw[(32 * pp + l) >> 2], sel);
-        const uint32_t ph = prmt(Hw[l >> 2], sel);
-        const uint32_t nib = (pl >> nsh) & 0x000F000Fu;
-        const uint32_t hb = ((ph >> (sh0 + 2 * pp)) << 4) & 0x00300030u;  // 2 qh bits -> bits 4..5
-        const uint32_t v = nib | hb | MAGIC;                                // fp16 1024 + q
-        o[j] = hmul2u(hsub2u(v, OFF), s4[2 * pp + (l >> 4)]);                // (q - 32) * sc, exact
+    for (int pp = 0; pp < 2; ++pp) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            // 6-bit codes of weights 32pp+4k .. +3, one per byte
+            const uint32_t q6 = ((Lw[8 * pp + k] >> nsh) & 0x0F0F0F0Fu) |
+                                (((Hw[k] >> (nsh + 2 * pp)) << 4) & 0x30303030u);
+            const uint32_t sc = s4[2 * pp + (k >> 2)];
+            const uint32_t a = (q6 & 0x003F003Fu) | MAGIC;          // fp16 1024 + q
+            const uint32_t b = ((q6 >> 8) & 0x003F003Fu) | MAGIC;
+            o[16 * pp + 2 * k] = hmul2u(hsub2u(a, OFF), sc);        // (q - 32) * sc, exact
+            o[16 * pp + 2 * k + 1] = hmul2u(hsub2u(b, OFF), sc);
+        }
     }
 }
 

@@ -82,12 +82,15 @@ __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* 
     if ((lane & 1) == 0) bsums[m * (K >> 4) + b * 16 + (lane >> 1)] = static_cast<int16_t>(s);
     if (lane == 0) dout[m * nb + b] = d;
     if constexpr (PREP) {
-        // the same values as fp16 (integers of at most 11 significant bits: exact)
+        // the same values as fp16 (integers of at most 11 significant bits: exact),
+        // each aligned group of 4 in the K order 0, 2, 1, 3 of the weight operand
         uint32_t o[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __half2 p2 = __halves2half2(__int2half_rn(q[2 * j]), __int2half_rn(q[2 * j + 1]));
-            o[j] = *reinterpret_cast<const uint32_t*>(&p2);
+        for (int g = 0; g < 2; ++g) {
+            const __half2 a = __halves2half2(__int2half_rn(q[4 * g]), __int2half_rn(q[4 * g + 2]));
+            const __half2 c = __halves2half2(__int2half_rn(q[4 * g + 1]), __int2half_rn(q[4 * g + 3]));
+            o[2 * g] = *reinterpret_cast<const uint32_t*>(&a);
+            o[2 * g + 1] = *reinterpret_cast<const uint32_t*>(&c);
         }
         *reinterpret_cast<uint4*>(prep.xh + m * K + b * 256 + lane * 8) = make_uint4(o[0], o[1], o[2], o[3]);
         if ((lane & 1) == 0) prep.xbs[m * (K >> 4) + b * 16 + (lane >> 1)] = __int2half_rn(s);
@@ -100,6 +103,8 @@ __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* 
 
 // Q8_K -> fp16 operand planes.  Every int8 value and every bsum (|bsum| <=
 // 16*127) is an integer of at most 11 significant bits, so fp16 holds it exactly.
+// xh keeps each aligned group of 4 values in the K order 0, 2, 1, 3, the order
+// in which the tile GEMM expands the weights (no byte permutes there).
 __global__ void xprep_kernel(const int8_t* __restrict__ qs, const float* __restrict__ d,
                              const int16_t* __restrict__ bsums, int64_t M, int64_t K, __half* __restrict__ xh,
                              __half* __restrict__ xbs, float* __restrict__ dxT, int64_t Mp,
@@ -117,10 +122,11 @@ __global__ void xprep_kernel(const int8_t* __restrict__ qs, const float* __restr
             uint32_t o[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+                // bytes 0..3 of word j are values 4j..4j+3: pairs (0, 2) and (1, 3)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int lo = static_cast<int8_t>((w[j] >> (16 * h)) & 0xff);
-                    const int hi = static_cast<int8_t>((w[j] >> (16 * h + 8)) & 0xff);
+                    const int lo = static_cast<int8_t>((w[j] >> (8 * h)) & 0xff);
+                    const int hi = static_cast<int8_t>((w[j] >> (8 * h + 16)) & 0xff);
                     const __half2 p = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
                     o[2 * j + h] = *reinterpret_cast<const uint32_t*>(&p);
                 }
