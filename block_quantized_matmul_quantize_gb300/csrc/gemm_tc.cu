@@ -76,8 +76,16 @@ namespace qg {
 namespace {
 
 constexpr int BN = 128;        // weight rows per CTA = MMA M
-constexpr int NWARPS = 16;
-constexpr int NTHREADS = NWARPS * 32;
+// Warps: 4 control, 4 or 8 unpack (one or two groups of four), 8 epilogue.
+// Q6_K's heavier expansion gets the second unpack group; for Q4_K it did not
+// pay for the registers it costs the epilogue (measured on GB300).
+template <int WT>
+struct Warps {
+    static constexpr int UNPACK_GROUPS = WT == 6 ? 2 : 1;
+    static constexpr int EPI0 = 4 + 4 * UNPACK_GROUPS;
+    static constexpr int N = EPI0 + 8;
+    static constexpr int THREADS = 32 * N;
+};
 constexpr int A_STAGES = 4;    // weight-operand K128 stages in TMEM (64 columns each)
 constexpr int A_TMEM_COL = 256;
 constexpr int KCH = 64;        // K elements per stage
@@ -91,7 +99,7 @@ constexpr int W_MMA = 1;
 constexpr int W_PROD_W = 2;
 constexpr int W_MMA2 = 3;
 constexpr int W_UNPACK0 = 4;
-constexpr int W_EPI0 = 8;
+
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -240,12 +248,14 @@ __device__ __forceinline__ void unpack_q6k_chunk(const uint8_t* blk, int c, cons
 }
 
 template <int WT, int BM>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
                    const __grid_constant__ CUtensorMap tm_xbs, const __grid_constant__ CUtensorMap tm_dx,
                    float* __restrict__ y, int64_t ldy, int M, int N, int nb, const TcWork wk,
                    uint32_t* __restrict__ status) {
     using L = Layout<WT, BM>;
+    constexpr int UG = Warps<WT>::UNPACK_GROUPS;
+    constexpr int W_EPI0 = Warps<WT>::EPI0;
     constexpr int R = L::RAW_SLOTS;
     constexpr int BS = L::B_STAGES;
     constexpr int SBN = SB_SLOTS;
@@ -317,7 +327,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (threadIdx.x == 0) {
         for (int r = 0; r < R; ++r) {
             mbar_init(&raw_full[r], 1);
-            mbar_init(&raw_empty[r], 4);
+            mbar_init(&raw_empty[r], 4 * UG);   // every unpack warp reads the block
         }
         for (int s = 0; s < A_STAGES; ++s) {
             mbar_init(&a_full[s], 4);
@@ -350,6 +360,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+
 
     if (warp == W_PROD_X) {
         // ------------------------------------------------ activation producer
@@ -519,9 +530,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-    } else if (warp >= W_UNPACK0 && warp < W_UNPACK0 + 4) {
+    } else if (warp >= W_UNPACK0 && warp < W_EPI0) {
         // ------------------------------------------------ unpack (thread = weight row)
-        constexpr int grp = 0;
+        // One or two groups of four warps (TMEM lanes 32*(warp%4).., as any
+        // warp must): with two, group g expands K128 step g of every
+        // superblock; group 0 also writes the superblock's side data.
+        const int grp = (warp - W_UNPACK0) >> 2;
+        const int j0 = UG == 2 ? grp : 0, j1 = UG == 2 ? grp + 1 : 2;   // this warp's K128 steps
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + A_TMEM_COL;
@@ -591,10 +606,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&sb_full[p]);
                     }
-                    // K128 steps: the second chunk is expanded while the first one's
-                    // tcgen05.st is in flight, one wait::st and one a_full per step
+                    // this warp's K128 steps: the second chunk is expanded while the
+                    // first one's tcgen05.st is in flight, one wait::st and one a_full
 #pragma unroll 1
-                    for (int j = 0; j < 2; ++j) {
+                    for (int j = j0; j < j1; ++j) {
                         const int g = 2 * t + j;
                         const int s = g % A_STAGES;
                         // sub-block scales of chunks 2j (bytes 0, 1) and 2j+1 (bytes 2, 3)
@@ -640,9 +655,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&sb_full[p]);
                     }
-                    // K128 steps, as for Q4_K
+                    // this warp's K128 steps, as for Q4_K
 #pragma unroll 1
-                    for (int j = 0; j < 2; ++j) {
+                    for (int j = j0; j < j1; ++j) {
                         const int g = 2 * t + j;
                         const int s = g % A_STAGES;
                         // the chunk's four sub-block scales: bytes 4c..4c+3 of the scale array
@@ -708,7 +723,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + buf * BM + col0;
                 if constexpr (CPT >= 16) {
                     // two 16-column loads in flight per wait
-                    constexpr int PAIR = CPT >= 32 ? 2 : 1;
+                    constexpr int PAIR = (CPT >= 32 && UG == 1) ? 2 : 1;   // registers allowing
 #pragma unroll
                     for (int ch = 0; ch < CPT / 16; ch += PAIR) {
                         uint32_t v[PAIR][16];
@@ -797,7 +812,7 @@ template <int WT, int BM>
 cudaError_t launch_t(const TcLaunch& a, cudaStream_t s) {
     using L = Layout<WT, BM>;
     const int grid = a.work.items < a.sm_count ? a.work.items : a.sm_count;
-    gemm_tc_kernel<WT, BM><<<grid, NTHREADS, L::TOTAL, s>>>(
+    gemm_tc_kernel<WT, BM><<<grid, Warps<WT>::THREADS, L::TOTAL, s>>>(
         *a.tm_w, *a.tm_xh, a.tm_xbs ? *a.tm_xbs : *a.tm_xh, *a.tm_dx, a.y, a.ldy, static_cast<int>(a.M),
         static_cast<int>(a.N), static_cast<int>(a.K / 256), a.work, a.status);
     return cudaGetLastError();

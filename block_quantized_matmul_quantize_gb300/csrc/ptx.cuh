@@ -129,6 +129,17 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                  : "memory");
 }
 
+// Per-warpgroup register budget (all four warps of an aligned warpgroup
+// execute it): give registers back / take more from what the CTA launched with.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Per-thread 16-byte asynchronous copy global -> shared (bypassing L1), and
 // its group commit / wait.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
