@@ -87,6 +87,22 @@ def test_every_tile_and_split(wtype, bm, splits):
         qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_SPLITS, 0)
 
 
+@pytest.mark.parametrize("wtype", [4, 6])
+def test_short_last_round_is_cut(wtype):
+    # more tiles than SMs, the last round 8 tiles: those are cut into K parts
+    # (the planner's choice on any SM count), the rest stay whole
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    M, K = 200, 2048
+    N = 128 * ((G + 8 + 1) // 2)                 # 2 token tiles x N/128 weight tiles = G + 8 or G + 9
+    w = weights(wtype, N, K, 41)
+    x = synth.gen_x(M, K, 42, outlier_frac=0.01)
+    qg.qgemm_reset_counters()
+    rows = np.unique(np.concatenate([sample_rows(M, 24, seed=3), [0, 127, 128, M - 1]]))
+    check(wtype, w, K, x, rows=rows, what=f"Q{wtype}_K M{M} N{N} K{K} on {G} SMs")
+    c = qg.qgemm_get_counters()
+    assert c["q4k_tc" if wtype == 4 else "q6k_tc"] == 1 and c["split_k"] == 1, c
+
+
 @pytest.mark.parametrize("wl", [synth.C0, synth.C1, synth.C2], ids=lambda w: w.name)
 def test_workload_full(wl):
     check(wl.wtype, wl.weights(), wl.K, wl.x(), what=wl.name)
