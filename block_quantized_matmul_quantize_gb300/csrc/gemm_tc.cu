@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int r = 0; r < R; ++r) {
             mbar_init(&raw_full[r], 1);
-            mbar_init(&raw_empty[r], 4 * UG);   // every unpack warp reads the block
+            mbar_init(&raw_empty[r], 4 * UG + (L::CORR ? 4 : 0));   // unpack warps (+ side-data warps)
         }
         for (int s = 0; s < A_STAGES; ++s) {
             mbar_init(&a_full[s], 4);
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             mbar_init(&b_empty[s], 1);
         }
         for (int p = 0; p < SBN; ++p) {
-            mbar_init(&sb_full[p], 1 + 4);
+            mbar_init(&sb_full[p], 1 + 4);   // producer's bytes + the four warps writing the slot
             mbar_init(&sb_empty[p], 8);   // the epilogue warps, after acc_full covered the MMAs reading it
         }
         for (int p = 0; p < 2; ++p) {
@@ -569,43 +569,11 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                 if constexpr (WT == 4) {
                     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
                     const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
-                    const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
                     const uint32_t sc03 = hdr.y & 0x3f3f3f3fu;
                     const uint32_t sc47 = (hdr.w & 0x0f0f0f0fu) | ((hdr.y >> 2) & 0x30303030u);
                     const bool main_on = (d != 0.0f);
-                    if (grp == 0) {
-                        const uint32_t mn03 = hdr.z & 0x3f3f3f3fu;
-                        const uint32_t mn47 = ((hdr.w >> 4) & 0x0f0f0f0fu) | ((hdr.z >> 2) & 0x30303030u);
-                        const float e = main_on ? d : dmin;
-                        const float ratio = main_on ? -dmin / d : -1.0f;
-                        if (!(fabsf(ratio) <= 1000.0f)) atomicOr(status, ST_Q4K_RANGE);
-                        uint32_t a1[8], a2[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int mj = ((j < 4 ? mn03 : mn47) >> (8 * (j & 3))) & 0xff;
-                            const float v = static_cast<float>(mj) * ratio;
-                            const __half h1 = __float2half_rn(v);
-                            const __half h2 = __float2half_rn(v - __half2float(h1));
-                            a1[j] = h2dup(h1);
-                            a2[j] = h2dup(h2);
-                        }
-                        if (!mbar_test_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1)) signal();
-                        ok = mbar_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1, abort_flag, status, 8);
-                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                        uint8_t* sb = sb_slot(p);
-                        // correction slabs, 32-byte swizzle: row * 32 + (chunk ^ ((row >> 2) & 1)) * 16
-                        uint8_t* s1 = sb + L::SB_ACORR + row * 32;
-                        uint8_t* s2 = s1 + BN * 32;
-                        const int x = (row >> 2) & 1;
-                        *reinterpret_cast<uint4*>(s1 + ((0 ^ x) << 4)) = make_uint4(a1[0], a1[1], a1[2], a1[3]);
-                        *reinterpret_cast<uint4*>(s1 + ((1 ^ x) << 4)) = make_uint4(a1[4], a1[5], a1[6], a1[7]);
-                        *reinterpret_cast<uint4*>(s2 + ((0 ^ x) << 4)) = make_uint4(a2[0], a2[1], a2[2], a2[3]);
-                        *reinterpret_cast<uint4*>(s2 + ((1 ^ x) << 4)) = make_uint4(a2[4], a2[5], a2[6], a2[7]);
-                        reinterpret_cast<float*>(sb + L::SB_E)[row] = e;
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&sb_full[p]);
-                    }
+                    // (the dmin correction operands and the scale e of this superblock
+                    // are written by the epilogue's side-data warps)
                     // this warp's K128 steps: the second chunk is expanded while the
                     // first one's tcgen05.st is in flight, one wait::st and one a_full
 #pragma unroll 1
@@ -702,6 +670,64 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
         int t = 0;
         uint32_t epi_phase = 0;
         bool ok = true;
+        // Q4_K: the second half's four warps also write the side data of each
+        // superblock (the dmin correction operands and the scale e, from the
+        // block header in the raw ring), SBN - 1 superblocks ahead of the
+        // accumulator they wait for, while the unpack warps only expand.
+        const bool side_writer = L::CORR && half == 1;
+        int ts = 0;         // next superblock whose side data is due
+        int total_sb = 0;   // this CTA's superblocks
+        if (side_writer) {
+            for (int wi = blockIdx.x; wi < num_work; wi += gridDim.x) {
+                int n0, m0, kb0, kb1, cut, part;
+                work_cut(wi, n0, m0, kb0, kb1, cut, part);
+                total_sb += kb1 - kb0;
+            }
+        }
+        auto side_upto = [&](int lim) -> bool {
+            for (; ts <= lim && ts < total_sb; ++ts) {
+                const int r = ts % R, ps = ts % SBN;
+                bool fine = mbar_wait(&raw_full[r], (ts / R) & 1, abort_flag, status, 15);
+                if (!__all_sync(0xffffffffu, fine)) return false;
+                const uint4 hdr = *reinterpret_cast<const uint4*>(raw_slot(r) + row * WTraits<WT>::RAW_BLOCK);
+                const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
+                const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
+                const uint32_t mn03 = hdr.z & 0x3f3f3f3fu;
+                const uint32_t mn47 = ((hdr.w >> 4) & 0x0f0f0f0fu) | ((hdr.z >> 2) & 0x30303030u);
+                const bool main_on = (d != 0.0f);
+                const float e = main_on ? d : dmin;
+                const float ratio = main_on ? -dmin / d : -1.0f;
+                if (!(fabsf(ratio) <= 1000.0f)) atomicOr(status, ST_Q4K_RANGE);
+                uint32_t a1[8], a2[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int mj = ((j < 4 ? mn03 : mn47) >> (8 * (j & 3))) & 0xff;
+                    const float v = static_cast<float>(mj) * ratio;
+                    const __half h1 = __float2half_rn(v);
+                    const __half h2 = __float2half_rn(v - __half2float(h1));
+                    a1[j] = h2dup(h1);
+                    a2[j] = h2dup(h2);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[r]);
+                fine = mbar_wait(&sb_empty[ps], ((ts / SBN) & 1) ^ 1, abort_flag, status, 16);
+                if (!__all_sync(0xffffffffu, fine)) return false;
+                uint8_t* sbw = sb_slot(ps);
+                // correction slabs, 32-byte swizzle: row * 32 + (chunk ^ ((row >> 2) & 1)) * 16
+                uint8_t* s1 = sbw + L::SB_ACORR + row * 32;
+                uint8_t* s2 = s1 + BN * 32;
+                const int x = (row >> 2) & 1;
+                *reinterpret_cast<uint4*>(s1 + ((0 ^ x) << 4)) = make_uint4(a1[0], a1[1], a1[2], a1[3]);
+                *reinterpret_cast<uint4*>(s1 + ((1 ^ x) << 4)) = make_uint4(a1[4], a1[5], a1[6], a1[7]);
+                *reinterpret_cast<uint4*>(s2 + ((0 ^ x) << 4)) = make_uint4(a2[0], a2[1], a2[2], a2[3]);
+                *reinterpret_cast<uint4*>(s2 + ((1 ^ x) << 4)) = make_uint4(a2[4], a2[5], a2[6], a2[7]);
+                reinterpret_cast<float*>(sbw + L::SB_E)[row] = e;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sb_full[ps]);
+            }
+            return true;
+        };
         for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
             int n0, m0, kb0, kb1, cut, part;
             work_cut(wi, n0, m0, kb0, kb1, cut, part);
@@ -711,6 +737,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             for (int b = kb0; b < kb1; ++b, ++t) {
                 const int buf = t & 1;
                 const int p = t % SBN;
+                if (side_writer && !side_upto(t + SBN - 1)) { ok = false; break; }
                 ok = mbar_wait(&acc_full[buf], (t >> 1) & 1, abort_flag, status, 10);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 ok = mbar_wait(&sb_full[p], (t / SBN) & 1, abort_flag, status, 11);
