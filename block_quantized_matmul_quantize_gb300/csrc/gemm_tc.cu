@@ -365,6 +365,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     if (warp == W_PROD_X) {
         // ------------------------------------------------ activation producer
         if (lane == 0) {
+            griddep_wait();   // the activation planes come from the preceding grid
             int g = 0;   // running stage counter
             bool ok = true;
             for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
@@ -417,6 +418,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                     const int p = t % SBN;
                     ok = mbar_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1, abort_flag, status, 1);
                     if (!ok) break;
+                    if (t == 0) griddep_wait();   // bsums and scales come from the preceding grid
                     uint8_t* sb = sb_slot(p);
                     mbar_arrive_expect_tx(&sb_full[p], (L::CORR ? BM * 32 : 0) + BM * 4);
                     if (L::CORR) tma_load_2d(&tm_xbs, &sb_full[p], sb + L::SB_BCORR, b * 16, m0);
@@ -780,6 +782,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             }
             if (!ok) break;
             if (cut >= 0) {
+                griddep_wait();   // the counters are zeroed by the preceding grid
                 // a part of a cut tile: publish the partial tile, and the part
                 // that completes the tile adds all parts (ascending) into acc
                 // (a part is stored column by column, element (row, col) at col*128 + row,
@@ -839,10 +842,23 @@ template <int WT, int BM>
 cudaError_t launch_t(const TcLaunch& a, cudaStream_t s) {
     using L = Layout<WT, BM>;
     const int grid = a.work.items < a.sm_count ? a.work.items : a.sm_count;
-    gemm_tc_kernel<WT, BM><<<grid, Warps<WT>::THREADS, L::TOTAL, s>>>(
-        *a.tm_w, *a.tm_xh, a.tm_xbs ? *a.tm_xbs : *a.tm_xh, *a.tm_dx, a.y, a.ldy, static_cast<int>(a.M),
-        static_cast<int>(a.N), static_cast<int>(a.K / 256), a.work, a.status);
-    return cudaGetLastError();
+    // A programmatic dependent of the preceding kernel: the CTAs may start
+    // (barrier set-up, weight loads and expansion) while that kernel finishes;
+    // every read of its output waits for it (griddep_wait).
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(Warps<WT>::THREADS);
+    cfg.dynamicSmemBytes = L::TOTAL;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const CUtensorMap tm_xbs = a.tm_xbs ? *a.tm_xbs : *a.tm_xh;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<WT, BM>, *a.tm_w, *a.tm_xh, tm_xbs, *a.tm_dx, a.y, a.ldy,
+                              static_cast<int>(a.M), static_cast<int>(a.N), static_cast<int>(a.K / 256), a.work,
+                              a.status);
 }
 
 template <int WT, int BM>

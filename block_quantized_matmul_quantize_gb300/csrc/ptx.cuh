@@ -87,6 +87,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     return mbar_wait_slow(bar, parity, abort_flag, status, site);
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialization may start once the preceding grid has signalled (or ended);
+// griddep_wait() then blocks the calling thread until the preceding grid has
+// completed and its memory operations are visible.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

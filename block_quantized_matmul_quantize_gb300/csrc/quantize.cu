@@ -17,6 +17,15 @@
 
 #include "internal.h"
 
+namespace {
+// The kernel that follows in the stream (the tile GEMM, launched as a
+// programmatic dependent) may start now: it loads and expands weights, which
+// this kernel does not touch, and waits for this grid before reading its output.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+}  // namespace
+
 namespace qg {
 
 namespace {
@@ -40,6 +49,7 @@ __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* 
                                                                   int64_t K, int64_t ldx, int8_t* __restrict__ qs,
                                                                   float* __restrict__ dout,
                                                                   int16_t* __restrict__ bsums, PrepOut prep) {
+    allow_dependent_launch();
     const int lane = threadIdx.x & 31;
     const int64_t nb = K >> 8;
     const int64_t chunk = static_cast<int64_t>(blockIdx.x) * QWARPS + (threadIdx.x >> 5);
@@ -109,6 +119,7 @@ __global__ void xprep_kernel(const int8_t* __restrict__ qs, const float* __restr
                              const int16_t* __restrict__ bsums, int64_t M, int64_t K, __half* __restrict__ xh,
                              __half* __restrict__ xbs, float* __restrict__ dxT, int64_t Mp,
                              int* __restrict__ counters) {
+    allow_dependent_launch();
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < TC_MAX_CUT_TILES; i += blockDim.x) counters[i] = 0;
     const int64_t nb = K >> 8;
