@@ -90,9 +90,13 @@ QGEMM_API int qgemm_quantize_q8k(const float *x, int64_t M, int64_t K, int64_t l
                        int16_t *bsums, qgemm_stream_t stream);
 
 /* ------------------------------------------------------------- GEMM ----
- * Workspace bytes the GEMM calls need for M tokens and depth K (holds the
- * fp16 tensor-core operand copy of the Q8_K activations).  0 when the small-M
- * path runs.  The workspace must be 256-B aligned. */
+ * Workspace bytes the GEMM calls need for M tokens, N weight rows and depth K
+ * on the current device: the fp16 tensor-core operand copy of the Q8_K
+ * activations (about 2.1 B per element of M*K), the cut-tile counters
+ * (4 KiB), and the partial tiles of the cut tiles (128 x BM fp32 per K part;
+ * tiles are cut when there are fewer of them than SMs, or when a last round
+ * would leave at least half of the SMs idle).  0 when the small-M path runs.
+ * The workspace must be 256-B aligned. */
 QGEMM_API size_t qgemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* qgemm_q4k: Y[M][N] = X_q8k[M][K] * W_q4k[N][K]^T.
@@ -105,6 +109,8 @@ QGEMM_API size_t qgemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   workspace, workspace_bytes   device scratch >= qgemm_workspace_bytes.
  * Accuracy: |Y - Y_exact| <= 2e-5 * sum_b |c_b| + 1e-6 per element, c_b the
  * contribution of superblock b (fp32 accumulation of exact integer partials).
+ * Y is deterministic for a given shape and device: a cut tile's K parts are
+ * summed in ascending part order, whichever part finishes last.
  * Value range: |dmin/d| <= 1000 per block (else device status
  * QGEMM_DEV_Q4K_RANGE is set and Y is not to be trusted).
  * Errors: EINVAL, EALIGN, EUNSUPPORTED (M, N >= 2^31), ECUDA. */
@@ -169,8 +175,10 @@ QGEMM_API int qgemm_q6k_prepared(const void *w_packed, int64_t N, int64_t K, con
  * (one per GPU that loads the library, held until the process exits).  It
  * allocates nothing.
  *   - Size limit: qgemm_workspace_bytes(M, N, K) must not exceed
- *     QGEMM_NOALLOC_SCRATCH_BYTES (16 MiB: M*K up to about 7.8 million, e.g.
- *     M = 512 at K = 11008 or M = 2048 at K = 3584); larger calls return
+ *     QGEMM_NOALLOC_SCRATCH_BYTES (16 MiB).  The operand copy alone allows
+ *     M*K up to about 7.8 million (e.g. M = 512 at K = 11008); grids with
+ *     cut tiles add their partial tiles on top (e.g. M = 512, K = 2048,
+ *     N = 11008 needs 9.7 MiB on a 152-SM GB300, 2.1 MiB of it the copy).  Larger calls return
  *     QGEMM_EUNSUPPORTED with a message and launch nothing.
  *   - The first call on each device looks up the scratch array's device
  *     address (cudaGetSymbolAddress) with that device current; make that
@@ -195,7 +203,7 @@ typedef struct {
     uint64_t q4k_small;    /* Q4_K small-M streaming launches       */
     uint64_t q6k_small;    /* Q6_K small-M streaming launches       */
     uint64_t q6k_prepack;  /* Q6_K repack launches                  */
-    uint64_t split_k;      /* GEMM launches that used split-K       */
+    uint64_t split_k;      /* GEMM launches with cut tiles (K parts) */
 } qgemm_counters;
 QGEMM_API int qgemm_get_counters(qgemm_counters *out);
 QGEMM_API int qgemm_reset_counters(void);
