@@ -153,7 +153,6 @@ struct Layout {
     static_assert(TOTAL <= SMEM_LIMIT, "shared memory budget");
 };
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) { return __byte_perm(a, 0u, sel); }
 
 __device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
@@ -170,6 +169,25 @@ __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
+__device__ __forceinline__ uint32_t hadd2u(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// Byte B of w as an exact fp16 in both halves, without a conversion
+// instruction: the byte under the exponent byte 0x64 is the fp16 1024 + v,
+// and subtracting 1024 leaves v.  Unsigned bytes (0..255); for a signed byte
+// pass w ^ 0x80808080 and subtract 1152 (1024 + 128) instead.
+template <int B>
+__device__ __forceinline__ uint32_t byte_h2(uint32_t w, uint32_t minus_bias) {
+    constexpr uint32_t sel = B | (4u << 4) | (B << 8) | (4u << 12);   // w[B], 0x64, w[B], 0x64
+    return hadd2u(__byte_perm(w, 0x64646464u, sel), minus_bias);
+}
+constexpr uint32_t H2_M1024 = 0xE400E400u;   // fp16 -1024 in both halves
+constexpr uint32_t H2_M1152 = 0xE480E480u;   // fp16 -1152
+constexpr uint32_t H2_1_16 = 0x2C002C00u;    // fp16 1/16
+constexpr uint32_t H2_M64 = 0xD400D400u;     // fp16 -64
+
 // a[0..3] += (S[0..3] * e) * dx[0..3], two columns per packed fp32 instruction
 __device__ __forceinline__ void fold4(float* a, const uint32_t* S, float2 ee, float4 dx) {
     const float2 lo = __ffma2_rn(__fmul2_rn(make_float2(__uint_as_float(S[0]), __uint_as_float(S[1])), ee),
@@ -586,10 +604,10 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                         const uint32_t scw = main_on ? (j == 0 ? sc03 : sc47) : 0u;
                         uint32_t v0[32], v1[32];
                         {
-                            const int sl = static_cast<int>(scw & 0xff), sh = static_cast<int>((scw >> 8) & 0xff);
-                            unpack_q4k_chunk(blk, 2 * j, h2dup(__int2half_rn(sl)), h2dup(__int2half_rn(-1024 * sl)),
-                                             h2dup(__float2half_rn(static_cast<float>(sh) * 0.0625f)),
-                                             h2dup(__int2half_rn(-64 * sh)), v0);
+                            // sc, -1024 sc for the low nibbles; sc/16, -64 sc for the high ones (all exact)
+                            const uint32_t sl = byte_h2<0>(scw, H2_M1024), sh = byte_h2<1>(scw, H2_M1024);
+                            unpack_q4k_chunk(blk, 2 * j, sl, hmul2u(sl, H2_M1024), hmul2u(sh, H2_1_16),
+                                             hmul2u(sh, H2_M64), v0);
                         }
                         signal();
                         ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
@@ -597,10 +615,9 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                         tc_fence_after();
                         tmem_st_32x32b_x32(lane_base + 64 * s, v0);
                         {
-                            const int sl = static_cast<int>((scw >> 16) & 0xff), sh = static_cast<int>(scw >> 24);
-                            unpack_q4k_chunk(blk, 2 * j + 1, h2dup(__int2half_rn(sl)), h2dup(__int2half_rn(-1024 * sl)),
-                                             h2dup(__float2half_rn(static_cast<float>(sh) * 0.0625f)),
-                                             h2dup(__int2half_rn(-64 * sh)), v1);
+                            const uint32_t sl = byte_h2<2>(scw, H2_M1024), sh = byte_h2<3>(scw, H2_M1024);
+                            unpack_q4k_chunk(blk, 2 * j + 1, sl, hmul2u(sl, H2_M1024), hmul2u(sh, H2_1_16),
+                                             hmul2u(sh, H2_M64), v1);
                         }
                         tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
                         pend = s;
@@ -632,9 +649,11 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                         const int s = g % A_STAGES;
                         // the chunk's four sub-block scales: bytes 4c..4c+3 of the scale array
                         auto scales = [&](uint32_t scw, uint32_t (&s4)[4]) {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                s4[q] = h2dup(__int2half_rn(static_cast<int8_t>((scw >> (8 * q)) & 0xff)));
+                            const uint32_t u = scw ^ 0x80808080u;   // signed bytes, offset by 128
+                            s4[0] = byte_h2<0>(u, H2_M1152);
+                            s4[1] = byte_h2<1>(u, H2_M1152);
+                            s4[2] = byte_h2<2>(u, H2_M1152);
+                            s4[3] = byte_h2<3>(u, H2_M1152);
                         };
                         uint32_t v0[32], v1[32];
                         {
