@@ -138,7 +138,14 @@ __global__ void __launch_bounds__(32 * SM_MAX_WARPS)
         cp_async_commit();
     };
 
-    issue_stage(0);   // first, so the weights are on their way while the activations load
+    // both stage buffers are in flight before the activations load: the
+    // weights do not depend on the preceding grid, so with a programmatic
+    // dependent launch they stream while that grid finishes (measured on
+    // GB300: loading the activations first did not shorten the kernel, and
+    // lost that overlap)
+    issue_stage(0);
+    if (nstage > 1) issue_stage(1);
+    griddep_wait();   // the activations come from the preceding grid
 
     // the slice's activations, all tokens, in registers
     uint32_t xa[MT][4], xb[MT][4];
@@ -166,12 +173,11 @@ __global__ void __launch_bounds__(32 * SM_MAX_WARPS)
 
     int it = 0;   // reduction batch counter (parity of the red buffer)
     for (int g = 0; g < nstage; ++g) {
-        if (g + 1 < nstage) {
-            issue_stage(g + 1);
+        // committed so far: stages 0 .. min(g + 1, nstage - 1)
+        if (g + 1 < nstage)
             cp_async_wait<1>();
-        } else {
+        else
             cp_async_wait<0>();
-        }
         __syncthreads();   // every thread's pieces of stage g have landed
         const uint8_t* buf = stage_mem + (g & 1) * S * row_bytes;
         const int ra = r0 + g * S, nr = min(S, r1 - ra);
@@ -262,6 +268,7 @@ __global__ void __launch_bounds__(32 * SM_MAX_WARPS)
             }
         }
         __syncthreads();   // stage buffer g & 1 is refilled next
+        if (g + 2 < nstage) issue_stage(g + 2);
     }
 }
 
@@ -293,6 +300,25 @@ cudaError_t small_occupancy(const void* kernel, int wt, int mt, int nb, int thre
     return cudaSuccess;
 }
 
+// A programmatic dependent launch of the small-M kernel: its CTAs may start
+// (and fetch weights) while the preceding kernel in the stream finishes; the
+// kernel waits for that grid before it reads the activations.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), int grid, int threads, size_t smem, cudaStream_t st,
+                             Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);   // (arguments converted to the parameter types)
+}
+
 template <int WT>
 cudaError_t launch_small_wt(const uint8_t* w, int64_t ldw, int N, int nb, const int8_t* xqs, const float* xd,
                             const int16_t* xbs, int M, float* y, int64_t ldy, int sm_count, cudaStream_t st) {
@@ -316,8 +342,8 @@ cudaError_t launch_small_wt(const uint8_t* w, int64_t ldw, int N, int nb, const 
         int stage_rows = static_cast<int>((rpc + 1) / 2);                                               \
         if (stage_rows > max_rows) stage_rows = max_rows;                                               \
         if (stage_rows < 1) stage_rows = 1;                                                             \
-        k<<<static_cast<int>(grid), threads, smem, st>>>(w, ldw, N, nb, xqs, xd, xbs, y, ldy, stage_rows); \
-        return cudaGetLastError();                                                                      \
+        return launch_dependent(k, static_cast<int>(grid), threads, smem, st, w,                        \
+                                ldw, N, nb, xqs, xd, xbs, y, ldy, stage_rows);                          \
     }
     switch (M) {
         QG_SMALL_CASE(1)
