@@ -19,7 +19,7 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG_DIR, "libqgemm.so")
 
 QGEMM_OK, QGEMM_EINVAL, QGEMM_EALIGN, QGEMM_EUNSUPPORTED, QGEMM_ECUDA, QGEMM_EDEVICE = range(6)
-QGEMM_DEV_TIMEOUT, QGEMM_DEV_Q4K_RANGE, QGEMM_DEV_Q6K_SCALE = 0x1, 0x2, 0x4
+QGEMM_DEV_TIMEOUT, QGEMM_DEV_Q4K_RANGE, QGEMM_DEV_Q6K_SCALE, QGEMM_DEV_BAD_EXPERT = 0x1, 0x2, 0x4, 0x8
 QGEMM_OPT_SMALL_M_MAX, QGEMM_OPT_FORCE_BM, QGEMM_OPT_FORCE_SPLITS = 0, 1, 2
 QGEMM_SMALL_M_DEFAULT = 8   # the library's default for QGEMM_OPT_SMALL_M_MAX
 
@@ -35,7 +35,8 @@ class QgemmError(RuntimeError):
 
 class _Counters(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
-                ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small", "q6k_prepack", "split_k")]
+                ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small", "q6k_prepack", "split_k",
+                 "routed")]
 
 
 _lib = None
@@ -63,6 +64,9 @@ def lib() -> ctypes.CDLL:
             "qgemm_quantize_q8k_prep": ([vp, i64, i64, i64, vp, vp, vp, vp, sz, vp], i32),
             "qgemm_q4k_prepared": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
             "qgemm_q6k_prepared": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
+            "qgemm_id_workspace_bytes": ([i64, i64, i64, i64], sz),
+            "qgemm_q4k_id": ([vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, i64, vp, sz, vp], i32),
+            "qgemm_q6k_id": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, i64, vp, sz, vp], i32),
             "qgemm_get_counters": ([ctypes.POINTER(_Counters)], i32),
             "qgemm_reset_counters": ([], i32),
             "qgemm_get_device_status": ([ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)], i32),
@@ -224,6 +228,45 @@ def qgemm_q6k_prepared(w_packed: torch.Tensor, N: int, K: int, x: Q8K, workspace
         y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
     _check(lib().qgemm_q6k_prepared(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
                                     y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return y
+
+
+def qgemm_id_workspace_bytes(M: int, top_k: int, experts: int, K: int) -> int:
+    return int(lib().qgemm_id_workspace_bytes(M, top_k, experts, K))
+
+
+def qgemm_q4k_id(w: torch.Tensor, experts: int, N: int, K: int, x: Q8K, ids: torch.Tensor,
+                 y: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Expert-routed GEMM: w uint8 [experts * N, ldw] Q4_K rows (expert e = rows e*N ..),
+    ids int32 [M, top_k]; returns Y fp32 [M * top_k, N], row i*top_k + s = W_{ids[i, s]} x_i."""
+    assert w.dtype == torch.uint8 and w.dim() == 2 and w.stride(1) == 1
+    assert ids.dtype == torch.int32 and ids.dim() == 2 and ids.is_contiguous()
+    M, top_k = ids.shape
+    assert M == x.M
+    if y is None:
+        y = torch.empty((M * top_k, N), dtype=torch.float32, device=x.qs.device)
+    if workspace is None:
+        workspace = torch.empty(max(qgemm_id_workspace_bytes(M, top_k, experts, K), 256), dtype=torch.uint8,
+                                device=x.qs.device)
+    _check(lib().qgemm_q4k_id(_ptr(w), experts, N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M,
+                              _ptr(ids), top_k, _ptr(y), y.stride(0), _ptr(workspace), workspace.numel(),
+                              _stream(stream)))
+    return y
+
+
+def qgemm_q6k_id(w_packed: torch.Tensor, experts: int, N: int, K: int, x: Q8K, ids: torch.Tensor,
+                 y: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """As qgemm_q4k_id, with the experts' Q6_K rows repacked by qgemm_q6k_prepack (N = experts * N)."""
+    assert ids.dtype == torch.int32 and ids.dim() == 2 and ids.is_contiguous()
+    M, top_k = ids.shape
+    assert M == x.M
+    if y is None:
+        y = torch.empty((M * top_k, N), dtype=torch.float32, device=x.qs.device)
+    if workspace is None:
+        workspace = torch.empty(max(qgemm_id_workspace_bytes(M, top_k, experts, K), 256), dtype=torch.uint8,
+                                device=x.qs.device)
+    _check(lib().qgemm_q6k_id(_ptr(w_packed), experts, N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(ids),
+                              top_k, _ptr(y), y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
 

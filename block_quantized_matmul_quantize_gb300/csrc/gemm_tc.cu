@@ -302,7 +302,9 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_work = wk.items;
+    // routed mode: the work list comes from the preceding (routing) grid
+    if (wk.experts > 0) griddep_wait();
+    const int num_work = wk.experts > 0 ? wk.n_tiles * wk.tile_off[wk.experts] : wk.items;
 
     auto b_stage = [&](int s) { return smem + L::OFF_B + s * L::B_STAGE; };
     auto raw_slot = [&](int r) { return smem + L::OFF_RAW + r * L::RAW; };
@@ -312,6 +314,24 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     // (cut tiles: cut = index among the cut tiles, part = its K part; -1 for whole tiles)
     auto work_cut = [&](int wi, int& n0, int& m0, int& kb0, int& kb1, int& cut, int& part) {
         int tile;
+        if (wk.experts > 0) {
+            // routed: item = (weight tile, global token tile); token tiles vary
+            // fastest; the expert is the one whose tile range holds the token tile
+            const int tt = wk.tile_off[wk.experts];
+            const int nt = wi / tt, gm = wi - nt * tt;
+            int lo = 0, hi = wk.experts - 1;   // largest e with tile_off[e] <= gm
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (wk.tile_off[mid] <= gm) lo = mid; else hi = mid - 1;
+            }
+            n0 = lo * N + nt * BN;   // weight rows of expert lo, stacked
+            m0 = wk.row_off[lo] + (gm - wk.tile_off[lo]) * BM;
+            kb0 = 0;
+            kb1 = nb;
+            cut = -1;
+            part = 0;
+            return;
+        }
         if (wi < wk.full_items) {
             tile = wi;
             cut = -1;
@@ -836,6 +856,21 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                     for (int j = 0; j < CPT; ++j) acc[j] += __ldcg(base + p2 * (BN * BM) + j * BN);
                 }
                 if (warp == W_EPI0 && lane == 0) wk.counters[cut] = 0;   // ready for the next call
+            }
+            if (wk.experts > 0) {
+                // routed: column n of the expert, token rows up to the expert's end,
+                // each written to its output row
+                const int e = n0 / N;
+                const int n = n0 - e * N + row;
+                const int m_end = wk.row_end[e];
+                if (!*abort_flag && n < N) {
+#pragma unroll
+                    for (int j = 0; j < CPT; ++j) {
+                        const int m = m0 + col0 + j;
+                        if (m < m_end) y[static_cast<int64_t>(wk.perm[m]) * ldy + n] = acc[j];
+                    }
+                }
+                continue;
             }
             const int n = n0 + row;
             if (!*abort_flag && n < N) {

@@ -14,6 +14,7 @@ enum : uint32_t {
     ST_TIMEOUT = 1u << 0,       // an mbarrier wait gave up (pipeline broken)
     ST_Q4K_RANGE = 1u << 1,     // Q4_K block with |dmin/d| too large for the fp16 correction operand
     ST_Q6K_SCALE = 1u << 2,     // Q6_K sub-scale with |sc| > 64 (fp16 operand not exact)
+    ST_BAD_EXPERT = 1u << 3,    // routed GEMM: an expert id outside [0, E) (that row is skipped)
 };
 // The status lives in two words: [0] = OR of the bits above, [1] = 1 + the
 // site id of the first wait that timed out (0 = none).
@@ -39,6 +40,30 @@ cudaError_t launch_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ld
 cudaError_t launch_xprep(const int8_t* qs, const float* d, const int16_t* bsums, int64_t M, int64_t K,
                          __half* xh, __half* xbs, float* dxT, int64_t Mp, int* counters, cudaStream_t s);
 
+// Expert routing (route.cu) for the routed GEMM (MUL_MAT_ID): the P = M *
+// top_k (token, slot) pairs are grouped by expert id.  Each expert's rows
+// start on a multiple of 4 (the GEMM loads the transposed scales with TMA,
+// whose innermost coordinate must be 16-byte aligned), so there are at most
+// P + 3E routed rows, the gaps being padding.  One CTA writes
+//   row_off [E + 1]  first routed row of each expert; row_off[E] = total rows;
+//   row_end [E]      one past the expert's last row (row_off[e] + its pairs);
+//   tile_off[E + 1]  prefix of bm-row token tiles per expert;
+//   perm    [rows]   the pair index (token * top_k + slot) of each routed row,
+//                    -1 for padding rows,
+// and ORs ST_BAD_EXPERT into status for ids outside [0, E) (those pairs get
+// no routed row).  The order of the pairs within an expert is not fixed; no
+// output value depends on it.
+constexpr int ROUTE_MAX_EXPERTS = 1024;
+inline int64_t routed_rows_max(int64_t P, int64_t E) { return P + 3 * E; }
+cudaError_t launch_route(const int32_t* ids, int64_t P, int E, int bm, int* row_off, int* row_end, int* tile_off,
+                         int* perm, uint32_t* status, cudaStream_t s);
+// The operand planes of the routed rows: row p of xh / xbs / dxT holds token
+// perm[p] / top_k's Q8_K values (as launch_xprep writes them); padding rows
+// and rows p >= row_off[E] up to Pp are zero.
+cudaError_t launch_xgather(const int8_t* qs, const float* d, const int16_t* bsums, int64_t K, int top_k,
+                           const int* perm, const int* rows_valid, int64_t P, __half* xh, __half* xbs, float* dxT,
+                           int64_t Pp, cudaStream_t s);
+
 // Work items of the tile GEMM: the first `full_items` tiles (token tiles
 // varying fastest) whole, then each remaining tile cut into `parts` K ranges.
 // A cut tile's parts write fp32 partial tiles to `partials` (slot = (tile -
@@ -53,6 +78,14 @@ struct TcWork {
     int items;            // full_items + (tiles - full_items) * parts
     float* partials;
     int* counters;
+    // Expert-routed GEMM (experts > 0): the token rows are the routed rows,
+    // grouped by expert; the work list is read from device memory (written by
+    // the routing kernel that precedes the GEMM).  No cut tiles in this mode.
+    int experts;          // E (0: the plain GEMM)
+    const int* tile_off;  // [E + 1] prefix of token tiles per expert
+    const int* row_off;   // [E + 1] first routed row of each expert (a multiple of 4)
+    const int* row_end;   // [E] one past the expert's last routed row
+    const int* perm;      // [rows] output row of each routed row
 };
 constexpr int TC_MAX_CUT_TILES = 1024;   // counters in a workspace
 

@@ -31,8 +31,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ------------------------------------------------------------ global state
-std::atomic<uint64_t> g_cnt[8];
-enum { C_QUANT, C_XPREP, C_Q4K_TC, C_Q6K_TC, C_Q4K_SMALL, C_Q6K_SMALL, C_PREPACK, C_SPLITK };
+std::atomic<uint64_t> g_cnt[9];
+enum { C_QUANT, C_XPREP, C_Q4K_TC, C_Q6K_TC, C_Q4K_SMALL, C_Q6K_SMALL, C_PREPACK, C_SPLITK, C_ROUTED };
 // SMALL_M_MAX defaults to the measured crossover: the streaming kernel wins up
 // to 8 tokens at K = N = 5120 and at K = 4096, N = 14336.
 std::atomic<int64_t> g_opt[3] = {{qg::SMALL_M_LIMIT}, {0}, {0}};
@@ -326,6 +326,123 @@ bool use_small(int wtype, int64_t M, int64_t K) {
     return M <= g_opt[QGEMM_OPT_SMALL_M_MAX].load() && qg::small_supported(wtype, M, K);
 }
 
+// ---- routed GEMM (MUL_MAT_ID): workspace = routing arrays, then the operand
+// planes of the P = M * top_k routed rows.
+struct IdWs {
+    int* row_off;    // [E + 1]
+    int* row_end;    // [E]
+    int* tile_off;   // [E + 1]
+    int* perm;       // [R], R = routed_rows_max(P, E)
+    __half* xh;      // [P][K]
+    __half* xbs;     // [P][K/16]
+    float* dxT;      // [nb][Pp]
+    int64_t Pp;
+};
+// routed rows (pairs plus per-expert padding to a multiple of 4) and their planes
+size_t id_route_bytes(int64_t P, int64_t E) {
+    return 3 * align256(size_t(E + 1) * 4) + align256(size_t(qg::routed_rows_max(P, E)) * 4);
+}
+IdWs id_ws(void* ws, int64_t P, int64_t E, int64_t K) {
+    const int64_t R = qg::routed_rows_max(P, E);
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    const size_t a = align256(size_t(E + 1) * 4);
+    IdWs w{};
+    w.row_off = reinterpret_cast<int*>(b);
+    w.row_end = reinterpret_cast<int*>(b + a);
+    w.tile_off = reinterpret_cast<int*>(b + 2 * a);
+    w.perm = reinterpret_cast<int*>(b + 3 * a);
+    uint8_t* planes = b + id_route_bytes(P, E);
+    w.Pp = (R + 3) / 4 * 4;
+    w.xh = reinterpret_cast<__half*>(planes);
+    w.xbs = reinterpret_cast<__half*>(planes + align256(size_t(R) * K * 2));
+    w.dxT = reinterpret_cast<float*>(planes + align256(size_t(R) * K * 2) + align256(size_t(R) * (K / 16) * 2));
+    return w;
+}
+// token-tile width from the mean number of routed rows per expert
+int id_bm(int64_t P, int64_t E) {
+    const int64_t fbm = g_opt[QGEMM_OPT_FORCE_BM].load();
+    if (fbm == 16 || fbm == 32 || fbm == 64 || fbm == 128) return static_cast<int>(fbm);
+    const int64_t avg = (P + E - 1) / E;
+    return avg <= 16 ? 16 : avg <= 32 ? 32 : avg <= 64 ? 64 : 128;
+}
+
+int run_id(int wtype, const void* w, int64_t E, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs,
+           const float* xd, const int16_t* xbsums, int64_t M, const int32_t* ids, int64_t top_k, float* y,
+           int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    DevState* ds = nullptr;
+    int rc = device_state(&ds);
+    if (rc) return rc;
+    const int64_t P = M * top_k;
+    const size_t need = qgemm_id_workspace_bytes(M, top_k, E, K);
+    if (!ws || ws_bytes < need)
+        return fail(QGEMM_EINVAL, "workspace of %zu bytes needed (got %zu)", need, ws ? ws_bytes : size_t(0));
+    if (!aligned(ws, 256)) return fail(QGEMM_EALIGN, "workspace must be 256-byte aligned");
+    const IdWs iw = id_ws(ws, P, E, K);
+    const int bm = id_bm(P, E);
+    const int64_t nb = K / 256;
+
+    const int64_t R = qg::routed_rows_max(P, E);
+    cudaError_t e = qg::launch_route(ids, P, static_cast<int>(E), bm, iw.row_off, iw.row_end, iw.tile_off, iw.perm,
+                                     ds->status, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "routing launch");
+    e = qg::launch_xgather(xqs, xd, xbsums, K, static_cast<int>(top_k), iw.perm, iw.row_off + E, R, iw.xh, iw.xbs,
+                           iw.dxT, iw.Pp, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "routed operand gather launch");
+
+    CUtensorMap tm_w, tm_xh, tm_xbs, tm_dx;
+    const int blk = wtype == 4 ? qg::Q4K_BLOCK : qg::Q6K_PACKED;
+    // the experts' weight rows stacked: E * N rows of the same row stride
+    if ((rc = make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, uint64_t(nb) * blk, E * N, ldw, blk, 128,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return rc;
+    if ((rc = make_map(&tm_xh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, iw.xh, K, R, uint64_t(K) * 2, 64, bm,
+                       CU_TENSOR_MAP_SWIZZLE_128B)))
+        return rc;
+    if ((rc = make_map(&tm_xbs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, iw.xbs, K / 16, R, uint64_t(K / 16) * 2, 16, bm,
+                       CU_TENSOR_MAP_SWIZZLE_32B)))
+        return rc;
+    if ((rc = make_map(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, iw.dxT, iw.Pp, nb, uint64_t(iw.Pp) * 4, bm, 1,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return rc;
+
+    qg::TcLaunch a{};
+    a.wtype = wtype;
+    a.bm = bm;
+    a.M = R;
+    a.N = N;
+    a.K = K;
+    a.work.n_tiles = static_cast<int>((N + 127) / 128);
+    a.work.m_tiles = 0;
+    a.work.parts = 1;
+    // the routed work list is read on the device; the grid is sized for its bound
+    const int64_t bound = int64_t(a.work.n_tiles) * ((P + bm - 1) / bm + E);
+    if (bound >= (int64_t(1) << 31)) return fail(QGEMM_EUNSUPPORTED, "routed work list too long");
+    a.work.full_items = static_cast<int>(bound);
+    a.work.items = static_cast<int>(bound);
+    a.work.experts = static_cast<int>(E);
+    a.work.tile_off = iw.tile_off;
+    a.work.row_off = iw.row_off;
+    a.work.row_end = iw.row_end;
+    a.work.perm = iw.perm;
+    a.sm_count = ds->sm_count;
+    a.y = y;
+    a.ldy = ldy;
+    a.status = ds->status;
+    a.tm_w = &tm_w;
+    a.tm_xh = &tm_xh;
+    a.tm_xbs = wtype == 4 ? &tm_xbs : nullptr;
+    a.tm_dx = &tm_dx;
+    cudaEvent_t evb = g_ev_before.load(), eva = g_ev_after.load();
+    if (evb) cudaEventRecord(evb, stream);
+    e = qg::launch_gemm_tc(a, stream);
+    if (eva) cudaEventRecord(eva, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "routed tile GEMM launch");
+    g_cnt[wtype == 4 ? C_Q4K_TC : C_Q6K_TC]++;
+    g_cnt[C_ROUTED]++;
+    return QGEMM_OK;
+}
+
+
 }  // namespace
 
 namespace qg {
@@ -374,6 +491,21 @@ static int gemm_common_checks(const void* w, int64_t N, int64_t K, const int8_t*
     if (!y) return fail(QGEMM_EINVAL, "y is null");
     if (ldy < N) return fail(QGEMM_EINVAL, "ldy (%lld) < N (%lld)", (long long)ldy, (long long)N);
     if (!aligned(y, 4)) return fail(QGEMM_EALIGN, "y must be 4-byte aligned");
+    return QGEMM_OK;
+}
+
+static int id_checks(const void* w, int64_t E, int64_t N, int64_t K, const int8_t* xqs, const float* xd,
+              const int16_t* xbsums, int64_t M, const int32_t* ids, int64_t top_k, float* y, int64_t ldy) {
+    int rc = gemm_common_checks(w, N, K, xqs, xd, xbsums, M, y, ldy);
+    if (rc) return rc;
+    if (E < 1 || E > qg::ROUTE_MAX_EXPERTS)
+        return fail(QGEMM_EINVAL, "experts must be in 1..%d (got %lld)", qg::ROUTE_MAX_EXPERTS, (long long)E);
+    if (top_k < 1) return fail(QGEMM_EINVAL, "top_k must be >= 1 (got %lld)", (long long)top_k);
+    if (E * N >= (int64_t(1) << 31)) return fail(QGEMM_EUNSUPPORTED, "experts * N must be below 2^31");
+    if (M * top_k >= (int64_t(1) << 31)) return fail(QGEMM_EUNSUPPORTED, "M * top_k must be below 2^31");
+    if (M == 0) return QGEMM_OK;
+    if (!ids) return fail(QGEMM_EINVAL, "ids is null");
+    if (!aligned(ids, 4)) return fail(QGEMM_EALIGN, "ids must be 4-byte aligned");
     return QGEMM_OK;
 }
 
@@ -483,7 +615,37 @@ int qgemm_get_counters(qgemm_counters* out) {
     out->q6k_small = g_cnt[C_Q6K_SMALL];
     out->q6k_prepack = g_cnt[C_PREPACK];
     out->split_k = g_cnt[C_SPLITK];
+    out->routed = g_cnt[C_ROUTED];
     return QGEMM_OK;
+}
+
+size_t qgemm_id_workspace_bytes(int64_t M, int64_t top_k, int64_t experts, int64_t K) {
+    if (M <= 0 || top_k < 1 || experts < 1 || K <= 0 || K % 256) return 0;
+    const int64_t P = M * top_k;
+    return id_route_bytes(P, experts) + plane_bytes(qg::routed_rows_max(P, experts), K);
+}
+
+int qgemm_q4k_id(const void* w, int64_t experts, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs,
+                 const float* xd, const int16_t* xbsums, int64_t M, const int32_t* ids, int64_t top_k, float* y,
+                 int64_t ldy, void* workspace, size_t workspace_bytes, qgemm_stream_t stream) {
+    clear_err();
+    int rc = id_checks(w, experts, N, K, xqs, xd, xbsums, M, ids, top_k, y, ldy);
+    if (rc || M == 0) return rc;
+    if (ldw < (K / 256) * qg::Q4K_BLOCK) return fail(QGEMM_EINVAL, "ldw smaller than a row of Q4_K blocks");
+    if (ldw % 16 != 0) return fail(QGEMM_EALIGN, "ldw must be a multiple of 16 bytes");
+    return run_id(4, w, experts, N, K, ldw, xqs, xd, xbsums, M, ids, top_k, y, ldy, workspace, workspace_bytes,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+int qgemm_q6k_id(const void* w_packed, int64_t experts, int64_t N, int64_t K, const int8_t* xqs, const float* xd,
+                 const int16_t* xbsums, int64_t M, const int32_t* ids, int64_t top_k, float* y, int64_t ldy,
+                 void* workspace, size_t workspace_bytes, qgemm_stream_t stream) {
+    clear_err();
+    int rc = id_checks(w_packed, experts, N, K, xqs, xd, xbsums, M, ids, top_k, y, ldy);
+    if (rc || M == 0) return rc;
+    const int64_t ldw = (K / 256) * qg::Q6K_PACKED;
+    return run_id(6, w_packed, experts, N, K, ldw, xqs, xd, xbsums, M, ids, top_k, y, ldy, workspace,
+                  workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int qgemm_reset_counters(void) {

@@ -162,6 +162,38 @@ QGEMM_API int qgemm_q6k_prepared(const void *w_packed, int64_t N, int64_t K, con
                                  const int16_t *xbsums, int64_t M, float *y, int64_t ldy, const void *workspace,
                                  size_t workspace_bytes, qgemm_stream_t stream);
 
+/* ------------------------------------ expert-routed GEMM (MUL_MAT_ID) ----
+ * The routed form of the GEMM that the pages test beside MUL_MAT (llama.cpp
+ * PR #214 "cuda: branch-free PTQ1_0 MMQ tile loader ...", test-backend-ops
+ * MUL_MAT_ID): E experts of N weight rows each, stored back to back (expert
+ * e's rows are rows e*N .. e*N+N-1 of one weight matrix), and for every token
+ * i and slot s < top_k an expert id; the output row of pair (i, s) is
+ *     Y[i*top_k + s][n] = sum_k W[ids[i*top_k + s]*N + n][k] * X_q8k[i][k]
+ * with the same accuracy bound as qgemm_q4k (per output element, c_b the
+ * contributions of expert ids[i][s]'s row n).
+ *   w, ldw      as qgemm_q4k, E*N rows (Q6_K: the 224-B repacked blocks of all
+ *               E*N rows, qgemm_q6k_prepack with N = E*N).
+ *   experts     E, 1..1024.   N, K, xqs, xd, xbsums, M: as qgemm_q4k.
+ *   ids         device, int32 [M][top_k], 4-B aligned; ids outside [0, E) set
+ *               device status QGEMM_DEV_BAD_EXPERT and their output rows are
+ *               left untouched.
+ *   top_k       slots per token, >= 1;  M * top_k and E * N below 2^31.
+ *   y           device, fp32 [M * top_k][ldy], ldy >= N, 4-B aligned.
+ *   workspace   >= qgemm_id_workspace_bytes(M, top_k, E, K), 256-B aligned:
+ *               the routing (pairs grouped by expert) and the operand planes of
+ *               the M * top_k routed rows.
+ * Three launches: routing, operand gather, and one tile GEMM over all
+ * experts (a token tile never mixes experts; the epilogue writes each row to
+ * its pair).  Y does not depend on the order of the pairs within an expert.
+ * Errors: as qgemm_q4k. */
+QGEMM_API size_t qgemm_id_workspace_bytes(int64_t M, int64_t top_k, int64_t experts, int64_t K);
+QGEMM_API int qgemm_q4k_id(const void *w, int64_t experts, int64_t N, int64_t K, int64_t ldw, const int8_t *xqs,
+                           const float *xd, const int16_t *xbsums, int64_t M, const int32_t *ids, int64_t top_k,
+                           float *y, int64_t ldy, void *workspace, size_t workspace_bytes, qgemm_stream_t stream);
+QGEMM_API int qgemm_q6k_id(const void *w_packed, int64_t experts, int64_t N, int64_t K, const int8_t *xqs,
+                           const float *xd, const int16_t *xbsums, int64_t M, const int32_t *ids, int64_t top_k,
+                           float *y, int64_t ldy, void *workspace, size_t workspace_bytes, qgemm_stream_t stream);
+
 /* -------------------------------------------- allocation-free Q4_K GEMM ----
  * The pages have no counterpart to this call; it serves callers that cannot
  * allocate device memory where they call the GEMM (for example a plugin
@@ -204,6 +236,7 @@ typedef struct {
     uint64_t q6k_small;    /* Q6_K small-M streaming launches       */
     uint64_t q6k_prepack;  /* Q6_K repack launches                  */
     uint64_t split_k;      /* GEMM launches with cut tiles (K parts) */
+    uint64_t routed;       /* expert-routed GEMM launches (_id)     */
 } qgemm_counters;
 QGEMM_API int qgemm_get_counters(qgemm_counters *out);
 QGEMM_API int qgemm_reset_counters(void);
@@ -212,6 +245,7 @@ QGEMM_API int qgemm_reset_counters(void);
 #define QGEMM_DEV_TIMEOUT 0x1u   /* a pipeline wait gave up (bounded waits) */
 #define QGEMM_DEV_Q4K_RANGE 0x2u /* a Q4_K block had |dmin/d| > 1000        */
 #define QGEMM_DEV_Q6K_SCALE 0x4u /* a Q6_K sub-scale had |sc| > 64          */
+#define QGEMM_DEV_BAD_EXPERT 0x8u /* a routed GEMM id was outside [0, E)    */
 /* Synchronizes the device, returns the status bits in *bits and the site of
  * the first timed-out wait (0 = none) in *site (may be NULL), then clears
  * both.  QGEMM_ECUDA if the device is unusable. */

@@ -67,6 +67,7 @@ class Oracle:
         L.oracle_gemm_q4k.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, vp]
         L.oracle_gemm_q6k.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, vp]
         L.oracle_brute.argtypes = [ctypes.c_int, vp, i64, i64, i64, vp, vp, i64, vp]
+        L.oracle_gemm_id.argtypes = [ctypes.c_int, vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, vp]
         for f in ("oracle_q4k_fields", "oracle_q4k_pack", "oracle_q6k_fields",
                   "oracle_q6k_pack", "oracle_dequant_q4k", "oracle_dequant_q6k",
                   "oracle_quantize_q8k", "oracle_q8k_to_aos", "oracle_q8k_from_aos",
@@ -155,6 +156,24 @@ class Oracle:
         y = np.zeros((R, N)); absc = np.zeros((R, N))
         fn = self.L.oracle_gemm_q4k if wtype == 4 else self.L.oracle_gemm_q6k
         fn(_p(w), N, K, w.shape[1], _p(qs), _p(d), _p(bs), M, _p(rows_arr), R, _p(y), _p(absc))
+        return y, absc
+
+    def gemm_id(self, wtype: int, w: np.ndarray, E: int, K: int, qs, d, bs, ids):
+        """w uint8 [E*N, row bytes] (E experts stacked); ids int32 [M, top_k].
+        Returns (y fp64 [M*top_k, N], absc fp64 [M*top_k, N]); rows of ids outside
+        [0, E) stay NaN."""
+        w = np.ascontiguousarray(w, np.uint8)
+        assert w.shape[0] % E == 0
+        N = w.shape[0] // E
+        qs = np.ascontiguousarray(qs, np.int8)
+        d = np.ascontiguousarray(d, np.float32)
+        bs = np.ascontiguousarray(bs, np.int16)
+        ids = np.ascontiguousarray(ids, np.int32)
+        M, top_k = ids.shape
+        assert qs.shape[0] == M
+        y = np.full((M * top_k, N), np.nan); absc = np.full((M * top_k, N), np.nan)
+        self.L.oracle_gemm_id(int(wtype), _p(w), E, N, K, w.shape[1], _p(qs), _p(d), _p(bs), M, _p(ids), top_k,
+                              _p(y), _p(absc))
         return y, absc
 
     def brute(self, wtype: int, w: np.ndarray, K: int, qs, d) -> np.ndarray:

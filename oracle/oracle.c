@@ -349,6 +349,27 @@ void oracle_gemm_q6k(const uint8_t *w, int64_t N, int64_t K, int64_t ldw,
     free(own);
 }
 
+void oracle_gemm_id(int type, const uint8_t *w, int64_t E, int64_t N, int64_t K, int64_t ldw,
+                    const int8_t *qs, const float *dx, const int16_t *bsums, int64_t M,
+                    const int32_t *ids, int64_t top_k, double *y, double *absc)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t s = 0; s < top_k; ++s) {
+            const int64_t pair = m * top_k + s;
+            const int64_t e = ids[pair];
+            if (e < 0 || e >= E)
+                continue;
+            /* expert e's rows, token m only */
+            const uint8_t *we = w + e * N * ldw;
+            double *yr = y + pair * N;
+            double *ar = absc ? absc + pair * N : NULL;
+            if (type == 4)
+                oracle_gemm_q4k(we, N, K, ldw, qs, dx, bsums, M, &m, 1, yr, ar);
+            else
+                oracle_gemm_q6k(we, N, K, ldw, qs, dx, bsums, M, &m, 1, yr, ar);
+        }
+}
+
 void oracle_brute(int type, const uint8_t *w, int64_t N, int64_t K, int64_t ldw,
                   const int8_t *qs, const float *dx, int64_t M, double *y)
 {

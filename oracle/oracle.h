@@ -95,6 +95,17 @@ void oracle_gemm_q6k(const uint8_t *w, int64_t N, int64_t K, int64_t ldw,
                      int64_t M, const int64_t *rows, int64_t nrows,
                      double *y, double *absc);
 
+/* Expert-routed GEMM (MUL_MAT_ID, tested beside MUL_MAT on the page
+ * "cuda: branch-free PTQ1_0 MMQ tile loader ..." (llama.cpp PR #214)):
+ * w holds E experts of N rows each, back to back (expert e = rows e*N ..
+ * e*N+N-1); for token m and slot s the expert e = ids[m*top_k + s] and
+ *   y[m*top_k + s][n] = the row-n, token-m output of expert e's GEMM above.
+ * Pairs whose id is outside [0, E) are left as they are in y (and absc).
+ * type 4 = Q4_K (ldw row stride), 6 = Q6_K (210-B blocks). */
+void oracle_gemm_id(int type, const uint8_t *w, int64_t E, int64_t N, int64_t K, int64_t ldw,
+                    const int8_t *qs, const float *dx, const int16_t *bsums, int64_t M,
+                    const int32_t *ids, int64_t top_k, double *y, double *absc);
+
 /* Brute force: dequantize W and X to fp64, then a plain triple loop.
  * type 4 = Q4_K, 6 = Q6_K.  y[M][N]. */
 void oracle_brute(int type, const uint8_t *w, int64_t N, int64_t K, int64_t ldw,

@@ -115,6 +115,18 @@ def gen_x(M: int, K: int, seed: int, sigma: float = 1.0, outlier_frac: float = 0
     return x
 
 
+def gen_ids(M: int, top_k: int, E: int, seed: int, skew: float = 0.0) -> np.ndarray:
+    """Expert ids int32 [M, top_k] of a synthetic router: per token, top_k
+    distinct experts drawn without replacement with weights (e+1)^-skew
+    (skew 0: uniform), by the keys u^(1/weight) of seeded uniforms u."""
+    assert 1 <= top_k <= E
+    u = uniform01(seed * 4 + 2, M * E).reshape(M, E)
+    wts = (np.arange(1, E + 1, dtype=np.float64)) ** (-skew)
+    keys = np.log(np.maximum(u, 1e-300)) / wts          # log of u^(1/w): order-preserving
+    order = np.argsort(-keys, axis=1, kind="stable")
+    return np.ascontiguousarray(order[:, :top_k]).astype(np.int32)
+
+
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str

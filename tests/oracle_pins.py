@@ -354,6 +354,40 @@ def check_gemm_rows_subset(orc):
     assert np.array_equal(y[rows], y2) and np.array_equal(a[rows], a2)
 
 
+def check_gemm_id_vs_brute(orc):
+    """Routed GEMM: row (m, s) equals expert ids[m, s]'s brute-force row m
+    (dequantized fp64 weights of that expert's N rows, then a plain dot)."""
+    r = _rng(23)
+    for wtype in (4, 6):
+        E, N, K, M, topk = 3, 4, 512, 5, 2
+        gen = synth.gen_q4k if wtype == 4 else synth.gen_q6k
+        w = gen(E * N, K, int(r.integers(1 << 30)))
+        qs, d, bs = orc.quantize_q8k(synth.gen_x(M, K, int(r.integers(1 << 30))))
+        ids = r.integers(0, E, (M, topk)).astype(np.int32)
+        ids[0] = [2, 2]                       # one token, the same expert twice
+        y, a = orc.gemm_id(wtype, w, E, K, qs, d, bs, ids)
+        for m in range(M):
+            for s in range(topk):
+                e = int(ids[m, s])
+                yb = orc.brute(wtype, w[e * N:(e + 1) * N], K, qs, d)[m]
+                row = m * topk + s
+                assert np.all(np.abs(y[row] - yb) <= 1e-12 * a[row] + 1e-300), (wtype, m, s)
+
+
+def check_gemm_id_bad_ids_and_slots(orc):
+    """Ids outside [0, E) leave their rows untouched; swapping a token's slots swaps its rows."""
+    E, N, K, M = 2, 3, 256, 3
+    w = synth.gen_q4k(E * N, K, 24)
+    qs, d, bs = orc.quantize_q8k(synth.gen_x(M, K, 25))
+    ids = np.array([[0, 1], [-1, 1], [1, E]], np.int32)
+    y, _ = orc.gemm_id(4, w, E, K, qs, d, bs, ids)
+    assert np.isnan(y[2]).all() and np.isnan(y[5]).all()
+    assert np.isfinite(y[[0, 1, 3, 4]]).all()
+    y2, _ = orc.gemm_id(4, w, E, K, qs, d, bs, ids[:, ::-1].copy())
+    assert np.array_equal(y[0], y2[1]) and np.array_equal(y[1], y2[0])
+    assert not np.array_equal(y[0], y[1])   # the two experts differ
+
+
 ALL_CHECKS = [
     check_half_decode,
     check_q4k_scale_bytes_hand, check_q4k_nibble_bytes_hand, check_q4k_roundtrip,
@@ -363,5 +397,5 @@ ALL_CHECKS = [
     check_q8k_matches_numpy_rounding, check_q8k_aos_roundtrip,
     check_gemm_vs_brute, check_gemm_unit_scales_q4k, check_gemm_zero_quants_q4k,
     check_gemm_subblock_scales_q4k, check_gemm_q6k_offset, check_gemm_q6k_subblock_scales,
-    check_gemm_rows_subset,
+    check_gemm_rows_subset, check_gemm_id_vs_brute, check_gemm_id_bad_ids_and_slots,
 ]

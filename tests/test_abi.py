@@ -111,6 +111,31 @@ def test_gemm_validation(L):
     assert L.qgemm_q6k_prepack(FAKE, 4, 256, 210, MISALIGNED, None) == qg.QGEMM_EALIGN
 
 
+def test_routed_validation(L):
+    F, H = L.qgemm_q4k_id, L.qgemm_q6k_id
+    ids_bad = ctypes.c_void_p(0x100002)
+
+    def q4(E=8, N=128, K=512, ldw=288, M=4, ids=FAKE, top_k=2, y=FAKE, ldy=128):
+        return F(FAKE, E, N, K, ldw, FAKE, FAKE, FAKE, M, ids, top_k, y, ldy, FAKE, 1 << 20, None)
+    assert q4(E=0) == qg.QGEMM_EINVAL
+    assert q4(E=1025) == qg.QGEMM_EINVAL
+    assert q4(top_k=0) == qg.QGEMM_EINVAL
+    assert q4(ids=None) == qg.QGEMM_EINVAL
+    assert q4(ids=ids_bad) == qg.QGEMM_EALIGN
+    assert q4(K=300) == qg.QGEMM_EINVAL
+    assert q4(ldw=296) == qg.QGEMM_EALIGN
+    assert q4(ldy=100) == qg.QGEMM_EINVAL
+    assert q4(E=8, N=1 << 28, ldy=1 << 28) == qg.QGEMM_EUNSUPPORTED   # E * N >= 2^31
+    assert q4(M=1 << 30, top_k=4) == qg.QGEMM_EUNSUPPORTED   # M * top_k >= 2^31
+    assert q4(M=0) == qg.QGEMM_OK                            # empty: nothing launched
+    assert H(FAKE, 8, 128, 512, FAKE, FAKE, FAKE, 4, FAKE, 0, FAKE, 128, FAKE, 1 << 20, None) == qg.QGEMM_EINVAL
+    # routed rows: 8 pairs + 3 padding rows per expert = 32; routing 3 x 256 B + perm 32 ints (-> 256);
+    # xh 32x512x2, xbs 32x32x2, dxT 2x32x4 (-> 256)
+    assert L.qgemm_id_workspace_bytes(4, 2, 8, 512) == 768 + 256 + 32768 + 2048 + 256
+    assert L.qgemm_id_workspace_bytes(0, 2, 8, 512) == 0
+    assert L.qgemm_id_workspace_bytes(4, 0, 8, 512) == 0
+
+
 def test_size_queries(L):
     assert L.qgemm_workspace_bytes(0, 8, 256) == 0
     assert L.qgemm_workspace_bytes(4, 8, 300) == 0

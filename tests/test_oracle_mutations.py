@@ -26,6 +26,8 @@ MUTATIONS = {
     "gemm_q6k_offset_31": ("dot += (int64_t)sc[j] * (I - 32 * (int64_t)bs[j]);", "dot += (int64_t)sc[j] * (I - 31 * (int64_t)bs[j]);"),
     "gemm_q6k_transposed_x": ("const int8_t *xq = qs + m * K + b * 256;\n                const int16_t *bs = bsums + m * (K / 16) + b * 16;\n                int64_t dot = 0;\n", "const int8_t *xq = qs + m * K + b * 256 + (b > 0 ? -256 : 0);\n                const int16_t *bs = bsums + m * (K / 16) + b * 16;\n                int64_t dot = 0;\n"),
     "gemm_absc_signed": ("absc[r * N + n] += fabs(cb);\n            }\n        }\n    }\n    free(own);\n}\n\nvoid oracle_gemm_q6k", "absc[r * N + n] += cb;\n            }\n        }\n    }\n    free(own);\n}\n\nvoid oracle_gemm_q6k"),
+    "gemm_id_expert_offset": ("const uint8_t *we = w + e * N * ldw;", "const uint8_t *we = w + e * ldw;"),
+    "gemm_id_pair_row": ("const int64_t pair = m * top_k + s;", "const int64_t pair = m + s * M;"),
     "brute_dmin_sign": ("w[i] = d * sc[i / 32] * q[i] - dmin * mn[i / 32];", "w[i] = d * sc[i / 32] * q[i] + dmin * mn[i / 32];"),
 }
 
