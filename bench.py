@@ -53,7 +53,11 @@ NCU_TRAFFIC_BYTES = {"q4k_m512_k2048_n11008_outliers": 15024128}
 
 
 def workloads():
-    return {w.name: w for w in synth.CONFIGS}
+    return {w.name: w for w in synth.CONFIGS + synth.ROUTED_CONFIGS}
+
+
+def routed(wl) -> bool:
+    return isinstance(wl, synth.RoutedWorkload)
 
 
 def measured_peaks():
@@ -144,6 +148,13 @@ def oracle_sample(wl, rows, x=None, w=None):
     w = wl.weights() if w is None else w
     x = wl.x() if x is None else x
     xs = np.ascontiguousarray(x[:rows])
+    if routed(wl):
+        ids = np.ascontiguousarray(wl.ids()[:rows])
+        t = time.perf_counter()
+        qs, d, bs = orc.quantize_q8k(xs)
+        orc.gemm_id(wl.wtype, w, wl.E, wl.K, qs, d, bs, ids)
+        dt = time.perf_counter() - t
+        return dt, 2.0 * rows * wl.top_k * wl.N * wl.K
     t = time.perf_counter()
     qs, d, bs = orc.quantize_q8k(xs)
     orc.gemm(wl.wtype, w, wl.K, qs, d, bs)
@@ -179,9 +190,13 @@ def run_reference(args, world, rank):
 
 
 def config_of(wl):
-    return {"workload": wl.name, "weights": "Q4_K" if wl.wtype == 4 else "Q6_K", "M": wl.M, "K": wl.K,
-            "N": wl.N, "x": f"{wl.sigma}*N(0,1)" + (", 1% columns x8" if wl.outlier_frac else ""),
-            "l2": "flushed before every step (256 MiB write outside the timed events)"}
+    c = {"workload": wl.name, "weights": "Q4_K" if wl.wtype == 4 else "Q6_K", "M": wl.M, "K": wl.K,
+         "N": wl.N, "x": f"{wl.sigma}*N(0,1)" + (", 1% columns x8" if getattr(wl, "outlier_frac", 0) else ""),
+         "l2": "flushed before every step (256 MiB write outside the timed events)"}
+    if routed(wl):
+        c.update({"experts": wl.E, "top_k": wl.top_k, "routing": f"synthetic top-{wl.top_k}, skew {wl.skew}",
+                  "routed_rows": wl.M * wl.top_k})
+    return c
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -225,17 +240,31 @@ def main():
     M, N, K = wl.M, wl.N, wl.K
     w_host, x_host = wl.weights(), wl.x()
     dev = torch.device("cuda", local)
+    is_routed = routed(wl)
+    rows_out = M * wl.top_k if is_routed else M           # output rows (routed: one per token and slot)
     w = torch.from_numpy(w_host).to(dev)
     if wl.wtype == 6:
-        w = qg.qgemm_q6k_prepack(w, N, K)
+        w = qg.qgemm_q6k_prepack(w, w_host.shape[0], K)
     x = torch.from_numpy(x_host).to(dev)
     q = qg.Q8K.empty(M, K, dev)
-    y = torch.empty((M, N), dtype=torch.float32, device=dev)
-    ws = torch.empty(max(qg.qgemm_workspace_bytes(M, N, K), 256), dtype=torch.uint8, device=dev)
+    y = torch.empty((rows_out, N), dtype=torch.float32, device=dev)
+    if is_routed:
+        ids = torch.from_numpy(wl.ids()).to(dev)
+        ws = torch.empty(max(qg.qgemm_id_workspace_bytes(M, wl.top_k, wl.E, K), 256), dtype=torch.uint8, device=dev)
+    else:
+        ws = torch.empty(max(qg.qgemm_workspace_bytes(M, N, K), 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
+        if is_routed:
+            # quantize, then route + gather + one tile GEMM over all experts
+            qg.qgemm_quantize_q8k(x, out=q)
+            if wl.wtype == 4:
+                qg.qgemm_q4k_id(w, wl.E, N, K, q, ids, y=y, workspace=ws)
+            else:
+                qg.qgemm_q6k_id(w, wl.E, N, K, q, ids, y=y, workspace=ws)
+            return
         # quantize, writing the GEMM's operand planes in the same launch, then multiply
         qg.qgemm_quantize_q8k_prep(x, ws, out=q)
         if wl.wtype == 4:
@@ -323,15 +352,17 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         mean_ms, gemm_mean_ms, eager_mean_ms = float(t[0]), float(t[1]), float(t[2])
 
-    ops = 2.0 * M * N * K
+    ops = 2.0 * rows_out * N * K
     value = world * ops / (mean_ms * 1e-3) / 1e12
     # library kernels per step, counted on the eager pass; the graph replays the same ones
+    # (a routed GEMM call is three: routing, operand gather, tile GEMM)
     per_step = sum(c1[k] - c0[k] for k in ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small"))
+    per_step += 2 * (c1["routed"] - c0["routed"])
     launches = per_step  # == K_steps x kernels per step, the count in each of the two timed loops
 
     # ---- end to end through the public API with host buffers
     x_pin = torch.from_numpy(x_host).pin_memory()
-    y_pin = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    y_pin = torch.empty((rows_out, N), dtype=torch.float32).pin_memory()
     e_s = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
     e_e = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
     for _ in range(3):
@@ -360,7 +391,7 @@ def main():
 
     if rank == 0:
         peaks, peak_src = measured_peaks()
-        wbytes = N * (K // 256) * wl.block_bytes
+        wbytes = w_host.shape[0] * (K // 256) * wl.block_bytes   # every expert's rows (routed)
         small = (c1["q4k_small"] + c1["q6k_small"]) > (c0["q4k_small"] + c0["q6k_small"])
         if small:
             # the streaming kernel is bound by the weight bytes it reads once
@@ -387,7 +418,7 @@ def main():
                       else "eager API calls",
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.nbytes),
-                    "d2h_bytes_per_step": int(M * N * 4)},
+                    "d2h_bytes_per_step": int(rows_out * N * 4)},
             "gpu_launches": int(launches),
             "clocks": sampler.summary(t0, t1),
             "device_status": bits,
@@ -402,8 +433,8 @@ def main():
                 runs += 1
             line["cpu_baseline"] = {"value": runs * cops / total / 1e12, "unit": UNIT, "cores": 1,
                                     "kind": "oracle",
-                                    "sample": f"{rows} of {M} token rows (quantize + GEMM over all N) x {runs} "
-                                              f"runs, {total:.1f} s"}
+                                    "sample": f"{rows} of {M} token rows (quantize + GEMM over all N"
+                                              f"{', both slots' if is_routed else ''}) x {runs} runs, {total:.1f} s"}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

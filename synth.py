@@ -170,3 +170,41 @@ def sweep(M: int) -> Workload:
 
 
 CONFIGS = (C0, C1, C2, C3) + tuple(sweep(m) for m in SWEEP_M)
+
+
+@dataclasses.dataclass(frozen=True)
+class RoutedWorkload:
+    """Expert-routed (MUL_MAT_ID) workload: E experts of N rows stacked, top_k
+    experts per token from the synthetic router (gen_ids)."""
+    name: str
+    wtype: int
+    M: int
+    K: int
+    N: int
+    E: int
+    top_k: int
+    w_seed: int
+    x_seed: int
+    ids_seed: int
+    sigma: float = 1.0
+    skew: float = 0.0
+
+    def weights(self) -> np.ndarray:
+        return (gen_q4k if self.wtype == 4 else gen_q6k)(self.E * self.N, self.K, self.w_seed)
+
+    def x(self) -> np.ndarray:
+        return gen_x(self.M, self.K, self.x_seed, self.sigma)
+
+    def ids(self) -> np.ndarray:
+        return gen_ids(self.M, self.top_k, self.E, self.ids_seed, self.skew)
+
+    @property
+    def block_bytes(self) -> int:
+        return Q4K_BYTES if self.wtype == 4 else Q6K_BYTES
+
+
+# A mixture-of-experts FFN projection (LLaMA-like expert shape): 8 experts,
+# 2 per token, 512 tokens -> 1024 routed rows, about 128 per expert.
+R0 = RoutedWorkload("q4k_moe_e8_top2_m512_k4096_n14336", 4, 512, 4096, 14336, 8, 2,
+                    w_seed=2000, x_seed=200007, ids_seed=2001, sigma=0.5)
+ROUTED_CONFIGS = (R0,)
