@@ -23,6 +23,9 @@ QGEMM_DEV_TIMEOUT, QGEMM_DEV_Q4K_RANGE, QGEMM_DEV_Q6K_SCALE, QGEMM_DEV_BAD_EXPER
 QGEMM_OPT_SMALL_M_MAX, QGEMM_OPT_FORCE_BM, QGEMM_OPT_FORCE_SPLITS = 0, 1, 2
 QGEMM_SMALL_M_DEFAULT = 8   # the library's default for QGEMM_OPT_SMALL_M_MAX
 
+QGEMM_OUT_F32, QGEMM_OUT_F16, QGEMM_OUT_BF16 = 0, 1, 2
+QGEMM_ACT_NONE, QGEMM_ACT_RELU, QGEMM_ACT_SILU, QGEMM_ACT_GELU = 0, 1, 2, 3
+
 Q4K_BLOCK_BYTES = 144
 Q6K_BLOCK_BYTES = 210
 
@@ -37,6 +40,10 @@ class _Counters(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
                 ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small", "q6k_prepack", "split_k",
                  "routed")]
+
+
+class _Epilogue(ctypes.Structure):
+    _fields_ = [("out_type", ctypes.c_int), ("activation", ctypes.c_int), ("bias", ctypes.c_void_p)]
 
 
 _lib = None
@@ -67,6 +74,9 @@ def lib() -> ctypes.CDLL:
             "qgemm_id_workspace_bytes": ([i64, i64, i64, i64], sz),
             "qgemm_q4k_id": ([vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, i64, vp, sz, vp], i32),
             "qgemm_q6k_id": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, i64, vp, sz, vp], i32),
+            "qgemm_q4k_ex": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, ctypes.POINTER(_Epilogue), vp, sz, vp],
+                             i32),
+            "qgemm_q6k_ex": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, ctypes.POINTER(_Epilogue), vp, sz, vp], i32),
             "qgemm_get_counters": ([ctypes.POINTER(_Counters)], i32),
             "qgemm_reset_counters": ([], i32),
             "qgemm_get_device_status": ([ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)], i32),
@@ -267,6 +277,46 @@ def qgemm_q6k_id(w_packed: torch.Tensor, experts: int, N: int, K: int, x: Q8K, i
                                 device=x.qs.device)
     _check(lib().qgemm_q6k_id(_ptr(w_packed), experts, N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(ids),
                               top_k, _ptr(y), y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return y
+
+
+_OUT_TYPES = {torch.float32: QGEMM_OUT_F32, torch.float16: QGEMM_OUT_F16, torch.bfloat16: QGEMM_OUT_BF16}
+
+
+def _epilogue(out_dtype, bias, activation) -> _Epilogue:
+    if bias is not None:
+        assert bias.dtype == torch.float32 and bias.is_contiguous()
+    return _Epilogue(_OUT_TYPES[out_dtype], int(activation), None if bias is None else bias.data_ptr())
+
+
+def qgemm_q4k_ex(w: torch.Tensor, N: int, K: int, x: Q8K, out_dtype=torch.float32, bias: torch.Tensor | None = None,
+                 activation: int = QGEMM_ACT_NONE, y: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out_dtype(act(X_q8k @ W_q4k^T + bias)); out_dtype float32 / float16 / bfloat16."""
+    assert w.dtype == torch.uint8 and w.dim() == 2 and w.stride(1) == 1
+    M = x.M
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.qs.device)
+    assert y.dtype == out_dtype
+    workspace = _workspace(M, N, K, workspace, x.qs.device)
+    ep = _epilogue(out_dtype, bias, activation)
+    _check(lib().qgemm_q4k_ex(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
+                              y.stride(0), ctypes.byref(ep), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return y
+
+
+def qgemm_q6k_ex(w_packed: torch.Tensor, N: int, K: int, x: Q8K, out_dtype=torch.float32,
+                 bias: torch.Tensor | None = None, activation: int = QGEMM_ACT_NONE, y: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """As qgemm_q4k_ex with repacked Q6_K weights."""
+    M = x.M
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.qs.device)
+    assert y.dtype == out_dtype
+    workspace = _workspace(M, N, K, workspace, x.qs.device)
+    ep = _epilogue(out_dtype, bias, activation)
+    _check(lib().qgemm_q6k_ex(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y), y.stride(0),
+                              ctypes.byref(ep), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
 

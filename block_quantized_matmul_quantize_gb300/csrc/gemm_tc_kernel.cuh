@@ -1,0 +1,960 @@
+// gemm_tc_kernel.cuh -- Q4_K / Q6_K weights x Q8_K activations on the sm_103a tensor
+// cores (tcgen05, TMEM accumulators, TMA-staged operands).
+//
+// The operation (the pages' prefill quantized matmul, "perf(KERNEL-QUANT-CIQ-
+// GEMM-ROCM): cooperative-tile WMMA kernels", vllm.cpp PR #3036, and llama.cpp's
+// mul_mat_q as read there, commit 2): Y[m][n] = sum over superblocks b of
+//   Q4_K: dx[m,b] * ( d[n,b] * sum_j sc_j * I_j - dmin[n,b] * sum_j m_j * B_j )
+//   Q6_K: dx[m,b] * d[n,b] * sum_j sc_j * (I_j - 32 * B_j)
+// with I_j the integer dot of sub-block j and B_j the activation sums.
+//
+// How this kernel computes it on sm_103a (no kind::i8 there):
+//   * One CTA owns 128 weight rows (the MMA's M) x BM tokens (the MMA's N)
+//     and, with split-K, a range of superblocks.  The lesson the pages arrive
+//     at (commit 2 and 4 of PR #3036; the Ampere mmq_x table of llama.cpp
+//     PR #214) is that a tile must be loaded once per CTA and shared by all
+//     its warps, and that the weight unpack must be amortised over many
+//     token rows: here TMA stages each tile once into shared memory and the
+//     single MMA-issuing thread feeds the whole tile to the tensor core.
+//   * Operands are fp16 holding exact integers: weights as sc_j*q (Q4_K,
+//     0..945) or sc_j*(q-32) (Q6_K, |.| <= 2048 for |sc_j| <= 64), tokens as
+//     the int8 q (|q| <= 127).  Products and their fp32 sums are exact while
+//     partial sums stay below 2^24, so the tensor core computes the per-
+//     superblock integer form sum_j sc_j * I_j.
+//   * The Q4_K dmin term rides along as two extra K=16 MMAs per superblock:
+//     A = the sub-mins times r = -dmin/d split into two fp16 parts (a1 + a2,
+//     about 22 significant bits), B = the 16 bsums in fp16.  The TMEM
+//     accumulator then holds  sum_j sc_j I_j - (dmin/d) sum_j m_j B_j  and the
+//     epilogue multiplies by d * dx.  (d = 0: the main part is zeroed and the
+//     multiplier is dmin with r = -1, exact.)
+//   * Per superblock the accumulator is read once (tcgen05.ld) and folded
+//     into fp32 registers: Y += (S * d) * dx.  Two TMEM accumulators let the
+//     MMA of superblock b+1 run while the epilogue drains superblock b.
+//
+//   * The unpacked weight operand never touches shared memory: each unpack
+//     thread builds its row's 64 fp16 values of a K64 chunk in registers and
+//     writes them to tensor memory with tcgen05.st; the MMA reads A from TMEM
+//     and B (the activations) from TMA-filled shared memory.  Shared-memory
+//     stores from the SM's load/store unit compete with TMA writes for the
+//     same shared-memory bandwidth (measured on GB300: four warps storing
+//     ~60 B/clk halve TMA delivery), so keeping them off the hot path keeps
+//     the activation stream fed.
+//
+// TMEM columns: [0, 2*BM) two fp32 accumulators (superblock t uses t & 1);
+// [256, 512) four 64-column K128 stages of the weight operand.
+//
+// MMA issue is the critical path.  On GB300 a tcgen05.mma (M128 N128 K16)
+// holds its issuing thread for ~55 of the ~64 cycles it runs, and the pipe
+// keeps only about one more queued, so the barrier waits, commits and loop
+// bookkeeping of a single issuing thread leave the tensor pipe idle between
+// MMAs (measured: ~35% busy with 4 MMAs per handshake).  Two issuing threads
+// in different warps, each owning one of the two accumulators (even / odd
+// superblocks), hide each other's bookkeeping; per thread the handshakes are
+// K128 (8 MMAs) with a non-blocking look-ahead probe of the next step's
+// barriers between the MMAs of the current one.
+//
+// Warp roles (16 warps, persistent CTAs looping over (n-tile, m-tile, split)
+// work items with token tiles varying fastest):
+//   warp 0      TMA producer of the activation stages (K128 or K256 per stage,
+//               one barrier each)
+//   warps 1, 3  MMA issuers (one thread each): even / odd superblocks; warp 1
+//               also owns the TMEM allocation
+//   warp 2      TMA producer: raw weight blocks (+ L2 prefetch ahead) and the
+//               per-superblock side data (bsums, dx)
+//   warps 4-7   unpack: thread = weight row; branch-free expand of each K64
+//               chunk into registers, tcgen05.st into TMEM
+//   warps 8-15  epilogue: warp w reads TMEM lanes 32*(w%4).. and half of the
+//               token columns, accumulates Y in registers, stores per tile
+// Every wait is bounded (see ptx.cuh); a timeout sets the status word and the
+// CTA runs to completion without touching Y.
+#pragma once
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "epilogue.cuh"
+#include "ptx.cuh"
+
+namespace qg {
+namespace {
+
+constexpr int BN = 128;        // weight rows per CTA = MMA M
+// Warps: 4 control, 4 or 8 unpack (one or two groups of four), 8 epilogue.
+// Q6_K's heavier expansion gets the second unpack group; for Q4_K it did not
+// pay for the registers it costs the epilogue (measured on GB300).
+template <int WT>
+struct Warps {
+    static constexpr int UNPACK_GROUPS = WT == 6 ? 2 : 1;
+    static constexpr int EPI0 = 4 + 4 * UNPACK_GROUPS;
+    static constexpr int N = EPI0 + 8;
+    static constexpr int THREADS = 32 * N;
+};
+constexpr int A_STAGES = 4;    // weight-operand K128 stages in TMEM (64 columns each)
+constexpr int A_TMEM_COL = 256;
+constexpr int KCH = 64;        // K elements per stage
+constexpr int SB_SLOTS = 3;    // per-superblock side-data slots
+constexpr int W_PREFETCH = 6;  // raw-weight L2 prefetch distance, in superblocks
+constexpr int SMEM_LIMIT = 232448;
+
+// warp roles
+constexpr int W_PROD_X = 0;
+constexpr int W_MMA = 1;
+constexpr int W_PROD_W = 2;
+constexpr int W_MMA2 = 3;
+constexpr int W_UNPACK0 = 4;
+
+
+__host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
+template <int WT>
+struct WTraits;
+template <>
+struct WTraits<4> {
+    static constexpr int RAW_BLOCK = Q4K_BLOCK;
+    static constexpr bool CORR = true;
+};
+template <>
+struct WTraits<6> {
+    static constexpr int RAW_BLOCK = Q6K_PACKED;
+    static constexpr bool CORR = false;
+};
+
+template <int WT, int BM>
+struct Layout {
+    static constexpr int RAW_SLOTS = 3;
+    static constexpr bool CORR = WTraits<WT>::CORR;
+    // An activation stage carries SCH K64 boxes that complete on one barrier:
+    // a whole superblock for BM <= 64, half of one for BM = 128.  (Measured on
+    // GB300: a TMA ring handing over 16 KB per barrier phase delivers about a
+    // third of what the same ring moves in 32 KB or 64 KB phases.)
+    static constexpr int SCH = BM >= 128 ? 2 : 4;
+    static constexpr int SPS = 4 / SCH;                  // stages per superblock
+    static constexpr int BOX = BM * 128;                 // one K64 box: BM rows x 128 B
+    static constexpr int B_STAGE = SCH * BOX;
+    static constexpr int RAW = BN * WTraits<WT>::RAW_BLOCK;
+    // per-superblock side slot
+    static constexpr int SB_ACORR = 0;                                       // 2 slabs x 128 rows x 32 B
+    static constexpr int SB_BCORR = CORR ? 2 * BN * 32 : 0;                 // BM rows x 32 B
+    static constexpr int SB_E = SB_BCORR + (CORR ? align_up(BM * 32, 1024) : 0);
+    static constexpr int SB_DX = SB_E + BN * 4;
+    static constexpr int SB = align_up(SB_DX + BM * 4, 1024);
+    // CTA layout: raw ring, side slots, then as many activation stages as fit (even count)
+    static constexpr int OFF_RAW = 0;
+    static constexpr int OFF_SB = OFF_RAW + align_up(RAW_SLOTS * RAW, 1024);
+    static constexpr int OFF_B = OFF_SB + SB_SLOTS * SB;
+    static constexpr int RESERVE = 1024 /* base alignment */ + 512 /* barriers, misc */;
+    static constexpr int B_STAGES = cmin(12, (SMEM_LIMIT - RESERVE - OFF_B) / B_STAGE) & ~1;
+    static constexpr int OFF_BAR = OFF_B + B_STAGES * B_STAGE;
+    static constexpr int NBAR = 2 * RAW_SLOTS + 2 * A_STAGES + 2 * B_STAGES + 2 * SB_SLOTS + 4 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int TOTAL = OFF_MISC + 16 + 1024;
+    static constexpr int CPT = BM / 2;                   // token columns per epilogue thread
+    static_assert(2 * BM <= A_TMEM_COL, "accumulators overlap the weight-operand stages");
+    static_assert(B_STAGES >= 4, "activation ring too shallow");
+    static_assert(NBAR * 8 + 16 <= 512, "barrier area");
+    static_assert(TOTAL <= SMEM_LIMIT, "shared memory budget");
+};
+
+
+__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t hsub2u(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t hadd2u(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// Byte B of w as an exact fp16 in both halves, without a conversion
+// instruction: the byte under the exponent byte 0x64 is the fp16 1024 + v,
+// and subtracting 1024 leaves v.  Unsigned bytes (0..255); for a signed byte
+// pass w ^ 0x80808080 and subtract 1152 (1024 + 128) instead.
+template <int B>
+__device__ __forceinline__ uint32_t byte_h2(uint32_t w, uint32_t minus_bias) {
+    constexpr uint32_t sel = B | (4u << 4) | (B << 8) | (4u << 12);   // w[B], 0x64, w[B], 0x64
+    return hadd2u(__byte_perm(w, 0x64646464u, sel), minus_bias);
+}
+constexpr uint32_t H2_M1024 = 0xE400E400u;   // fp16 -1024 in both halves
+constexpr uint32_t H2_M1152 = 0xE480E480u;   // fp16 -1152
+constexpr uint32_t H2_1_16 = 0x2C002C00u;    // fp16 1/16
+constexpr uint32_t H2_M64 = 0xD400D400u;     // fp16 -64
+
+// a[0..3] += (S[0..3] * e) * dx[0..3], two columns per packed fp32 instruction
+__device__ __forceinline__ void fold4(float* a, const uint32_t* S, float2 ee, float4 dx) {
+    const float2 lo = __ffma2_rn(__fmul2_rn(make_float2(__uint_as_float(S[0]), __uint_as_float(S[1])), ee),
+                                 make_float2(dx.x, dx.y), make_float2(a[0], a[1]));
+    const float2 hi = __ffma2_rn(__fmul2_rn(make_float2(__uint_as_float(S[2]), __uint_as_float(S[3])), ee),
+                                 make_float2(dx.z, dx.w), make_float2(a[2], a[3]));
+    a[0] = lo.x;
+    a[1] = lo.y;
+    a[2] = hi.x;
+    a[3] = hi.y;
+}
+
+__device__ __forceinline__ uint32_t h2dup(__half h) {
+    const uint32_t u = __half_as_ushort(h);
+    return u | (u << 16);
+}
+
+// ---------------------------------------------------------------- unpack
+// Both expanders write the K positions of every aligned group of 4 in the
+// order 0, 2, 1, 3 (fp16 pair (w[4k], w[4k+2]), then (w[4k+1], w[4k+3])):
+// two weights two bytes apart sit in one 32-bit word with no byte permute.
+// The activation operand (xh) is written in the same order, so the MMA's
+// dot products are unchanged; groups of 4 never straddle a 16-value group,
+// so the bsums are unchanged too.
+//
+// Q4_K: expand K64 chunk c of one 144-byte block into 64 fp16 values sc_j*q:
+// words 0..15 from the low nibbles (sub-block 2c), words 16..31 from the high
+// nibbles (sub-block 2c+1).
+__device__ __forceinline__ void unpack_q4k_chunk(const uint8_t* blk, int c, uint32_t scL, uint32_t cL,
+                                                 uint32_t scH, uint32_t cH, uint32_t (&o)[32]) {
+    const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
+    const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c + 16);
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    constexpr uint32_t MAGIC = 0x64006400u;  // fp16 1024 in both halves
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        // bytes 4k..4k+3 hold weights 4k..4k+3 (low nibbles) and 32+4k.. (high nibbles)
+        const uint32_t wk = w[k], sk = w[k] >> 8;
+        o[2 * k] = hfma2u((wk & 0x000F000Fu) | MAGIC, scL, cL);           // (1024+q)*sc - 1024*sc
+        o[2 * k + 1] = hfma2u((sk & 0x000F000Fu) | MAGIC, scL, cL);
+        o[16 + 2 * k] = hfma2u((wk & 0x00F000F0u) | MAGIC, scH, cH);      // (1024+16q)*sc/16 - 64*sc
+        o[17 + 2 * k] = hfma2u((sk & 0x00F000F0u) | MAGIC, scH, cH);
+    }
+}
+
+// Q6_K: K64 chunk c = weights 64c..64c+63 of a 224-byte packed block, as
+// fp16 (q-32)*sc.  Half h = c/2; low nibbles for c even, high for c odd; qh
+// bits 4*(c&1) + 2*pp for the first (pp = 0) and second (pp = 1) 32 weights.
+__device__ __forceinline__ void unpack_q6k_chunk(const uint8_t* blk, int c, const uint32_t (&s4)[4],
+                                                 uint32_t (&o)[32]) {
+    const int h = c >> 1, hn = c & 1;
+    const uint4* Lp = reinterpret_cast<const uint4*>(blk + 64 * h);
+    const uint4* Hp = reinterpret_cast<const uint4*>(blk + 128 + 32 * h);
+    const uint4 l0 = Lp[0], l1 = Lp[1], l2 = Lp[2], l3 = Lp[3];
+    const uint4 h0 = Hp[0], h1 = Hp[1];
+    const uint32_t Lw[16] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w,
+                             l2.x, l2.y, l2.z, l2.w, l3.x, l3.y, l3.z, l3.w};
+    const uint32_t Hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    constexpr uint32_t MAGIC = 0x64006400u;
+    constexpr uint32_t OFF = 0x64206420u;  // fp16 1056 = 1024 + 32 in both halves
+    const int nsh = 4 * hn;                 // low or high nibble
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            // 6-bit codes of weights 32pp+4k .. +3, one per byte
+            const uint32_t q6 = ((Lw[8 * pp + k] >> nsh) & 0x0F0F0F0Fu) |
+                                (((Hw[k] >> (nsh + 2 * pp)) << 4) & 0x30303030u);
+            const uint32_t sc = s4[2 * pp + (k >> 2)];
+            const uint32_t a = (q6 & 0x003F003Fu) | MAGIC;          // fp16 1024 + q
+            const uint32_t b = ((q6 >> 8) & 0x003F003Fu) | MAGIC;
+            o[16 * pp + 2 * k] = hmul2u(hsub2u(a, OFF), sc);        // (q - 32) * sc, exact
+            o[16 * pp + 2 * k + 1] = hmul2u(hsub2u(b, OFF), sc);
+        }
+    }
+}
+
+// Kernel variants, each compiled only with the code it needs (measured on
+// GB300: routing and epilogue code in one kernel doubled the register
+// spills and slowed the plain GEMM by 5-8%):
+//   VAR_PLAIN   fp32 output, the work list from the host plan;
+//   VAR_EPI     plus the output epilogue (bias, activation, fp16/bf16 output);
+//   VAR_ROUTED  the routed GEMM (work list and output rows from the routing).
+enum : int { VAR_PLAIN = 0, VAR_EPI = 1, VAR_ROUTED = 2 };
+template <int WT, int BM, int VAR>
+__global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
+                   const __grid_constant__ CUtensorMap tm_xbs, const __grid_constant__ CUtensorMap tm_dx,
+                   void* __restrict__ y, int64_t ldy, const Epi epi, int M, int N, int nb, const TcWork wk,
+                   uint32_t* __restrict__ status) {
+    using L = Layout<WT, BM>;
+    constexpr int UG = Warps<WT>::UNPACK_GROUPS;
+    constexpr int W_EPI0 = Warps<WT>::EPI0;
+    constexpr int R = L::RAW_SLOTS;
+    constexpr int BS = L::B_STAGES;
+    constexpr int SBN = SB_SLOTS;
+    // With two-box stages and as many activation stages as weight-operand
+    // stages, every K128 step consumes exactly one stage of each ring, so one
+    // commit (on a_empty) releases both and the activation producers wait on it.
+    constexpr bool MERGED_RELEASE = (L::SCH == 2) && (BS == A_STAGES);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+    uint64_t* raw_full = bars;
+    uint64_t* raw_empty = raw_full + R;
+    uint64_t* a_full = raw_empty + R;
+    uint64_t* a_empty = a_full + A_STAGES;
+    uint64_t* b_full = a_empty + A_STAGES;
+    uint64_t* b_empty = b_full + BS;
+    uint64_t* sb_full = b_empty + BS;
+    uint64_t* sb_empty = sb_full + SBN;
+    uint64_t* acc_full = sb_empty + SBN;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* epi_bar = acc_empty + 2;   // the 8 epilogue warps, for cut tiles
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // routed mode: the work list comes from the preceding (routing) grid
+    constexpr bool EPI = VAR == VAR_EPI;
+    constexpr bool ROUTED = VAR == VAR_ROUTED;
+    if constexpr (ROUTED) griddep_wait();
+    int num_work = wk.items;
+    if constexpr (ROUTED) num_work = wk.n_tiles * wk.tile_off[wk.experts];
+
+    auto b_stage = [&](int s) { return smem + L::OFF_B + s * L::B_STAGE; };
+    auto raw_slot = [&](int r) { return smem + L::OFF_RAW + r * L::RAW; };
+    auto sb_slot = [&](int p) { return smem + L::OFF_SB + p * L::SB; };
+    // work item -> (n0, m0, kb0, kb1); token tiles vary fastest, so the CTAs
+    // running at the same time share weight tiles (one DRAM read, L2 hits after)
+    // (cut tiles: cut = index among the cut tiles, part = its K part; -1 for whole tiles)
+    auto work_cut = [&](int wi, int& n0, int& m0, int& kb0, int& kb1, int& cut, int& part) {
+        int tile;
+        if constexpr (ROUTED) {
+            // routed: item = (weight tile, global token tile); token tiles vary
+            // fastest; the expert is the one whose tile range holds the token tile
+            const int tt = wk.tile_off[wk.experts];
+            const int nt = wi / tt, gm = wi - nt * tt;
+            int lo = 0, hi = wk.experts - 1;   // largest e with tile_off[e] <= gm
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (wk.tile_off[mid] <= gm) lo = mid; else hi = mid - 1;
+            }
+            n0 = lo * N + nt * BN;   // weight rows of expert lo, stacked
+            m0 = wk.row_off[lo] + (gm - wk.tile_off[lo]) * BM;
+            kb0 = 0;
+            kb1 = nb;
+            cut = -1;
+            part = 0;
+            return;
+        }
+        if (wi < wk.full_items) {
+            tile = wi;
+            cut = -1;
+            part = 0;
+            kb0 = 0;
+            kb1 = nb;
+        } else {
+            const int j = wi - wk.full_items;
+            cut = j / wk.parts;
+            part = j - cut * wk.parts;
+            tile = wk.full_items + cut;
+            kb0 = static_cast<int>(static_cast<int64_t>(nb) * part / wk.parts);
+            kb1 = static_cast<int>(static_cast<int64_t>(nb) * (part + 1) / wk.parts);
+        }
+        n0 = (tile / wk.m_tiles) * BN;
+        m0 = (tile % wk.m_tiles) * BM;
+    };
+    auto work_of = [&](int wi, int& n0, int& m0, int& kb0, int& kb1) {
+        int cut, part;
+        work_cut(wi, n0, m0, kb0, kb1, cut, part);
+    };
+    // The i-th superblock a work item visits: its K range rotated by the weight-
+    // tile index, so that the CTAs sharing a token tile at the same time read
+    // different activation lines instead of queueing on the same ones.  (The
+    // fp32 sum over superblocks is order-independent up to rounding.)
+    auto sb_at = [&](int i, int k0, int k1, int n0) {
+        const int len = k1 - k0;
+        return k0 + (i - k0 + n0 / BN) % len;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int r = 0; r < R; ++r) {
+            mbar_init(&raw_full[r], 1);
+            mbar_init(&raw_empty[r], 4 * UG + (L::CORR ? 4 : 0));   // unpack warps (+ side-data warps)
+        }
+        for (int s = 0; s < A_STAGES; ++s) {
+            mbar_init(&a_full[s], 4);
+            mbar_init(&a_empty[s], 1);
+        }
+        for (int s = 0; s < BS; ++s) {
+            mbar_init(&b_full[s], 1);
+            mbar_init(&b_empty[s], 1);
+        }
+        for (int p = 0; p < SBN; ++p) {
+            mbar_init(&sb_full[p], 1 + 4);   // producer's bytes + the four warps writing the slot
+            mbar_init(&sb_empty[p], 8);   // the epilogue warps, after acc_full covered the MMAs reading it
+        }
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(&acc_full[p], 1);
+            mbar_init(&acc_empty[p], 8);
+        }
+        mbar_init(epi_bar, 8);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == W_PROD_X && lane == 0) tma_prefetch_desc(&tm_xh);
+    if (warp == W_PROD_W && lane == 0) {
+        tma_prefetch_desc(&tm_w);
+        tma_prefetch_desc(&tm_dx);
+        if (L::CORR) tma_prefetch_desc(&tm_xbs);
+    }
+    if (warp == W_MMA) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+
+    if (warp == W_PROD_X) {
+        // ------------------------------------------------ activation producer
+        if (lane == 0) {
+            griddep_wait();   // the activation planes come from the preceding grid
+            int g = 0;   // running stage counter
+            bool ok = true;
+            for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
+                int n0, m0, kb0, kb1;
+                work_of(wi, n0, m0, kb0, kb1);
+                for (int i = kb0; i < kb1 && ok; ++i) {
+                    const int b = sb_at(i, kb0, kb1, n0);
+                    for (int h = 0; h < L::SPS; ++h, ++g) {
+                        const int s = g % BS;
+                        ok = mbar_wait(MERGED_RELEASE ? &a_empty[s] : &b_empty[s], ((g / BS) & 1) ^ 1, abort_flag,
+                                       status, 2);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(&b_full[s], L::B_STAGE);
+#pragma unroll
+                        for (int q = 0; q < L::SCH; ++q)
+                            tma_load_2d(&tm_xh, &b_full[s], b_stage(s) + q * L::BOX, b * 256 + KCH * (h * L::SCH + q),
+                                        m0);
+                    }
+                }
+            }
+        }
+    } else if (warp == W_PROD_W) {
+        // ------------------------------------------------ weight + side-data producer
+        if (lane == 0) {
+            int t = 0;
+            bool ok = true;
+            // L2 prefetch cursor, W_PREFETCH superblocks ahead of the loads
+            int pwi = blockIdx.x, pb = 0, pb1 = 0, pn0 = 0, pm0 = 0, pk0 = 0;
+            if (pwi < num_work) work_of(pwi, pn0, pm0, pk0, pb1), pb = pk0;
+            auto prefetch_next = [&]() {
+                if (pwi >= num_work) return;
+                tma_prefetch_l2_2d(&tm_w, sb_at(pb, pk0, pb1, pn0) * WTraits<WT>::RAW_BLOCK, pn0);
+                if (++pb >= pb1) {
+                    pwi += gridDim.x;
+                    if (pwi < num_work) work_of(pwi, pn0, pm0, pk0, pb1), pb = pk0;
+                }
+            };
+            for (int i = 0; i < W_PREFETCH; ++i) prefetch_next();
+            for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
+                int n0, m0, kb0, kb1;
+                work_of(wi, n0, m0, kb0, kb1);
+                for (int i = kb0; i < kb1; ++i, ++t) {
+                    const int b = sb_at(i, kb0, kb1, n0);
+                    prefetch_next();
+                    const int r = t % R;
+                    ok = mbar_wait(&raw_empty[r], ((t / R) & 1) ^ 1, abort_flag, status, 3);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&raw_full[r], L::RAW);
+                    tma_load_2d(&tm_w, &raw_full[r], raw_slot(r), b * WTraits<WT>::RAW_BLOCK, n0);
+                    const int p = t % SBN;
+                    ok = mbar_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1, abort_flag, status, 1);
+                    if (!ok) break;
+                    if (t == 0) griddep_wait();   // bsums and scales come from the preceding grid
+                    uint8_t* sb = sb_slot(p);
+                    mbar_arrive_expect_tx(&sb_full[p], (L::CORR ? BM * 32 : 0) + BM * 4);
+                    if (L::CORR) tma_load_2d(&tm_xbs, &sb_full[p], sb + L::SB_BCORR, b * 16, m0);
+                    tma_load_2d(&tm_dx, &sb_full[p], sb + L::SB_DX, m0, b);
+                }
+            }
+        }
+    } else if (warp == W_MMA || warp == W_MMA2) {
+        // ------------------------------------------------ MMA issuers
+        // Thread `par` takes the superblocks t with t % 2 == par, i.e. always
+        // accumulator `par`, A stages 2*par and 2*par+1 and (two-box stages)
+        // the same two activation stages.  Per superblock: two K128 steps of 8
+        // MMAs (+2 correction MMAs for Q4_K) and up to four commits; readiness
+        // of the next step, the side slot and the next accumulator is probed
+        // without blocking between the MMAs of the current step.
+        if (lane == 0) {
+            const int par = (warp == W_MMA) ? 0 : 1;
+            constexpr uint32_t IDESC = idesc_f16_f32(BN, BM);
+            // descriptor of activation stage 0; stage s, box q, K-step kk adds (s*B_STAGE + q*BOX + 32*kk) >> 4
+            const uint64_t bdesc0 = smem_desc(smem_u32(b_stage(0)), 16, 1024, SWZ_128B);
+            // correction operands of side slot 0; slot p adds (p * SB) >> 4
+            const uint32_t sb0 = smem_u32(sb_slot(0));
+            const uint64_t acorr0 = smem_desc(sb0 + L::SB_ACORR, 16, 256, SWZ_32B);
+            const uint64_t bcorr0 = smem_desc(sb0 + L::SB_BCORR, 16, 256, SWZ_32B);
+            const uint32_t d_tmem = tmem_base + par * BM;
+            // stage index and phase parity of K128 step j of superblock t, in each ring
+            auto a_at = [&](int t, int j, int& s, uint32_t& ph) {
+                const int g = 2 * t + j;
+                s = g % A_STAGES;
+                ph = static_cast<uint32_t>(g / A_STAGES) & 1u;
+            };
+            auto b_at = [&](int t, int j, int& s, uint32_t& ph) {
+                const int g = t * L::SPS + (2 * j) / L::SCH;
+                s = g % BS;
+                ph = static_cast<uint32_t>(g / BS) & 1u;
+            };
+            int t = 0;
+            bool step_ok = false;   // next step's A (and B) stage seen complete
+            bool acc_ok = false;    // next superblock's accumulator seen free
+            bool ok = true;
+            for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
+                int n0, m0, kb0, kb1;
+                work_of(wi, n0, m0, kb0, kb1);
+                for (int b = kb0; b < kb1 && ok; ++b, ++t) {
+                    if ((t & 1) != par) continue;
+                    const int p = t % SBN;
+                    if (!acc_ok) {
+                        ok = mbar_wait(&acc_empty[par], ((t >> 1) & 1) ^ 1, abort_flag, status, 4);
+                        if (!ok) break;
+                    }
+                    bool sb_ok = !L::CORR;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {   // K128 steps: chunks 2h, 2h+1
+                        const int q0 = (2 * h) % L::SCH;   // first box of the step in its B stage
+                        int sa, sx;
+                        uint32_t pa, px;
+                        a_at(t, h, sa, pa);
+                        b_at(t, h, sx, px);
+                        if (!step_ok) {
+                            ok = mbar_wait(&a_full[sa], pa, abort_flag, status, 12);
+                            if (ok && q0 == 0) ok = mbar_wait(&b_full[sx], px, abort_flag, status, 5);
+                            if (!ok) break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a0 = tmem_base + A_TMEM_COL + 64 * sa;
+                        const uint64_t bd = bdesc0 + static_cast<uint64_t>((sx * L::B_STAGE + q0 * L::BOX) >> 4);
+                        mma_f16_ta(d_tmem, a0, bd, IDESC, h != 0);
+                        mma_f16_ta(d_tmem, a0 + 8, bd + 2, IDESC, 1u);
+                        mma_f16_ta(d_tmem, a0 + 16, bd + 4, IDESC, 1u);
+                        mma_f16_ta(d_tmem, a0 + 24, bd + 6, IDESC, 1u);
+                        // probes, while these run: this thread's next step is step 1 of
+                        // superblock t, or step 0 of superblock t + 2
+                        const bool last_b = (q0 + 2 == L::SCH);   // this step ends its B stage
+                        {
+                            const int nt = h == 0 ? t : t + 2, nh = h ^ 1;
+                            int na, nx;
+                            uint32_t npa, npx;
+                            a_at(nt, nh, na, npa);
+                            b_at(nt, nh, nx, npx);
+                            const bool ta = mbar_test_wait(&a_full[na], npa);
+                            const bool tb = ((2 * nh) % L::SCH != 0) || mbar_test_wait(&b_full[nx], npx);
+                            if (h == 0) {
+                                if (L::CORR) sb_ok = mbar_test_wait(&sb_full[p], (t / SBN) & 1);
+                            } else {
+                                acc_ok = mbar_test_wait(&acc_empty[par], (((t + 2) >> 1) & 1) ^ 1);
+                            }
+                            step_ok = ta && tb;
+                        }
+                        const uint64_t bd1 = bd + (L::BOX >> 4);
+                        mma_f16_ta(d_tmem, a0 + 32, bd1, IDESC, 1u);
+                        mma_f16_ta(d_tmem, a0 + 40, bd1 + 2, IDESC, 1u);
+                        mma_f16_ta(d_tmem, a0 + 48, bd1 + 4, IDESC, 1u);
+                        mma_f16_ta(d_tmem, a0 + 56, bd1 + 6, IDESC, 1u);
+                        // frees the A stage (and, with MERGED_RELEASE, the B stage of this step)
+                        mma_commit(&a_empty[sa]);
+                        if (last_b && !MERGED_RELEASE) mma_commit(&b_empty[sx]);
+                    }
+                    if (!ok) break;
+                    if (L::CORR) {
+                        if (!sb_ok) {
+                            ok = mbar_wait(&sb_full[p], (t / SBN) & 1, abort_flag, status, 6);
+                            if (!ok) break;
+                        }
+                        tc_fence_after();
+                        const uint64_t po = static_cast<uint64_t>((p * L::SB) >> 4);
+                        mma_f16(d_tmem, acorr0 + po, bcorr0 + po, IDESC, 1u);
+                        mma_f16(d_tmem, acorr0 + po + ((BN * 32) >> 4), bcorr0 + po, IDESC, 1u);
+                    }
+                    // completion of everything so far: the epilogue then also frees side slot p
+                    mma_commit(&acc_full[par]);
+                }
+            }
+        }
+    } else if (warp >= W_UNPACK0 && warp < W_EPI0) {
+        // ------------------------------------------------ unpack (thread = weight row)
+        // One or two groups of four warps (TMEM lanes 32*(warp%4).., as any
+        // warp must): with two, group g expands K128 step g of every
+        // superblock; group 0 also writes the superblock's side data.
+        const int grp = (warp - W_UNPACK0) >> 2;
+        const int j0 = UG == 2 ? grp : 0, j1 = UG == 2 ? grp + 1 : 2;   // this warp's K128 steps
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + A_TMEM_COL;
+        // A K128 step's a_full is signalled only after the next chunk has been
+        // expanded, so the wait for its tcgen05.st to land overlaps that work;
+        // it is signalled at once before any wait that might block.
+        int pend = -1;   // A stage whose a_full is still to be signalled
+        auto signal = [&]() {
+            if (pend >= 0) {
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[pend]);
+                pend = -1;
+            }
+        };
+        int t = 0;
+        bool ok = true;
+        for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
+            int n0, m0, kb0, kb1;
+            work_of(wi, n0, m0, kb0, kb1);
+            for (int b = kb0; b < kb1; ++b, ++t) {
+                const int r = t % R;
+                if (!mbar_test_wait(&raw_full[r], (t / R) & 1)) signal();
+                ok = mbar_wait(&raw_full[r], (t / R) & 1, abort_flag, status, 7);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                const uint8_t* blk = raw_slot(r) + row * WTraits<WT>::RAW_BLOCK;
+                const int p = t % SBN;
+
+                if constexpr (WT == 4) {
+                    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+                    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
+                    const uint32_t sc03 = hdr.y & 0x3f3f3f3fu;
+                    const uint32_t sc47 = (hdr.w & 0x0f0f0f0fu) | ((hdr.y >> 2) & 0x30303030u);
+                    const bool main_on = (d != 0.0f);
+                    // (the dmin correction operands and the scale e of this superblock
+                    // are written by the epilogue's side-data warps)
+                    // this warp's K128 steps: the second chunk is expanded while the
+                    // first one's tcgen05.st is in flight, one wait::st and one a_full
+#pragma unroll 1
+                    for (int j = j0; j < j1; ++j) {
+                        const int g = 2 * t + j;
+                        const int s = g % A_STAGES;
+                        // sub-block scales of chunks 2j (bytes 0, 1) and 2j+1 (bytes 2, 3)
+                        const uint32_t scw = main_on ? (j == 0 ? sc03 : sc47) : 0u;
+                        uint32_t v0[32], v1[32];
+                        {
+                            // sc, -1024 sc for the low nibbles; sc/16, -64 sc for the high ones (all exact)
+                            const uint32_t sl = byte_h2<0>(scw, H2_M1024), sh = byte_h2<1>(scw, H2_M1024);
+                            unpack_q4k_chunk(blk, 2 * j, sl, hmul2u(sl, H2_M1024), hmul2u(sh, H2_1_16),
+                                             hmul2u(sh, H2_M64), v0);
+                        }
+                        signal();
+                        ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
+                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                        tc_fence_after();
+                        tmem_st_32x32b_x32(lane_base + 64 * s, v0);
+                        {
+                            const uint32_t sl = byte_h2<2>(scw, H2_M1024), sh = byte_h2<3>(scw, H2_M1024);
+                            unpack_q4k_chunk(blk, 2 * j + 1, sl, hmul2u(sl, H2_M1024), hmul2u(sh, H2_1_16),
+                                             hmul2u(sh, H2_M64), v1);
+                        }
+                        tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
+                        pend = s;
+                    }
+                    if (!ok) break;
+                } else {
+                    const uint4 scv = *reinterpret_cast<const uint4*>(blk + 192);
+                    const uint32_t sw[4] = {scv.x, scv.y, scv.z, scv.w};
+                    bool bad = false;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int v = static_cast<int8_t>((sw[j >> 2] >> (8 * (j & 3))) & 0xff);
+                        bad |= (v > 64) || (v < -64);
+                    }
+                    if (grp == 0) {
+                        if (bad) atomicOr(status, ST_Q6K_SCALE);
+                        const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
+                        if (!mbar_test_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1)) signal();
+                        ok = mbar_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1, abort_flag, status, 8);
+                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                        reinterpret_cast<float*>(sb_slot(p) + L::SB_E)[row] = d;
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sb_full[p]);
+                    }
+                    // this warp's K128 steps, as for Q4_K
+#pragma unroll 1
+                    for (int j = j0; j < j1; ++j) {
+                        const int g = 2 * t + j;
+                        const int s = g % A_STAGES;
+                        // the chunk's four sub-block scales: bytes 4c..4c+3 of the scale array
+                        auto scales = [&](uint32_t scw, uint32_t (&s4)[4]) {
+                            const uint32_t u = scw ^ 0x80808080u;   // signed bytes, offset by 128
+                            s4[0] = byte_h2<0>(u, H2_M1152);
+                            s4[1] = byte_h2<1>(u, H2_M1152);
+                            s4[2] = byte_h2<2>(u, H2_M1152);
+                            s4[3] = byte_h2<3>(u, H2_M1152);
+                        };
+                        uint32_t v0[32], v1[32];
+                        {
+                            uint32_t s4[4];
+                            scales(j == 0 ? sw[0] : sw[2], s4);
+                            unpack_q6k_chunk(blk, 2 * j, s4, v0);
+                        }
+                        signal();
+                        ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
+                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                        tc_fence_after();
+                        tmem_st_32x32b_x32(lane_base + 64 * s, v0);
+                        {
+                            uint32_t s4[4];
+                            scales(j == 0 ? sw[1] : sw[3], s4);
+                            unpack_q6k_chunk(blk, 2 * j + 1, s4, v1);
+                        }
+                        tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
+                        pend = s;
+                    }
+                    if (!ok) break;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[r]);
+            }
+        }
+        signal();
+    } else if (warp >= W_EPI0) {
+        // ------------------------------------------------ epilogue
+        constexpr int CPT = L::CPT;
+        const int quad = warp & 3;
+        const int half = (warp - W_EPI0) >> 2;
+        const int row = 32 * quad + lane;
+        const int col0 = half * CPT;
+        int t = 0;
+        uint32_t epi_phase = 0;
+        bool ok = true;
+        // Q4_K: the second half's four warps also write the side data of each
+        // superblock (the dmin correction operands and the scale e, from the
+        // block header in the raw ring), SBN - 1 superblocks ahead of the
+        // accumulator they wait for, while the unpack warps only expand.
+        const bool side_writer = L::CORR && half == 1;
+        int ts = 0;         // next superblock whose side data is due
+        int total_sb = 0;   // this CTA's superblocks
+        if (side_writer) {
+            for (int wi = blockIdx.x; wi < num_work; wi += gridDim.x) {
+                int n0, m0, kb0, kb1, cut, part;
+                work_cut(wi, n0, m0, kb0, kb1, cut, part);
+                total_sb += kb1 - kb0;
+            }
+        }
+        auto side_upto = [&](int lim) -> bool {
+            for (; ts <= lim && ts < total_sb; ++ts) {
+                const int r = ts % R, ps = ts % SBN;
+                bool fine = mbar_wait(&raw_full[r], (ts / R) & 1, abort_flag, status, 15);
+                if (!__all_sync(0xffffffffu, fine)) return false;
+                const uint4 hdr = *reinterpret_cast<const uint4*>(raw_slot(r) + row * WTraits<WT>::RAW_BLOCK);
+                const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
+                const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
+                const uint32_t mn03 = hdr.z & 0x3f3f3f3fu;
+                const uint32_t mn47 = ((hdr.w >> 4) & 0x0f0f0f0fu) | ((hdr.z >> 2) & 0x30303030u);
+                const bool main_on = (d != 0.0f);
+                const float e = main_on ? d : dmin;
+                const float ratio = main_on ? -dmin / d : -1.0f;
+                if (!(fabsf(ratio) <= 1000.0f)) atomicOr(status, ST_Q4K_RANGE);
+                uint32_t a1[8], a2[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int mj = ((j < 4 ? mn03 : mn47) >> (8 * (j & 3))) & 0xff;
+                    const float v = static_cast<float>(mj) * ratio;
+                    const __half h1 = __float2half_rn(v);
+                    const __half h2 = __float2half_rn(v - __half2float(h1));
+                    a1[j] = h2dup(h1);
+                    a2[j] = h2dup(h2);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[r]);
+                fine = mbar_wait(&sb_empty[ps], ((ts / SBN) & 1) ^ 1, abort_flag, status, 16);
+                if (!__all_sync(0xffffffffu, fine)) return false;
+                uint8_t* sbw = sb_slot(ps);
+                // correction slabs, 32-byte swizzle: row * 32 + (chunk ^ ((row >> 2) & 1)) * 16
+                uint8_t* s1 = sbw + L::SB_ACORR + row * 32;
+                uint8_t* s2 = s1 + BN * 32;
+                const int x = (row >> 2) & 1;
+                *reinterpret_cast<uint4*>(s1 + ((0 ^ x) << 4)) = make_uint4(a1[0], a1[1], a1[2], a1[3]);
+                *reinterpret_cast<uint4*>(s1 + ((1 ^ x) << 4)) = make_uint4(a1[4], a1[5], a1[6], a1[7]);
+                *reinterpret_cast<uint4*>(s2 + ((0 ^ x) << 4)) = make_uint4(a2[0], a2[1], a2[2], a2[3]);
+                *reinterpret_cast<uint4*>(s2 + ((1 ^ x) << 4)) = make_uint4(a2[4], a2[5], a2[6], a2[7]);
+                reinterpret_cast<float*>(sbw + L::SB_E)[row] = e;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sb_full[ps]);
+            }
+            return true;
+        };
+        for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
+            int n0, m0, kb0, kb1, cut, part;
+            work_cut(wi, n0, m0, kb0, kb1, cut, part);
+            float acc[CPT];
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
+            for (int b = kb0; b < kb1; ++b, ++t) {
+                const int buf = t & 1;
+                const int p = t % SBN;
+                if (side_writer && !side_upto(t + SBN - 1)) { ok = false; break; }
+                ok = mbar_wait(&acc_full[buf], (t >> 1) & 1, abort_flag, status, 10);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                ok = mbar_wait(&sb_full[p], (t / SBN) & 1, abort_flag, status, 11);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                const uint8_t* sb = sb_slot(p);
+                const float e = reinterpret_cast<const float*>(sb + L::SB_E)[row];
+                const float2 ee = make_float2(e, e);
+                const float4* dx4 = reinterpret_cast<const float4*>(sb + L::SB_DX) + col0 / 4;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + buf * BM + col0;
+                if constexpr (CPT >= 16) {
+                    // two 16-column loads in flight per wait
+                    constexpr int PAIR = (CPT >= 32 && UG == 1) ? 2 : 1;   // registers allowing
+#pragma unroll
+                    for (int ch = 0; ch < CPT / 16; ch += PAIR) {
+                        uint32_t v[PAIR][16];
+#pragma unroll
+                        for (int u = 0; u < PAIR; ++u) tmem_ld_32x32b_x16(taddr + 16 * (ch + u), v[u]);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int u = 0; u < PAIR; ++u) {
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                fold4(acc + 16 * (ch + u) + 4 * q4, v[u] + 4 * q4, ee, dx4[4 * (ch + u) + q4]);
+                        }
+                    }
+                } else {
+                    uint32_t v[8];
+                    tmem_ld_32x32b_x8(taddr, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q4 = 0; q4 < 2; ++q4) fold4(acc + 4 * q4, v + 4 * q4, ee, dx4[q4]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&acc_empty[buf]);
+                    mbar_arrive(&sb_empty[p]);
+                }
+            }
+            if (!ok) break;
+            if (cut >= 0) {
+                griddep_wait();   // the counters are zeroed by the preceding grid
+                // a part of a cut tile: publish the partial tile, and the part
+                // that completes the tile adds all parts (ascending) into acc
+                // (a part is stored column by column, element (row, col) at col*128 + row,
+                // so that each warp-wide store or load is one contiguous 128-B line)
+                float* mine = wk.partials + (static_cast<int64_t>(cut) * wk.parts + part) * (BN * BM) +
+                              col0 * BN + row;
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) __stcg(mine + j * BN, acc[j]);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(epi_bar);
+                ok = mbar_wait(epi_bar, epi_phase, abort_flag, status, 13);   // every warp's partial is out
+                epi_phase ^= 1u;
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                if (warp == W_EPI0 && lane == 0) {
+                    __threadfence();
+                    *last_flag = (atomicAdd(&wk.counters[cut], 1) == wk.parts - 1);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(epi_bar);
+                ok = mbar_wait(epi_bar, epi_phase, abort_flag, status, 14);   // the flag is set
+                epi_phase ^= 1u;
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                if (!*last_flag) continue;
+                // all parts, this one included, from memory in ascending order
+                __threadfence();
+                const float* base = wk.partials + static_cast<int64_t>(cut) * wk.parts * (BN * BM) + col0 * BN + row;
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) acc[j] = __ldcg(base + j * BN);
+                for (int p2 = 1; p2 < wk.parts; ++p2) {
+#pragma unroll
+                    for (int j = 0; j < CPT; ++j) acc[j] += __ldcg(base + p2 * (BN * BM) + j * BN);
+                }
+                if (warp == W_EPI0 && lane == 0) wk.counters[cut] = 0;   // ready for the next call
+            }
+            if constexpr (ROUTED) {
+                // routed: column n of the expert, token rows up to the expert's end,
+                // each written to its output row
+                const int e = n0 / N;
+                const int n = n0 - e * N + row;
+                const int m_end = wk.row_end[e];
+                if (!*abort_flag && n < N) {
+                    if constexpr (!EPI) {
+                        float* yf = static_cast<float*>(y);
+#pragma unroll
+                        for (int j = 0; j < CPT; ++j) {
+                            const int m = m0 + col0 + j;
+                            if (m < m_end) yf[static_cast<int64_t>(wk.perm[m]) * ldy + n] = acc[j];
+                        }
+                    } else {
+                        const float bn = epi.bias ? epi.bias[n] : 0.0f;
+#pragma unroll
+                        for (int j = 0; j < CPT; ++j) {
+                            const int m = m0 + col0 + j;
+                            if (m < m_end)
+                                epi_store(y, static_cast<int64_t>(wk.perm[m]) * ldy + n,
+                                          epi_value(acc[j], bn, epi.act), epi.out);
+                        }
+                    }
+                }
+                continue;
+            }
+            const int n = n0 + row;
+            if (!*abort_flag && n < N) {
+                if constexpr (!EPI) {
+                    float* yf = static_cast<float*>(y);
+#pragma unroll
+                    for (int j = 0; j < CPT; ++j) {
+                        const int m = m0 + col0 + j;
+                        if (m < M) yf[static_cast<int64_t>(m) * ldy + n] = acc[j];
+                    }
+                } else {
+                    const float bn = epi.bias ? epi.bias[n] : 0.0f;
+#pragma unroll
+                    for (int j = 0; j < CPT; ++j) {
+                        const int m = m0 + col0 + j;
+                        if (m < M)
+                            epi_store(y, static_cast<int64_t>(m) * ldy + n, epi_value(acc[j], bn, epi.act), epi.out);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == W_MMA) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+template <int WT, int BM, int VAR>
+cudaError_t launch_t(const TcLaunch& a, cudaStream_t s) {
+    using L = Layout<WT, BM>;
+    const int grid = a.work.items < a.sm_count ? a.work.items : a.sm_count;
+    // A programmatic dependent of the preceding kernel: the CTAs may start
+    // (barrier set-up, weight loads and expansion) while that kernel finishes;
+    // every read of its output waits for it (griddep_wait).
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(Warps<WT>::THREADS);
+    cfg.dynamicSmemBytes = L::TOTAL;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const CUtensorMap tm_xbs = a.tm_xbs ? *a.tm_xbs : *a.tm_xh;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<WT, BM, VAR>, *a.tm_w, *a.tm_xh, tm_xbs, *a.tm_dx, a.y, a.ldy, a.epi,
+                              static_cast<int>(a.M), static_cast<int>(a.N), static_cast<int>(a.K / 256), a.work,
+                              a.status);
+}
+
+template <int WT, int BM, int VAR>
+cudaError_t prepare_t() {
+    return cudaFuncSetAttribute(gemm_tc_kernel<WT, BM, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Layout<WT, BM>::TOTAL);
+}
+
+}  // namespace
+}  // namespace qg

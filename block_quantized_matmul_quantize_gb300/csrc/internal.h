@@ -22,6 +22,17 @@ enum : uint32_t {
 constexpr uint64_t QG_WAIT_NS = 2000000000ull;  // 2 s of wall time per wait
 constexpr uint32_t QG_WAIT_ITERS = 1u << 28;    // and at most this many polls
 
+// Output epilogue (the pages' OutT output type, plus an optional fused bias
+// and activation), applied where a kernel stores a finished output element:
+//   y = out_type(act(acc + bias[n])).
+enum : int { OUT_F32 = 0, OUT_F16 = 1, OUT_BF16 = 2 };
+enum : int { ACT_NONE = 0, ACT_RELU = 1, ACT_SILU = 2, ACT_GELU = 3 };
+struct Epi {
+    int out;             // OUT_*
+    int act;             // ACT_*
+    const float* bias;   // [N] or nullptr
+};
+
 constexpr int Q4K_BLOCK = 144;
 constexpr int Q6K_BLOCK = 210;
 constexpr int Q6K_PACKED = 224;                 // 210 B + 14 B of zero padding (16-B aligned)
@@ -95,8 +106,9 @@ struct TcLaunch {
     int64_t M, N, K;
     TcWork work;
     int sm_count;         // persistent grid: min(work items, SMs)
-    float* y;
-    int64_t ldy;
+    void* y;              // element type per epi.out
+    int64_t ldy;          // in elements
+    Epi epi;
     uint32_t* status;
     const CUtensorMap* tm_w;    // raw weight blocks, 2D uint8
     const CUtensorMap* tm_xh;   // fp16 [M][K], box {64, bm}, 128B swizzle
@@ -106,6 +118,12 @@ struct TcLaunch {
 size_t tc_smem_bytes(int wtype, int bm);
 cudaError_t tc_prepare(int wtype, int bm);   // sets the dynamic smem attribute (per device)
 cudaError_t launch_gemm_tc(const TcLaunch& a, cudaStream_t s);
+// (the epilogue instantiations, gemm_tc_epi.cu; launch_gemm_tc dispatches to them)
+cudaError_t tc_prepare_epi(int wtype, int bm);
+cudaError_t launch_gemm_tc_epi(const TcLaunch& a, cudaStream_t s);
+// (the routed instantiations, gemm_tc_routed.cu: work.experts > 0)
+cudaError_t tc_prepare_routed(int wtype, int bm);
+cudaError_t launch_gemm_tc_routed(const TcLaunch& a, cudaStream_t s);
 
 // Small-M streaming path (smallm.cu): M <= SMALL_M_LIMIT tokens, reads the
 // Q8_K planes directly (no workspace).
@@ -118,8 +136,9 @@ struct SmallLaunch {
     const int8_t* xqs;
     const float* xd;
     const int16_t* xbs;
-    float* y;
-    int64_t ldy;
+    void* y;              // element type per epi.out
+    int64_t ldy;          // in elements
+    Epi epi;
     int sm_count;
     uint32_t* status;
 };

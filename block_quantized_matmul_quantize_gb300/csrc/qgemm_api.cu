@@ -223,8 +223,8 @@ WsPlanes ws_planes(void* ws, int64_t M, int64_t K) {
 }
 
 int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs, const float* xd,
-           const int16_t* xbsums, int64_t M, float* y, int64_t ldy, void* ws, size_t ws_bytes,
-           cudaStream_t stream, bool prepared) {
+           const int16_t* xbsums, int64_t M, void* y, int64_t ldy, void* ws, size_t ws_bytes,
+           cudaStream_t stream, bool prepared, const qg::Epi& epi = qg::Epi{}) {
     DevState* ds = nullptr;
     int rc = device_state(&ds);
     if (rc) return rc;
@@ -276,6 +276,7 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
     a.sm_count = ds->sm_count;
     a.y = y;
     a.ldy = ldy;
+    a.epi = epi;
     a.status = ds->status;
     a.tm_w = &tm_w;
     a.tm_xh = &tm_xh;
@@ -293,7 +294,8 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
 
 // Small-M path: the Q8_K planes are read directly; no workspace, one launch.
 int run_small(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs, const float* xd,
-              const int16_t* xbsums, int64_t M, float* y, int64_t ldy, cudaStream_t stream) {
+              const int16_t* xbsums, int64_t M, void* y, int64_t ldy, cudaStream_t stream,
+              const qg::Epi& epi = qg::Epi{}) {
     DevState* ds = nullptr;
     int rc = device_state(&ds);
     if (rc) return rc;
@@ -309,6 +311,7 @@ int run_small(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const
     a.xbs = xbsums;
     a.y = y;
     a.ldy = ldy;
+    a.epi = epi;
     a.sm_count = ds->sm_count;
     a.status = ds->status;
     cudaEvent_t evb = g_ev_before.load(), eva = g_ev_after.load();
@@ -479,7 +482,7 @@ size_t qgemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 }
 
 static int gemm_common_checks(const void* w, int64_t N, int64_t K, const int8_t* xqs, const float* xd,
-                              const int16_t* xbsums, int64_t M, float* y, int64_t ldy) {
+                              const int16_t* xbsums, int64_t M, const void* y, int64_t ldy, int y_align = 4) {
     int rc = check_mk(M, K);
     if (rc) return rc;
     if (N < 1) return fail(QGEMM_EINVAL, "N must be >= 1 (got %lld)", (long long)N);
@@ -490,7 +493,7 @@ static int gemm_common_checks(const void* w, int64_t N, int64_t K, const int8_t*
     if ((rc = check_q8k(xqs, xd, xbsums))) return rc;
     if (!y) return fail(QGEMM_EINVAL, "y is null");
     if (ldy < N) return fail(QGEMM_EINVAL, "ldy (%lld) < N (%lld)", (long long)ldy, (long long)N);
-    if (!aligned(y, 4)) return fail(QGEMM_EALIGN, "y must be 4-byte aligned");
+    if (!aligned(y, y_align)) return fail(QGEMM_EALIGN, "y must be %d-byte aligned", y_align);
     return QGEMM_OK;
 }
 
@@ -603,6 +606,59 @@ int qgemm_q6k_prepared(const void* w_packed, int64_t N, int64_t K, const int8_t*
         return run_small(6, w_packed, N, K, ldw, xqs, xd, xbsums, M, y, ldy, reinterpret_cast<cudaStream_t>(stream));
     return run_tc(6, w_packed, N, K, ldw, xqs, xd, xbsums, M, y, ldy, const_cast<void*>(workspace), workspace_bytes,
                   reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+// The output epilogue of the _ex calls: validated, then passed to the kernels.
+static int epi_checks(const qgemm_epilogue* ep, qg::Epi* out, int* y_align) {
+    *out = qg::Epi{};
+    *y_align = 4;
+    if (!ep) return QGEMM_OK;   // fp32, no bias, no activation
+    if (ep->out_type < QGEMM_OUT_F32 || ep->out_type > QGEMM_OUT_BF16)
+        return fail(QGEMM_EINVAL, "unknown out_type %d", ep->out_type);
+    if (ep->activation < QGEMM_ACT_NONE || ep->activation > QGEMM_ACT_GELU)
+        return fail(QGEMM_EINVAL, "unknown activation %d", ep->activation);
+    if (ep->bias && !aligned(ep->bias, 4)) return fail(QGEMM_EALIGN, "bias must be 4-byte aligned");
+    out->out = ep->out_type;
+    out->act = ep->activation;
+    out->bias = ep->bias;
+    *y_align = ep->out_type == QGEMM_OUT_F32 ? 4 : 2;
+    return QGEMM_OK;
+}
+
+int qgemm_q4k_ex(const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs, const float* xd,
+                 const int16_t* xbsums, int64_t M, void* y, int64_t ldy, const qgemm_epilogue* epilogue,
+                 void* workspace, size_t workspace_bytes, qgemm_stream_t stream) {
+    clear_err();
+    qg::Epi epi;
+    int y_align = 4;
+    int rc = epi_checks(epilogue, &epi, &y_align);
+    if (rc) return rc;
+    rc = gemm_common_checks(w, N, K, xqs, xd, xbsums, M, y, ldy, y_align);
+    if (rc || M == 0) return rc;
+    if (ldw < (K / 256) * qg::Q4K_BLOCK) return fail(QGEMM_EINVAL, "ldw smaller than a row of Q4_K blocks");
+    if (ldw % 16 != 0) return fail(QGEMM_EALIGN, "ldw must be a multiple of 16 bytes");
+    if (use_small(4, M, K))
+        return run_small(4, w, N, K, ldw, xqs, xd, xbsums, M, y, ldy, reinterpret_cast<cudaStream_t>(stream), epi);
+    return run_tc(4, w, N, K, ldw, xqs, xd, xbsums, M, y, ldy, workspace, workspace_bytes,
+                  reinterpret_cast<cudaStream_t>(stream), false, epi);
+}
+
+int qgemm_q6k_ex(const void* w_packed, int64_t N, int64_t K, const int8_t* xqs, const float* xd,
+                 const int16_t* xbsums, int64_t M, void* y, int64_t ldy, const qgemm_epilogue* epilogue,
+                 void* workspace, size_t workspace_bytes, qgemm_stream_t stream) {
+    clear_err();
+    qg::Epi epi;
+    int y_align = 4;
+    int rc = epi_checks(epilogue, &epi, &y_align);
+    if (rc) return rc;
+    rc = gemm_common_checks(w_packed, N, K, xqs, xd, xbsums, M, y, ldy, y_align);
+    if (rc || M == 0) return rc;
+    const int64_t ldw = (K / 256) * qg::Q6K_PACKED;
+    if (use_small(6, M, K))
+        return run_small(6, w_packed, N, K, ldw, xqs, xd, xbsums, M, y, ldy, reinterpret_cast<cudaStream_t>(stream),
+                         epi);
+    return run_tc(6, w_packed, N, K, ldw, xqs, xd, xbsums, M, y, ldy, workspace, workspace_bytes,
+                  reinterpret_cast<cudaStream_t>(stream), false, epi);
 }
 
 int qgemm_get_counters(qgemm_counters* out) {

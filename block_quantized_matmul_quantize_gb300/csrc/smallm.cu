@@ -37,6 +37,7 @@
 #include <unordered_map>
 
 #include "internal.h"
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace qg {
@@ -81,8 +82,8 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[P], int lane) {
 template <int WT, int MT>
 __global__ void __launch_bounds__(32 * SM_MAX_WARPS)
     smallm_kernel(const uint8_t* __restrict__ w, int64_t ldw, int N, int nb, const int8_t* __restrict__ xqs,
-                  const float* __restrict__ xd, const int16_t* __restrict__ xbs, float* __restrict__ y,
-                  int64_t ldy, int stage_rows) {
+                  const float* __restrict__ xd, const int16_t* __restrict__ xbs, void* __restrict__ y,
+                  int64_t ldy, const Epi epi, int stage_rows) {
     constexpr int BLK = SmallTraits<WT>::BLOCK;
     constexpr int P = pow2_at_least(MT);      // token slots per row
     constexpr int VALS = 16;                  // values per thread per reduction batch
@@ -263,7 +264,8 @@ __global__ void __launch_bounds__(32 * SM_MAX_WARPS)
                 if (m < MT && q0 + rr < nr) {
                     float sum = 0.0f;
                     for (int u = 0; u < nw; ++u) sum += rbuf[u][lane];
-                    y[static_cast<int64_t>(m) * ldy + n] = sum;
+                    epi_store(y, static_cast<int64_t>(m) * ldy + n,
+                              epi_value(sum, epi.bias ? epi.bias[n] : 0.0f, epi.act), epi.out);
                 }
             }
         }
@@ -321,7 +323,8 @@ cudaError_t launch_dependent(void (*kernel)(Params...), int grid, int threads, s
 
 template <int WT>
 cudaError_t launch_small_wt(const uint8_t* w, int64_t ldw, int N, int nb, const int8_t* xqs, const float* xd,
-                            const int16_t* xbs, int M, float* y, int64_t ldy, int sm_count, cudaStream_t st) {
+                            const int16_t* xbs, int M, void* y, int64_t ldy, const Epi& epi, int sm_count,
+                            cudaStream_t st) {
     const int threads = 32 * ((nb + 3) / 4);
     const int row_bytes = nb * SmallTraits<WT>::BLOCK;
     // stage: whole rows, at most about SM_STAGE_BYTES; two stage buffers per CTA
@@ -343,7 +346,7 @@ cudaError_t launch_small_wt(const uint8_t* w, int64_t ldw, int N, int nb, const 
         if (stage_rows > max_rows) stage_rows = max_rows;                                               \
         if (stage_rows < 1) stage_rows = 1;                                                             \
         return launch_dependent(k, static_cast<int>(grid), threads, smem, st, w,                        \
-                                ldw, N, nb, xqs, xd, xbs, y, ldy, stage_rows);                          \
+                                ldw, N, nb, xqs, xd, xbs, y, ldy, epi, stage_rows);                     \
     }
     switch (M) {
         QG_SMALL_CASE(1)
@@ -373,9 +376,9 @@ cudaError_t launch_small(const SmallLaunch& a, cudaStream_t st) {
     const uint8_t* w = static_cast<const uint8_t*>(a.w);
     if (a.wtype == 4)
         return launch_small_wt<4>(w, a.ldw, static_cast<int>(a.N), nb, a.xqs, a.xd, a.xbs, static_cast<int>(a.M),
-                                  a.y, a.ldy, a.sm_count, st);
+                                  a.y, a.ldy, a.epi, a.sm_count, st);
     return launch_small_wt<6>(w, a.ldw, static_cast<int>(a.N), nb, a.xqs, a.xd, a.xbs, static_cast<int>(a.M), a.y,
-                              a.ldy, a.sm_count, st);
+                              a.ldy, a.epi, a.sm_count, st);
 }
 
 }  // namespace qg

@@ -194,6 +194,39 @@ QGEMM_API int qgemm_q6k_id(const void *w_packed, int64_t experts, int64_t N, int
                            const float *xd, const int16_t *xbsums, int64_t M, const int32_t *ids, int64_t top_k,
                            float *y, int64_t ldy, void *workspace, size_t workspace_bytes, qgemm_stream_t stream);
 
+/* ------------------------------------------------ output epilogue ----
+ * The GEMM with its output epilogue fused into the final store: the output
+ * type (the pages' OutT template parameter of the BigTile kernels, vllm.cpp
+ * PR #3036 commit 4) and an optional bias and activation:
+ *     y[m][n] = out_type( act( acc[m][n] + bias[n] ) )
+ * acc the fp32 GEMM result of qgemm_q4k / qgemm_q6k (same accuracy bound);
+ * act evaluated in fp32 (ReLU max(v, 0); SiLU v / (1 + exp(-v)); GELU in
+ * its erf form 0.5 v (1 + erf(v / sqrt 2))); fp16 / bf16 outputs rounded to
+ * nearest even.  epilogue == NULL: fp32 output, no bias, no activation.
+ *   out_type     QGEMM_OUT_F32 / _F16 / _BF16: the element type of y.
+ *   bias         device fp32 [N], 4-B aligned, or NULL.
+ *   y, ldy       y aligned to its element size (4 or 2 bytes); ldy in elements.
+ * Other arguments and errors as qgemm_q4k / qgemm_q6k (EINVAL for an unknown
+ * out_type or activation, EALIGN for a misaligned bias). */
+#define QGEMM_OUT_F32 0
+#define QGEMM_OUT_F16 1
+#define QGEMM_OUT_BF16 2
+#define QGEMM_ACT_NONE 0
+#define QGEMM_ACT_RELU 1
+#define QGEMM_ACT_SILU 2
+#define QGEMM_ACT_GELU 3
+typedef struct {
+    int out_type;
+    int activation;
+    const float *bias;
+} qgemm_epilogue;
+QGEMM_API int qgemm_q4k_ex(const void *w, int64_t N, int64_t K, int64_t ldw, const int8_t *xqs, const float *xd,
+                           const int16_t *xbsums, int64_t M, void *y, int64_t ldy, const qgemm_epilogue *epilogue,
+                           void *workspace, size_t workspace_bytes, qgemm_stream_t stream);
+QGEMM_API int qgemm_q6k_ex(const void *w_packed, int64_t N, int64_t K, const int8_t *xqs, const float *xd,
+                           const int16_t *xbsums, int64_t M, void *y, int64_t ldy, const qgemm_epilogue *epilogue,
+                           void *workspace, size_t workspace_bytes, qgemm_stream_t stream);
+
 /* -------------------------------------------- allocation-free Q4_K GEMM ----
  * The pages have no counterpart to this call; it serves callers that cannot
  * allocate device memory where they call the GEMM (for example a plugin

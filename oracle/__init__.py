@@ -68,6 +68,7 @@ class Oracle:
         L.oracle_gemm_q6k.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, vp]
         L.oracle_brute.argtypes = [ctypes.c_int, vp, i64, i64, i64, vp, vp, i64, vp]
         L.oracle_gemm_id.argtypes = [ctypes.c_int, vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, vp]
+        L.oracle_epilogue.argtypes = [vp, i64, i64, vp, ctypes.c_int]
         for f in ("oracle_q4k_fields", "oracle_q4k_pack", "oracle_q6k_fields",
                   "oracle_q6k_pack", "oracle_dequant_q4k", "oracle_dequant_q6k",
                   "oracle_quantize_q8k", "oracle_q8k_to_aos", "oracle_q8k_from_aos",
@@ -175,6 +176,15 @@ class Oracle:
         self.L.oracle_gemm_id(int(wtype), _p(w), E, N, K, w.shape[1], _p(qs), _p(d), _p(bs), M, _p(ids), top_k,
                               _p(y), _p(absc))
         return y, absc
+
+    def epilogue(self, y: np.ndarray, bias=None, act: int = 0) -> np.ndarray:
+        """act(y + bias[n]) in fp64 on a copy of y [R, N] (act 0 none, 1 ReLU, 2 SiLU, 3 GELU)."""
+        out = np.array(y, dtype=np.float64, order="C", copy=True)
+        R, N = out.shape
+        b = None if bias is None else np.ascontiguousarray(bias, np.float32)
+        assert b is None or b.shape == (N,)
+        self.L.oracle_epilogue(_p(out), R, N, None if b is None else _p(b), int(act))
+        return out
 
     def brute(self, wtype: int, w: np.ndarray, K: int, qs, d) -> np.ndarray:
         w = np.ascontiguousarray(w, np.uint8)

@@ -370,6 +370,21 @@ void oracle_gemm_id(int type, const uint8_t *w, int64_t E, int64_t N, int64_t K,
         }
 }
 
+void oracle_epilogue(double *y, int64_t R, int64_t N, const float *bias, int act)
+{
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t n = 0; n < N; ++n) {
+            double v = y[r * N + n] + (bias ? (double)bias[n] : 0.0);
+            if (act == 1)
+                v = v > 0.0 ? v : 0.0;
+            else if (act == 2)
+                v = v / (1.0 + exp(-v));
+            else if (act == 3)
+                v = 0.5 * v * (1.0 + erf(v / sqrt(2.0)));
+            y[r * N + n] = v;
+        }
+}
+
 void oracle_brute(int type, const uint8_t *w, int64_t N, int64_t K, int64_t ldw,
                   const int8_t *qs, const float *dx, int64_t M, double *y)
 {

@@ -106,6 +106,13 @@ void oracle_gemm_id(int type, const uint8_t *w, int64_t E, int64_t N, int64_t K,
                     const int8_t *qs, const float *dx, const int16_t *bsums, int64_t M,
                     const int32_t *ids, int64_t top_k, double *y, double *absc);
 
+/* Output epilogue, in place on y[R][N] in fp64:
+ *   y[r][n] = act(y[r][n] + bias[n])   (bias may be NULL)
+ * act: 0 none, 1 ReLU max(v, 0), 2 SiLU v / (1 + exp(-v)),
+ *      3 GELU 0.5 v (1 + erf(v / sqrt 2)).
+ * (Rounding to an fp16 / bf16 output type is left to the caller.) */
+void oracle_epilogue(double *y, int64_t R, int64_t N, const float *bias, int act);
+
 /* Brute force: dequantize W and X to fp64, then a plain triple loop.
  * type 4 = Q4_K, 6 = Q6_K.  y[M][N]. */
 void oracle_brute(int type, const uint8_t *w, int64_t N, int64_t K, int64_t ldw,

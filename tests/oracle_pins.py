@@ -388,6 +388,35 @@ def check_gemm_id_bad_ids_and_slots(orc):
     assert not np.array_equal(y[0], y[1])   # the two experts differ
 
 
+def check_epilogue_values(orc):
+    """Printed constants: sigmoid(1) = 0.7310585786300049 (SiLU(1)), the standard
+    normal CDF Phi(1) = 0.8413447460685429 (GELU(1)) and 1 - Phi(1) (-GELU(-1));
+    ReLU by sign; large arguments pass through or vanish."""
+    y = np.array([[1.0, -1.0, 0.0, 20.0, -20.0, 3.0, -2.0]])
+    relu = orc.epilogue(y, act=1)[0]
+    assert np.array_equal(relu, [1.0, 0.0, 0.0, 20.0, 0.0, 3.0, 0.0])
+    silu = orc.epilogue(y, act=2)[0]
+    assert abs(silu[0] - 0.7310585786300049) < 1e-15 and silu[2] == 0.0
+    assert abs(silu[3] - 20.0) < 1e-6 and abs(silu[4]) < 1e-7
+    gelu = orc.epilogue(y, act=3)[0]
+    assert abs(gelu[0] - 0.8413447460685429) < 1e-15 and abs(gelu[1] + 0.15865525393145707) < 1e-15
+    assert gelu[2] == 0.0 and gelu[3] == 20.0 and abs(gelu[4]) < 1e-80
+    assert np.array_equal(orc.epilogue(y, act=0), y)
+
+
+def check_epilogue_odd_part_and_bias(orc):
+    """For all three activations act(v) - act(-v) = v; a bias is added per column before the activation."""
+    r = _rng(26)
+    v = r.normal(0, 3, (5, 9))
+    for act in (1, 2, 3):
+        d = orc.epilogue(v, act=act) - orc.epilogue(-v, act=act)
+        assert np.all(np.abs(d - v) <= 1e-12 * (1 + np.abs(v))), act
+    b = r.normal(0, 1, 9).astype(np.float32)
+    assert np.array_equal(orc.epilogue(v, bias=b), v + b.astype(np.float64)[None, :])
+    relu_b = orc.epilogue(v, bias=b, act=1)
+    assert np.array_equal(relu_b, np.maximum(v + b.astype(np.float64)[None, :], 0.0))
+
+
 ALL_CHECKS = [
     check_half_decode,
     check_q4k_scale_bytes_hand, check_q4k_nibble_bytes_hand, check_q4k_roundtrip,
@@ -398,4 +427,5 @@ ALL_CHECKS = [
     check_gemm_vs_brute, check_gemm_unit_scales_q4k, check_gemm_zero_quants_q4k,
     check_gemm_subblock_scales_q4k, check_gemm_q6k_offset, check_gemm_q6k_subblock_scales,
     check_gemm_rows_subset, check_gemm_id_vs_brute, check_gemm_id_bad_ids_and_slots,
+    check_epilogue_values, check_epilogue_odd_part_and_bias,
 ]

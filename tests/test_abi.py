@@ -136,6 +136,24 @@ def test_routed_validation(L):
     assert L.qgemm_id_workspace_bytes(4, 0, 8, 512) == 0
 
 
+def test_epilogue_validation(L):
+    ep = qg._Epilogue(qg.QGEMM_OUT_F16, qg.QGEMM_ACT_SILU, None)
+    F = L.qgemm_q4k_ex
+
+    def q4(e, y=FAKE, ldy=128):
+        return F(FAKE, 128, 512, 288, FAKE, FAKE, FAKE, 4, y, ldy, ctypes.byref(e) if e else None, FAKE, 1 << 20,
+                 None)
+    assert q4(qg._Epilogue(3, 0, None)) == qg.QGEMM_EINVAL          # unknown output type
+    assert q4(qg._Epilogue(0, 4, None)) == qg.QGEMM_EINVAL          # unknown activation
+    assert q4(qg._Epilogue(0, 1, 0x100002)) == qg.QGEMM_EALIGN      # bias not 4-byte aligned
+    assert q4(ep, y=ctypes.c_void_p(0x100001)) == qg.QGEMM_EALIGN   # fp16 y must be 2-byte aligned
+    assert q4(None, y=ctypes.c_void_p(0x100002)) == qg.QGEMM_EALIGN  # fp32 y must be 4-byte aligned
+    assert q4(ep, ldy=100) == qg.QGEMM_EINVAL
+    assert F(FAKE, 128, 512, 288, FAKE, FAKE, FAKE, 0, FAKE, 128, ctypes.byref(ep), FAKE, 1 << 20, None) == 0
+    assert L.qgemm_q6k_ex(FAKE, 128, 384, FAKE, FAKE, FAKE, 4, FAKE, 128, ctypes.byref(ep), FAKE, 1 << 20,
+                          None) == qg.QGEMM_EINVAL
+
+
 def test_size_queries(L):
     assert L.qgemm_workspace_bytes(0, 8, 256) == 0
     assert L.qgemm_workspace_bytes(4, 8, 300) == 0

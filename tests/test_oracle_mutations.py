@@ -28,6 +28,9 @@ MUTATIONS = {
     "gemm_absc_signed": ("absc[r * N + n] += fabs(cb);\n            }\n        }\n    }\n    free(own);\n}\n\nvoid oracle_gemm_q6k", "absc[r * N + n] += cb;\n            }\n        }\n    }\n    free(own);\n}\n\nvoid oracle_gemm_q6k"),
     "gemm_id_expert_offset": ("const uint8_t *we = w + e * N * ldw;", "const uint8_t *we = w + e * ldw;"),
     "gemm_id_pair_row": ("const int64_t pair = m * top_k + s;", "const int64_t pair = m + s * M;"),
+    "epilogue_silu_sign": ("v = v / (1.0 + exp(-v));", "v = v / (1.0 + exp(v));"),
+    "epilogue_gelu_scale": ("v = 0.5 * v * (1.0 + erf(v / sqrt(2.0)));", "v = 0.5 * v * (1.0 + erf(v / 2.0));"),
+    "epilogue_bias_row": ("(bias ? (double)bias[n] : 0.0)", "(bias ? (double)bias[r % N] : 0.0)"),
     "brute_dmin_sign": ("w[i] = d * sc[i / 32] * q[i] - dmin * mn[i / 32];", "w[i] = d * sc[i / 32] * q[i] + dmin * mn[i / 32];"),
 }
 
