@@ -34,4 +34,48 @@ __device__ __forceinline__ void epi_store(void* y, int64_t idx, float v, int out
         static_cast<float*>(y)[idx] = v;
 }
 
+// The epilogue over a thread's C accumulators (one output column n, C
+// consecutive rows m0 .. m0+C-1 with row stride ldy), with each decision taken
+// once outside an unrolled loop: a per-element switch, unrolled C times with
+// the inlined expf / erff, made the kernel's code several times larger (and
+// the GEMM twice as slow, measured on GB300).
+// bn: bias[n] (0 without a bias), loaded by the caller ahead of time.
+// SiLU uses the fast exponential and divide (__expf, __fdividef: relative
+// error a few 1e-6 for |v| < 20, far below an fp16 output's rounding); GELU
+// the library erff.
+template <int C>
+__device__ __forceinline__ void epi_tile(float (&acc)[C], const Epi& epi, float bn, void* y, int64_t ldy, int n,
+                                         int m0, int m_end) {
+    if (epi.bias) {
+#pragma unroll
+        for (int j = 0; j < C; ++j) acc[j] += bn;
+    }
+    if (epi.act == ACT_RELU) {
+#pragma unroll
+        for (int j = 0; j < C; ++j) acc[j] = fmaxf(acc[j], 0.0f);
+    } else if (epi.act == ACT_SILU) {
+#pragma unroll
+        for (int j = 0; j < C; ++j) acc[j] = __fdividef(acc[j], 1.0f + __expf(-acc[j]));
+    } else if (epi.act == ACT_GELU) {
+#pragma unroll
+        for (int j = 0; j < C; ++j) acc[j] = 0.5f * acc[j] * (1.0f + erff(acc[j] * 0.70710678118654752f));
+    }
+    if (epi.out == OUT_F16) {
+        __half* yh = static_cast<__half*>(y);
+#pragma unroll
+        for (int j = 0; j < C; ++j)
+            if (m0 + j < m_end) yh[static_cast<int64_t>(m0 + j) * ldy + n] = __float2half_rn(acc[j]);
+    } else if (epi.out == OUT_BF16) {
+        __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
+#pragma unroll
+        for (int j = 0; j < C; ++j)
+            if (m0 + j < m_end) yb[static_cast<int64_t>(m0 + j) * ldy + n] = __float2bfloat16_rn(acc[j]);
+    } else {
+        float* yf = static_cast<float*>(y);
+#pragma unroll
+        for (int j = 0; j < C; ++j)
+            if (m0 + j < m_end) yf[static_cast<int64_t>(m0 + j) * ldy + n] = acc[j];
+    }
+}
+
 }  // namespace qg

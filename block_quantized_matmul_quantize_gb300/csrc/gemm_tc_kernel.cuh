@@ -787,6 +787,10 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             float acc[CPT];
 #pragma unroll
             for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
+            float bias_n = 0.0f;   // (epilogue variant) loaded now, used at the tile's store
+            if constexpr (EPI) {
+                if (epi.bias && n0 + row < N) bias_n = epi.bias[n0 + row];
+            }
             for (int b = kb0; b < kb1; ++b, ++t) {
                 const int buf = t & 1;
                 const int p = t % SBN;
@@ -906,13 +910,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                         if (m < M) yf[static_cast<int64_t>(m) * ldy + n] = acc[j];
                     }
                 } else {
-                    const float bn = epi.bias ? epi.bias[n] : 0.0f;
-#pragma unroll
-                    for (int j = 0; j < CPT; ++j) {
-                        const int m = m0 + col0 + j;
-                        if (m < M)
-                            epi_store(y, static_cast<int64_t>(m) * ldy + n, epi_value(acc[j], bn, epi.act), epi.out);
-                    }
+                    epi_tile<CPT>(acc, epi, bias_n, y, ldy, n, m0 + col0, M);
                 }
             }
         }

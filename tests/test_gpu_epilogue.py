@@ -3,8 +3,9 @@ fp32 / fp16 / bf16, optional bias, ReLU / SiLU / GELU) on the GPU vs the
 oracle's fp64 GEMM followed by the oracle's fp64 epilogue.
 
 Tolerance per element: the GEMM bound scaled by 1.2 (each activation's slope
-is at most ~1.13), plus 4e-7 |ref| for the fp32 activation, plus the output
-type's half-ulp (2^-11 |ref| for fp16, 2^-8 |ref| for bf16), plus 1e-6."""
+is at most ~1.13), plus 5e-6 |ref| for the fp32 activation (SiLU uses the fast
+exponential and divide: a few 1e-6 relative), plus the output type's half-ulp
+(2^-11 |ref| for fp16, 2^-8 |ref| for bf16), plus 1e-6."""
 import numpy as np
 import pytest
 import torch
@@ -48,7 +49,7 @@ def check(wtype, M, N, K, out_name, act_name, with_bias, seed):
     y = run_ex(wtype, w, K, q, out, bias, ACT[act_name])
     yr, absc = oracle_gemm(wtype, w, K, *q8k_numpy(q))
     ref = oracle.get().epilogue(yr, bias, ACT[act_name])
-    tol = 1.2 * (2e-5 * absc + 1e-6) + (4e-7 + rel) * np.abs(ref) + 1e-6
+    tol = 1.2 * (2e-5 * absc + 1e-6) + (5e-6 + rel) * np.abs(ref) + 1e-6
     err = np.abs(y - ref)
     bad = err > tol
     assert not bad.any(), (f"Q{wtype}_K M{M} {out_name} {act_name} bias={with_bias}: {bad.sum()} elements, "
