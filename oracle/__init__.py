@@ -26,6 +26,7 @@ CFLAGS = ["-O2", "-std=c11", "-fno-fast-math", "-ffp-contract=off",
 Q4K_BYTES = 144
 Q6K_BYTES = 210
 Q8K_BYTES = 292
+PTQ1_BYTES = 28
 
 
 def build(src: str = SRC, out: str = DEFAULT_LIB, force: bool = False) -> str:
@@ -69,6 +70,10 @@ class Oracle:
         L.oracle_brute.argtypes = [ctypes.c_int, vp, i64, i64, i64, vp, vp, i64, vp]
         L.oracle_gemm_id.argtypes = [ctypes.c_int, vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, vp]
         L.oracle_epilogue.argtypes = [vp, i64, i64, vp, ctypes.c_int]
+        L.oracle_ptq1_fields.argtypes = [vp, vp, vp]
+        L.oracle_ptq1_pack.argtypes = [ctypes.c_uint16, vp, vp]
+        L.oracle_dequant_ptq1.argtypes = [vp, vp]
+        L.oracle_gemm_ptq1.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, i64, vp, vp]
         for f in ("oracle_q4k_fields", "oracle_q4k_pack", "oracle_q6k_fields",
                   "oracle_q6k_pack", "oracle_dequant_q4k", "oracle_dequant_q6k",
                   "oracle_quantize_q8k", "oracle_q8k_to_aos", "oracle_q8k_from_aos",
@@ -106,8 +111,25 @@ class Oracle:
         self.L.oracle_q6k_pack(int(d_bits), _p(sc), _p(q), _p(blk))
         return blk
 
+    def ptq1_fields(self, blk: np.ndarray):
+        """(d, t int32 [128]) of one 28-byte PTQ1_0 block (t in 0..2, value t - 1)."""
+        blk = np.ascontiguousarray(blk, dtype=np.uint8)
+        d = np.zeros(1); t = np.zeros(128, np.int32)
+        self.L.oracle_ptq1_fields(_p(blk), _p(d), _p(t))
+        return float(d[0]), t
+
+    def ptq1_pack(self, d_bits: int, t) -> np.ndarray:
+        t = np.ascontiguousarray(t, np.int32)
+        blk = np.zeros(PTQ1_BYTES, np.uint8)
+        self.L.oracle_ptq1_pack(int(d_bits), _p(t), _p(blk))
+        return blk
+
     def dequant(self, wtype: int, blk: np.ndarray) -> np.ndarray:
         blk = np.ascontiguousarray(blk, dtype=np.uint8)
+        if wtype == 1:
+            w = np.zeros(128)
+            self.L.oracle_dequant_ptq1(_p(blk), _p(w))
+            return w
         w = np.zeros(256)
         fn = self.L.oracle_dequant_q4k if wtype == 4 else self.L.oracle_dequant_q6k
         fn(_p(blk), _p(w))
@@ -155,6 +177,9 @@ class Oracle:
             assert rows_arr.size == 0 or (rows_arr.min() >= 0 and rows_arr.max() < M)
         R = rows_arr.size
         y = np.zeros((R, N)); absc = np.zeros((R, N))
+        if wtype == 1:
+            self.L.oracle_gemm_ptq1(_p(w), N, K, w.shape[1], _p(qs), _p(d), M, _p(rows_arr), R, _p(y), _p(absc))
+            return y, absc
         fn = self.L.oracle_gemm_q4k if wtype == 4 else self.L.oracle_gemm_q6k
         fn(_p(w), N, K, w.shape[1], _p(qs), _p(d), _p(bs), M, _p(rows_arr), R, _p(y), _p(absc))
         return y, absc

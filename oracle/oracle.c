@@ -174,6 +174,90 @@ void oracle_dequant_q6k(const uint8_t *blk, double w[256])
  *              away from zero;
  *   bsums[g] = sum of q_{16g .. 16g+15}.
  */
+/* ---- PTQ1_0: 24 qs bytes (5 trits each), 2 qh bytes (4 trits each), fp16 d */
+static int ptq1_digit(int byte, int i)
+{
+    int v = byte;
+    for (int k = 0; k < i; ++k)
+        v /= 3;
+    return v % 3;
+}
+
+void oracle_ptq1_fields(const uint8_t *blk, double *d, int t[128])
+{
+    for (int k = 0; k < 120; ++k)
+        t[k] = ptq1_digit(blk[k % 24], k / 24);
+    for (int r = 0; r < 8; ++r)
+        t[120 + r] = ptq1_digit(blk[24 + r % 2], r / 2);
+    *d = oracle_half_to_double(rd16(blk + 26));
+}
+
+void oracle_ptq1_pack(uint16_t d_bits, const int t[128], uint8_t *blk)
+{
+    for (int j = 0; j < 24; ++j) {
+        int v = 0;
+        for (int i = 4; i >= 0; --i)
+            v = 3 * v + t[24 * i + j];
+        blk[j] = (uint8_t)v;
+    }
+    for (int h = 0; h < 2; ++h) {
+        int v = 0;
+        for (int i = 3; i >= 0; --i)
+            v = 3 * v + t[120 + 2 * i + h];
+        blk[24 + h] = (uint8_t)v;
+    }
+    wr16(blk + 26, d_bits);
+}
+
+void oracle_dequant_ptq1(const uint8_t *blk, double w[128])
+{
+    double d;
+    int t[128];
+    oracle_ptq1_fields(blk, &d, t);
+    for (int k = 0; k < 128; ++k)
+        w[k] = d * (double)(t[k] - 1);
+}
+
+void oracle_gemm_ptq1(const uint8_t *w, int64_t N, int64_t K, int64_t ldw,
+                      const int8_t *qs, const float *dx, int64_t M, const int64_t *rows, int64_t nrows,
+                      double *y, double *absc)
+{
+    int64_t nb = K / 256;
+    int64_t *own = NULL;
+    if (!rows) {
+        own = (int64_t *)malloc((size_t)(M > 0 ? M : 1) * sizeof(int64_t));
+        for (int64_t i = 0; i < M; ++i)
+            own[i] = i;
+        rows = own;
+        nrows = M;
+    }
+    for (int64_t r = 0; r < nrows; ++r)
+        for (int64_t n = 0; n < N; ++n) {
+            y[r * N + n] = 0.0;
+            if (absc)
+                absc[r * N + n] = 0.0;
+        }
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < nb; ++b) {
+            double d[2];
+            int t[2][128];
+            for (int h = 0; h < 2; ++h)
+                oracle_ptq1_fields(w + n * ldw + (2 * b + h) * ORACLE_PTQ1_BYTES, &d[h], t[h]);
+            for (int64_t r = 0; r < nrows; ++r) {
+                const int8_t *xq = qs + rows[r] * K + b * 256;
+                int64_t I[2] = {0, 0};
+                for (int h = 0; h < 2; ++h)
+                    for (int k = 0; k < 128; ++k)
+                        I[h] += (int64_t)(t[h][k] - 1) * xq[128 * h + k];
+                double cb = (double)dx[rows[r] * nb + b] * (d[0] * (double)I[0] + d[1] * (double)I[1]);
+                y[r * N + n] += cb;
+                if (absc)
+                    absc[r * N + n] += fabs(cb);
+            }
+        }
+    free(own);
+}
+
 void oracle_quantize_q8k(const float *x, int64_t M, int64_t K, int64_t ldx,
                          int8_t *qs, float *d, int16_t *bsums)
 {
@@ -396,6 +480,11 @@ void oracle_brute(int type, const uint8_t *w, int64_t N, int64_t K, int64_t ldw,
             xd[m * K + k] = (double)dx[m * nb + k / 256] * (double)qs[m * K + k];
     for (int64_t n = 0; n < N; ++n) {
         for (int64_t b = 0; b < nb; ++b) {
+            if (type == 1) {   /* PTQ1_0: two 128-weight blocks per 256 */
+                oracle_dequant_ptq1(w + n * ldw + (2 * b) * ORACLE_PTQ1_BYTES, wd + b * 256);
+                oracle_dequant_ptq1(w + n * ldw + (2 * b + 1) * ORACLE_PTQ1_BYTES, wd + b * 256 + 128);
+                continue;
+            }
             const uint8_t *blk = w + n * ldw + b * (type == 4 ? ORACLE_Q4K_BYTES : ORACLE_Q6K_BYTES);
             if (type == 4)
                 oracle_dequant_q4k(blk, wd + b * 256);

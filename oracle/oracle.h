@@ -46,6 +46,7 @@ extern "C" {
 #define ORACLE_QK 256          /* weights per superblock            */
 #define ORACLE_Q4K_BYTES 144   /* 2+2+12+128                        */
 #define ORACLE_Q6K_BYTES 210   /* 128+64+16+2                       */
+#define ORACLE_PTQ1_BYTES 28   /* 24+2+2, 128 ternary weights        */
 #define ORACLE_Q8K_BYTES 292   /* 4+256+32 (interop AoS form)       */
 
 /* IEEE binary16 bit pattern -> double (exact). */
@@ -68,6 +69,25 @@ void oracle_q6k_pack(uint16_t d_bits, const int sc[16], const int q[256],
 /* Dequantize one block to 256 doubles (the spec formulas, in fp64). */
 void oracle_dequant_q4k(const uint8_t *blk, double w[256]);
 void oracle_dequant_q6k(const uint8_t *blk, double w[256]);
+
+/* PTQ1_0 ("cuda: branch-free PTQ1_0 MMQ tile loader ...", llama.cpp PR #214,
+ * commit "load_tiles_ptq1_0"): 128 ternary weights in 28 bytes -- qs words
+ * 0-5 (24 bytes, 5 trits each), word 6 = qh[0] | qh[1] << 8 | d << 16 (two
+ * bytes of 4 trits each, then the fp16 scale).  The pages leave the trit
+ * order open; the reading here: a byte holds its digits base 3, least
+ * significant first (digit i = (byte / 3^i) mod 3), a digit t stands for the
+ * value t - 1, and the weights are digit-major -- weight k < 120 is digit
+ * k / 24 of qs byte k % 24, weight 120 + r is digit r / 2 of qh byte r % 2.
+ *   w_k = d * (t_k - 1). */
+void oracle_ptq1_fields(const uint8_t *blk, double *d, int t[128]);
+void oracle_ptq1_pack(uint16_t d_bits, const int t[128], uint8_t *blk);
+void oracle_dequant_ptq1(const uint8_t *blk, double w[128]);
+/* Y = X_q8k * W_ptq1^T as for Q4_K/Q6_K, K a multiple of 256 (two blocks per
+ * Q8_K superblock b): c_b = dx[m][b] * (d_0 * I_0 + d_1 * I_1), I the exact
+ * integer dot of the block's t - 1 with the activations. */
+void oracle_gemm_ptq1(const uint8_t *w, int64_t N, int64_t K, int64_t ldw,
+                      const int8_t *qs, const float *dx, int64_t M, const int64_t *rows, int64_t nrows,
+                      double *y, double *absc);
 
 /* Q8_K quantizer, rows of x[M][ldx] fp32 with K % 256 == 0.
  * Outputs (SoA): qs[M][K] int8, d[M][K/256] fp32, bsums[M][K/16] int16. */
@@ -114,7 +134,7 @@ void oracle_gemm_id(int type, const uint8_t *w, int64_t E, int64_t N, int64_t K,
 void oracle_epilogue(double *y, int64_t R, int64_t N, const float *bias, int act);
 
 /* Brute force: dequantize W and X to fp64, then a plain triple loop.
- * type 4 = Q4_K, 6 = Q6_K.  y[M][N]. */
+ * type 4 = Q4_K, 6 = Q6_K, 1 = PTQ1_0.  y[M][N]. */
 void oracle_brute(int type, const uint8_t *w, int64_t N, int64_t K, int64_t ldw,
                   const int8_t *qs, const float *dx, int64_t M, double *y);
 

@@ -98,6 +98,23 @@ def gen_q6k(N: int, K: int, seed: int) -> np.ndarray:
     return w.reshape(N, nb * Q6K_BYTES)
 
 
+PTQ1_BYTES = 28
+
+
+def gen_ptq1(N: int, K: int, seed: int) -> np.ndarray:
+    """PTQ1_0 weights, uint8 [N, (K/128)*28]: 24 qs bytes drawn uniform over the
+    243 five-trit values, 2 qh bytes over the 81 four-trit values, fp16 d @26
+    drawn uniform in [1e-3, 1e-2] (each valid byte value is equally likely, so
+    every trit is uniform over {0, 1, 2})."""
+    assert K % 256 == 0
+    nb = K // 128
+    qs = (splitmix64(seed * 4 + 1, N * nb * 24) % np.uint64(243)).astype(np.uint8).reshape(N * nb, 24)
+    qh = (splitmix64(seed * 4 + 2, N * nb * 2) % np.uint64(81)).astype(np.uint8).reshape(N * nb, 2)
+    d = fp16_uniform_bits(seed * 4 + 3, N * nb, 1e-3, 1e-2)
+    w = np.concatenate([qs, qh, d.view(np.uint8).reshape(-1, 2)], axis=1)
+    return np.ascontiguousarray(w.reshape(N, nb * PTQ1_BYTES))
+
+
 def outlier_columns(K: int, seed: int, frac: float = 0.01) -> np.ndarray:
     """round(frac*K) distinct column indices, chosen by a seeded shuffle."""
     k = int(round(frac * K))

@@ -417,6 +417,71 @@ def check_epilogue_odd_part_and_bias(orc):
     assert np.array_equal(relu_b, np.maximum(v + b.astype(np.float64)[None, :], 0.0))
 
 
+def check_ptq1_bytes_hand(orc):
+    """Hand-derived PTQ1_0 bytes: a lone trit 1 at weight k = 24 i + j sets qs
+    byte j to 3^i; weight 120 + r sets qh byte r % 2 to 3^(r // 2); all 2s give
+    242 (qs) and 80 (qh); d sits little-endian at byte 26."""
+    t = np.zeros(128, np.int32)
+    t[49] = 1                       # i = 2, j = 1
+    t[123] = 1                      # r = 3: qh byte 1, digit 1
+    blk = orc.ptq1_pack(0x3800, t)
+    exp = np.zeros(28, np.uint8)
+    exp[1] = 9
+    exp[25] = 3
+    exp[26], exp[27] = 0x00, 0x38
+    assert np.array_equal(blk, exp), blk
+    blk2 = orc.ptq1_pack(0x3C00, np.full(128, 2, np.int32))
+    assert (blk2[:24] == 242).all() and (blk2[24:26] == 80).all()
+    # decode of a hand-built byte: 5 = 2 + 1*3 -> weight 5 is +d, weight 29 is 0, all others -d
+    raw = np.zeros(28, np.uint8)
+    raw[5] = 5
+    raw[26], raw[27] = 0x00, 0x38   # d = 0.5
+    w = orc.dequant(1, raw)
+    want = np.full(128, -0.5)
+    want[5], want[29] = 0.5, 0.0
+    assert np.array_equal(w, want)
+
+
+def check_ptq1_roundtrip(orc):
+    """Every valid byte value decodes to its 5 (qs) or 4 (qh) base-3 digits and packs back."""
+    r = _rng(27)
+    for _ in range(20):
+        t = r.integers(0, 3, 128).astype(np.int32)
+        d_bits = int(r.integers(0x1000, 0x5000))
+        d, t2 = orc.ptq1_fields(orc.ptq1_pack(d_bits, t))
+        assert np.array_equal(t, t2) and d == orc.half_to_double(d_bits)
+    blk = np.zeros(28, np.uint8)
+    for v in range(243):
+        blk[7] = v
+        _, t = orc.ptq1_fields(blk)
+        digits = [t[24 * i + 7] for i in range(5)]
+        assert sum(dg * 3 ** i for i, dg in enumerate(digits)) == v
+    blk[7] = 0
+    for v in range(81):
+        blk[24] = v
+        _, t = orc.ptq1_fields(blk)
+        assert sum(t[120 + 2 * i] * 3 ** i for i in range(4)) == v
+
+
+def check_gemm_ptq1(orc):
+    """PTQ1_0 GEMM vs the brute force (dequantized weights, plain dot); all +1
+    weights with d = 1 and activation scale 1 give numpy's integer row sums."""
+    r = _rng(28)
+    for (M, N, K) in ((1, 1, 256), (3, 4, 512), (5, 2, 768)):
+        w = synth.gen_ptq1(N, K, int(r.integers(1 << 30)))
+        qs, d, bs = orc.quantize_q8k(synth.gen_x(M, K, int(r.integers(1 << 30))))
+        y, absc = orc.gemm(1, w, K, qs, d, bs)
+        yb = orc.brute(1, w, K, qs, d)
+        assert np.all(np.abs(y - yb) <= 1e-12 * absc + 1e-300), (M, N, K)
+    K, M = 512, 3
+    blk = orc.ptq1_pack(0x3C00, np.full(128, 2, np.int32))
+    w = np.tile(blk, (2, K // 128))
+    qs, d, bs = _q8k_direct(r, M, K)
+    y, _ = orc.gemm(1, w, K, qs, d, bs)
+    tot = qs.astype(np.int64).sum(axis=1).astype(np.float64)
+    assert np.array_equal(y, np.stack([tot, tot], axis=1))
+
+
 ALL_CHECKS = [
     check_half_decode,
     check_q4k_scale_bytes_hand, check_q4k_nibble_bytes_hand, check_q4k_roundtrip,
@@ -428,4 +493,5 @@ ALL_CHECKS = [
     check_gemm_subblock_scales_q4k, check_gemm_q6k_offset, check_gemm_q6k_subblock_scales,
     check_gemm_rows_subset, check_gemm_id_vs_brute, check_gemm_id_bad_ids_and_slots,
     check_epilogue_values, check_epilogue_odd_part_and_bias,
+    check_ptq1_bytes_hand, check_ptq1_roundtrip, check_gemm_ptq1,
 ]

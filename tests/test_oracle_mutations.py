@@ -31,6 +31,9 @@ MUTATIONS = {
     "epilogue_silu_sign": ("v = v / (1.0 + exp(-v));", "v = v / (1.0 + exp(v));"),
     "epilogue_gelu_scale": ("v = 0.5 * v * (1.0 + erf(v / sqrt(2.0)));", "v = 0.5 * v * (1.0 + erf(v / 2.0));"),
     "epilogue_bias_row": ("(bias ? (double)bias[n] : 0.0)", "(bias ? (double)bias[r % N] : 0.0)"),
+    "ptq1_digit_order": ("t[k] = ptq1_digit(blk[k % 24], k / 24);", "t[k] = ptq1_digit(blk[k % 24], 4 - k / 24);"),
+    "ptq1_qh_byte": ("t[120 + r] = ptq1_digit(blk[24 + r % 2], r / 2);", "t[120 + r] = ptq1_digit(blk[24 + r / 4], r % 4);"),
+    "ptq1_gemm_offset": ("I[h] += (int64_t)(t[h][k] - 1) * xq[128 * h + k];", "I[h] += (int64_t)t[h][k] * xq[128 * h + k];"),
     "brute_dmin_sign": ("w[i] = d * sc[i / 32] * q[i] - dmin * mn[i / 32];", "w[i] = d * sc[i / 32] * q[i] + dmin * mn[i / 32];"),
 }
 
