@@ -39,7 +39,7 @@ class QgemmError(RuntimeError):
 class _Counters(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
                 ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small", "q6k_prepack", "split_k",
-                 "routed")]
+                 "routed", "ptq1_tc", "ptq1_prepack")]
 
 
 class _Epilogue(ctypes.Structure):
@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
             "qgemm_q4k_ex": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, ctypes.POINTER(_Epilogue), vp, sz, vp],
                              i32),
             "qgemm_q6k_ex": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, ctypes.POINTER(_Epilogue), vp, sz, vp], i32),
+            "qgemm_ptq1_packed_bytes": ([i64, i64], sz),
+            "qgemm_ptq1_prepack": ([vp, i64, i64, i64, vp, vp], i32),
+            "qgemm_ptq1": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
             "qgemm_get_counters": ([ctypes.POINTER(_Counters)], i32),
             "qgemm_reset_counters": ([], i32),
             "qgemm_get_device_status": ([ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)], i32),
@@ -317,6 +320,29 @@ def qgemm_q6k_ex(w_packed: torch.Tensor, N: int, K: int, x: Q8K, out_dtype=torch
     ep = _epilogue(out_dtype, bias, activation)
     _check(lib().qgemm_q6k_ex(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y), y.stride(0),
                               ctypes.byref(ep), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return y
+
+
+PTQ1_BLOCK_BYTES = 28
+
+
+def qgemm_ptq1_prepack(w: torch.Tensor, N: int, K: int, stream=None) -> torch.Tensor:
+    """PTQ1_0 rows uint8 [N, ldw] (28-byte blocks) -> repacked uint8 [N, K/4] (32-byte blocks)."""
+    assert w.dtype == torch.uint8 and w.dim() == 2 and w.stride(1) == 1
+    out = torch.empty((N, K // 4), dtype=torch.uint8, device=w.device)
+    _check(lib().qgemm_ptq1_prepack(_ptr(w), N, K, w.stride(0), _ptr(out), _stream(stream)))
+    return out
+
+
+def qgemm_ptq1(w_packed: torch.Tensor, N: int, K: int, x: Q8K, y: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y[M, N] = X_q8k @ W_ptq1^T from qgemm_ptq1_prepack's output."""
+    M = x.M
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
+    workspace = _workspace(M, N, K, workspace, x.qs.device)
+    _check(lib().qgemm_ptq1(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y), y.stride(0),
+                            _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
 

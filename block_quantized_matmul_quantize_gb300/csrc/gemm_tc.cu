@@ -11,18 +11,22 @@ size_t tc_smem_bytes(int wtype, int bm) {
     if (wtype == W && bm == B) return Layout<W, B>::TOTAL;
     QG_CASE(4, 16) QG_CASE(4, 32) QG_CASE(4, 64) QG_CASE(4, 128)
     QG_CASE(6, 16) QG_CASE(6, 32) QG_CASE(6, 64) QG_CASE(6, 128)
+    QG_CASE(1, 16) QG_CASE(1, 32) QG_CASE(1, 64) QG_CASE(1, 128)
 #undef QG_CASE
     return 0;
 }
 
 cudaError_t tc_prepare(int wtype, int bm) {
-    cudaError_t e = tc_prepare_epi(wtype, bm);
-    if (e == cudaSuccess) e = tc_prepare_routed(wtype, bm);
-    if (e != cudaSuccess) return e;
+    if (wtype == 4 || wtype == 6) {   // (the epilogue and routed variants: Q4_K and Q6_K)
+        cudaError_t e = tc_prepare_epi(wtype, bm);
+        if (e == cudaSuccess) e = tc_prepare_routed(wtype, bm);
+        if (e != cudaSuccess) return e;
+    }
 #define QG_CASE(W, B) \
     if (wtype == W && bm == B) return prepare_t<W, B, VAR_PLAIN>();
     QG_CASE(4, 16) QG_CASE(4, 32) QG_CASE(4, 64) QG_CASE(4, 128)
     QG_CASE(6, 16) QG_CASE(6, 32) QG_CASE(6, 64) QG_CASE(6, 128)
+    QG_CASE(1, 16) QG_CASE(1, 32) QG_CASE(1, 64) QG_CASE(1, 128)
 #undef QG_CASE
     return cudaErrorInvalidValue;
 }
@@ -34,6 +38,7 @@ cudaError_t launch_gemm_tc(const TcLaunch& a, cudaStream_t s) {
     if (a.wtype == W && a.bm == B) return launch_t<W, B, VAR_PLAIN>(a, s);
     QG_CASE(4, 16) QG_CASE(4, 32) QG_CASE(4, 64) QG_CASE(4, 128)
     QG_CASE(6, 16) QG_CASE(6, 32) QG_CASE(6, 64) QG_CASE(6, 128)
+    QG_CASE(1, 16) QG_CASE(1, 32) QG_CASE(1, 64) QG_CASE(1, 128)
 #undef QG_CASE
     return cudaErrorInvalidValue;
 }

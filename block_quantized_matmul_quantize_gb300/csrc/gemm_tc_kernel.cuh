@@ -83,7 +83,7 @@ constexpr int BN = 128;        // weight rows per CTA = MMA M
 // pay for the registers it costs the epilogue (measured on GB300).
 template <int WT>
 struct Warps {
-    static constexpr int UNPACK_GROUPS = WT == 6 ? 2 : 1;
+    static constexpr int UNPACK_GROUPS = WT == 4 ? 1 : 2;
     static constexpr int EPI0 = 4 + 4 * UNPACK_GROUPS;
     static constexpr int N = EPI0 + 8;
     static constexpr int THREADS = 32 * N;
@@ -116,6 +116,12 @@ struct WTraits<4> {
 template <>
 struct WTraits<6> {
     static constexpr int RAW_BLOCK = Q6K_PACKED;
+    static constexpr bool CORR = false;
+};
+// PTQ1_0: a superblock's two 128-weight blocks, each repacked to 32 bytes
+template <>
+struct WTraits<1> {
+    static constexpr int RAW_BLOCK = 2 * PTQ1_PACKED;
     static constexpr bool CORR = false;
 };
 
@@ -265,6 +271,60 @@ __device__ __forceinline__ void unpack_q6k_chunk(const uint8_t* blk, int c, cons
             o[16 * pp + 2 * k + 1] = hmul2u(hsub2u(b, OFF), sc);
         }
     }
+}
+
+// PTQ1_0 ("cuda: branch-free PTQ1_0 MMQ tile loader ...", llama.cpp PR
+// #214): one 32-byte block (28 + 4 zero) -> its 128 weights as fp16
+// (t - 1) * d, weights 0..63 in v0 and 64..127 in v1, each aligned group of 4
+// in the K order 0, 2, 1, 3.  Weight 24 i + 4 w + b (b < 4) is base-3 digit i
+// of qs byte 4 w + b, so a qs word and a digit give one aligned group of 4:
+// bytes 0 and 2 of the word (16-bit lanes of w & 0x00ff00ff) hold weights b =
+// 0 and 2, bytes 1 and 3 weights 1 and 3.  One division by 3 per digit and
+// lane pair, x / 3 = (x * 171) >> 9 (exact for x < 256, no carry between the
+// lanes); the digit lands in bits 0-1 of its lane, under the fp16 exponent
+// 0x64 (1024 + t), and (1024 + t - 1025) * d is exact.  Weights 120 + r are
+// digit r / 2 of qh byte r % 2.  No branch depends on the lane or the data.
+__device__ __forceinline__ void unpack_ptq1_block(const uint8_t* blk, uint32_t (&v0)[32], uint32_t (&v1)[32]) {
+    const uint4 a = *reinterpret_cast<const uint4*>(blk);
+    const uint4 b = *reinterpret_cast<const uint4*>(blk + 16);
+    const uint32_t qw[6] = {a.x, a.y, a.z, a.w, b.x, b.y};
+    const uint32_t tail = b.z;                        // qh[0] | qh[1] << 8 | d << 16
+    const uint32_t d2 = (tail >> 16) * 0x10001u;      // fp16 d in both halves
+    constexpr uint32_t MAGIC = 0x64006400u, M1025 = 0xE401E401u;   // fp16 1024 | t, -1025
+    auto val = [&](uint32_t t2) { return hmul2u(hadd2u(t2 | MAGIC, M1025), d2); };
+#pragma unroll
+    for (int w = 0; w < 6; ++w) {
+        uint32_t xl = qw[w] & 0x00ff00ffu, xh = (qw[w] >> 8) & 0x00ff00ffu;
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+            const uint32_t ql = ((xl * 171u) >> 9) & 0x007f007fu, qh = ((xh * 171u) >> 9) & 0x007f007fu;
+            const int k = 24 * i + 4 * w;             // first weight of the group (a constant here)
+            const uint32_t lo = val(xl - 3u * ql), hi = val(xh - 3u * qh);   // weights k, k+2 / k+1, k+3
+            if (k < 64) {
+                v0[k >> 1] = lo;
+                v0[(k >> 1) + 1] = hi;
+            } else {
+                v1[(k - 64) >> 1] = lo;
+                v1[((k - 64) >> 1) + 1] = hi;
+            }
+            xl = ql;
+            xh = qh;
+        }
+    }
+    // qh[0] in lane 0, qh[1] in lane 1: digits i of both bytes per step
+    uint32_t x = (tail & 0xffu) | ((tail & 0xff00u) << 8);
+    uint32_t dg[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t q = ((x * 171u) >> 9) & 0x007f007fu;
+        dg[i] = x - 3u * q;
+        x = q;
+    }
+    // group 120..123: (qh0 digit 0, qh0 digit 1), (qh1 digit 0, qh1 digit 1); 124..127 with digits 2, 3
+    v1[28] = val(__byte_perm(dg[0], dg[1], 0x5410));
+    v1[29] = val(__byte_perm(dg[0], dg[1], 0x7632));
+    v1[30] = val(__byte_perm(dg[2], dg[3], 0x5410));
+    v1[31] = val(__byte_perm(dg[2], dg[3], 0x7632));
 }
 
 // Kernel variants, each compiled only with the code it needs (measured on
@@ -651,6 +711,33 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                             unpack_q4k_chunk(blk, 2 * j + 1, sl, hmul2u(sl, H2_M1024), hmul2u(sh, H2_1_16),
                                              hmul2u(sh, H2_M64), v1);
                         }
+                        tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
+                        pend = s;
+                    }
+                    if (!ok) break;
+                } else if constexpr (WT == 1) {
+                    // PTQ1_0: the scale d is folded into the operand (an exact fp16
+                    // product), so the superblock's epilogue factor e is 1
+                    if (grp == 0) {
+                        if (!mbar_test_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1)) signal();
+                        ok = mbar_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1, abort_flag, status, 8);
+                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                        reinterpret_cast<float*>(sb_slot(p) + L::SB_E)[row] = 1.0f;
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sb_full[p]);
+                    }
+                    // this warp's K128 steps: step j is block j of the superblock
+#pragma unroll 1
+                    for (int j = j0; j < j1; ++j) {
+                        const int g = 2 * t + j;
+                        const int s = g % A_STAGES;
+                        uint32_t v0[32], v1[32];
+                        unpack_ptq1_block(blk + PTQ1_PACKED * j, v0, v1);
+                        signal();
+                        ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
+                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                        tc_fence_after();
+                        tmem_st_32x32b_x32(lane_base + 64 * s, v0);
                         tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
                         pend = s;
                     }

@@ -36,6 +36,8 @@ struct Epi {
 constexpr int Q4K_BLOCK = 144;
 constexpr int Q6K_BLOCK = 210;
 constexpr int Q6K_PACKED = 224;                 // 210 B + 14 B of zero padding (16-B aligned)
+constexpr int PTQ1_BLOCK = 28;                  // 128 ternary weights: 24 B qs, 2 B qh, fp16 d
+constexpr int PTQ1_PACKED = 32;                 // 28 B + 4 B of zero padding (16-B aligned)
 
 // ---- kernels' host launchers (each returns cudaError_t of the launch) ----
 // With xh != nullptr the same launch also writes the tile GEMM's operand
@@ -148,6 +150,8 @@ cudaError_t launch_small(const SmallLaunch& a, cudaStream_t s);
 // Record a one-line message for qgemm_last_error() and return `code`.
 int set_last_error(int code, const char* msg);
 
+cudaError_t launch_ptq1_prepack(const uint8_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* out,
+                                cudaStream_t s);
 cudaError_t launch_q6k_prepack(const uint8_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* out,
                                cudaStream_t s);
 

@@ -31,8 +31,9 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ------------------------------------------------------------ global state
-std::atomic<uint64_t> g_cnt[9];
-enum { C_QUANT, C_XPREP, C_Q4K_TC, C_Q6K_TC, C_Q4K_SMALL, C_Q6K_SMALL, C_PREPACK, C_SPLITK, C_ROUTED };
+std::atomic<uint64_t> g_cnt[11];
+enum { C_QUANT, C_XPREP, C_Q4K_TC, C_Q6K_TC, C_Q4K_SMALL, C_Q6K_SMALL, C_PREPACK, C_SPLITK, C_ROUTED, C_PTQ1_TC,
+       C_PTQ1_PREPACK };
 // SMALL_M_MAX defaults to the measured crossover: the streaming kernel wins up
 // to 8 tokens at K = N = 5120 and at K = 4096, N = 14336.
 std::atomic<int64_t> g_opt[3] = {{qg::SMALL_M_LIMIT}, {0}, {0}};
@@ -66,7 +67,7 @@ int device_state(DevState** out) {
         st.init = true;
         e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status), g_qgemm_status);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
-        for (int wt : {4, 6})
+        for (int wt : {4, 6, 1})
             for (int bm : {16, 32, 64, 128})
                 if (e == cudaSuccess) e = qg::tc_prepare(wt, bm);
         st.init_err = e;
@@ -250,7 +251,7 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
     }
 
     CUtensorMap tm_w, tm_xh, tm_xbs, tm_dx;
-    const int blk = wtype == 4 ? qg::Q4K_BLOCK : qg::Q6K_PACKED;
+    const int blk = wtype == 4 ? qg::Q4K_BLOCK : wtype == 6 ? qg::Q6K_PACKED : 2 * qg::PTQ1_PACKED;
     if ((rc = make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, uint64_t(nb) * blk, N, ldw, blk, 128,
                        CU_TENSOR_MAP_SWIZZLE_NONE)))
         return rc;
@@ -287,7 +288,7 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
     e = qg::launch_gemm_tc(a, stream);
     if (eva) cudaEventRecord(eva, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tile GEMM launch");
-    g_cnt[wtype == 4 ? C_Q4K_TC : C_Q6K_TC]++;
+    g_cnt[wtype == 4 ? C_Q4K_TC : wtype == 6 ? C_Q6K_TC : C_PTQ1_TC]++;
     if (pl.work.parts > 1) g_cnt[C_SPLITK]++;
     return QGEMM_OK;
 }
@@ -672,7 +673,39 @@ int qgemm_get_counters(qgemm_counters* out) {
     out->q6k_prepack = g_cnt[C_PREPACK];
     out->split_k = g_cnt[C_SPLITK];
     out->routed = g_cnt[C_ROUTED];
+    out->ptq1_tc = g_cnt[C_PTQ1_TC];
+    out->ptq1_prepack = g_cnt[C_PTQ1_PREPACK];
     return QGEMM_OK;
+}
+
+size_t qgemm_ptq1_packed_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % 256) return 0;
+    return size_t(N) * size_t(K / 128) * qg::PTQ1_PACKED;
+}
+
+int qgemm_ptq1_prepack(const void* w, int64_t N, int64_t K, int64_t ldw, void* w_packed, qgemm_stream_t stream) {
+    clear_err();
+    if (N < 1) return fail(QGEMM_EINVAL, "N must be >= 1");
+    if (K < 256 || K % 256) return fail(QGEMM_EINVAL, "K must be a positive multiple of 256");
+    if (!w || !w_packed) return fail(QGEMM_EINVAL, "null pointer");
+    if (ldw < (K / 128) * qg::PTQ1_BLOCK) return fail(QGEMM_EINVAL, "ldw smaller than a row of PTQ1_0 blocks");
+    if (!aligned(w_packed, 16)) return fail(QGEMM_EALIGN, "w_packed must be 16-byte aligned");
+    cudaError_t e = qg::launch_ptq1_prepack(static_cast<const uint8_t*>(w), N, K, ldw,
+                                            static_cast<uint8_t*>(w_packed), reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "prepack launch");
+    g_cnt[C_PTQ1_PREPACK]++;
+    return QGEMM_OK;
+}
+
+int qgemm_ptq1(const void* w_packed, int64_t N, int64_t K, const int8_t* xqs, const float* xd, const int16_t* xbsums,
+               int64_t M, float* y, int64_t ldy, void* workspace, size_t workspace_bytes, qgemm_stream_t stream) {
+    clear_err();
+    int rc = gemm_common_checks(w_packed, N, K, xqs, xd, xbsums, M, y, ldy);
+    if (rc || M == 0) return rc;
+    const int64_t ldw = (K / 128) * qg::PTQ1_PACKED;
+    // (every M on the tile GEMM: the small-M streaming kernel has no PTQ1_0 decode)
+    return run_tc(1, w_packed, N, K, ldw, xqs, xd, xbsums, M, y, ldy, workspace, workspace_bytes,
+                  reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 size_t qgemm_id_workspace_bytes(int64_t M, int64_t top_k, int64_t experts, int64_t K) {

@@ -155,23 +155,25 @@ __global__ void xprep_kernel(const int8_t* __restrict__ qs, const float* __restr
     }
 }
 
-// Q6_K 210-byte blocks -> 224-byte blocks (same bytes, 14 zero bytes after),
-// so that every block and every row starts on a 16-byte boundary.
-__global__ void q6k_prepack_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t nb, int64_t ldw,
-                                   uint8_t* __restrict__ out) {
-    const int64_t total = N * nb * (Q6K_PACKED / 16);
+// SRC-byte blocks -> DST-byte blocks (the same bytes, zeros after), so that
+// every block and every row starts on a 16-byte boundary: Q6_K 210 -> 224,
+// PTQ1_0 28 -> 32.
+template <int SRC, int DST>
+__global__ void prepack_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t nb, int64_t ldw,
+                               uint8_t* __restrict__ out) {
+    const int64_t total = N * nb * (DST / 16);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int64_t blk = i / (Q6K_PACKED / 16);
-        const int part = static_cast<int>(i - blk * (Q6K_PACKED / 16));
+        const int64_t blk = i / (DST / 16);
+        const int part = static_cast<int>(i - blk * (DST / 16));
         const int64_t n = blk / nb;
         const int64_t b = blk - n * nb;
-        const uint8_t* src = w + n * ldw + b * Q6K_BLOCK;
+        const uint8_t* src = w + n * ldw + b * SRC;
         uint8_t v[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int off = part * 16 + j;
-            v[j] = off < Q6K_BLOCK ? src[off] : 0;
+            v[j] = off < SRC ? src[off] : 0;
         }
         uint4 o;
         o.x = v[0] | (v[1] << 8) | (v[2] << 16) | (static_cast<uint32_t>(v[3]) << 24);
@@ -218,7 +220,15 @@ cudaError_t launch_q6k_prepack(const uint8_t* w, int64_t N, int64_t K, int64_t l
                                cudaStream_t s) {
     const int64_t nb = K >> 8;
     const int64_t work = N * nb * (Q6K_PACKED / 16);
-    q6k_prepack_kernel<<<grid_for(work, 256), 256, 0, s>>>(w, N, nb, ldw, out);
+    prepack_kernel<Q6K_BLOCK, Q6K_PACKED><<<grid_for(work, 256), 256, 0, s>>>(w, N, nb, ldw, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ptq1_prepack(const uint8_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* out,
+                                cudaStream_t s) {
+    const int64_t nb = K >> 7;   // 128-weight blocks
+    const int64_t work = N * nb * (PTQ1_PACKED / 16);
+    prepack_kernel<PTQ1_BLOCK, PTQ1_PACKED><<<grid_for(work, 256), 256, 0, s>>>(w, N, nb, ldw, out);
     return cudaGetLastError();
 }
 

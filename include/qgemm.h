@@ -194,6 +194,29 @@ QGEMM_API int qgemm_q6k_id(const void *w_packed, int64_t experts, int64_t N, int
                            const float *xd, const int16_t *xbsums, int64_t M, const int32_t *ids, int64_t top_k,
                            float *y, int64_t ldy, void *workspace, size_t workspace_bytes, qgemm_stream_t stream);
 
+/* ---------------------------------------------------------- PTQ1_0 ----
+ * Ternary weights ("cuda: branch-free PTQ1_0 MMQ tile loader ...", llama.cpp
+ * PR #214): 28-byte blocks of 128 weights -- 24 qs bytes of 5 base-3 digits
+ * each, 2 qh bytes of 4, fp16 d at byte 26.  A byte holds its digits least
+ * significant first (digit i = (byte / 3^i) mod 3); digit t means t - 1;
+ * weight 24 i + j is digit i of qs byte j (j < 24), weight 120 + r digit r / 2
+ * of qh byte r % 2.  w = d * (t - 1).  (The pages give the word layout; the
+ * digit order within it is this library's reading, and its oracle is its own
+ * codec.)
+ * qgemm_ptq1_prepack: N rows of K/128 blocks (row stride ldw bytes, ldw >=
+ *   (K/128)*28) -> 32-byte blocks (the same 28 bytes, 4 zero), rows of K/4
+ *   bytes, w_packed 16-B aligned, qgemm_ptq1_packed_bytes(N, K) bytes.
+ * qgemm_ptq1: Y[M][N] = X_q8k[M][K] * W^T from the repacked weights, K a
+ *   multiple of 256; arguments, workspace and errors as qgemm_q4k.  The tile
+ *   GEMM runs for every M (d is folded into the fp16 operand exactly).
+ *   Accuracy: |Y - Y_exact| <= 2e-5 * sum_b |c_b| + 1e-6. */
+QGEMM_API size_t qgemm_ptq1_packed_bytes(int64_t N, int64_t K);
+QGEMM_API int qgemm_ptq1_prepack(const void *w, int64_t N, int64_t K, int64_t ldw, void *w_packed,
+                                 qgemm_stream_t stream);
+QGEMM_API int qgemm_ptq1(const void *w_packed, int64_t N, int64_t K, const int8_t *xqs, const float *xd,
+                         const int16_t *xbsums, int64_t M, float *y, int64_t ldy, void *workspace,
+                         size_t workspace_bytes, qgemm_stream_t stream);
+
 /* ------------------------------------------------ output epilogue ----
  * The GEMM with its output epilogue fused into the final store: the output
  * type (the pages' OutT template parameter of the BigTile kernels, vllm.cpp
@@ -270,6 +293,8 @@ typedef struct {
     uint64_t q6k_prepack;  /* Q6_K repack launches                  */
     uint64_t split_k;      /* GEMM launches with cut tiles (K parts) */
     uint64_t routed;       /* expert-routed GEMM launches (_id)     */
+    uint64_t ptq1_tc;      /* PTQ1_0 tile GEMM launches             */
+    uint64_t ptq1_prepack; /* PTQ1_0 repack launches                */
 } qgemm_counters;
 QGEMM_API int qgemm_get_counters(qgemm_counters *out);
 QGEMM_API int qgemm_reset_counters(void);

@@ -154,6 +154,19 @@ def test_epilogue_validation(L):
                           None) == qg.QGEMM_EINVAL
 
 
+def test_ptq1_validation(L):
+    P, G = L.qgemm_ptq1_prepack, L.qgemm_ptq1
+    assert P(FAKE, 0, 256, 56, FAKE, None) == qg.QGEMM_EINVAL
+    assert P(FAKE, 4, 384, 84, FAKE, None) == qg.QGEMM_EINVAL            # K not a multiple of 256
+    assert P(FAKE, 4, 256, 55, FAKE, None) == qg.QGEMM_EINVAL            # ldw < 2 blocks of 28 B
+    assert P(FAKE, 4, 256, 56, MISALIGNED, None) == qg.QGEMM_EALIGN
+    assert G(FAKE, 128, 300, FAKE, FAKE, FAKE, 4, FAKE, 128, FAKE, 1 << 20, None) == qg.QGEMM_EINVAL
+    assert G(MISALIGNED, 128, 512, FAKE, FAKE, FAKE, 4, FAKE, 128, FAKE, 1 << 20, None) == qg.QGEMM_EALIGN
+    assert G(FAKE, 128, 512, FAKE, FAKE, FAKE, 0, FAKE, 128, FAKE, 1 << 20, None) == qg.QGEMM_OK
+    assert L.qgemm_ptq1_packed_bytes(3, 512) == 3 * 4 * 32
+    assert L.qgemm_ptq1_packed_bytes(3, 384) == 0
+
+
 def test_size_queries(L):
     assert L.qgemm_workspace_bytes(0, 8, 256) == 0
     assert L.qgemm_workspace_bytes(4, 8, 300) == 0

@@ -1,0 +1,94 @@
+"""PTQ1_0 ternary weights (qgemm_ptq1_prepack / qgemm_ptq1) on the GPU vs the
+CPU oracle's codec and GEMM: |Y - Y_oracle| <= 2e-5 * sum_b |c_b| + 1e-6.
+
+Coverage: the repack's bytes, ragged M / N around every tile width, every
+tile width forced, cut tiles, a sampled K = 5120 workload (the pages measure
+PTQ1_0 on K = 5120 projections), blocks with d = 0 and all-extreme trits, the
+launch counters and the device status."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import block_quantized_matmul_quantize_gb300 as qg
+from gpu_common import device_status_clean, ensure_built, gpu_quantize, q8k_numpy, to_dev
+from parity_util import assert_gemm_close, oracle_gemm, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
+    yield
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
+
+
+def run(w_np, K, q):
+    N = w_np.shape[0]
+    wp = qg.qgemm_ptq1_prepack(to_dev(w_np), N, K)
+    y = qg.qgemm_ptq1(wp, N, K, q)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def check(w, K, x, rows=None, what=""):
+    q = gpu_quantize(x)
+    qg.qgemm_reset_counters()
+    y = run(w, K, q)
+    c = qg.qgemm_get_counters()
+    assert c["ptq1_tc"] == 1 and c["ptq1_prepack"] == 1, c
+    yr, absc = oracle_gemm(1, w, K, *q8k_numpy(q), rows=rows)
+    assert_gemm_close(y if rows is None else y[rows], yr, absc, what)
+
+
+def test_prepack_bytes():
+    N, K = 5, 768
+    w = synth.gen_ptq1(N, K, 3)
+    wp = qg.qgemm_ptq1_prepack(to_dev(w), N, K).cpu().numpy()
+    blocks = w.reshape(N, K // 128, 28)
+    want = np.concatenate([blocks, np.zeros((N, K // 128, 4), np.uint8)], axis=2).reshape(N, K // 4)
+    assert np.array_equal(wp, want)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 256), (3, 130, 512), (9, 200, 768), (17, 128, 1024), (64, 256, 512),
+                                   (65, 136, 512), (128, 256, 1024), (129, 130, 768), (257, 384, 512)])
+def test_ragged_shapes(M, N, K):
+    check(synth.gen_ptq1(N, K, 11 + M), K, synth.gen_x(M, K, 12 + M, outlier_frac=0.01), what=f"M{M} N{N} K{K}")
+
+
+@pytest.mark.parametrize("bm", [16, 32, 64, 128])
+def test_every_tile_width(bm):
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, bm)
+    try:
+        check(synth.gen_ptq1(300, 2048, 21), 2048, synth.gen_x(100, 2048, 22), what=f"bm{bm}")
+    finally:
+        qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
+
+
+def test_extreme_blocks():
+    orc = oracle.get()
+    N, K, M = 128, 512, 40
+    r = np.random.default_rng(7)
+    blocks = []
+    for n in range(N):
+        row = []
+        for b in range(K // 128):
+            kind = (n + b) % 4
+            t = (np.full(128, 2) if kind == 0 else np.zeros(128, int) if kind == 1
+                 else r.integers(0, 3, 128))
+            d_bits = 0x0000 if kind == 3 else int(r.integers(0x1400, 0x2400))
+            row.append(orc.ptq1_pack(d_bits, t))
+        blocks.append(np.concatenate(row))
+    check(np.stack(blocks), K, synth.gen_x(M, K, 8), what="extreme PTQ1_0 blocks")
+
+
+def test_k5120_sampled():
+    M, N, K = 512, 5120, 5120
+    check(synth.gen_ptq1(N, K, 31), K, synth.gen_x(M, K, 32), rows=sample_rows(M, 24, seed=4), what="M512 K5120 N5120")
+
+
+def test_device_status_clean_at_end():
+    device_status_clean()
