@@ -53,7 +53,7 @@ NCU_TRAFFIC_BYTES = {"q4k_m512_k2048_n11008_outliers": 15023616}
 
 
 def workloads():
-    return {w.name: w for w in synth.CONFIGS + synth.ROUTED_CONFIGS}
+    return {w.name: w for w in synth.CONFIGS + synth.ROUTED_CONFIGS + synth.PTQ1_CONFIGS}
 
 
 def routed(wl) -> bool:
@@ -190,7 +190,7 @@ def run_reference(args, world, rank):
 
 
 def config_of(wl):
-    c = {"workload": wl.name, "weights": "Q4_K" if wl.wtype == 4 else "Q6_K", "M": wl.M, "K": wl.K,
+    c = {"workload": wl.name, "weights": {4: "Q4_K", 6: "Q6_K", 1: "PTQ1_0"}[wl.wtype], "M": wl.M, "K": wl.K,
          "N": wl.N, "x": f"{wl.sigma}*N(0,1)" + (", 1% columns x8" if getattr(wl, "outlier_frac", 0) else ""),
          "l2": "flushed before every step (256 MiB write outside the timed events)"}
     if routed(wl):
@@ -236,7 +236,7 @@ def main():
             dist.barrier()
 
     wl = workloads()[args.workload]
-    assert wl.wtype == 4 or wl.wtype == 6
+    assert wl.wtype in (4, 6, 1)
     M, N, K = wl.M, wl.N, wl.K
     w_host, x_host = wl.weights(), wl.x()
     dev = torch.device("cuda", local)
@@ -245,6 +245,8 @@ def main():
     w = torch.from_numpy(w_host).to(dev)
     if wl.wtype == 6:
         w = qg.qgemm_q6k_prepack(w, w_host.shape[0], K)
+    elif wl.wtype == 1:
+        w = qg.qgemm_ptq1_prepack(w, w_host.shape[0], K)
     x = torch.from_numpy(x_host).to(dev)
     q = qg.Q8K.empty(M, K, dev)
     y = torch.empty((rows_out, N), dtype=torch.float32, device=dev)
@@ -264,6 +266,11 @@ def main():
                 qg.qgemm_q4k_id(w, wl.E, N, K, q, ids, y=y, workspace=ws)
             else:
                 qg.qgemm_q6k_id(w, wl.E, N, K, q, ids, y=y, workspace=ws)
+            return
+        if wl.wtype == 1:
+            # quantize, then the PTQ1_0 GEMM (operand preparation inside the call)
+            qg.qgemm_quantize_q8k(x, out=q)
+            qg.qgemm_ptq1(w, N, K, q, y=y, workspace=ws)
             return
         # quantize, writing the GEMM's operand planes in the same launch, then multiply
         qg.qgemm_quantize_q8k_prep(x, ws, out=q)
@@ -356,7 +363,8 @@ def main():
     value = world * ops / (mean_ms * 1e-3) / 1e12
     # library kernels per step, counted on the eager pass; the graph replays the same ones
     # (a routed GEMM call is three: routing, operand gather, tile GEMM)
-    per_step = sum(c1[k] - c0[k] for k in ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small"))
+    per_step = sum(c1[k] - c0[k] for k in ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small",
+                                            "ptq1_tc"))
     per_step += 2 * (c1["routed"] - c0["routed"])
     launches = per_step  # == K_steps x kernels per step, the count in each of the two timed loops
 

@@ -157,14 +157,16 @@ class Workload:
     outlier_frac: float = 0.0
 
     def weights(self) -> np.ndarray:
-        return (gen_q4k if self.wtype == 4 else gen_q6k)(self.N, self.K, self.w_seed)
+        gen = {4: gen_q4k, 6: gen_q6k, 1: gen_ptq1}[self.wtype]
+        return gen(self.N, self.K, self.w_seed)
 
     def x(self) -> np.ndarray:
         return gen_x(self.M, self.K, self.x_seed, self.sigma, self.outlier_frac)
 
     @property
     def block_bytes(self) -> int:
-        return Q4K_BYTES if self.wtype == 4 else Q6K_BYTES
+        """Weight bytes per 256 weights of a row."""
+        return {4: Q4K_BYTES, 6: Q6K_BYTES, 1: 2 * PTQ1_BYTES}[self.wtype]
 
 
 def _c(i: int, name: str, wtype: int, M: int, K: int, N: int, **kw) -> Workload:
@@ -187,6 +189,11 @@ def sweep(M: int) -> Workload:
 
 
 CONFIGS = (C0, C1, C2, C3) + tuple(sweep(m) for m in SWEEP_M)
+
+# PTQ1_0 ternary weights at the K = 5120 projection shape the pages measure
+# PTQ1_0 prefill on (a 2048-token prompt).
+T0 = Workload("ptq1_m2048_k5120_n5120", 1, 2048, 5120, 5120, w_seed=3000, x_seed=300007)
+PTQ1_CONFIGS = (T0,)
 
 
 @dataclasses.dataclass(frozen=True)
