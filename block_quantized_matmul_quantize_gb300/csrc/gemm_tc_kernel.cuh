@@ -284,47 +284,79 @@ __device__ __forceinline__ void unpack_q6k_chunk(const uint8_t* blk, int c, cons
 // lanes); the digit lands in bits 0-1 of its lane, under the fp16 exponent
 // 0x64 (1024 + t), and (1024 + t - 1025) * d is exact.  Weights 120 + r are
 // digit r / 2 of qh byte r % 2.  No branch depends on the lane or the data.
-__device__ __forceinline__ void unpack_ptq1_block(const uint8_t* blk, uint32_t (&v0)[32], uint32_t (&v1)[32]) {
+// Expanded in two halves (v0 = weights 0..63, then v1 = 64..127), so that
+// only one half and the words' lane pairs after two divisions (st) are live:
+// weights 0..63 are digits 0 and 1 of every qs word and digit 2 of words 0..3.
+struct Ptq1State {
+    uint32_t xl[6], xh[6];   // each word's lane pairs divided by 9
+    uint32_t tail, d2;
+};
+__device__ __forceinline__ uint32_t ptq1_val(uint32_t t2, uint32_t d2) {
+    // (1024 + t - 1025) * d: exact in fp16 for t in {0, 1, 2}
+    return hmul2u(hadd2u(t2 | 0x64006400u, 0xE401E401u), d2);
+}
+__device__ __forceinline__ void ptq1_div3(uint32_t x, uint32_t& q, uint32_t& t) {
+    q = ((x * 171u) >> 9) & 0x007f007fu;   // x / 3 in both 16-bit lanes (x < 256)
+    t = x - 3u * q;
+}
+__device__ __forceinline__ void unpack_ptq1_lo(const uint8_t* blk, Ptq1State& st, uint32_t (&v0)[32]) {
     const uint4 a = *reinterpret_cast<const uint4*>(blk);
     const uint4 b = *reinterpret_cast<const uint4*>(blk + 16);
     const uint32_t qw[6] = {a.x, a.y, a.z, a.w, b.x, b.y};
-    const uint32_t tail = b.z;                        // qh[0] | qh[1] << 8 | d << 16
-    const uint32_t d2 = (tail >> 16) * 0x10001u;      // fp16 d in both halves
-    constexpr uint32_t MAGIC = 0x64006400u, M1025 = 0xE401E401u;   // fp16 1024 | t, -1025
-    auto val = [&](uint32_t t2) { return hmul2u(hadd2u(t2 | MAGIC, M1025), d2); };
+    st.tail = b.z;                                   // qh[0] | qh[1] << 8 | d << 16
+    st.d2 = (st.tail >> 16) * 0x10001u;              // fp16 d in both halves
 #pragma unroll
     for (int w = 0; w < 6; ++w) {
-        uint32_t xl = qw[w] & 0x00ff00ffu, xh = (qw[w] >> 8) & 0x00ff00ffu;
+        uint32_t xl = qw[w] & 0x00ff00ffu, xh = (qw[w] >> 8) & 0x00ff00ffu, ql, qh, tl, th;
 #pragma unroll
-        for (int i = 0; i < 5; ++i) {
-            const uint32_t ql = ((xl * 171u) >> 9) & 0x007f007fu, qh = ((xh * 171u) >> 9) & 0x007f007fu;
-            const int k = 24 * i + 4 * w;             // first weight of the group (a constant here)
-            const uint32_t lo = val(xl - 3u * ql), hi = val(xh - 3u * qh);   // weights k, k+2 / k+1, k+3
-            if (k < 64) {
-                v0[k >> 1] = lo;
-                v0[(k >> 1) + 1] = hi;
-            } else {
-                v1[(k - 64) >> 1] = lo;
-                v1[((k - 64) >> 1) + 1] = hi;
+        for (int i = 0; i < 2; ++i) {                // weights 24 i + 4 w .. + 3
+            ptq1_div3(xl, ql, tl);
+            ptq1_div3(xh, qh, th);
+            v0[12 * i + 2 * w] = ptq1_val(tl, st.d2);
+            v0[12 * i + 2 * w + 1] = ptq1_val(th, st.d2);
+            xl = ql;
+            xh = qh;
+        }
+        st.xl[w] = xl;
+        st.xh[w] = xh;
+        if (w < 4) {                                 // digit 2 of words 0..3: weights 48 + 4 w
+            ptq1_div3(xl, ql, tl);
+            ptq1_div3(xh, qh, th);
+            v0[24 + 2 * w] = ptq1_val(tl, st.d2);
+            v0[25 + 2 * w] = ptq1_val(th, st.d2);
+        }
+    }
+}
+__device__ __forceinline__ void unpack_ptq1_hi(const Ptq1State& st, uint32_t (&v1)[32]) {
+#pragma unroll
+    for (int w = 0; w < 6; ++w) {
+        uint32_t xl = st.xl[w], xh = st.xh[w], ql, qh, tl, th;
+#pragma unroll
+        for (int i = 2; i < 5; ++i) {
+            ptq1_div3(xl, ql, tl);
+            ptq1_div3(xh, qh, th);
+            const int k = 24 * i + 4 * w;            // first weight of the group
+            if (k >= 64) {                           // (digit 2 of words 0..3 went to v0)
+                v1[(k - 64) >> 1] = ptq1_val(tl, st.d2);
+                v1[((k - 64) >> 1) + 1] = ptq1_val(th, st.d2);
             }
             xl = ql;
             xh = qh;
         }
     }
     // qh[0] in lane 0, qh[1] in lane 1: digits i of both bytes per step
-    uint32_t x = (tail & 0xffu) | ((tail & 0xff00u) << 8);
-    uint32_t dg[4];
+    uint32_t x = (st.tail & 0xffu) | ((st.tail & 0xff00u) << 8), dg[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t q = ((x * 171u) >> 9) & 0x007f007fu;
-        dg[i] = x - 3u * q;
+        uint32_t q;
+        ptq1_div3(x, q, dg[i]);
         x = q;
     }
     // group 120..123: (qh0 digit 0, qh0 digit 1), (qh1 digit 0, qh1 digit 1); 124..127 with digits 2, 3
-    v1[28] = val(__byte_perm(dg[0], dg[1], 0x5410));
-    v1[29] = val(__byte_perm(dg[0], dg[1], 0x7632));
-    v1[30] = val(__byte_perm(dg[2], dg[3], 0x5410));
-    v1[31] = val(__byte_perm(dg[2], dg[3], 0x7632));
+    v1[28] = ptq1_val(__byte_perm(dg[0], dg[1], 0x5410), st.d2);
+    v1[29] = ptq1_val(__byte_perm(dg[0], dg[1], 0x7632), st.d2);
+    v1[30] = ptq1_val(__byte_perm(dg[2], dg[3], 0x5410), st.d2);
+    v1[31] = ptq1_val(__byte_perm(dg[2], dg[3], 0x7632), st.d2);
 }
 
 // Kernel variants, each compiled only with the code it needs (measured on
@@ -731,13 +763,15 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                     for (int j = j0; j < j1; ++j) {
                         const int g = 2 * t + j;
                         const int s = g % A_STAGES;
+                        Ptq1State pst;
                         uint32_t v0[32], v1[32];
-                        unpack_ptq1_block(blk + PTQ1_PACKED * j, v0, v1);
+                        unpack_ptq1_lo(blk + PTQ1_PACKED * j, pst, v0);
                         signal();
                         ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
                         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                         tc_fence_after();
                         tmem_st_32x32b_x32(lane_base + 64 * s, v0);
+                        unpack_ptq1_hi(pst, v1);
                         tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
                         pend = s;
                     }
