@@ -268,9 +268,8 @@ def main():
                 qg.qgemm_q6k_id(w, wl.E, N, K, q, ids, y=y, workspace=ws)
             return
         if wl.wtype == 1:
-            # quantize, then the PTQ1_0 GEMM (operand preparation inside the call)
-            qg.qgemm_quantize_q8k(x, out=q)
-            qg.qgemm_ptq1(w, N, K, q, y=y, workspace=ws)
+            qg.qgemm_quantize_q8k_prep(x, ws, out=q)
+            qg.qgemm_ptq1_prepared(w, N, K, q, ws, y=y)
             return
         # quantize, writing the GEMM's operand planes in the same launch, then multiply
         qg.qgemm_quantize_q8k_prep(x, ws, out=q)

@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
             "qgemm_ptq1_packed_bytes": ([i64, i64], sz),
             "qgemm_ptq1_prepack": ([vp, i64, i64, i64, vp, vp], i32),
             "qgemm_ptq1": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
+            "qgemm_ptq1_prepared": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
             "qgemm_get_counters": ([ctypes.POINTER(_Counters)], i32),
             "qgemm_reset_counters": ([], i32),
             "qgemm_get_device_status": ([ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)], i32),
@@ -343,6 +344,17 @@ def qgemm_ptq1(w_packed: torch.Tensor, N: int, K: int, x: Q8K, y: torch.Tensor |
     workspace = _workspace(M, N, K, workspace, x.qs.device)
     _check(lib().qgemm_ptq1(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y), y.stride(0),
                             _ptr(workspace), workspace.numel(), _stream(stream)))
+    return y
+
+
+def qgemm_ptq1_prepared(w_packed: torch.Tensor, N: int, K: int, x: Q8K, workspace: torch.Tensor,
+                        y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """qgemm_ptq1 from a workspace that qgemm_quantize_q8k_prep filled for the same X."""
+    M = x.M
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
+    _check(lib().qgemm_ptq1_prepared(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
+                                     y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
 

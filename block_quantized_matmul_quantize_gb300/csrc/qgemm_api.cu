@@ -708,6 +708,17 @@ int qgemm_ptq1(const void* w_packed, int64_t N, int64_t K, const int8_t* xqs, co
                   reinterpret_cast<cudaStream_t>(stream), false);
 }
 
+int qgemm_ptq1_prepared(const void* w_packed, int64_t N, int64_t K, const int8_t* xqs, const float* xd,
+                        const int16_t* xbsums, int64_t M, float* y, int64_t ldy, const void* workspace,
+                        size_t workspace_bytes, qgemm_stream_t stream) {
+    clear_err();
+    int rc = gemm_common_checks(w_packed, N, K, xqs, xd, xbsums, M, y, ldy);
+    if (rc || M == 0) return rc;
+    const int64_t ldw = (K / 128) * qg::PTQ1_PACKED;
+    return run_tc(1, w_packed, N, K, ldw, xqs, xd, xbsums, M, y, ldy, const_cast<void*>(workspace), workspace_bytes,
+                  reinterpret_cast<cudaStream_t>(stream), true);
+}
+
 size_t qgemm_id_workspace_bytes(int64_t M, int64_t top_k, int64_t experts, int64_t K) {
     if (M <= 0 || top_k < 1 || experts < 1 || K <= 0 || K % 256) return 0;
     const int64_t P = M * top_k;

@@ -90,5 +90,18 @@ def test_k5120_sampled():
     check(synth.gen_ptq1(N, K, 31), K, synth.gen_x(M, K, 32), rows=sample_rows(M, 24, seed=4), what="M512 K5120 N5120")
 
 
+def test_prepared_workspace():
+    M, N, K = 70, 260, 1024
+    w = synth.gen_ptq1(N, K, 41)
+    x = synth.gen_x(M, K, 42)
+    wp = qg.qgemm_ptq1_prepack(to_dev(w), N, K)
+    ws = torch.empty(qg.qgemm_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    q = qg.qgemm_quantize_q8k_prep(to_dev(x), ws)
+    y = qg.qgemm_ptq1_prepared(wp, N, K, q, ws)
+    torch.cuda.synchronize()
+    yr, absc = oracle_gemm(1, w, K, *q8k_numpy(q))
+    assert_gemm_close(y.cpu().numpy(), yr, absc, "PTQ1_0 prepared")
+
+
 def test_device_status_clean_at_end():
     device_status_clean()
