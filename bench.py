@@ -49,7 +49,7 @@ DEFAULT_WORKLOAD = synth.C1.name
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
 # kernel, from the ncu capture summarised under profiles/ (absent until
 # measured, and removed whenever the kernel changes).
-NCU_TRAFFIC_BYTES = {"q4k_m512_k2048_n11008_outliers": 15023616}
+NCU_TRAFFIC_BYTES = {"q4k_m512_k2048_n11008_outliers": 15017984}
 
 
 def workloads():
@@ -258,25 +258,28 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step_on(xin, yout, ids_in=None):
         if is_routed:
             # quantize, then route + gather + one tile GEMM over all experts
-            qg.qgemm_quantize_q8k(x, out=q)
+            qg.qgemm_quantize_q8k(xin, out=q)
             if wl.wtype == 4:
-                qg.qgemm_q4k_id(w, wl.E, N, K, q, ids, y=y, workspace=ws)
+                qg.qgemm_q4k_id(w, wl.E, N, K, q, ids_in, y=yout, workspace=ws)
             else:
-                qg.qgemm_q6k_id(w, wl.E, N, K, q, ids, y=y, workspace=ws)
+                qg.qgemm_q6k_id(w, wl.E, N, K, q, ids_in, y=yout, workspace=ws)
             return
         if wl.wtype == 1:
-            qg.qgemm_quantize_q8k_prep(x, ws, out=q)
-            qg.qgemm_ptq1_prepared(w, N, K, q, ws, y=y)
+            qg.qgemm_quantize_q8k_prep(xin, ws, out=q)
+            qg.qgemm_ptq1_prepared(w, N, K, q, ws, y=yout)
             return
         # quantize, writing the GEMM's operand planes in the same launch, then multiply
-        qg.qgemm_quantize_q8k_prep(x, ws, out=q)
+        qg.qgemm_quantize_q8k_prep(xin, ws, out=q)
         if wl.wtype == 4:
-            qg.qgemm_q4k_prepared(w, N, K, q, ws, y=y)
+            qg.qgemm_q4k_prepared(w, N, K, q, ws, y=yout)
         else:
-            qg.qgemm_q6k_prepared(w, N, K, q, ws, y=y)
+            qg.qgemm_q6k_prepared(w, N, K, q, ws, y=yout)
+
+    def step():
+        step_on(x, y, ids if is_routed else None)
 
     sampler = ClockSampler(gpu_id_for_smi(local))
     # warm-up, then about half a second more so that clocks settle
@@ -367,32 +370,53 @@ def main():
     per_step += 2 * (c1["routed"] - c0["routed"])
     launches = per_step  # == K_steps x kernels per step, the count in each of the two timed loops
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  The inputs (X, and
+    # the expert ids of a routed step) start in pinned host memory and Y ends
+    # there, both crossing the host link inside the timed region.  Two ways:
+    #   zero-copy: the quantizer reads X and the GEMM's epilogue writes Y in
+    #              host memory directly (the library's kernels move the bytes);
+    #   copies:    cudaMemcpyAsync of X to the device, the step, and a copy of Y back.
     x_pin = torch.from_numpy(x_host).pin_memory()
     y_pin = torch.empty((rows_out, N), dtype=torch.float32).pin_memory()
-    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
-    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
-    for _ in range(3):
+    ids_pin = torch.from_numpy(wl.ids()).pin_memory() if is_routed else None
+    h2d_bytes = int(x_host.nbytes) + (int(ids_pin.nbytes) if is_routed else 0)
+    d2h_bytes = int(rows_out * N * 4)
+
+    def e2e_zero_copy():
+        step_on(x_pin, y_pin, ids_pin)
+
+    def e2e_copies():
         x.copy_(x_pin, non_blocking=True)
+        if is_routed:
+            ids.copy_(ids_pin, non_blocking=True)
         step()
         y_pin.copy_(y, non_blocking=True)
-    torch.cuda.synchronize()
-    barrier()
-    for i in range(K_steps):
-        flush.zero_()
-        e_s[i].record(stream)
-        x.copy_(x_pin, non_blocking=True)
-        step()
-        y_pin.copy_(y, non_blocking=True)
-        e_e[i].record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    e2e_ms = sum(e_s[i].elapsed_time(e_e[i]) for i in range(K_steps)) / K_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+
+    def time_e2e(fn):
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        barrier()
+        for i in range(K_steps):
+            flush.zero_()
+            e_s[i].record(stream)
+            fn()
+            e_e[i].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms = sum(e_s[i].elapsed_time(e_e[i]) for i in range(K_steps)) / K_steps
+        if world > 1:
+            t = torch.tensor([ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t[0])
+        return ms
+
+    e2e_ms = time_e2e(e2e_zero_copy)
+    e2e_copies_ms = time_e2e(e2e_copies)
     e2e_value = world * ops / (e2e_ms * 1e-3) / 1e12
+    e2e_copies_value = world * ops / (e2e_copies_ms * 1e-3) / 1e12
 
     bits, site = qg.qgemm_get_device_status()
 
@@ -424,8 +448,11 @@ def main():
             "launch": "one CUDA graph per step (captured from the API calls)" if graph is not None
                       else "eager API calls",
             "roofline": roof,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.nbytes),
-                    "d2h_bytes_per_step": int(rows_out * N * 4)},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
+                    "d2h_bytes_per_step": d2h_bytes, "ms_per_step": e2e_ms,
+                    "path": "zero-copy: X read and Y written in pinned host memory by the library's kernels",
+                    "copies": {"value": e2e_copies_value, "ms_per_step": e2e_copies_ms,
+                               "path": "cudaMemcpyAsync of X and Y around the device step"}},
             "gpu_launches": int(launches),
             "clocks": sampler.summary(t0, t1),
             "device_status": bits,

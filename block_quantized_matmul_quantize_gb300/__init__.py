@@ -101,8 +101,23 @@ def _check(rc: int) -> None:
         raise QgemmError(rc, lib().qgemm_last_error().decode())
 
 
-def _ptr(t: torch.Tensor | None):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+def _ptr(t: torch.Tensor | None, host_ok: bool = False):
+    """The address the kernels use.  Device tensors only, except where
+    `host_ok`: X, the expert ids and Y may also be pinned host tensors, which
+    the kernels read or write across the host link (pageable memory is
+    refused here, before anything is launched)."""
+    if t is None:
+        return None
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError("a CUDA tensor is required here" if not host_ok else
+                         "X, ids and Y must be CUDA tensors or pinned host tensors (Tensor.pin_memory())")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _device_of(t: torch.Tensor) -> torch.device:
+    """Where outputs derived from `t` go: its own device, or the current CUDA
+    device for a pinned host tensor."""
+    return t.device if t.is_cuda else torch.device("cuda", torch.cuda.current_device())
 
 
 def _stream(stream) -> ctypes.c_void_p:
@@ -141,8 +156,8 @@ def qgemm_quantize_q8k(x: torch.Tensor, out: Q8K | None = None, stream=None) -> 
     assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     if out is None:
-        out = Q8K.empty(M, K, x.device)
-    _check(lib().qgemm_quantize_q8k(_ptr(x), M, K, x.stride(0), _ptr(out.qs), _ptr(out.d), _ptr(out.bsums),
+        out = Q8K.empty(M, K, _device_of(x))
+    _check(lib().qgemm_quantize_q8k(_ptr(x, True), M, K, x.stride(0), _ptr(out.qs), _ptr(out.d), _ptr(out.bsums),
                                     _stream(stream)))
     return out
 
@@ -166,7 +181,7 @@ def qgemm_q4k(w: torch.Tensor, N: int, K: int, x: Q8K, y: torch.Tensor | None = 
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
     workspace = _workspace(M, N, K, workspace, x.qs.device)
-    _check(lib().qgemm_q4k(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
+    _check(lib().qgemm_q4k(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y, True),
                            y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
@@ -179,7 +194,7 @@ def qgemm_q4k_noalloc(w: torch.Tensor, N: int, K: int, x: Q8K, y: torch.Tensor |
     M = x.M
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
-    _check(lib().qgemm_q4k_noalloc(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
+    _check(lib().qgemm_q4k_noalloc(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y, True),
                                    y.stride(0), _stream(stream)))
     return y
 
@@ -204,7 +219,7 @@ def qgemm_q6k(w_packed: torch.Tensor, N: int, K: int, x: Q8K, y: torch.Tensor | 
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
     workspace = _workspace(M, N, K, workspace, x.qs.device)
-    _check(lib().qgemm_q6k(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y), y.stride(0),
+    _check(lib().qgemm_q6k(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y, True), y.stride(0),
                            _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
@@ -216,8 +231,8 @@ def qgemm_quantize_q8k_prep(x: torch.Tensor, workspace: torch.Tensor, out: Q8K |
     assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     if out is None:
-        out = Q8K.empty(M, K, x.device)
-    _check(lib().qgemm_quantize_q8k_prep(_ptr(x), M, K, x.stride(0), _ptr(out.qs), _ptr(out.d), _ptr(out.bsums),
+        out = Q8K.empty(M, K, _device_of(x))
+    _check(lib().qgemm_quantize_q8k_prep(_ptr(x, True), M, K, x.stride(0), _ptr(out.qs), _ptr(out.d), _ptr(out.bsums),
                                          _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
 
@@ -229,7 +244,7 @@ def qgemm_q4k_prepared(w: torch.Tensor, N: int, K: int, x: Q8K, workspace: torch
     M = x.M
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
-    _check(lib().qgemm_q4k_prepared(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
+    _check(lib().qgemm_q4k_prepared(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y, True),
                                     y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
@@ -240,7 +255,7 @@ def qgemm_q6k_prepared(w_packed: torch.Tensor, N: int, K: int, x: Q8K, workspace
     M = x.M
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
-    _check(lib().qgemm_q6k_prepared(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
+    _check(lib().qgemm_q6k_prepared(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y, True),
                                     y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
@@ -263,7 +278,7 @@ def qgemm_q4k_id(w: torch.Tensor, experts: int, N: int, K: int, x: Q8K, ids: tor
         workspace = torch.empty(max(qgemm_id_workspace_bytes(M, top_k, experts, K), 256), dtype=torch.uint8,
                                 device=x.qs.device)
     _check(lib().qgemm_q4k_id(_ptr(w), experts, N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M,
-                              _ptr(ids), top_k, _ptr(y), y.stride(0), _ptr(workspace), workspace.numel(),
+                              _ptr(ids, True), top_k, _ptr(y, True), y.stride(0), _ptr(workspace), workspace.numel(),
                               _stream(stream)))
     return y
 
@@ -279,8 +294,8 @@ def qgemm_q6k_id(w_packed: torch.Tensor, experts: int, N: int, K: int, x: Q8K, i
     if workspace is None:
         workspace = torch.empty(max(qgemm_id_workspace_bytes(M, top_k, experts, K), 256), dtype=torch.uint8,
                                 device=x.qs.device)
-    _check(lib().qgemm_q6k_id(_ptr(w_packed), experts, N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(ids),
-                              top_k, _ptr(y), y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
+    _check(lib().qgemm_q6k_id(_ptr(w_packed), experts, N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(ids, True),
+                              top_k, _ptr(y, True), y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
 
@@ -304,7 +319,7 @@ def qgemm_q4k_ex(w: torch.Tensor, N: int, K: int, x: Q8K, out_dtype=torch.float3
     assert y.dtype == out_dtype
     workspace = _workspace(M, N, K, workspace, x.qs.device)
     ep = _epilogue(out_dtype, bias, activation)
-    _check(lib().qgemm_q4k_ex(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
+    _check(lib().qgemm_q4k_ex(_ptr(w), N, K, w.stride(0), _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y, True),
                               y.stride(0), ctypes.byref(ep), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
@@ -319,7 +334,7 @@ def qgemm_q6k_ex(w_packed: torch.Tensor, N: int, K: int, x: Q8K, out_dtype=torch
     assert y.dtype == out_dtype
     workspace = _workspace(M, N, K, workspace, x.qs.device)
     ep = _epilogue(out_dtype, bias, activation)
-    _check(lib().qgemm_q6k_ex(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y), y.stride(0),
+    _check(lib().qgemm_q6k_ex(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y, True), y.stride(0),
                               ctypes.byref(ep), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
@@ -342,7 +357,7 @@ def qgemm_ptq1(w_packed: torch.Tensor, N: int, K: int, x: Q8K, y: torch.Tensor |
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
     workspace = _workspace(M, N, K, workspace, x.qs.device)
-    _check(lib().qgemm_ptq1(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y), y.stride(0),
+    _check(lib().qgemm_ptq1(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y, True), y.stride(0),
                             _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 
@@ -353,7 +368,7 @@ def qgemm_ptq1_prepared(w_packed: torch.Tensor, N: int, K: int, x: Q8K, workspac
     M = x.M
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.qs.device)
-    _check(lib().qgemm_ptq1_prepared(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y),
+    _check(lib().qgemm_ptq1_prepared(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y, True),
                                      y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
 

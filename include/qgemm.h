@@ -28,6 +28,14 @@
  *     device memory.  Scratch ("workspace") is passed in, sized by a query
  *     function -- the caller-owned-scratch convention of the pages
  *     (hip_linear_attention_prefill_scratch_bytes, hip-ep PR #627).
+ *   - Three arrays may instead live in page-locked host memory that the
+ *     device can address (cudaHostAlloc, or cudaHostRegister with
+ *     cudaHostRegisterMapped, under unified addressing): the fp32 X of the
+ *     quantizers, the expert ids of the routed calls, and every GEMM's Y.
+ *     The kernels then move those bytes across the host link themselves,
+ *     with no staging copy: X and ids are read once per call, and Y is
+ *     written once and never read back.  Every other array (weights, Q8_K
+ *     planes, workspace) must be device memory; this is not checked.
  *   - Calls enqueue work on `stream` and return; they do not synchronize.
  *   - Argument errors are reported synchronously and nothing is launched
  *     (a nonzero status, so the caller can fall back: "the launcher returns

@@ -194,3 +194,16 @@ def test_options_and_counters(L):
     assert L.qgemm_get_counters(ctypes.byref(c)) == 0
     assert c.q4k_tc == 0 and c.quantize == 0
     assert L.qgemm_get_counters(None) == qg.QGEMM_EINVAL
+
+
+def test_binding_refuses_pageable_host_tensors(L):
+    """X, ids and Y may be pinned host tensors, never pageable ones; every
+    other argument must be a CUDA tensor.  The binding refuses before the
+    library is called, so this runs without a GPU."""
+    import torch
+    out = qg.Q8K(torch.zeros((2, 256), dtype=torch.int8), torch.zeros((2, 1)),
+                 torch.zeros((2, 16), dtype=torch.int16))
+    with pytest.raises(ValueError, match="pinned host tensors"):
+        qg.qgemm_quantize_q8k(torch.zeros((2, 256)), out=out)
+    with pytest.raises(ValueError, match="CUDA tensor is required"):
+        qg.qgemm_q4k(torch.zeros((8, 144), dtype=torch.uint8), 8, 256, out, y=torch.zeros((2, 8)))
