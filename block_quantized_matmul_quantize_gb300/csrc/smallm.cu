@@ -8,33 +8,38 @@
 // integer dot products on the CUDA cores beats the tile GEMM.
 //
 // Design on sm_103a:
-//   * Each CTA owns a contiguous range of weight rows; thread = a fixed
-//     32-weight slice of K (warp w covers blocks 4w .. 4w+3, 8 threads per
-//     block), so one row is read by the CTA as a few fully used 512-B runs.
-//   * The weights are staged in shared memory by every thread copying its own
-//     16-byte pieces with cp.async, a stage of several rows at a time, double
-//     buffered: the whole stage is in flight at once from all threads.
-//     (Measured on GB300: 1D bulk copies from one producer thread per CTA
-//     moved a DRAM-resident row range at ~3 B/clk per CTA, and register
-//     prefetch a couple of rows ahead kept too few bytes in flight.)
+//   * One CTA per SM.  One producer thread streams the CTA's contiguous range
+//     of weight rows into a shared-memory ring with 1D bulk copies (TMA), a
+//     stage of whole rows per copy, up to 16 stages and ~200 KB per ring.
+//     (Measured on GB300: a read-only stream needs ~64 KB in flight per SM to
+//     reach ~6.4 TB/s; per-thread cp.async stopped near 3.8 TB/s however deep
+//     its ring, while bulk copies of 16-48 KB reach 6.3-6.4 TB/s.  A grid of
+//     ~600 small CTAs also cost ~1.3 us more to launch than one of 152.)
+//   * The stage's rows are dealt round-robin to RL "row lanes", each a group
+//     of WPR = ceil(K/1024) consumer warps that together cover one row's K:
+//     warp wk of a row lane owns blocks 4wk .. 4wk+3, lane = a fixed
+//     32-weight slice (8 lanes per block).
 //   * The slice's Q8_K activations of all M tokens (int8 values, the two
 //     bsums it needs, the block scale dx) stay in registers for the whole
-//     kernel.
+//     kernel.  They are read with plain loads after the wait for the
+//     preceding grid, beside the weight stream rather than behind it.
 //   * Integer part with dp4a, exact: per block and token the slice adds
 //       Q4_K: dx * (d * (sc_lo*I_lo + sc_hi*I_hi) - dmin * (m_lo*B_lo + m_hi*B_hi))
 //       Q6_K: dx * d * (sc_a*(I_a - 32*B_a) + sc_b*(I_b - 32*B_b))
 //     with I the int dot of unsigned weight codes and int8 activations and B
 //     the activation sums over the slice's 16-value groups (the bsums).
 //     Every integer partial stays below 2^24, so its fp32 conversion is exact.
-//   * Rows go in batches: per batch one reduce-scatter over the warp (about
-//     one shuffle per output value), one barrier, and warp 0 adds the warps'
-//     partials and stores the batch (consecutive lanes -> consecutive rows).
-// There are no waits other than the CTA barrier, which every thread reaches
-// the same number of times.
+//   * Per stage, each warp reduces its rows x M tokens over its lanes (about
+//     one shuffle per output), writes the partials to shared memory, and the
+//     row lane's warps meet at one named barrier; warp 0 of the row lane adds
+//     the WPR partials in a fixed order and stores.  Y is deterministic.
+// Every mbarrier wait is bounded (a timeout records a status bit and the
+// warp carries on without data, so it still meets its row lane at every
+// named barrier); the producer waits for its copies in flight before it ends.
 #include <cuda_fp16.h>
 
 #include <mutex>
-#include <unordered_map>
+#include <unordered_set>
 
 #include "internal.h"
 #include "epilogue.cuh"
@@ -43,8 +48,11 @@
 namespace qg {
 namespace {
 
-constexpr int SM_MAX_WARPS = 15;              // warps per CTA: K <= 15360
-constexpr int SM_STAGE_BYTES = 24 * 1024;     // weight bytes per staging buffer (whole rows)
+constexpr int SM_MAX_WPR = 15;                 // warps per row: K <= 15360
+constexpr int SM_MAX_ROW_LANES = 15;           // named barriers 1..15
+constexpr int SM_MAX_SLOTS = 16;               // ring stages
+constexpr int SM_RING_BYTES = 200 * 1024;      // weight ring per CTA
+constexpr int SM_SLOT_TARGET = 48 * 1024;      // bytes per stage, at most (unless one row lane's rows exceed it)
 
 template <int WT>
 struct SmallTraits;
@@ -58,6 +66,15 @@ struct SmallTraits<6> {
 };
 
 __host__ __device__ constexpr int pow2_at_least(int m) { return m <= 1 ? 1 : m <= 2 ? 2 : m <= 4 ? 4 : 8; }
+
+// Consumer warps per CTA at most, by token count: the activations of MT
+// tokens live in registers (8*MT words + 2*MT bsums + MT scales per lane).
+__host__ __device__ constexpr int small_max_warps(int mt) { return mt <= 2 ? 20 : mt <= 4 ? 16 : 15; }
+// Rows per row lane and stage, at most: the stage's R x pow2(MT) outputs of
+// a warp are reduced in one pass (at most 16 values per lane).
+__host__ __device__ constexpr int small_stage_rows(int wt, int mt) {
+    return wt == 6 ? 2 : pow2_at_least(mt) >= 8 ? 2 : 4;
+}
 
 // Sum v[0..P) over the 32 lanes; afterwards lane l holds the total of value
 // l / (32 / P) (lanes l % (32/P) == 0 are the representatives).
@@ -79,26 +96,79 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[P], int lane) {
     return r;
 }
 
+// Barrier of the `threads` threads of one row lane (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void row_lane_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 template <int WT, int MT>
-__global__ void __launch_bounds__(32 * SM_MAX_WARPS)
+__global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
     smallm_kernel(const uint8_t* __restrict__ w, int64_t ldw, int N, int nb, const int8_t* __restrict__ xqs,
                   const float* __restrict__ xd, const int16_t* __restrict__ xbs, void* __restrict__ y,
-                  int64_t ldy, const Epi epi, int stage_rows) {
+                  int64_t ldy, const Epi epi, int wpr, int rl, int rps, int nsb, uint32_t* status) {
     constexpr int BLK = SmallTraits<WT>::BLOCK;
-    constexpr int P = pow2_at_least(MT);      // token slots per row
-    constexpr int VALS = 16;                  // values per thread per reduction batch
-    constexpr int RB = VALS / P;              // rows per batch
-    __shared__ float red[2][SM_MAX_WARPS][32];
-    extern __shared__ __align__(16) uint8_t stage_mem[];   // [2][stage_rows][row_bytes]
+    constexpr int P = pow2_at_least(MT);          // token slots per row
+    constexpr int R = small_stage_rows(WT, MT);   // rows per row lane and stage, at most
+    constexpr int VALS = R * P;                   // outputs per stage and warp
+    static_assert(VALS <= 16, "stage shape");
+    __shared__ float red[2][small_max_warps(MT)][VALS];
+    __shared__ uint64_t full[SM_MAX_SLOTS], empty[SM_MAX_SLOTS];
+    __shared__ int abort_flag;
+    extern __shared__ __align__(128) uint8_t ring[];   // [nsb][srw rows of row_bytes]
 
     const int K = nb * 256;
-    const int nw = blockDim.x >> 5;
+    const int row_bytes = nb * BLK;
+    const int srw = rl * rps;                     // rows per stage
+    const int slot_bytes = srw * row_bytes;
+    const int ncons = rl * wpr;                   // consumer warps; warp ncons is the producer
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r0 = static_cast<int>(static_cast<int64_t>(N) * blockIdx.x / gridDim.x);
     const int r1 = static_cast<int>(static_cast<int64_t>(N) * (blockIdx.x + 1) / gridDim.x);
+    const int nst = (r1 - r0 + srw - 1) / srw;    // stages of this CTA
 
-    const int b = 4 * warp + (lane >> 3);   // this thread's block
-    const int sub = lane & 7;               // and its 32-weight slice in it
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < nsb; ++i) {
+            mbar_init(&full[i], 1);          // the producer's expect_tx; completes on the bytes
+            mbar_init(&empty[i], ncons);     // one arrival per consumer warp
+        }
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == ncons) {
+        // ---- producer: whole-row stages by 1D bulk copies.  The weights do
+        // not depend on the preceding grid: no wait for it here, so with a
+        // programmatic dependent launch they stream while it finishes.
+        if (lane == 0) {
+            int issued = 0;
+            for (int g = 0; g < nst; ++g) {
+                const int sl = g % nsb;
+                if (g >= nsb && !mbar_wait(&empty[sl], ((g / nsb) - 1) & 1, &abort_flag, status, 20)) break;
+                const int ra = r0 + g * srw;
+                const int nr = min(srw, r1 - ra);
+                uint8_t* dst = ring + static_cast<size_t>(sl) * slot_bytes;
+                mbar_arrive_expect_tx(&full[sl], static_cast<uint32_t>(nr * row_bytes));
+                if (ldw == row_bytes) {
+                    bulk_load(dst, w + static_cast<int64_t>(ra) * ldw, static_cast<uint32_t>(nr * row_bytes), &full[sl]);
+                } else {
+                    for (int q = 0; q < nr; ++q)
+                        bulk_load(dst + q * row_bytes, w + static_cast<int64_t>(ra + q) * ldw,
+                                  static_cast<uint32_t>(row_bytes), &full[sl]);
+                }
+                ++issued;
+            }
+            // the copies still in flight land before the CTA may end
+            for (int g = issued > nsb ? issued - nsb : 0; g < issued; ++g)
+                mbar_wait(&full[g % nsb], (g / nsb) & 1, &abort_flag, status, 21);
+        }
+        return;
+    }
+
+    // ---- consumers: row lane lj takes rows lj, lj + rl, ... of every stage
+    const int lj = warp / wpr, wk = warp - lj * wpr;
+    const int b = 4 * wk + (lane >> 3);   // this lane's block
+    const int sub = lane & 7;             // and its 32-weight slice in it
     const bool active = b < nb;
     // K offsets (within the block) of the slice's two 16-value groups, and
     // the byte offsets of its weights in a block
@@ -117,35 +187,6 @@ __global__ void __launch_bounds__(32 * SM_MAX_WARPS)
         wq1 = 128 + 32 * hh + 16 * s;          // qh bytes
     }
 
-    // ---- weight staging: stage g holds rows r0 + g*S .. + S of this CTA
-    const int row_bytes = nb * BLK;
-    const int S = stage_rows;
-    const int nstage = (r1 - r0 + S - 1) / S;
-    // this thread's 16-byte pieces of a row (offsets inside its block)
-    const bool hdr_copier = WT == 4 ? sub == 0 : sub < 2;   // Q4_K header / Q6_K scales+d
-    const int hdr_off = WT == 4 ? 0 : 192 + 16 * sub;
-    auto issue_stage = [&](int g) {
-        uint8_t* buf = stage_mem + (g & 1) * S * row_bytes;
-        const int ra = r0 + g * S, nr = min(S, r1 - ra);
-        if (active) {
-            for (int q = 0; q < nr; ++q) {
-                const uint8_t* src = w + static_cast<int64_t>(ra + q) * ldw + b * BLK;
-                uint8_t* dst = buf + q * row_bytes + b * BLK;
-                cp_async16(dst + wq0, src + wq0);
-                if constexpr (WT == 6) cp_async16(dst + wq1, src + wq1);
-                if (hdr_copier) cp_async16(dst + hdr_off, src + hdr_off);
-            }
-        }
-        cp_async_commit();
-    };
-
-    // both stage buffers are in flight before the activations load: the
-    // weights do not depend on the preceding grid, so with a programmatic
-    // dependent launch they stream while that grid finishes (measured on
-    // GB300: loading the activations first did not shorten the kernel, and
-    // lost that overlap)
-    issue_stage(0);
-    if (nstage > 1) issue_stage(1);
     griddep_wait();   // the activations come from the preceding grid
 
     // the slice's activations, all tokens, in registers
@@ -172,134 +213,124 @@ __global__ void __launch_bounds__(32 * SM_MAX_WARPS)
         }
     }
 
-    int it = 0;   // reduction batch counter (parity of the red buffer)
-    for (int g = 0; g < nstage; ++g) {
-        // committed so far: stages 0 .. min(g + 1, nstage - 1)
-        if (g + 1 < nstage)
-            cp_async_wait<1>();
-        else
-            cp_async_wait<0>();
-        __syncthreads();   // every thread's pieces of stage g have landed
-        const uint8_t* buf = stage_mem + (g & 1) * S * row_bytes;
-        const int ra = r0 + g * S, nr = min(S, r1 - ra);
-        for (int q0 = 0; q0 < nr; q0 += RB, ++it) {
-            float v[VALS];
+    // A failed wait (timeout, status recorded) does not end the loop: the
+    // warp still meets its row lane at every barrier, only without data.
+    bool ok = true;
+    for (int g = 0; g < nst; ++g) {
+        const int sl = g % nsb;
+        const int ra = r0 + g * srw;
+        const int nr = min(srw, r1 - ra);
+        if (ok) ok = mbar_wait(&full[sl], (g / nsb) & 1, &abort_flag, status, 22);
+        float v[VALS];
 #pragma unroll
-            for (int t = 0; t < VALS; ++t) v[t] = 0.0f;
+        for (int t = 0; t < VALS; ++t) v[t] = 0.0f;
+        const uint8_t* slot = ring + static_cast<size_t>(sl) * slot_bytes + b * BLK;
 #pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                if (q0 + rr >= nr || !active) break;   // nr uniform over the CTA
-                const uint8_t* blk = buf + (q0 + rr) * row_bytes + b * BLK;
-                if constexpr (WT == 4) {
-                    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
-                    const uint4 qv = *reinterpret_cast<const uint4*>(blk + wq0);
-                    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
-                    const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
-                    // 6-bit sub-block scales and mins (bytes 4..15 of the block)
-                    const uint32_t sc03 = hdr.y & 0x3f3f3f3fu;
-                    const uint32_t sc47 = (hdr.w & 0x0f0f0f0fu) | ((hdr.y >> 2) & 0x30303030u);
-                    const uint32_t mn03 = hdr.z & 0x3f3f3f3fu;
-                    const uint32_t mn47 = ((hdr.w >> 4) & 0x0f0f0f0fu) | ((hdr.z >> 2) & 0x30303030u);
-                    const int c = sub >> 1;
-                    const int sh = 16 * (c & 1);
-                    const uint32_t scw = c < 2 ? sc03 : sc47, mnw = c < 2 ? mn03 : mn47;
-                    const int sc_lo = (scw >> sh) & 0xff, sc_hi = (scw >> (sh + 8)) & 0xff;
-                    const int mn_lo = (mnw >> sh) & 0xff, mn_hi = (mnw >> (sh + 8)) & 0xff;
-                    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-                    uint32_t lo[4], hi[4];
+        for (int rr = 0; rr < R; ++rr) {
+            const int q = lj + rl * rr;
+            if (rr >= rps || q >= nr || !ok || !active) break;
+            const uint8_t* blk = slot + q * row_bytes;
+            if constexpr (WT == 4) {
+                const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+                const uint4 qv = *reinterpret_cast<const uint4*>(blk + wq0);
+                const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
+                const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
+                // 6-bit sub-block scales and mins (bytes 4..15 of the block)
+                const uint32_t sc03 = hdr.y & 0x3f3f3f3fu;
+                const uint32_t sc47 = (hdr.w & 0x0f0f0f0fu) | ((hdr.y >> 2) & 0x30303030u);
+                const uint32_t mn03 = hdr.z & 0x3f3f3f3fu;
+                const uint32_t mn47 = ((hdr.w >> 4) & 0x0f0f0f0fu) | ((hdr.z >> 2) & 0x30303030u);
+                const int c = sub >> 1;
+                const int sh = 16 * (c & 1);
+                const uint32_t scw = c < 2 ? sc03 : sc47, mnw = c < 2 ? mn03 : mn47;
+                const int sc_lo = (scw >> sh) & 0xff, sc_hi = (scw >> (sh + 8)) & 0xff;
+                const int mn_lo = (mnw >> sh) & 0xff, mn_hi = (mnw >> (sh + 8)) & 0xff;
+                const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                uint32_t lo[4], hi[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        lo[k] = qw[k] & 0x0f0f0f0fu;
-                        hi[k] = (qw[k] >> 4) & 0x0f0f0f0fu;
-                    }
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        int il = 0, ih = 0;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            il = __dp4a(static_cast<int>(lo[k]), static_cast<int>(xa[m][k]), il);
-                            ih = __dp4a(static_cast<int>(hi[k]), static_cast<int>(xb[m][k]), ih);
-                        }
-                        const int s1 = sc_lo * il + sc_hi * ih;
-                        const int s2 = mn_lo * bsa[m] + mn_hi * bsb[m];
-                        v[rr * P + m] = dx[m] * fmaf(d, static_cast<float>(s1), -dmin * static_cast<float>(s2));
-                    }
-                } else {
-                    const uint4 ql = *reinterpret_cast<const uint4*>(blk + wq0);
-                    const uint4 qh = *reinterpret_cast<const uint4*>(blk + wq1);
-                    const uint2 scv = *reinterpret_cast<const uint2*>(blk + 192 + 8 * (sub >> 2));
-                    const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
-                    const int pp = (sub >> 1) & 1, ga = sub & 3;   // ga = 2*pp + s: group in its chunk
-                    const int sc_a = static_cast<int8_t>((scv.x >> (8 * ga)) & 0xffu);
-                    const int sc_b = static_cast<int8_t>((scv.y >> (8 * ga)) & 0xffu);
-                    const uint32_t lw[4] = {ql.x, ql.y, ql.z, ql.w};
-                    const uint32_t hw[4] = {qh.x, qh.y, qh.z, qh.w};
-                    uint32_t qa[4], qb[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        qa[k] = (lw[k] & 0x0f0f0f0fu) | (((hw[k] >> (2 * pp)) & 0x03030303u) << 4);
-                        qb[k] = ((lw[k] >> 4) & 0x0f0f0f0fu) | (((hw[k] >> (4 + 2 * pp)) & 0x03030303u) << 4);
-                    }
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        int ia = 0, ib = 0;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            ia = __dp4a(static_cast<int>(qa[k]), static_cast<int>(xa[m][k]), ia);
-                            ib = __dp4a(static_cast<int>(qb[k]), static_cast<int>(xb[m][k]), ib);
-                        }
-                        const int sv = sc_a * (ia - 32 * bsa[m]) + sc_b * (ib - 32 * bsb[m]);
-                        v[rr * P + m] = (dx[m] * d) * static_cast<float>(sv);
-                    }
+                for (int k = 0; k < 4; ++k) {
+                    lo[k] = qw[k] & 0x0f0f0f0fu;
+                    hi[k] = (qw[k] >> 4) & 0x0f0f0f0fu;
                 }
-            }
-            // lane l now holds the warp total of value t = l / (32 / VALS), i.e.
-            // row t / P, token t % P of the batch
-            const float tot = reduce_scatter<VALS>(v, lane);
-            float (*rbuf)[32] = red[it & 1];
-            if ((lane & (32 / VALS - 1)) == 0) rbuf[warp][lane / (32 / VALS)] = tot;
-            __syncthreads();
-            if (warp == 0 && lane < VALS) {
-                const int rr = lane / P, m = lane % P, n = ra + q0 + rr;
-                if (m < MT && q0 + rr < nr) {
-                    float sum = 0.0f;
-                    for (int u = 0; u < nw; ++u) sum += rbuf[u][lane];
-                    epi_store(y, static_cast<int64_t>(m) * ldy + n,
-                              epi_value(sum, epi.bias ? epi.bias[n] : 0.0f, epi.act), epi.out);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    int il = 0, ih = 0;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        il = __dp4a(static_cast<int>(lo[k]), static_cast<int>(xa[m][k]), il);
+                        ih = __dp4a(static_cast<int>(hi[k]), static_cast<int>(xb[m][k]), ih);
+                    }
+                    const int s1 = sc_lo * il + sc_hi * ih;
+                    const int s2 = mn_lo * bsa[m] + mn_hi * bsb[m];
+                    v[rr * P + m] = dx[m] * fmaf(d, static_cast<float>(s1), -dmin * static_cast<float>(s2));
+                }
+            } else {
+                const uint4 ql = *reinterpret_cast<const uint4*>(blk + wq0);
+                const uint4 qh = *reinterpret_cast<const uint4*>(blk + wq1);
+                const uint2 scv = *reinterpret_cast<const uint2*>(blk + 192 + 8 * (sub >> 2));
+                const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
+                const int pp = (sub >> 1) & 1, ga = sub & 3;   // ga = 2*pp + s: group in its chunk
+                const int sc_a = static_cast<int8_t>((scv.x >> (8 * ga)) & 0xffu);
+                const int sc_b = static_cast<int8_t>((scv.y >> (8 * ga)) & 0xffu);
+                const uint32_t lw[4] = {ql.x, ql.y, ql.z, ql.w};
+                const uint32_t hw[4] = {qh.x, qh.y, qh.z, qh.w};
+                uint32_t qa[4], qb[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    qa[k] = (lw[k] & 0x0f0f0f0fu) | (((hw[k] >> (2 * pp)) & 0x03030303u) << 4);
+                    qb[k] = ((lw[k] >> 4) & 0x0f0f0f0fu) | (((hw[k] >> (4 + 2 * pp)) & 0x03030303u) << 4);
+                }
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    int ia = 0, ib = 0;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        ia = __dp4a(static_cast<int>(qa[k]), static_cast<int>(xa[m][k]), ia);
+                        ib = __dp4a(static_cast<int>(qb[k]), static_cast<int>(xb[m][k]), ib);
+                    }
+                    const int sv = sc_a * (ia - 32 * bsa[m]) + sc_b * (ib - 32 * bsb[m]);
+                    v[rr * P + m] = (dx[m] * d) * static_cast<float>(sv);
                 }
             }
         }
-        __syncthreads();   // stage buffer g & 1 is refilled next
-        if (g + 2 < nstage) issue_stage(g + 2);
+        __syncwarp();   // every lane of the warp is done with the slot
+        if (lane == 0) mbar_arrive(&empty[sl]);
+
+        // lane l now holds the warp total of value t = l / (32 / VALS), i.e.
+        // row lj + rl * (t / P), token t % P of the stage
+        const float tot = reduce_scatter<VALS>(v, lane);
+        if ((lane & (32 / VALS - 1)) == 0) red[g & 1][warp][lane / (32 / VALS)] = tot;
+        // the row lane's partials are out; warp 0 of the row lane adds them.
+        // (red[g & 1] is written again at stage g + 2, after the barrier of
+        // stage g + 1, which warp 0 reaches only once this sum is done.)
+        row_lane_sync(1 + lj, 32 * wpr);
+        if (wk == 0 && lane < VALS && ok) {
+            const int rr = lane / P, m = lane % P, q = lj + rl * rr;
+            if (m < MT && rr < rps && q < nr) {
+                float sum = 0.0f;
+                for (int u = 0; u < wpr; ++u) sum += red[g & 1][lj * wpr + u][lane];
+                const int n = ra + q;
+                epi_store(y, static_cast<int64_t>(m) * ldy + n,
+                          epi_value(sum, epi.bias ? epi.bias[n] : 0.0f, epi.act), epi.out);
+            }
+        }
     }
 }
 
-// Resident CTAs per SM of one kernel instantiation and shape, looked up once
-// per device (the dynamic shared-memory limit is raised on first use).
-cudaError_t small_occupancy(const void* kernel, int wt, int mt, int nb, int threads, size_t smem, int* occ) {
+// The ring is above the default 48 KB of dynamic shared memory: raise each
+// instantiation's limit once per device.
+cudaError_t ensure_smem_limit(const void* kernel, size_t bytes) {
     static std::mutex mtx;
-    static std::unordered_map<uint64_t, int> cache;
+    static std::unordered_set<uint64_t> done;   // (device, kernel)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const uint64_t key = (static_cast<uint64_t>(dev) << 32) | (static_cast<uint64_t>(wt) << 24) |
-                         (static_cast<uint64_t>(mt) << 16) | static_cast<uint64_t>(nb);
+    const uint64_t key = (static_cast<uint64_t>(dev) << 56) ^ reinterpret_cast<uint64_t>(kernel);
     std::lock_guard<std::mutex> lk(mtx);
-    auto it = cache.find(key);
-    if (it != cache.end()) {
-        *occ = it->second;
-        return cudaSuccess;
-    }
-    // the limit belongs to the kernel, shared by every shape: raise it to the
-    // most any shape asks (two stages of at most SM_STAGE_BYTES whole rows)
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * SM_STAGE_BYTES);
-    if (e != cudaSuccess) return e;
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
-    if (e != cudaSuccess) return e;
-    *occ = n < 1 ? 1 : n;
-    cache[key] = *occ;
-    return cudaSuccess;
+    if (done.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess) done.insert(key);
+    return e;
 }
 
 // A programmatic dependent launch of the small-M kernel: its CTAs may start
@@ -324,29 +355,28 @@ cudaError_t launch_dependent(void (*kernel)(Params...), int grid, int threads, s
 template <int WT>
 cudaError_t launch_small_wt(const uint8_t* w, int64_t ldw, int N, int nb, const int8_t* xqs, const float* xd,
                             const int16_t* xbs, int M, void* y, int64_t ldy, const Epi& epi, int sm_count,
-                            cudaStream_t st) {
-    const int threads = 32 * ((nb + 3) / 4);
+                            uint32_t* status, cudaStream_t st) {
+    const int wpr = (nb + 3) / 4;   // warps per row lane
+    if (wpr < 1 || wpr > SM_MAX_WPR || sm_count < 1) return cudaErrorInvalidValue;
+    const int grid = sm_count < N ? sm_count : N;   // one CTA per SM
     const int row_bytes = nb * SmallTraits<WT>::BLOCK;
-    // stage: whole rows, at most about SM_STAGE_BYTES; two stage buffers per CTA
-    int max_rows = SM_STAGE_BYTES / row_bytes;   // >= 1: a row is at most 60 * 224 B
-    if (max_rows < 1) return cudaErrorInvalidValue;
-    const size_t smem = static_cast<size_t>(2) * max_rows * row_bytes;
-    // grid: as many CTAs as are resident at once, at most one per stage of rows
 #define QG_SMALL_CASE(MT)                                                                               \
     case MT: {                                                                                          \
         auto k = smallm_kernel<WT, MT>;                                                                 \
-        int occ = 0;                                                                                    \
-        cudaError_t e = small_occupancy(reinterpret_cast<const void*>(k), WT, MT, nb, threads, smem, &occ); \
+        int rl = small_max_warps(MT) / wpr;                                                             \
+        if (rl > SM_MAX_ROW_LANES) rl = SM_MAX_ROW_LANES;                                               \
+        /* rows per row lane and stage: a stage of at most SM_SLOT_TARGET bytes, one row each at least */ \
+        int rps = SM_SLOT_TARGET / (rl * row_bytes);                                                    \
+        if (rps > small_stage_rows(WT, MT)) rps = small_stage_rows(WT, MT);                             \
+        if (rps < 1) rps = 1;                                                                           \
+        const int slot = rl * rps * row_bytes;                                                          \
+        int nsb = SM_RING_BYTES / slot;                                                                 \
+        if (nsb > SM_MAX_SLOTS) nsb = SM_MAX_SLOTS;                                                     \
+        if (nsb < 2) return cudaErrorInvalidValue;                                                      \
+        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(k), SM_RING_BYTES);             \
         if (e != cudaSuccess) return e;                                                                 \
-        int64_t grid = static_cast<int64_t>(sm_count) * occ;                                            \
-        if (grid > N) grid = N;                                                                         \
-        /* at least two stages per CTA, so the second one loads while the first is used */             \
-        const int64_t rpc = (N + grid - 1) / grid;                                                      \
-        int stage_rows = static_cast<int>((rpc + 1) / 2);                                               \
-        if (stage_rows > max_rows) stage_rows = max_rows;                                               \
-        if (stage_rows < 1) stage_rows = 1;                                                             \
-        return launch_dependent(k, static_cast<int>(grid), threads, smem, st, w,                        \
-                                ldw, N, nb, xqs, xd, xbs, y, ldy, epi, stage_rows);                     \
+        return launch_dependent(k, grid, 32 * (rl * wpr + 1), static_cast<size_t>(nsb) * slot, st, w, ldw, N, \
+                                nb, xqs, xd, xbs, y, ldy, epi, wpr, rl, rps, nsb, status);              \
     }
     switch (M) {
         QG_SMALL_CASE(1)
@@ -368,7 +398,7 @@ cudaError_t launch_small_wt(const uint8_t* w, int64_t ldw, int N, int nb, const 
 bool small_supported(int wtype, int64_t M, int64_t K) {
     (void)wtype;
     const int64_t nb = K / 256;
-    return M >= 1 && M <= SMALL_M_LIMIT && (nb + 3) / 4 <= SM_MAX_WARPS;
+    return M >= 1 && M <= SMALL_M_LIMIT && (nb + 3) / 4 <= SM_MAX_WPR;
 }
 
 cudaError_t launch_small(const SmallLaunch& a, cudaStream_t st) {
@@ -376,9 +406,9 @@ cudaError_t launch_small(const SmallLaunch& a, cudaStream_t st) {
     const uint8_t* w = static_cast<const uint8_t*>(a.w);
     if (a.wtype == 4)
         return launch_small_wt<4>(w, a.ldw, static_cast<int>(a.N), nb, a.xqs, a.xd, a.xbs, static_cast<int>(a.M),
-                                  a.y, a.ldy, a.epi, a.sm_count, st);
+                                  a.y, a.ldy, a.epi, a.sm_count, a.status, st);
     return launch_small_wt<6>(w, a.ldw, static_cast<int>(a.N), nb, a.xqs, a.xd, a.xbs, static_cast<int>(a.M), a.y,
-                              a.ldy, a.epi, a.sm_count, st);
+                              a.ldy, a.epi, a.sm_count, a.status, st);
 }
 
 }  // namespace qg
