@@ -837,6 +837,9 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     } else if (warp >= W_EPI0) {
         // ------------------------------------------------ epilogue
         constexpr int CPT = L::CPT;
+        // The tile's store goes through TMEM (see below).  Not for the routed
+        // variant: there it raised the spills of the per-superblock loop.
+        constexpr bool STAGED = CPT >= 32 && !ROUTED;
         const int quad = warp & 3;
         const int half = (warp - W_EPI0) >> 2;
         const int row = 32 * quad + lane;
@@ -952,12 +955,22 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
+                // (STAGED: the item's last accumulator is released after the tile's store)
+                const bool hold = STAGED && b == kb1 - 1;
                 if (lane == 0) {
-                    mbar_arrive(&acc_empty[buf]);
+                    if (!hold) mbar_arrive(&acc_empty[buf]);
                     mbar_arrive(&sb_empty[p]);
                 }
             }
             if (!ok) break;
+            const int hbuf = (t - 1) & 1;   // the accumulator of the item's last superblock
+            auto release_held = [&]() {
+                if constexpr (STAGED) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[hbuf]);
+                }
+            };
             if (cut >= 0) {
                 griddep_wait();   // the counters are zeroed by the preceding grid
                 // a part of a cut tile: publish the partial tile, and the part
@@ -983,7 +996,10 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                 ok = mbar_wait(epi_bar, epi_phase, abort_flag, status, 14);   // the flag is set
                 epi_phase ^= 1u;
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                if (!*last_flag) continue;
+                if (!*last_flag) {
+                    release_held();
+                    continue;
+                }
                 // all parts, this one included, from memory in ascending order
                 __threadfence();
                 const float* base = wk.partials + static_cast<int64_t>(cut) * wk.parts * (BN * BM) + col0 * BN + row;
@@ -994,6 +1010,51 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                     for (int j = 0; j < CPT; ++j) acc[j] += __ldcg(base + p2 * (BN * BM) + j * BN);
                 }
                 if (warp == W_EPI0 && lane == 0) wk.counters[cut] = 0;   // ready for the next call
+            }
+            if constexpr (STAGED) {
+                // The finished tile goes out through the TMEM slot of the item's
+                // last accumulator: two stores, then a rolled loop over 8-column
+                // chunks.  (Measured on GB300: the 64-way unrolled store is
+                // several KB of code run once per tile; cold in the instruction
+                // cache it held every role behind the epilogue ~3 us per tile.)
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + hbuf * BM + col0;
+#pragma unroll
+                for (int h = 0; h < CPT / 32; ++h) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[32 * h + j]);
+                    tmem_st_32x32b_x32(taddr + 32 * h, r);
+                }
+                tmem_st_wait();
+                const int n = n0 + row;
+                const bool live = !*abort_flag && n < N;
+                float bn = 0.0f;
+                if constexpr (EPI) bn = bias_n;
+#pragma unroll 1
+                for (int c = 0; c < CPT; c += 8) {
+                    uint32_t v[8];
+                    __syncwarp();   // (the TMEM load is warp-collective: every lane, converged)
+                    tmem_ld_32x32b_x8(taddr + c, v);
+                    tmem_ld_wait();
+                    const int mc = m0 + col0 + c;
+                    if (live) {
+                        if constexpr (!EPI) {
+                            float* yp = static_cast<float*>(y) + static_cast<int64_t>(mc) * ldy + n;
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                if (mc + u < M) *yp = __uint_as_float(v[u]);
+                                yp += ldy;
+                            }
+                        } else {
+                            float vv[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) vv[u] = __uint_as_float(v[u]);
+                            epi_tile<8>(vv, epi, bn, y, ldy, n, mc, M);
+                        }
+                    }
+                }
+                release_held();
+                continue;
             }
             if constexpr (ROUTED) {
                 // routed: column n of the expert, token rows up to the expert's end,
