@@ -50,18 +50,18 @@ DEFAULT_WORKLOAD = synth.C1.name
 # kernel, from the ncu capture summarised under profiles/ (absent until
 # measured, and removed whenever the kernel changes).
 NCU_TRAFFIC_BYTES = {
-    "q4k_m512_k2048_n11008_outliers": 15017984,
-    "q4k_m64_k2048_n2048": 2718976,
-    "q6k_m512_k11008_n2048": 31182848,
-    "q4k_m2048_k4096_n14336": 119673088,
+    "q4k_m512_k2048_n11008_outliers": 15011840,
+    "q4k_m64_k2048_n2048": 2715136,
+    "q6k_m512_k11008_n2048": 31179520,
+    "q4k_m2048_k4096_n14336": 119772928,
     "q4k_sweep_m1_k5120_n5120": 14780928,
     "q4k_sweep_m4_k5120_n5120": 14810624,
     "q4k_sweep_m8_k5120_n5120": 14830336,
-    "q4k_sweep_m64_k5120_n5120": 15527680,
-    "q4k_sweep_m512_k5120_n5120": 20452096,
-    "q4k_sweep_m2048_k5120_n5120": 44666880,
-    "q4k_moe_e8_top2_m512_k4096_n14336": 319216896,
-    "ptq1_m2048_k5120_n5120": 33524224,
+    "q4k_sweep_m64_k5120_n5120": 15521792,
+    "q4k_sweep_m512_k5120_n5120": 20441856,
+    "q4k_sweep_m2048_k5120_n5120": 44628480,
+    "q4k_moe_e8_top2_m512_k4096_n14336": 319418112,
+    "ptq1_m2048_k5120_n5120": 33791488,
 }
 
 
