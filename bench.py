@@ -50,18 +50,18 @@ DEFAULT_WORKLOAD = synth.C1.name
 # kernel, from the ncu capture summarised under profiles/ (absent until
 # measured, and removed whenever the kernel changes).
 NCU_TRAFFIC_BYTES = {
-    "q4k_m512_k2048_n11008_outliers": 15011840,
+    "q4k_m512_k2048_n11008_outliers": 15012608,
     "q4k_m64_k2048_n2048": 2715136,
-    "q6k_m512_k11008_n2048": 31179520,
-    "q4k_m2048_k4096_n14336": 119772928,
+    "q6k_m512_k11008_n2048": 31176704,
+    "q4k_m2048_k4096_n14336": 120304640,
     "q4k_sweep_m1_k5120_n5120": 14780928,
     "q4k_sweep_m4_k5120_n5120": 14810624,
     "q4k_sweep_m8_k5120_n5120": 14830336,
-    "q4k_sweep_m64_k5120_n5120": 15521792,
-    "q4k_sweep_m512_k5120_n5120": 20441856,
-    "q4k_sweep_m2048_k5120_n5120": 44628480,
-    "q4k_moe_e8_top2_m512_k4096_n14336": 319418112,
-    "ptq1_m2048_k5120_n5120": 33791488,
+    "q4k_sweep_m64_k5120_n5120": 15523584,
+    "q4k_sweep_m512_k5120_n5120": 20443136,
+    "q4k_sweep_m2048_k5120_n5120": 44840448,
+    "q4k_moe_e8_top2_m512_k4096_n14336": 319335424,
+    "ptq1_m2048_k5120_n5120": 34377984,
 }
 
 
