@@ -838,7 +838,9 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
         // ------------------------------------------------ epilogue
         constexpr int CPT = L::CPT;
         // The tile's store goes through TMEM (see below).  Not for the routed
-        // variant: there it raised the spills of the per-superblock loop.
+        // variant: there it raised the spills of the per-superblock loop from
+        // 8 to 204 B and slowed the 8-expert M=512 K=4096 N=14336 call from
+        // 231 to 308 us (measured on GB300).
         constexpr bool STAGED = CPT >= 32 && !ROUTED;
         const int quad = warp & 3;
         const int half = (warp - W_EPI0) >> 2;
