@@ -52,7 +52,7 @@ DEFAULT_WORKLOAD = synth.C1.name
 NCU_TRAFFIC_BYTES = {
     "q4k_m512_k2048_n11008_outliers": 15012608,
     "q4k_m64_k2048_n2048": 2715136,
-    "q6k_m512_k11008_n2048": 31176704,
+    "q6k_m512_k11008_n2048": 31173888,
     "q4k_m2048_k4096_n14336": 120304640,
     "q4k_sweep_m1_k5120_n5120": 14780928,
     "q4k_sweep_m4_k5120_n5120": 14810624,

