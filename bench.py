@@ -20,6 +20,13 @@ gaps between its kernels.  The same K steps then run once more as eager calls,
 with the GEMM kernel alone timed by events the library records around its
 launch (qgemm_set_profile_events).
 
+End to end (the "e2e" key): the same steps through the same API calls, with X
+(and a routed step's expert ids) starting in pinned host memory and Y ending
+there.  The library's kernels read X and write Y across the host link
+themselves (zero-copy).  The same step with cudaMemcpyAsync copies of X and Y
+around the device step is reported beside it (e2e.copies).  Both count the
+bytes that cross the link each step.
+
 --impl reference times the CPU oracle (the parity authority) on bounded
 samples of the same workload on the host cores: the reference arm.
 """
