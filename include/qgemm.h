@@ -145,8 +145,8 @@ QGEMM_API int qgemm_q6k(const void *w_packed, int64_t N, int64_t K, const int8_t
 /* ------------------------------------------------ prepared workspace ----
  * A step that quantizes and then multiplies can skip one launch: the
  * quantizer writes the tile GEMM's fp16 operand planes into the GEMM's
- * workspace in the same pass (the pages' "fuse the quantize into the GEMM
- * producer" direction; the pages have no such call).
+ * workspace in the same pass (a step toward fusing the quantizer into the
+ * GEMM's producer; the pages have no such call).
  *
  * qgemm_quantize_q8k_prep: exactly qgemm_quantize_q8k (same Q8_K planes,
  * bit-exact), and in the same launch it fills `workspace` (>=
