@@ -83,7 +83,8 @@ QGEMM_API const char *qgemm_last_error(void);
 /* ------------------------------------------------------------- Q8_K ----
  * qgemm_quantize_q8k: fp32 activations -> Q8_K planes (step "quantize the
  * activations" that precedes the GEMM; PR #3036 commit 5, EnsureQuantScratch).
- *   x      device, fp32 [M][ldx] row-major, 16-B aligned, ldx % 4 == 0,
+ *   x      device or pinned host (Conventions), fp32 [M][ldx] row-major,
+ *          16-B aligned, ldx % 4 == 0,
  *          ldx >= K; values must be finite.
  *   M      rows (tokens), M >= 0 (M == 0: nothing to do, QGEMM_OK).
  *   K      columns, K >= 256 and K % 256 == 0.
@@ -113,7 +114,8 @@ QGEMM_API size_t qgemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   N      weight rows, N >= 1.     K: K >= 256, K % 256 == 0.
  *   xqs, xd, xbsums   the Q8_K planes of M tokens (as qgemm_quantize_q8k
  *          writes them).   M >= 0 (0: nothing to do).
- *   y      device, fp32 [M][ldy], ldy >= N, 4-B aligned.  Overwritten.
+ *   y      device or pinned host (Conventions), fp32 [M][ldy], ldy >= N,
+ *          4-B aligned.  Overwritten.
  *   workspace, workspace_bytes   device scratch >= qgemm_workspace_bytes.
  * Accuracy: |Y - Y_exact| <= 2e-5 * sum_b |c_b| + 1e-6 per element, c_b the
  * contribution of superblock b (fp32 accumulation of exact integer partials).
@@ -182,11 +184,11 @@ QGEMM_API int qgemm_q6k_prepared(const void *w_packed, int64_t N, int64_t K, con
  *   w, ldw      as qgemm_q4k, E*N rows (Q6_K: the 224-B repacked blocks of all
  *               E*N rows, qgemm_q6k_prepack with N = E*N).
  *   experts     E, 1..1024.   N, K, xqs, xd, xbsums, M: as qgemm_q4k.
- *   ids         device, int32 [M][top_k], 4-B aligned; ids outside [0, E) set
+ *   ids         device or pinned host, int32 [M][top_k], 4-B aligned; ids outside [0, E) set
  *               device status QGEMM_DEV_BAD_EXPERT and their output rows are
  *               left untouched.
  *   top_k       slots per token, >= 1;  M * top_k and E * N below 2^31.
- *   y           device, fp32 [M * top_k][ldy], ldy >= N, 4-B aligned.
+ *   y           device or pinned host, fp32 [M * top_k][ldy], ldy >= N, 4-B aligned.
  *   workspace   >= qgemm_id_workspace_bytes(M, top_k, E, K), 256-B aligned:
  *               the routing (pairs grouped by expert) and the operand planes of
  *               the M * top_k routed rows.
