@@ -219,6 +219,24 @@ def config_of(wl):
     return c
 
 
+def max_over_ranks(values, world, device):
+    """Each rank's timings -> the slowest rank's, element by element (the job
+    lasts as long as its slowest replica).  One all-reduce of the whole list."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_tops(world, ops_per_rank, ms):
+    """Whole-job throughput under weak scaling: the work of all `world` ranks
+    over the slowest rank's time per step (ms)."""
+    return world * ops_per_rank / (ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -376,13 +394,10 @@ def main():
     mean_ms = sum(step_ms) / K_steps
     eager_mean_ms = sum(eager_ms) / K_steps
     gemm_mean_ms = sum(gemm_ms) / K_steps
-    if world > 1:
-        t = torch.tensor([mean_ms, gemm_mean_ms, eager_mean_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_ms, gemm_mean_ms, eager_mean_ms = float(t[0]), float(t[1]), float(t[2])
+    mean_ms, gemm_mean_ms, eager_mean_ms = max_over_ranks([mean_ms, gemm_mean_ms, eager_mean_ms], world, dev)
 
     ops = 2.0 * rows_out * N * K
-    value = world * ops / (mean_ms * 1e-3) / 1e12
+    value = job_tops(world, ops, mean_ms)
     # library kernels per step, counted on the eager pass; the graph replays the same ones
     # (a routed GEMM call is three: routing, operand gather, tile GEMM)
     per_step = sum(c1[k] - c0[k] for k in ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small",
@@ -427,16 +442,12 @@ def main():
         torch.cuda.synchronize()
         barrier()
         ms = sum(e_s[i].elapsed_time(e_e[i]) for i in range(K_steps)) / K_steps
-        if world > 1:
-            t = torch.tensor([ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t[0])
-        return ms
+        return max_over_ranks([ms], world, dev)[0]
 
     e2e_ms = time_e2e(e2e_zero_copy)
     e2e_copies_ms = time_e2e(e2e_copies)
-    e2e_value = world * ops / (e2e_ms * 1e-3) / 1e12
-    e2e_copies_value = world * ops / (e2e_copies_ms * 1e-3) / 1e12
+    e2e_value = job_tops(world, ops, e2e_ms)
+    e2e_copies_value = job_tops(world, ops, e2e_copies_ms)
 
     bits, site = qg.qgemm_get_device_status()
 
