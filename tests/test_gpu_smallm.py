@@ -70,6 +70,16 @@ def test_shapes(wtype, M, N, K):
     run_small(wtype, weights(wtype, N, K, 7 * N + K), K, synth.gen_x(M, K, N + M), f"Q{wtype}_K M{M} N{N} K{K}")
 
 
+# Each CTA streams more stages than its shared-memory ring holds, so the
+# producer waits for consumed slots and refills them.  Ring geometry for these
+# launches on 152 SMs (stages per CTA against ring slots): Q4_K M=1 K=1024,
+# 12 against 5; Q6_K M=8 K=2048, 20 against 8; Q4_K M=5 K=5120, 27 against 11.
+@pytest.mark.parametrize("wtype,M,N,K", [(4, 1, 96000, 1024), (6, 8, 40000, 2048), (4, 5, 24000, 5120)])
+def test_ring_wraps(wtype, M, N, K):
+    run_small(wtype, weights(wtype, N, K, 3 * M + 1), K, synth.gen_x(M, K, 5 * M + 2, outlier_frac=0.01),
+              f"Q{wtype}_K M{M} N{N} K{K} (ring wraps)")
+
+
 @pytest.mark.parametrize("M", [1, 4, 8])
 def test_sweep_workload(M):
     wl = synth.sweep(M)
