@@ -41,7 +41,9 @@
 //     the activation stream fed.
 //
 // TMEM columns: [0, 2*BM) two fp32 accumulators (superblock t uses t & 1);
-// [256, 512) four 64-column K128 stages of the weight operand.
+// [256, 512) four 64-column K128 stages of the weight operand.  A finished
+// tile goes out through the slot of its last superblock's accumulator, which
+// is released to the MMA only after that store.
 //
 // MMA issue is the critical path.  On GB300 a tcgen05.mma (M128 N128 K16)
 // holds its issuing thread for ~55 of the ~64 cycles it runs, and the pipe
@@ -53,8 +55,9 @@
 // K128 (8 MMAs) with a non-blocking look-ahead probe of the next step's
 // barriers between the MMAs of the current one.
 //
-// Warp roles (16 warps, persistent CTAs looping over (n-tile, m-tile, split)
-// work items with token tiles varying fastest):
+// Warp roles (16 warps for Q4_K, 20 for Q6_K and PTQ1_0, whose heavier
+// expansion has a second unpack group; persistent CTAs looping over (n-tile,
+// m-tile, split) work items with token tiles varying fastest):
 //   warp 0      TMA producer of the activation stages (K128 or K256 per stage,
 //               one barrier each)
 //   warps 1, 3  MMA issuers (one thread each): even / odd superblocks; warp 1
@@ -62,9 +65,12 @@
 //   warp 2      TMA producer: raw weight blocks (+ L2 prefetch ahead) and the
 //               per-superblock side data (bsums, dx)
 //   warps 4-7   unpack: thread = weight row; branch-free expand of each K64
-//               chunk into registers, tcgen05.st into TMEM
-//   warps 8-15  epilogue: warp w reads TMEM lanes 32*(w%4).. and half of the
+//               chunk into registers, tcgen05.st into TMEM (Q6_K, PTQ1_0:
+//               warps 4-11, group g expanding K128 step g of each superblock)
+//   last 8      epilogue: warp w reads TMEM lanes 32*(w%4).. and half of the
 //               token columns, accumulates Y in registers, stores per tile
+//               through TMEM in a rolled loop; for Q4_K the second half also
+//               writes each superblock's dmin-correction operands and scale e
 // Every wait is bounded (see ptx.cuh); a timeout sets the status word and the
 // CTA runs to completion without touching Y.
 #pragma once
