@@ -7,7 +7,8 @@
   scaled x8.
 - The router: top_k distinct experts per token, uniform without skew, and
   weighted toward low expert ids with skew.
-- The benchmark workloads' shapes and seeds are the ones the design lists."""
+- The benchmark workloads: shapes, seeds (1000 + i for weights, (1000 + i) * 100
+  + 7 for X; 1004 and 100400 + M for the sweep), scales and outlier columns."""
 import numpy as np
 import pytest
 
