@@ -67,6 +67,7 @@ NCU_TRAFFIC_BYTES = {
     "q4k_sweep_m64_k5120_n5120": 15523584,
     "q4k_sweep_m512_k5120_n5120": 20443136,
     "q4k_sweep_m2048_k5120_n5120": 44840448,
+    "q4k_sweep_m8192_k5120_n5120": 1683155968,
     "q4k_moe_e8_top2_m512_k4096_n14336": 319335424,
     "ptq1_m2048_k5120_n5120": 34377984,
 }
