@@ -18,8 +18,8 @@
  *         int8 scales[16] (sub-block j = weights 16j..16j+15), fp16 d;
  *         w = d*sc_j*(q - 32).
  *   Q8_K, 256 activations: fp32 d = amax/127, int8 q = round-half-away(x/d)
- *         clamped to +-127, int16 bsums[16] = sums of each 16 q (the
- *         "BlockQ8_K (292B/256 elements)" of PR #3036, commit 4).  Here kept
+ *         clamped to +-127, int16 bsums[16] = sums of each 16 q (PR #3036,
+ *         commit 4, gives the block as 292 bytes per 256 elements).  Here kept
  *         as three planes: qs [M][K] int8, d [M][K/256] fp32, bsums [M][K/16]
  *         int16, each contiguous with row stride K, K/256, K/16 elements.
  *
@@ -38,8 +38,8 @@
  *     planes, workspace) must be device memory; this is not checked.
  *   - Calls enqueue work on `stream` and return; they do not synchronize.
  *   - Argument errors are reported synchronously and nothing is launched
- *     (a nonzero status, so the caller can fall back: "the launcher returns
- *     nonzero and the runtime falls back", hip-ep PR #627).  Unsupported
+ *     (a nonzero status, so the caller can fall back to another path, the
+ *     convention of hip-ep PR #627).  Unsupported
  *     shapes are declined, never computed wrongly.  qgemm_last_error()
  *     gives a one-line reason (thread-local).
  *   - Y is fully overwritten (beta = 0).
@@ -81,8 +81,8 @@ QGEMM_API int qgemm_version(void);
 QGEMM_API const char *qgemm_last_error(void);
 
 /* ------------------------------------------------------------- Q8_K ----
- * qgemm_quantize_q8k: fp32 activations -> Q8_K planes (step "quantize the
- * activations" that precedes the GEMM; PR #3036 commit 5, EnsureQuantScratch).
+ * qgemm_quantize_q8k: fp32 activations -> Q8_K planes (the activation
+ * quantization that precedes the GEMM; PR #3036 commit 5, EnsureQuantScratch).
  *   x      device or pinned host (Conventions), fp32 [M][ldx] row-major,
  *          16-B aligned, ldx % 4 == 0,
  *          ldx >= K; values must be finite.
