@@ -27,9 +27,27 @@ namespace {
 static __device__ __align__(256) uint8_t g_noalloc_scratch[QGEMM_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
-cudaError_t g_setup_err[kMaxDevices];
-void* g_scratch_ptr[kMaxDevices];
+std::mutex g_setup_mtx;
+void* g_scratch_ptr[kMaxDevices];   // set once the lookup has succeeded on that device
+
+// The device address of this device's copy of the scratch array, looked up
+// with that device current.  A failed lookup is not remembered: the next call
+// tries again.  Its error is also taken off the runtime's last-error slot, so
+// that it is not reported later by an unrelated launch check.
+cudaError_t scratch_of(int dev, void** out) {
+    std::lock_guard<std::mutex> lk(g_setup_mtx);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            cudaGetLastError();
+            return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+        }
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
 
 }  // namespace
 
@@ -50,22 +68,18 @@ extern "C" int qgemm_q4k_noalloc(const void* w, int64_t N, int64_t K, int64_t ld
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return qg::set_last_error(QGEMM_ECUDA, "qgemm_q4k_noalloc: no usable current device");
-    // Set-up, once per device, with that device current: look up the device
-    // address of this device's copy of the scratch array.
-    std::call_once(g_once[dev], [dev] {
-        void* p = nullptr;
-        g_setup_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        g_scratch_ptr[dev] = p;
-    });
-    if (g_setup_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) {
+    // Set-up, once per device (retried until it succeeds), with that device
+    // current: look up the device address of this device's scratch array.
+    void* scratch = nullptr;
+    e = scratch_of(dev, &scratch);
+    if (e != cudaSuccess) {
         char msg[200];
-        snprintf(msg, sizeof(msg), "qgemm_q4k_noalloc: cudaGetSymbolAddress failed: %s",
-                 cudaGetErrorString(g_setup_err[dev]));
+        snprintf(msg, sizeof(msg), "qgemm_q4k_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
         return qg::set_last_error(QGEMM_ECUDA, msg);
     }
     // Everything the GEMM reads from the scratch is first written by the
     // operand-preparation kernel of the same call, so nothing has to be
     // cleared between calls.
-    return qgemm_q4k(w, N, K, ldw, xqs, xd, xbsums, M, y, ldy, g_scratch_ptr[dev], QGEMM_NOALLOC_SCRATCH_BYTES,
+    return qgemm_q4k(w, N, K, ldw, xqs, xd, xbsums, M, y, ldy, scratch, QGEMM_NOALLOC_SCRATCH_BYTES,
                      stream);
 }

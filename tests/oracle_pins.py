@@ -62,6 +62,28 @@ def check_q4k_scale_bytes_hand(orc):
     assert mn[1] == 6 and mn[5] == 4 + 32, mn
 
 
+def check_q4k_header_bytes_hand(orc):
+    """The block header, written byte by byte (no pack function): fp16 d in
+    bytes 0-1 and fp16 dmin in bytes 2-3, little-endian."""
+    blk = np.zeros(144, np.uint8)
+    blk[0:4] = [0x00, 0x3C, 0x00, 0x40]          # d = 1.0 (0x3C00), dmin = 2.0 (0x4000)
+    d, dmin, _, _, _ = orc.q4k_fields(blk)
+    assert (d, dmin) == (1.0, 2.0), (d, dmin)
+    blk[0:4] = [0x00, 0x38, 0x00, 0x3C]          # d = 0.5, dmin = 1.0
+    blk[4] = 3                                   # sc_0 = 3
+    blk[8] = 5                                   # m_0 = 5
+    blk[16] = 0x07                               # q_0 = 7, q_32 = 0
+    d, dmin, _, _, _ = orc.q4k_fields(blk)
+    assert (d, dmin) == (0.5, 1.0), (d, dmin)
+    w = orc.dequant(4, blk)
+    assert w[0] == 0.5 * 3 * 7 - 1.0 * 5, w[0]   # d * sc_0 * q_0 - dmin * m_0
+    assert w[1] == -5.0, w[1]                    # q_1 = 0
+    # the packer writes the same bytes
+    sc = np.zeros(8, int); mn = np.zeros(8, int); q = np.zeros(256, int)
+    sc[0], mn[0], q[0] = 3, 5, 7
+    assert np.array_equal(orc.q4k_pack(0x3800, 0x3C00, sc, mn, q), blk)
+
+
 def check_q4k_nibble_bytes_hand(orc):
     """qs byte 32c+l: low nibble = weight 64c+l, high nibble = weight 64c+32+l."""
     blk = np.zeros(144, np.uint8)
@@ -484,7 +506,7 @@ def check_gemm_ptq1(orc):
 
 ALL_CHECKS = [
     check_half_decode,
-    check_q4k_scale_bytes_hand, check_q4k_nibble_bytes_hand, check_q4k_roundtrip,
+    check_q4k_header_bytes_hand, check_q4k_scale_bytes_hand, check_q4k_nibble_bytes_hand, check_q4k_roundtrip,
     check_q4k_dequant_hand,
     check_q6k_bytes_hand, check_q6k_roundtrip, check_q6k_dequant_hand,
     check_q8k_bound_and_extremes, check_q8k_ties, check_q8k_bsums,

@@ -71,3 +71,16 @@ def sample_rows(M, n, seed, tail=8):
     rows = set(r.choice(M, size=min(n, M), replace=False).tolist())
     rows |= {0} | set(range(max(0, M - tail), M))
     return np.array(sorted(rows), dtype=np.int64)
+
+
+def tile_rows(M, n, seed, bm=128, tail=16):
+    """Rows for a sampled parity check at large M: n seeded random rows, one
+    seeded row inside every bm-token tile, the first row, and the last
+    `tail` rows plus every row of a ragged last tile (M % bm != 0)."""
+    r = np.random.default_rng(seed)
+    rows = set(r.choice(M, size=min(n, M), replace=False).tolist())
+    for t0 in range(0, M, bm):
+        rows.add(int(r.integers(t0, min(M, t0 + bm))))
+    last = M - (M % bm) if M % bm else M - min(M, tail)
+    rows |= {0} | set(range(max(0, min(last, M - tail)), M))
+    return np.array(sorted(rows), dtype=np.int64)

@@ -19,7 +19,7 @@ import synth
 import block_quantized_matmul_quantize_gb300 as qg
 from gpu_common import (assert_q8k_equal, device_status_clean, ensure_built, gpu_gemm, gpu_quantize,
                         q8k_numpy, to_dev)
-from parity_util import assert_gemm_close, oracle_gemm, sample_rows
+from parity_util import assert_gemm_close, oracle_gemm, sample_rows, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -111,7 +111,8 @@ def test_workload_full(wl):
 @pytest.mark.parametrize("wl", [synth.C3] + [synth.sweep(m) for m in synth.SWEEP_M],
                          ids=lambda w: w.name)
 def test_workload_sampled(wl):
-    rows = None if wl.M <= 64 else sample_rows(wl.M, 48, seed=wl.M)
+    # at least 256 rows, one in every 128-token tile, and the tail rows
+    rows = None if wl.M <= 256 else tile_rows(wl.M, 256, seed=wl.M)
     check(wl.wtype, wl.weights(), wl.K, wl.x(), rows=rows, what=wl.name)
 
 

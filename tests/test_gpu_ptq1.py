@@ -13,7 +13,7 @@ import oracle
 import synth
 import block_quantized_matmul_quantize_gb300 as qg
 from gpu_common import device_status_clean, ensure_built, gpu_quantize, q8k_numpy, to_dev
-from parity_util import assert_gemm_close, oracle_gemm, sample_rows
+from parity_util import assert_gemm_close, oracle_gemm, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -87,7 +87,7 @@ def test_extreme_blocks():
 
 def test_k5120_sampled():
     M, N, K = 512, 5120, 5120
-    check(synth.gen_ptq1(N, K, 31), K, synth.gen_x(M, K, 32), rows=sample_rows(M, 24, seed=4), what="M512 K5120 N5120")
+    check(synth.gen_ptq1(N, K, 31), K, synth.gen_x(M, K, 32), rows=tile_rows(M, 256, seed=4), what="M512 K5120 N5120")
 
 
 def test_prepared_workspace():

@@ -22,7 +22,7 @@ import oracle
 import synth
 import block_quantized_matmul_quantize_gb300 as qg
 from gpu_common import device_status_clean, ensure_built, gpu_quantize, q8k_numpy, to_dev
-from parity_util import assert_gemm_close, oracle_gemm, sample_rows
+from parity_util import assert_gemm_close, oracle_gemm, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -84,7 +84,7 @@ def test_several_tiles_per_cta(wtype, M, N, K, bm):
         y = run(wtype, w, K, q)
     finally:
         qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
-    rows = sample_rows(M, 6, 52 + M, tail=3)
+    rows = tile_rows(M, 32, 52 + M, bm=bm, tail=3)
     yr, absc = oracle_gemm(wtype, w, K, *q8k_numpy(q), rows=rows)
     assert_gemm_close(y[rows], yr, absc, f"Q{wtype}_K M{M} N{N} K{K} BM{bm}")
     device_status_clean()
@@ -104,7 +104,7 @@ def test_several_tiles_per_cta_with_epilogue(out_name, act_name, bm):
         y = run(4, w, K, q, out=out, bias=bias, act=ACT[act_name])
     finally:
         qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
-    rows = sample_rows(M, 6, 64, tail=3)
+    rows = tile_rows(M, 32, 64, bm=bm, tail=3)
     yr, absc = oracle_gemm(4, w, K, *q8k_numpy(q), rows=rows)
     ref = oracle.get().epilogue(yr, bias, ACT[act_name])
     tol = 1.2 * (2e-5 * absc + 1e-6) + (5e-6 + rel) * np.abs(ref) + 1e-6

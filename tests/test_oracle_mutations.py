@@ -1,6 +1,8 @@
 """Plant mistakes in a copy of the oracle (on the CPU) and check that the pins
 catch every one of them: a pin suite that passes a broken oracle proves
-nothing.  Each mutant is built from oracle.c with one textual change."""
+nothing.  Each mutant is built from oracle.c with one textual change (or,
+where one mistake must be made in two places to survive the round trips, a
+list of changes)."""
 import os
 import shutil
 
@@ -34,6 +36,11 @@ MUTATIONS = {
     "ptq1_digit_order": ("t[k] = ptq1_digit(blk[k % 24], k / 24);", "t[k] = ptq1_digit(blk[k % 24], 4 - k / 24);"),
     "ptq1_qh_byte": ("t[120 + r] = ptq1_digit(blk[24 + r % 2], r / 2);", "t[120 + r] = ptq1_digit(blk[24 + r / 4], r % 4);"),
     "ptq1_gemm_offset": ("I[h] += (int64_t)(t[h][k] - 1) * xq[128 * h + k];", "I[h] += (int64_t)t[h][k] * xq[128 * h + k];"),
+    # d and dmin swapped in both the decoder and the packer (their round trip still agrees)
+    "q4k_d_dmin_swapped": [("*d = oracle_half_to_double(rd16(blk));\n    *dmin = oracle_half_to_double(rd16(blk + 2));",
+                            "*d = oracle_half_to_double(rd16(blk + 2));\n    *dmin = oracle_half_to_double(rd16(blk));"),
+                           ("wr16(blk, d_bits);\n    wr16(blk + 2, dmin_bits);",
+                            "wr16(blk + 2, d_bits);\n    wr16(blk, dmin_bits);")],
     "brute_dmin_sign": ("w[i] = d * sc[i / 32] * q[i] - dmin * mn[i / 32];", "w[i] = d * sc[i / 32] * q[i] + dmin * mn[i / 32];"),
 }
 
@@ -51,12 +58,14 @@ def _fails(orc):
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_mutant_is_caught(name, tmp_path):
     src = open(oracle.SRC).read()
-    old, new = MUTATIONS[name]
-    assert src.count(old) == 1, f"mutation anchor for {name} not unique/present"
+    changes = MUTATIONS[name]
+    for old, new in ([changes] if isinstance(changes, tuple) else changes):
+        assert src.count(old) == 1, f"mutation anchor for {name} not unique/present"
+        src = src.replace(old, new)
     mdir = tmp_path / "mut"
     mdir.mkdir()
     shutil.copy(os.path.join(oracle.HERE, "oracle.h"), mdir / "oracle.h")
-    (mdir / "oracle.c").write_text(src.replace(old, new))
+    (mdir / "oracle.c").write_text(src)
     lib = oracle.build(str(mdir / "oracle.c"), str(mdir / "liboracle_mut.so"), force=True)
     failed = _fails(oracle.Oracle(lib))
     assert failed, f"no pin catches mutation {name}"

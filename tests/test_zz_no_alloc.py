@@ -7,13 +7,13 @@ the library instead of a caller workspace.  This file is collected last so a
 run that stops at the first failure has already run every other test.
 
 Checked here, through the C ABI: two calls in a row (of different shapes, so
-the second one runs over the first one's leftover scratch) match the
-workspace entry point qgemm_q4k within the GEMM tolerance, and a call too
-large for the built-in scratch is refused without launching anything.
+the second one runs over the first one's leftover scratch) each match the CPU
+oracle's Y within the GEMM tolerance, and give the same bits as the workspace
+entry point qgemm_q4k on the same inputs; a call too large for the built-in
+scratch is refused without launching anything.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
@@ -34,7 +34,7 @@ def _noalloc(L, w, N, K, q, y):
                                y.stride(0), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+def test_noalloc_matches_oracle_twice():
     ensure_built()
     L = qg.lib()
     for call, (M, N, K) in enumerate(((300, 520, 2048), (37, 256, 1024))):
@@ -42,14 +42,16 @@ def test_noalloc_matches_workspace_entry_point_twice():
         x_np = synth.gen_x(M, K, 62 + call, outlier_frac=0.01)
         w = to_dev(w_np)
         q = gpu_quantize(x_np)
-        y_ref = qg.qgemm_q4k(w, N, K, q)                  # existing entry point, caller workspace
         y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
         rc = _noalloc(L, w, N, K, q, y)
         assert rc == qg.QGEMM_OK, L.qgemm_last_error().decode()
         torch.cuda.synchronize()
-        _, absc = oracle_gemm(4, w_np, K, *q8k_numpy(q))
-        assert_gemm_close(y.cpu().numpy(), y_ref.cpu().numpy().astype(np.float64), absc,
-                          f"noalloc call {call + 1} vs qgemm_q4k")
+        y_or, absc = oracle_gemm(4, w_np, K, *q8k_numpy(q))
+        assert_gemm_close(y.cpu().numpy(), y_or, absc, f"noalloc call {call + 1} vs the oracle")
+        # the same kernels as the workspace entry point: the same bits
+        y_ws = qg.qgemm_q4k(w, N, K, q)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ws), f"noalloc call {call + 1}: Y differs from qgemm_q4k's"
     bits, site = qg.qgemm_get_device_status()
     assert bits == 0, f"device status {bits:#x} site {site}"
 
