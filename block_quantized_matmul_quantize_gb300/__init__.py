@@ -18,7 +18,7 @@ import torch
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG_DIR, "libqgemm.so")
 
-QGEMM_OK, QGEMM_EINVAL, QGEMM_EALIGN, QGEMM_EUNSUPPORTED, QGEMM_ECUDA, QGEMM_EDEVICE = range(6)
+QGEMM_OK, QGEMM_EINVAL, QGEMM_EALIGN, QGEMM_EUNSUPPORTED, QGEMM_ECUDA, QGEMM_ETIMEOUT, QGEMM_EDEVICE = range(7)
 QGEMM_DEV_TIMEOUT, QGEMM_DEV_Q4K_RANGE, QGEMM_DEV_Q6K_SCALE, QGEMM_DEV_BAD_EXPERT = 0x1, 0x2, 0x4, 0x8
 QGEMM_OPT_SMALL_M_MAX, QGEMM_OPT_FORCE_BM, QGEMM_OPT_FORCE_SPLITS = 0, 1, 2
 QGEMM_SMALL_M_DEFAULT = 8   # the library's default for QGEMM_OPT_SMALL_M_MAX
@@ -63,6 +63,11 @@ def lib() -> ctypes.CDLL:
             "qgemm_last_error": ([], ctypes.c_char_p),
             "qgemm_quantize_q8k": ([vp, i64, i64, i64, vp, vp, vp, vp], i32),
             "qgemm_workspace_bytes": ([i64, i64, i64], sz),
+            "qgemm_q8k_bytes": ([i64, i64], sz),
+            "qgemm_q8k_planes": ([vp, i64, i64, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp)], i32),
+            "qgemm_q8k_aos_bytes": ([i64, i64], sz),
+            "qgemm_pack_q8k_aos": ([vp, vp, vp, i64, i64, vp, vp], i32),
+            "qgemm_unpack_q8k_aos": ([vp, i64, i64, vp, vp, vp, vp], i32),
             "qgemm_q4k": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
             "qgemm_q4k_noalloc": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp], i32),
             "qgemm_q6k_packed_bytes": ([i64, i64], sz),
@@ -145,6 +150,44 @@ class Q8K:
         return Q8K(torch.empty((M, K), dtype=torch.int8, device=device),
                    torch.empty((M, K // 256), dtype=torch.float32, device=device),
                    torch.empty((M, K // 16), dtype=torch.int16, device=device))
+
+
+def qgemm_q8k_bytes(M: int, K: int) -> int:
+    return int(lib().qgemm_q8k_bytes(M, K))
+
+
+def q8k_in_buffer(buf: torch.Tensor, M: int, K: int) -> "Q8K":
+    """The three Q8_K planes inside one caller-owned buffer of at least
+    qgemm_q8k_bytes(M, K) bytes (uint8, 256-B aligned), as views of it."""
+    assert buf.dtype == torch.uint8 and buf.is_contiguous()
+    assert buf.numel() >= qgemm_q8k_bytes(M, K)
+    qs, d, bs = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+    _check(lib().qgemm_q8k_planes(_ptr(buf), M, K, ctypes.byref(qs), ctypes.byref(d), ctypes.byref(bs)))
+    base = buf.data_ptr()
+    o_d, o_bs = d.value - base, bs.value - base
+    return Q8K(buf[:M * K].view(torch.int8).view(M, K),
+               buf[o_d:o_d + M * (K // 256) * 4].view(torch.float32).view(M, K // 256),
+               buf[o_bs:o_bs + M * (K // 16) * 2].view(torch.int16).view(M, K // 16))
+
+
+def qgemm_q8k_aos_bytes(M: int, K: int) -> int:
+    return int(lib().qgemm_q8k_aos_bytes(M, K))
+
+
+def qgemm_pack_q8k_aos(x: "Q8K", out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Q8K planes -> uint8 [M * K/256 * 292] of 292-byte blocks (d, qs, bsums)."""
+    if out is None:
+        out = torch.empty(max(qgemm_q8k_aos_bytes(x.M, x.K), 4), dtype=torch.uint8, device=x.qs.device)
+    _check(lib().qgemm_pack_q8k_aos(_ptr(x.qs), _ptr(x.d), _ptr(x.bsums), x.M, x.K, _ptr(out), _stream(stream)))
+    return out
+
+
+def qgemm_unpack_q8k_aos(aos: torch.Tensor, M: int, K: int, out: "Q8K | None" = None, stream=None) -> "Q8K":
+    """292-byte blocks -> Q8K planes."""
+    if out is None:
+        out = Q8K.empty(M, K, aos.device)
+    _check(lib().qgemm_unpack_q8k_aos(_ptr(aos), M, K, _ptr(out.qs), _ptr(out.d), _ptr(out.bsums), _stream(stream)))
+    return out
 
 
 def qgemm_version() -> int:
@@ -384,9 +427,21 @@ def qgemm_reset_counters() -> None:
 
 
 def qgemm_get_device_status() -> tuple[int, int]:
+    """(bits, site) of the current device's status word, which is then
+    cleared.  A set bit is reported, not raised (the C call returns
+    QGEMM_ETIMEOUT / QGEMM_EDEVICE for it); other failures raise."""
     bits, site = ctypes.c_uint32(0), ctypes.c_uint32(0)
-    _check(lib().qgemm_get_device_status(ctypes.byref(bits), ctypes.byref(site)))
+    rc = lib().qgemm_get_device_status(ctypes.byref(bits), ctypes.byref(site))
+    if rc not in (QGEMM_OK, QGEMM_ETIMEOUT, QGEMM_EDEVICE):
+        _check(rc)
     return int(bits.value), int(site.value)
+
+
+def qgemm_device_status_code() -> tuple[int, int, int]:
+    """(return code, bits, site) of qgemm_get_device_status, unraised."""
+    bits, site = ctypes.c_uint32(0), ctypes.c_uint32(0)
+    rc = lib().qgemm_get_device_status(ctypes.byref(bits), ctypes.byref(site))
+    return int(rc), int(bits.value), int(site.value)
 
 
 def qgemm_set_option(option: int, value: int) -> None:

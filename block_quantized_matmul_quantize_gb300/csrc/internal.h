@@ -150,6 +150,12 @@ cudaError_t launch_small(const SmallLaunch& a, cudaStream_t s);
 // Record a one-line message for qgemm_last_error() and return `code`.
 int set_last_error(int code, const char* msg);
 
+// Q8_K planes <-> 292-byte blocks {fp32 d; int8 qs[256]; int16 bsums[16]}
+// (4-byte aligned aos), M*K/256 blocks in row-major block order.
+constexpr int Q8K_AOS_BLOCK = 292;
+cudaError_t launch_q8k_aos(int8_t* qs, float* d, int16_t* bsums, int64_t M, int64_t K, void* aos, bool to_aos,
+                           cudaStream_t s);
+
 cudaError_t launch_ptq1_prepack(const uint8_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* out,
                                 cudaStream_t s);
 cudaError_t launch_q6k_prepack(const uint8_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* out,

@@ -475,6 +475,60 @@ int qgemm_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t
     return QGEMM_OK;
 }
 
+size_t qgemm_q8k_bytes(int64_t M, int64_t K) {
+    if (M <= 0 || K <= 0 || K % 256) return 0;
+    return align256(size_t(M) * K) + align256(size_t(M) * (K / 256) * 4) + align256(size_t(M) * (K / 16) * 2);
+}
+
+int qgemm_q8k_planes(void* base, int64_t M, int64_t K, int8_t** qs, float** d, int16_t** bsums) {
+    clear_err();
+    int rc = check_mk(M, K);
+    if (rc) return rc;
+    if (!base || !qs || !d || !bsums) return fail(QGEMM_EINVAL, "null pointer");
+    if (!aligned(base, 256)) return fail(QGEMM_EALIGN, "the Q8_K buffer must be 256-byte aligned");
+    uint8_t* b = static_cast<uint8_t*>(base);
+    *qs = reinterpret_cast<int8_t*>(b);
+    *d = reinterpret_cast<float*>(b + align256(size_t(M) * K));
+    *bsums = reinterpret_cast<int16_t*>(b + align256(size_t(M) * K) + align256(size_t(M) * (K / 256) * 4));
+    return QGEMM_OK;
+}
+
+size_t qgemm_q8k_aos_bytes(int64_t M, int64_t K) {
+    if (M <= 0 || K <= 0 || K % 256) return 0;
+    return size_t(M) * size_t(K / 256) * qg::Q8K_AOS_BLOCK;
+}
+
+static int aos_common(const void* aos, int64_t M, int64_t K, const int8_t* qs, const float* d,
+                      const int16_t* bsums) {
+    int rc = check_mk(M, K);
+    if (rc || M == 0) return rc;
+    if (!aos) return fail(QGEMM_EINVAL, "null 292-byte block buffer");
+    if (!aligned(aos, 4)) return fail(QGEMM_EALIGN, "the 292-byte block buffer must be 4-byte aligned");
+    return check_q8k(qs, d, bsums);
+}
+
+int qgemm_pack_q8k_aos(const int8_t* qs, const float* d, const int16_t* bsums, int64_t M, int64_t K, void* aos,
+                       qgemm_stream_t stream) {
+    clear_err();
+    int rc = aos_common(aos, M, K, qs, d, bsums);
+    if (rc || M == 0) return rc;
+    cudaError_t e = qg::launch_q8k_aos(const_cast<int8_t*>(qs), const_cast<float*>(d), const_cast<int16_t*>(bsums),
+                                       M, K, aos, true, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "Q8_K pack launch");
+    return QGEMM_OK;
+}
+
+int qgemm_unpack_q8k_aos(const void* aos, int64_t M, int64_t K, int8_t* qs, float* d, int16_t* bsums,
+                         qgemm_stream_t stream) {
+    clear_err();
+    int rc = aos_common(aos, M, K, qs, d, bsums);
+    if (rc || M == 0) return rc;
+    cudaError_t e = qg::launch_q8k_aos(qs, d, bsums, M, K, const_cast<void*>(aos), false,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "Q8_K unpack launch");
+    return QGEMM_OK;
+}
+
 size_t qgemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || K <= 0 || K % 256) return 0;
     const size_t base = plane_bytes(M, K) + COUNTER_BYTES;
@@ -768,6 +822,9 @@ int qgemm_get_device_status(uint32_t* bits, uint32_t* site) {
     if (e != cudaSuccess) return cuda_fail(e, "clearing device status");
     if (bits) *bits = h[0];
     if (site) *site = h[1];
+    if (h[0] & QGEMM_DEV_TIMEOUT)
+        return fail(QGEMM_ETIMEOUT, "a pipeline wait gave up (site %u); the kernel left Y unwritten", h[1]);
+    if (h[0]) return fail(QGEMM_EDEVICE, "device-side value check failed (status bits %#x)", h[0]);
     return QGEMM_OK;
 }
 

@@ -184,6 +184,38 @@ __global__ void prepack_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t
     }
 }
 
+// Q8_K planes <-> the pages' 292-byte block ("BlockQ8_K (292B/256 elements)",
+// vllm.cpp PR #3036, commit 4), field order d (fp32), qs[256] (int8),
+// bsums[16] (int16).  292 is a multiple of 4, so every field of every block
+// starts on a 4-byte boundary: one warp per block moves its 73 32-bit words
+// (word 0 = d, words 1..64 = qs, words 65..72 = bsums), no arithmetic.
+constexpr int AOS_WORDS = 73;
+template <bool TO_AOS>
+__global__ void q8k_aos_kernel(int8_t* __restrict__ qs, float* __restrict__ d, int16_t* __restrict__ bsums,
+                               int64_t M, int64_t K, uint32_t* __restrict__ aos) {
+    const int64_t nb = K >> 8;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int lane = threadIdx.x & 31;
+    for (int64_t blk = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); blk < M * nb;
+         blk += warps) {
+        const int64_t m = blk / nb, b = blk - m * nb;
+        uint32_t* a = aos + blk * AOS_WORDS;
+        uint32_t* q = reinterpret_cast<uint32_t*>(qs + m * K + b * 256);
+        uint32_t* s = reinterpret_cast<uint32_t*>(bsums + m * (K >> 4) + b * 16);
+        uint32_t* dd = reinterpret_cast<uint32_t*>(d + m * nb + b);
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const int wd = lane + 32 * i;
+            if (wd >= AOS_WORDS) break;
+            uint32_t* plane = wd == 0 ? dd : wd <= 64 ? q + (wd - 1) : s + (wd - 65);
+            if constexpr (TO_AOS)
+                a[wd] = *plane;
+            else
+                *plane = a[wd];
+        }
+    }
+}
+
 int grid_for(int64_t work, int threads) {
     int64_t g = (work + threads - 1) / threads;
     const int64_t cap = 152 * 16;
@@ -213,6 +245,21 @@ cudaError_t launch_xprep(const int8_t* qs, const float* d, const int16_t* bsums,
                          __half* xh, __half* xbs, float* dxT, int64_t Mp, int* counters, cudaStream_t s) {
     const int64_t work = M * (K >> 4) + (K >> 8) * Mp;
     xprep_kernel<<<grid_for(work, 256), 256, 0, s>>>(qs, d, bsums, M, K, xh, xbs, dxT, Mp, counters);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q8k_aos(int8_t* qs, float* d, int16_t* bsums, int64_t M, int64_t K, void* aos, bool to_aos,
+                           cudaStream_t s) {
+    const int64_t blocks = M * (K >> 8);
+    const int per_cta = 8;   // warps (blocks of Q8_K) per CTA
+    int64_t grid = (blocks + per_cta - 1) / per_cta;
+    if (grid > 152 * 16) grid = 152 * 16;
+    if (to_aos)
+        q8k_aos_kernel<true><<<static_cast<unsigned>(grid), 32 * per_cta, 0, s>>>(qs, d, bsums, M, K,
+                                                                              static_cast<uint32_t*>(aos));
+    else
+        q8k_aos_kernel<false><<<static_cast<unsigned>(grid), 32 * per_cta, 0, s>>>(qs, d, bsums, M, K,
+                                                                               static_cast<uint32_t*>(aos));
     return cudaGetLastError();
 }
 

@@ -71,7 +71,8 @@ typedef enum {
     QGEMM_EALIGN = 2,       /* pointer or stride not aligned as required     */
     QGEMM_EUNSUPPORTED = 3, /* shape outside what the kernels handle         */
     QGEMM_ECUDA = 4,        /* a CUDA launch or runtime call failed          */
-    QGEMM_EDEVICE = 5       /* device-side check failed (see status)         */
+    QGEMM_ETIMEOUT = 5,     /* a kernel's bounded wait gave up (device status) */
+    QGEMM_EDEVICE = 6       /* a device-side value check failed (status)     */
 } qgemm_status;
 
 /* Library version, major*10000 + minor*100 + patch. */
@@ -97,6 +98,36 @@ QGEMM_API const char *qgemm_last_error(void);
  * Errors: EINVAL (sizes, null), EALIGN, ECUDA (launch). */
 QGEMM_API int qgemm_quantize_q8k(const float *x, int64_t M, int64_t K, int64_t ldx, int8_t *qs, float *d,
                        int16_t *bsums, qgemm_stream_t stream);
+
+/* Caller-owned Q8_K storage (the pages' caller-owned-scratch convention,
+ * hip_linear_attention_prefill_scratch_bytes, hip-ep PR #627):
+ * qgemm_q8k_bytes(M, K) is the size of one buffer that holds the three planes
+ * of M rows of depth K (0 for M <= 0 or K not a positive multiple of 256);
+ * qgemm_q8k_planes splits such a buffer (256-B aligned) into the plane
+ * pointers the other calls take: qs at offset 0, then d, then bsums, each
+ * plane starting on a 256-B boundary.  Host-only arithmetic, no device access.
+ * Errors: EINVAL (sizes, null), EALIGN (base). */
+QGEMM_API size_t qgemm_q8k_bytes(int64_t M, int64_t K);
+QGEMM_API int qgemm_q8k_planes(void *base, int64_t M, int64_t K, int8_t **qs, float **d, int16_t **bsums);
+
+/* The pages' 292-byte Q8_K block ("BlockQ8_K (292B/256 elements)", PR #3036,
+ * commit 4), for exchange with code that keeps Q8_K as an array of blocks.
+ * Field order within a block (this library's reading; the page gives only
+ * the size): fp32 d at byte 0, int8 qs[256] at byte 4, int16 bsums[16] at
+ * byte 260, little-endian.  Block (m, b) -- row m, superblock b -- is block
+ * number m*(K/256) + b of the array.
+ *   qgemm_q8k_aos_bytes(M, K) = M*(K/256)*292 (0 for bad sizes).
+ *   qgemm_pack_q8k_aos:   planes (device, as qgemm_quantize_q8k writes them,
+ *                         16-B aligned) -> aos (device, 4-B aligned).
+ *   qgemm_unpack_q8k_aos: aos -> planes.
+ * One device kernel each, enqueued on `stream`; the bytes are copied, not
+ * recomputed, so both directions are exact.  M == 0: nothing to do.
+ * Errors: EINVAL (sizes, null), EALIGN, ECUDA (launch). */
+QGEMM_API size_t qgemm_q8k_aos_bytes(int64_t M, int64_t K);
+QGEMM_API int qgemm_pack_q8k_aos(const int8_t *qs, const float *d, const int16_t *bsums, int64_t M, int64_t K,
+                                 void *aos, qgemm_stream_t stream);
+QGEMM_API int qgemm_unpack_q8k_aos(const void *aos, int64_t M, int64_t K, int8_t *qs, float *d, int16_t *bsums,
+                                   qgemm_stream_t stream);
 
 /* ------------------------------------------------------------- GEMM ----
  * Workspace bytes the GEMM calls need for M tokens, N weight rows and depth K
@@ -321,7 +352,10 @@ QGEMM_API int qgemm_reset_counters(void);
 #define QGEMM_DEV_BAD_EXPERT 0x8u /* a routed GEMM id was outside [0, E)    */
 /* Synchronizes the device, returns the status bits in *bits and the site of
  * the first timed-out wait (0 = none) in *site (may be NULL), then clears
- * both.  QGEMM_ECUDA if the device is unusable. */
+ * both.  Return value: QGEMM_OK when no bit was set; QGEMM_ETIMEOUT when a
+ * bounded wait gave up (the kernel stopped early and did not write the
+ * affected output tiles: Y is incomplete); QGEMM_EDEVICE when only value
+ * checks fired; QGEMM_ECUDA if the device is unusable. */
 QGEMM_API int qgemm_get_device_status(uint32_t *bits, uint32_t *site);
 
 /* ----------------------------------------------------------- options ----

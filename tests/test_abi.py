@@ -178,6 +178,34 @@ def test_size_queries(L):
     assert L.qgemm_q6k_packed_bytes(3, 100) == 0
 
 
+def test_q8k_storage_queries(L):
+    assert L.qgemm_q8k_bytes(0, 256) == 0 and L.qgemm_q8k_bytes(3, 300) == 0
+    M, K = 3, 768
+    # qs 2304 -> 2304 (256-B multiple), d 3*3*4 = 36 -> 256, bsums 3*48*2 = 288 -> 512
+    assert L.qgemm_q8k_bytes(M, K) == 2304 + 256 + 512
+    qs, d, bs = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+    base = 0x100000
+    assert L.qgemm_q8k_planes(ctypes.c_void_p(base), M, K, ctypes.byref(qs), ctypes.byref(d),
+                              ctypes.byref(bs)) == qg.QGEMM_OK
+    assert (qs.value, d.value, bs.value) == (base, base + 2304, base + 2304 + 256)
+    assert L.qgemm_q8k_planes(ctypes.c_void_p(base + 16), M, K, ctypes.byref(qs), ctypes.byref(d),
+                              ctypes.byref(bs)) == qg.QGEMM_EALIGN
+    assert L.qgemm_q8k_planes(None, M, K, ctypes.byref(qs), ctypes.byref(d), ctypes.byref(bs)) == qg.QGEMM_EINVAL
+    assert L.qgemm_q8k_planes(ctypes.c_void_p(base), M, 100, ctypes.byref(qs), ctypes.byref(d),
+                              ctypes.byref(bs)) == qg.QGEMM_EINVAL
+    # the pages' 292-byte block
+    assert L.qgemm_q8k_aos_bytes(M, K) == M * 3 * 292
+    assert L.qgemm_q8k_aos_bytes(M, 100) == 0
+    P, U = L.qgemm_pack_q8k_aos, L.qgemm_unpack_q8k_aos
+    assert P(FAKE, FAKE, FAKE, 0, 256, FAKE, None) == qg.QGEMM_OK            # empty
+    assert P(FAKE, FAKE, FAKE, 2, 100, FAKE, None) == qg.QGEMM_EINVAL
+    assert P(FAKE, FAKE, FAKE, 2, 256, None, None) == qg.QGEMM_EINVAL
+    assert P(FAKE, FAKE, FAKE, 2, 256, ctypes.c_void_p(0x100002), None) == qg.QGEMM_EALIGN
+    assert P(MISALIGNED, FAKE, FAKE, 2, 256, FAKE, None) == qg.QGEMM_EALIGN
+    assert U(FAKE, 2, 256, FAKE, None, FAKE, None) == qg.QGEMM_EINVAL
+    assert U(ctypes.c_void_p(0x100001), 2, 256, FAKE, FAKE, FAKE, None) == qg.QGEMM_EALIGN
+
+
 def test_options_and_counters(L):
     assert L.qgemm_get_option(qg.QGEMM_OPT_SMALL_M_MAX) == qg.QGEMM_SMALL_M_DEFAULT == 8
     assert L.qgemm_set_option(qg.QGEMM_OPT_SMALL_M_MAX, 9) == qg.QGEMM_EINVAL
