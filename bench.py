@@ -74,7 +74,7 @@ NCU_TRAFFIC_BYTES = {
 
 
 def workloads():
-    return {w.name: w for w in synth.CONFIGS + synth.ROUTED_CONFIGS + synth.PTQ1_CONFIGS}
+    return {w.name: w for w in synth.CONFIGS + synth.FULLSCALE_CONFIGS + synth.ROUTED_CONFIGS + synth.PTQ1_CONFIGS}
 
 
 def routed(wl) -> bool:

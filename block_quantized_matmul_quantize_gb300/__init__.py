@@ -19,7 +19,8 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG_DIR, "libqgemm.so")
 
 QGEMM_OK, QGEMM_EINVAL, QGEMM_EALIGN, QGEMM_EUNSUPPORTED, QGEMM_ECUDA, QGEMM_ETIMEOUT, QGEMM_EDEVICE = range(7)
-QGEMM_DEV_TIMEOUT, QGEMM_DEV_Q4K_RANGE, QGEMM_DEV_Q6K_SCALE, QGEMM_DEV_BAD_EXPERT = 0x1, 0x2, 0x4, 0x8
+QGEMM_DEV_TIMEOUT, QGEMM_DEV_Q4K_RANGE, QGEMM_DEV_BAD_EXPERT = 0x1, 0x2, 0x8
+QGEMM_DEBUG_EXPAND_BYTES = 1152
 QGEMM_OPT_SMALL_M_MAX, QGEMM_OPT_FORCE_BM, QGEMM_OPT_FORCE_SPLITS = 0, 1, 2
 QGEMM_SMALL_M_DEFAULT = 8   # the library's default for QGEMM_OPT_SMALL_M_MAX
 
@@ -86,6 +87,7 @@ def lib() -> ctypes.CDLL:
             "qgemm_ptq1_prepack": ([vp, i64, i64, i64, vp, vp], i32),
             "qgemm_ptq1": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
             "qgemm_ptq1_prepared": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
+            "qgemm_debug_expand": ([i32, vp, i64, vp, vp], i32),
             "qgemm_get_counters": ([ctypes.POINTER(_Counters)], i32),
             "qgemm_reset_counters": ([], i32),
             "qgemm_get_device_status": ([ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)], i32),
@@ -414,6 +416,14 @@ def qgemm_ptq1_prepared(w_packed: torch.Tensor, N: int, K: int, x: Q8K, workspac
     _check(lib().qgemm_ptq1_prepared(_ptr(w_packed), N, K, _ptr(x.qs), _ptr(x.d), _ptr(x.bsums), M, _ptr(y, True),
                                      y.stride(0), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y
+
+
+def qgemm_debug_expand(wtype: int, blocks: torch.Tensor, nblocks: int, stream=None) -> torch.Tensor:
+    """The tile GEMM's weight expansion of `nblocks` superblock rows (test
+    diagnostic): uint32 [nblocks, QGEMM_DEBUG_EXPAND_BYTES / 4] records."""
+    out = torch.empty((max(nblocks, 1), QGEMM_DEBUG_EXPAND_BYTES // 4), dtype=torch.int32, device=blocks.device)
+    _check(lib().qgemm_debug_expand(wtype, _ptr(blocks), nblocks, _ptr(out), _stream(stream)))
+    return out[:nblocks]
 
 
 def qgemm_get_counters() -> dict:

@@ -79,6 +79,7 @@
 #include "internal.h"
 #include "epilogue.cuh"
 #include "ptx.cuh"
+#include "unpack.cuh"
 
 namespace qg {
 namespace {
@@ -114,21 +115,28 @@ __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
 template <int WT>
 struct WTraits;
+// RAW_BLOCK: bytes of one weight row's superblock as staged; CORR: the Q4_K
+// dmin correction rides along as two extra MMAs; SPLIT: the weight operand
+// has a second (lo) part (Q6_K's full int8 sub-scale range), so its stages
+// are K64 (hi and lo side by side) instead of K128.
 template <>
 struct WTraits<4> {
     static constexpr int RAW_BLOCK = Q4K_BLOCK;
     static constexpr bool CORR = true;
+    static constexpr bool SPLIT = false;
 };
 template <>
 struct WTraits<6> {
     static constexpr int RAW_BLOCK = Q6K_PACKED;
     static constexpr bool CORR = false;
+    static constexpr bool SPLIT = true;
 };
 // PTQ1_0: a superblock's two 128-weight blocks, each repacked to 32 bytes
 template <>
 struct WTraits<1> {
     static constexpr int RAW_BLOCK = 2 * PTQ1_PACKED;
     static constexpr bool CORR = false;
+    static constexpr bool SPLIT = false;
 };
 
 template <int WT, int BM>
@@ -158,49 +166,16 @@ struct Layout {
     static constexpr int B_STAGES = cmin(12, (SMEM_LIMIT - RESERVE - OFF_B) / B_STAGE) & ~1;
     static constexpr int OFF_BAR = OFF_B + B_STAGES * B_STAGE;
     static constexpr int NBAR = 2 * RAW_SLOTS + 2 * A_STAGES + 2 * B_STAGES + 2 * SB_SLOTS + 4 + 1;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int TOTAL = OFF_MISC + 16 + 1024;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM address, abort and last-part flags
+    static constexpr int OFF_LOFLAG = OFF_MISC + 16;        // per weight-operand stage: a lo part was written
+    static constexpr int TOTAL = OFF_LOFLAG + 4 * A_STAGES + 1024;
     static constexpr int CPT = BM / 2;                   // token columns per epilogue thread
     static_assert(2 * BM <= A_TMEM_COL, "accumulators overlap the weight-operand stages");
     static_assert(B_STAGES >= 4, "activation ring too shallow");
-    static_assert(NBAR * 8 + 16 <= 512, "barrier area");
+    static_assert(NBAR * 8 + 16 + 4 * A_STAGES <= 512, "barrier area");
     static_assert(TOTAL <= SMEM_LIMIT, "shared memory budget");
 };
 
-
-__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t hsub2u(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-__device__ __forceinline__ uint32_t hadd2u(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-// Byte B of w as an exact fp16 in both halves, without a conversion
-// instruction: the byte under the exponent byte 0x64 is the fp16 1024 + v,
-// and subtracting 1024 leaves v.  Unsigned bytes (0..255); for a signed byte
-// pass w ^ 0x80808080 and subtract 1152 (1024 + 128) instead.
-template <int B>
-__device__ __forceinline__ uint32_t byte_h2(uint32_t w, uint32_t minus_bias) {
-    constexpr uint32_t sel = B | (4u << 4) | (B << 8) | (4u << 12);   // w[B], 0x64, w[B], 0x64
-    return hadd2u(__byte_perm(w, 0x64646464u, sel), minus_bias);
-}
-constexpr uint32_t H2_M1024 = 0xE400E400u;   // fp16 -1024 in both halves
-constexpr uint32_t H2_M1152 = 0xE480E480u;   // fp16 -1152
-constexpr uint32_t H2_1_16 = 0x2C002C00u;    // fp16 1/16
-constexpr uint32_t H2_M64 = 0xD400D400u;     // fp16 -64
 
 // a[0..3] += (S[0..3] * e) * dx[0..3], two columns per packed fp32 instruction
 __device__ __forceinline__ void fold4(float* a, const uint32_t* S, float2 ee, float4 dx) {
@@ -214,159 +189,6 @@ __device__ __forceinline__ void fold4(float* a, const uint32_t* S, float2 ee, fl
     a[3] = hi.y;
 }
 
-__device__ __forceinline__ uint32_t h2dup(__half h) {
-    const uint32_t u = __half_as_ushort(h);
-    return u | (u << 16);
-}
-
-// ---------------------------------------------------------------- unpack
-// Both expanders write the K positions of every aligned group of 4 in the
-// order 0, 2, 1, 3 (fp16 pair (w[4k], w[4k+2]), then (w[4k+1], w[4k+3])):
-// two weights two bytes apart sit in one 32-bit word with no byte permute.
-// The activation operand (xh) is written in the same order, so the MMA's
-// dot products are unchanged; groups of 4 never straddle a 16-value group,
-// so the bsums are unchanged too.
-//
-// Q4_K: expand K64 chunk c of one 144-byte block into 64 fp16 values sc_j*q:
-// words 0..15 from the low nibbles (sub-block 2c), words 16..31 from the high
-// nibbles (sub-block 2c+1).
-__device__ __forceinline__ void unpack_q4k_chunk(const uint8_t* blk, int c, uint32_t scL, uint32_t cL,
-                                                 uint32_t scH, uint32_t cH, uint32_t (&o)[32]) {
-    const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
-    const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c + 16);
-    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    constexpr uint32_t MAGIC = 0x64006400u;  // fp16 1024 in both halves
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        // bytes 4k..4k+3 hold weights 4k..4k+3 (low nibbles) and 32+4k.. (high nibbles)
-        const uint32_t wk = w[k], sk = w[k] >> 8;
-        o[2 * k] = hfma2u((wk & 0x000F000Fu) | MAGIC, scL, cL);           // (1024+q)*sc - 1024*sc
-        o[2 * k + 1] = hfma2u((sk & 0x000F000Fu) | MAGIC, scL, cL);
-        o[16 + 2 * k] = hfma2u((wk & 0x00F000F0u) | MAGIC, scH, cH);      // (1024+16q)*sc/16 - 64*sc
-        o[17 + 2 * k] = hfma2u((sk & 0x00F000F0u) | MAGIC, scH, cH);
-    }
-}
-
-// Q6_K: K64 chunk c = weights 64c..64c+63 of a 224-byte packed block, as
-// fp16 (q-32)*sc.  Half h = c/2; low nibbles for c even, high for c odd; qh
-// bits 4*(c&1) + 2*pp for the first (pp = 0) and second (pp = 1) 32 weights.
-__device__ __forceinline__ void unpack_q6k_chunk(const uint8_t* blk, int c, const uint32_t (&s4)[4],
-                                                 uint32_t (&o)[32]) {
-    const int h = c >> 1, hn = c & 1;
-    const uint4* Lp = reinterpret_cast<const uint4*>(blk + 64 * h);
-    const uint4* Hp = reinterpret_cast<const uint4*>(blk + 128 + 32 * h);
-    const uint4 l0 = Lp[0], l1 = Lp[1], l2 = Lp[2], l3 = Lp[3];
-    const uint4 h0 = Hp[0], h1 = Hp[1];
-    const uint32_t Lw[16] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w,
-                             l2.x, l2.y, l2.z, l2.w, l3.x, l3.y, l3.z, l3.w};
-    const uint32_t Hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-    constexpr uint32_t MAGIC = 0x64006400u;
-    constexpr uint32_t OFF = 0x64206420u;  // fp16 1056 = 1024 + 32 in both halves
-    const int nsh = 4 * hn;                 // low or high nibble
-#pragma unroll
-    for (int pp = 0; pp < 2; ++pp) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            // 6-bit codes of weights 32pp+4k .. +3, one per byte
-            const uint32_t q6 = ((Lw[8 * pp + k] >> nsh) & 0x0F0F0F0Fu) |
-                                (((Hw[k] >> (nsh + 2 * pp)) << 4) & 0x30303030u);
-            const uint32_t sc = s4[2 * pp + (k >> 2)];
-            // bytes 0, 2 (a) and 1, 3 (b) of q6 under the fp16 exponent byte 0x64:
-            // 1024 + q, one byte permute each (measured on GB300: 3.5% off the
-            // M=512 K=11008 N=2048 GEMM against a mask-and-or and a shift)
-            const uint32_t a = __byte_perm(q6, MAGIC, 0x7250);
-            const uint32_t b = __byte_perm(q6, MAGIC, 0x7351);
-            o[16 * pp + 2 * k] = hmul2u(hsub2u(a, OFF), sc);        // (q - 32) * sc, exact
-            o[16 * pp + 2 * k + 1] = hmul2u(hsub2u(b, OFF), sc);
-        }
-    }
-}
-
-// PTQ1_0 ("cuda: branch-free PTQ1_0 MMQ tile loader ...", llama.cpp PR
-// #214): one 32-byte block (28 + 4 zero) -> its 128 weights as fp16
-// (t - 1) * d, weights 0..63 in v0 and 64..127 in v1, each aligned group of 4
-// in the K order 0, 2, 1, 3.  Weight 24 i + 4 w + b (b < 4) is base-3 digit i
-// of qs byte 4 w + b, so a qs word and a digit give one aligned group of 4:
-// bytes 0 and 2 of the word (16-bit lanes of w & 0x00ff00ff) hold weights b =
-// 0 and 2, bytes 1 and 3 weights 1 and 3.  One division by 3 per digit and
-// lane pair, x / 3 = (x * 171) >> 9 (exact for x < 256, no carry between the
-// lanes); the digit lands in bits 0-1 of its lane, under the fp16 exponent
-// 0x64 (1024 + t), and (1024 + t - 1025) * d is exact.  Weights 120 + r are
-// digit r / 2 of qh byte r % 2.  No branch depends on the lane or the data.
-// Expanded in two halves (v0 = weights 0..63, then v1 = 64..127), so that
-// only one half and the words' lane pairs after two divisions (st) are live:
-// weights 0..63 are digits 0 and 1 of every qs word and digit 2 of words 0..3.
-struct Ptq1State {
-    uint32_t xl[6], xh[6];   // each word's lane pairs divided by 9
-    uint32_t tail, d2;
-};
-__device__ __forceinline__ uint32_t ptq1_val(uint32_t t2, uint32_t d2) {
-    // (1024 + t - 1025) * d: exact in fp16 for t in {0, 1, 2}
-    return hmul2u(hadd2u(t2 | 0x64006400u, 0xE401E401u), d2);
-}
-__device__ __forceinline__ void ptq1_div3(uint32_t x, uint32_t& q, uint32_t& t) {
-    q = ((x * 171u) >> 9) & 0x007f007fu;   // x / 3 in both 16-bit lanes (x < 256)
-    t = x - 3u * q;
-}
-__device__ __forceinline__ void unpack_ptq1_lo(const uint8_t* blk, Ptq1State& st, uint32_t (&v0)[32]) {
-    const uint4 a = *reinterpret_cast<const uint4*>(blk);
-    const uint4 b = *reinterpret_cast<const uint4*>(blk + 16);
-    const uint32_t qw[6] = {a.x, a.y, a.z, a.w, b.x, b.y};
-    st.tail = b.z;                                   // qh[0] | qh[1] << 8 | d << 16
-    st.d2 = (st.tail >> 16) * 0x10001u;              // fp16 d in both halves
-#pragma unroll
-    for (int w = 0; w < 6; ++w) {
-        uint32_t xl = qw[w] & 0x00ff00ffu, xh = (qw[w] >> 8) & 0x00ff00ffu, ql, qh, tl, th;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {                // weights 24 i + 4 w .. + 3
-            ptq1_div3(xl, ql, tl);
-            ptq1_div3(xh, qh, th);
-            v0[12 * i + 2 * w] = ptq1_val(tl, st.d2);
-            v0[12 * i + 2 * w + 1] = ptq1_val(th, st.d2);
-            xl = ql;
-            xh = qh;
-        }
-        st.xl[w] = xl;
-        st.xh[w] = xh;
-        if (w < 4) {                                 // digit 2 of words 0..3: weights 48 + 4 w
-            ptq1_div3(xl, ql, tl);
-            ptq1_div3(xh, qh, th);
-            v0[24 + 2 * w] = ptq1_val(tl, st.d2);
-            v0[25 + 2 * w] = ptq1_val(th, st.d2);
-        }
-    }
-}
-__device__ __forceinline__ void unpack_ptq1_hi(const Ptq1State& st, uint32_t (&v1)[32]) {
-#pragma unroll
-    for (int w = 0; w < 6; ++w) {
-        uint32_t xl = st.xl[w], xh = st.xh[w], ql, qh, tl, th;
-#pragma unroll
-        for (int i = 2; i < 5; ++i) {
-            ptq1_div3(xl, ql, tl);
-            ptq1_div3(xh, qh, th);
-            const int k = 24 * i + 4 * w;            // first weight of the group
-            if (k >= 64) {                           // (digit 2 of words 0..3 went to v0)
-                v1[(k - 64) >> 1] = ptq1_val(tl, st.d2);
-                v1[((k - 64) >> 1) + 1] = ptq1_val(th, st.d2);
-            }
-            xl = ql;
-            xh = qh;
-        }
-    }
-    // qh[0] in lane 0, qh[1] in lane 1: digits i of both bytes per step
-    uint32_t x = (st.tail & 0xffu) | ((st.tail & 0xff00u) << 8), dg[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t q;
-        ptq1_div3(x, q, dg[i]);
-        x = q;
-    }
-    // group 120..123: (qh0 digit 0, qh0 digit 1), (qh1 digit 0, qh1 digit 1); 124..127 with digits 2, 3
-    v1[28] = ptq1_val(__byte_perm(dg[0], dg[1], 0x5410), st.d2);
-    v1[29] = ptq1_val(__byte_perm(dg[0], dg[1], 0x7632), st.d2);
-    v1[30] = ptq1_val(__byte_perm(dg[2], dg[3], 0x5410), st.d2);
-    v1[31] = ptq1_val(__byte_perm(dg[2], dg[3], 0x7632), st.d2);
-}
 
 // Kernel variants, each compiled only with the code it needs (measured on
 // GB300: routing and epilogue code in one kernel doubled the register
@@ -387,10 +209,16 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     constexpr int R = L::RAW_SLOTS;
     constexpr int BS = L::B_STAGES;
     constexpr int SBN = SB_SLOTS;
+    // Weight-operand stages: K128 (8 MMAs) per stage, or for SPLIT (Q6_K) K64
+    // with the hi part in the stage's first 32 columns and the lo part in the
+    // other 32 (4 + 4 MMAs; the lo MMAs only when some row wrote a lo part).
+    constexpr bool SPLIT = WTraits<WT>::SPLIT;
+    constexpr int KSTEP = SPLIT ? 64 : 128;
+    constexpr int STEPS = 256 / KSTEP;   // weight-operand stages per superblock
     // With two-box stages and as many activation stages as weight-operand
     // stages, every K128 step consumes exactly one stage of each ring, so one
     // commit (on a_empty) releases both and the activation producers wait on it.
-    constexpr bool MERGED_RELEASE = (L::SCH == 2) && (BS == A_STAGES);
+    constexpr bool MERGED_RELEASE = !SPLIT && (L::SCH == 2) && (BS == A_STAGES);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -409,6 +237,9 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
+    // SPLIT: byte q of word s is set by unpack warp q when it wrote a nonzero lo
+    // part into stage s (before its a_full arrival; read by the issuer after the wait)
+    volatile uint32_t* lo_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_LOFLAG);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -580,9 +411,12 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     } else if (warp == W_MMA || warp == W_MMA2) {
         // ------------------------------------------------ MMA issuers
         // Thread `par` takes the superblocks t with t % 2 == par, i.e. always
-        // accumulator `par`, A stages 2*par and 2*par+1 and (two-box stages)
-        // the same two activation stages.  Per superblock: two K128 steps of 8
-        // MMAs (+2 correction MMAs for Q4_K) and up to four commits; readiness
+        // accumulator `par`, weight-operand stages 2*par and 2*par+1 and (two-
+        // box activation stages) the same two activation stages: every stage
+        // barrier is waited on by one thread, phase after phase.  Per
+        // superblock: STEPS weight-operand steps (two K128 steps of 8 MMAs, or
+        // for SPLIT four K64 steps of 4 hi MMAs plus 4 lo MMAs where a lo part
+        // was written), +2 correction MMAs for Q4_K, and the commits; readiness
         // of the next step, the side slot and the next accumulator is probed
         // without blocking between the MMAs of the current step.
         if (lane == 0) {
@@ -595,16 +429,27 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             const uint64_t acorr0 = smem_desc(sb0 + L::SB_ACORR, 16, 256, SWZ_32B);
             const uint64_t bcorr0 = smem_desc(sb0 + L::SB_BCORR, 16, 256, SWZ_32B);
             const uint32_t d_tmem = tmem_base + par * BM;
-            // stage index and phase parity of K128 step j of superblock t, in each ring
-            auto a_at = [&](int t, int j, int& s, uint32_t& ph) {
-                const int g = 2 * t + j;
-                s = g % A_STAGES;
-                ph = static_cast<uint32_t>(g / A_STAGES) & 1u;
+            // weight-operand stage and phase parity of step h of superblock t.
+            // K128: g = 2t + h over the four stages (superblocks of parity par
+            // use stages 2par, 2par+1).  SPLIT: the superblocks of parity par use
+            // stage 2par + (h & 1), twice each (steps h and h + 2).
+            auto a_at = [&](int t, int h, int& s, uint32_t& ph) {
+                if constexpr (SPLIT) {
+                    s = 2 * (t & 1) + (h & 1);
+                    ph = static_cast<uint32_t>(2 * (t >> 1) + (h >> 1)) & 1u;
+                } else {
+                    const int g = 2 * t + h;
+                    s = g % A_STAGES;
+                    ph = static_cast<uint32_t>(g / A_STAGES) & 1u;
+                }
             };
-            auto b_at = [&](int t, int j, int& s, uint32_t& ph) {
-                const int g = t * L::SPS + (2 * j) / L::SCH;
+            // activation stage of step h of superblock t, and the step's first box in it
+            auto b_at = [&](int t, int h, int& s, uint32_t& ph, int& q0) {
+                const int kk = h * (KSTEP / 64);
+                const int g = t * L::SPS + kk / L::SCH;
                 s = g % BS;
                 ph = static_cast<uint32_t>(g / BS) & 1u;
+                q0 = kk % L::SCH;
             };
             int t = 0;
             bool step_ok = false;   // next step's A (and B) stage seen complete
@@ -622,12 +467,11 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                     }
                     bool sb_ok = !L::CORR;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {   // K128 steps: chunks 2h, 2h+1
-                        const int q0 = (2 * h) % L::SCH;   // first box of the step in its B stage
-                        int sa, sx;
+                    for (int h = 0; h < STEPS; ++h) {
+                        int sa, sx, q0;
                         uint32_t pa, px;
                         a_at(t, h, sa, pa);
-                        b_at(t, h, sx, px);
+                        b_at(t, h, sx, px, q0);
                         if (!step_ok) {
                             ok = mbar_wait(&a_full[sa], pa, abort_flag, status, 12);
                             if (ok && q0 == 0) ok = mbar_wait(&b_full[sx], px, abort_flag, status, 5);
@@ -636,33 +480,41 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                         tc_fence_after();
                         const uint32_t a0 = tmem_base + A_TMEM_COL + 64 * sa;
                         const uint64_t bd = bdesc0 + static_cast<uint64_t>((sx * L::B_STAGE + q0 * L::BOX) >> 4);
+                        bool lo = false;   // (SPLIT) some row of this stage has a lo part
+                        if constexpr (SPLIT) lo = (lo_flag[sa] != 0u);
                         mma_f16_ta(d_tmem, a0, bd, IDESC, h != 0);
                         mma_f16_ta(d_tmem, a0 + 8, bd + 2, IDESC, 1u);
                         mma_f16_ta(d_tmem, a0 + 16, bd + 4, IDESC, 1u);
                         mma_f16_ta(d_tmem, a0 + 24, bd + 6, IDESC, 1u);
-                        // probes, while these run: this thread's next step is step 1 of
-                        // superblock t, or step 0 of superblock t + 2
-                        const bool last_b = (q0 + 2 == L::SCH);   // this step ends its B stage
+                        // probes, while these run: this thread's next step is step h + 1
+                        // of superblock t, or step 0 of superblock t + 2
+                        const bool last_b = (q0 + KSTEP / 64 == L::SCH);   // this step ends its B stage
                         {
-                            const int nt = h == 0 ? t : t + 2, nh = h ^ 1;
-                            int na, nx;
+                            const int nt = h + 1 < STEPS ? t : t + 2, nh = (h + 1) % STEPS;
+                            int na, nx, nq;
                             uint32_t npa, npx;
                             a_at(nt, nh, na, npa);
-                            b_at(nt, nh, nx, npx);
+                            b_at(nt, nh, nx, npx, nq);
                             const bool ta = mbar_test_wait(&a_full[na], npa);
-                            const bool tb = ((2 * nh) % L::SCH != 0) || mbar_test_wait(&b_full[nx], npx);
-                            if (h == 0) {
-                                if (L::CORR) sb_ok = mbar_test_wait(&sb_full[p], (t / SBN) & 1);
-                            } else {
-                                acc_ok = mbar_test_wait(&acc_empty[par], (((t + 2) >> 1) & 1) ^ 1);
-                            }
+                            const bool tb = (nq != 0) || mbar_test_wait(&b_full[nx], npx);
+                            if (h == 0 && L::CORR) sb_ok = mbar_test_wait(&sb_full[p], (t / SBN) & 1);
+                            if (h == STEPS - 1) acc_ok = mbar_test_wait(&acc_empty[par], (((t + 2) >> 1) & 1) ^ 1);
                             step_ok = ta && tb;
                         }
-                        const uint64_t bd1 = bd + (L::BOX >> 4);
-                        mma_f16_ta(d_tmem, a0 + 32, bd1, IDESC, 1u);
-                        mma_f16_ta(d_tmem, a0 + 40, bd1 + 2, IDESC, 1u);
-                        mma_f16_ta(d_tmem, a0 + 48, bd1 + 4, IDESC, 1u);
-                        mma_f16_ta(d_tmem, a0 + 56, bd1 + 6, IDESC, 1u);
+                        if constexpr (SPLIT) {
+                            if (lo) {   // the lo part, against the same activation box
+                                mma_f16_ta(d_tmem, a0 + 32, bd, IDESC, 1u);
+                                mma_f16_ta(d_tmem, a0 + 40, bd + 2, IDESC, 1u);
+                                mma_f16_ta(d_tmem, a0 + 48, bd + 4, IDESC, 1u);
+                                mma_f16_ta(d_tmem, a0 + 56, bd + 6, IDESC, 1u);
+                            }
+                        } else {
+                            const uint64_t bd1 = bd + (L::BOX >> 4);
+                            mma_f16_ta(d_tmem, a0 + 32, bd1, IDESC, 1u);
+                            mma_f16_ta(d_tmem, a0 + 40, bd1 + 2, IDESC, 1u);
+                            mma_f16_ta(d_tmem, a0 + 48, bd1 + 4, IDESC, 1u);
+                            mma_f16_ta(d_tmem, a0 + 56, bd1 + 6, IDESC, 1u);
+                        }
                         // frees the A stage (and, with MERGED_RELEASE, the B stage of this step)
                         mma_commit(&a_empty[sa]);
                         if (last_b && !MERGED_RELEASE) mma_commit(&b_empty[sx]);
@@ -686,8 +538,11 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     } else if (warp >= W_UNPACK0 && warp < W_EPI0) {
         // ------------------------------------------------ unpack (thread = weight row)
         // One or two groups of four warps (TMEM lanes 32*(warp%4).., as any
-        // warp must): with two, group g expands K128 step g of every
-        // superblock; group 0 also writes the superblock's side data.
+        // warp must).  Q4_K: one group.  PTQ1_0: group g expands K128 step g
+        // of every superblock; group 0 also writes the superblock's side data.
+        // Q6_K (SPLIT): group g owns the superblocks t with t % 2 == g -- the
+        // same ones as MMA thread g -- and expands all four K64 steps of each
+        // into weight-operand stages 2g and 2g+1, writing its side data too.
         const int grp = (warp - W_UNPACK0) >> 2;
         const int j0 = UG == 2 ? grp : 0, j1 = UG == 2 ? grp + 1 : 2;   // this warp's K128 steps
         const int quad = warp & 3;
@@ -706,6 +561,9 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                 pend = -1;
             }
         };
+        // (SPLIT) bit i: this warp's lo columns of stage 2*grp + i may be nonzero
+        // (TMEM starts with unknown contents)
+        int lo_dirty = 3;
         int t = 0;
         bool ok = true;
         for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
@@ -720,11 +578,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                 const int p = t % SBN;
 
                 if constexpr (WT == 4) {
-                    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
-                    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
-                    const uint32_t sc03 = hdr.y & 0x3f3f3f3fu;
-                    const uint32_t sc47 = (hdr.w & 0x0f0f0f0fu) | ((hdr.y >> 2) & 0x30303030u);
-                    const bool main_on = (d != 0.0f);
+                    const Q4kScales qs4 = q4k_scales(*reinterpret_cast<const uint4*>(blk));
                     // (the dmin correction operands and the scale e of this superblock
                     // are written by the epilogue's side-data warps)
                     // this warp's K128 steps: the second chunk is expanded while the
@@ -734,24 +588,15 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                         const int g = 2 * t + j;
                         const int s = g % A_STAGES;
                         // sub-block scales of chunks 2j (bytes 0, 1) and 2j+1 (bytes 2, 3)
-                        const uint32_t scw = main_on ? (j == 0 ? sc03 : sc47) : 0u;
+                        const uint32_t scw = j == 0 ? qs4.sc03 : qs4.sc47;
                         uint32_t v0[32], v1[32];
-                        {
-                            // sc, -1024 sc for the low nibbles; sc/16, -64 sc for the high ones (all exact)
-                            const uint32_t sl = byte_h2<0>(scw, H2_M1024), sh = byte_h2<1>(scw, H2_M1024);
-                            unpack_q4k_chunk(blk, 2 * j, sl, hmul2u(sl, H2_M1024), hmul2u(sh, H2_1_16),
-                                             hmul2u(sh, H2_M64), v0);
-                        }
+                        q4k_expand<0>(blk, 2 * j, scw, qs4.p2, v0);
                         signal();
                         ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
                         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                         tc_fence_after();
                         tmem_st_32x32b_x32(lane_base + 64 * s, v0);
-                        {
-                            const uint32_t sl = byte_h2<2>(scw, H2_M1024), sh = byte_h2<3>(scw, H2_M1024);
-                            unpack_q4k_chunk(blk, 2 * j + 1, sl, hmul2u(sl, H2_M1024), hmul2u(sh, H2_1_16),
-                                             hmul2u(sh, H2_M64), v1);
-                        }
+                        q4k_expand<1>(blk, 2 * j + 1, scw, qs4.p2, v1);
                         tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
                         pend = s;
                     }
@@ -786,16 +631,15 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                     }
                     if (!ok) break;
                 } else {
-                    const uint4 scv = *reinterpret_cast<const uint4*>(blk + 192);
-                    const uint32_t sw[4] = {scv.x, scv.y, scv.z, scv.w};
-                    bool bad = false;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int v = static_cast<int8_t>((sw[j >> 2] >> (8 * (j & 3))) & 0xff);
-                        bad |= (v > 64) || (v < -64);
+                    // Q6_K.  The other group's superblock: only its raw slot's phase.
+                    if ((t & 1) != grp) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&raw_empty[r]);
+                        continue;
                     }
-                    if (grp == 0) {
-                        if (bad) atomicOr(status, ST_Q6K_SCALE);
+                    // sub-block scales split into exact hi and lo parts (q6k_split)
+                    const uint4 scv = *reinterpret_cast<const uint4*>(blk + 192);
+                    {
                         const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
                         if (!mbar_test_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1)) signal();
                         ok = mbar_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1, abort_flag, status, 8);
@@ -804,39 +648,38 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&sb_full[p]);
                     }
-                    // this warp's K128 steps, as for Q4_K
+                    // K64 step c into stage 2*grp + (c & 1): hi part in its first 32
+                    // columns; the lo part in the other 32 where some row of the warp has
+                    // one (else zeros, written only if the columns may hold old values)
 #pragma unroll 1
-                    for (int j = j0; j < j1; ++j) {
-                        const int g = 2 * t + j;
-                        const int s = g % A_STAGES;
+                    for (int c = 0; c < 4; ++c) {
+                        const int s = 2 * grp + (c & 1);
+                        const int use = 2 * (t >> 1) + (c >> 1);   // the stage's phase
                         // the chunk's four sub-block scales: bytes 4c..4c+3 of the scale array
-                        auto scales = [&](uint32_t scw, uint32_t (&s4)[4]) {
-                            const uint32_t u = scw ^ 0x80808080u;   // signed bytes, offset by 128
-                            s4[0] = byte_h2<0>(u, H2_M1152);
-                            s4[1] = byte_h2<1>(u, H2_M1152);
-                            s4[2] = byte_h2<2>(u, H2_M1152);
-                            s4[3] = byte_h2<3>(u, H2_M1152);
-                        };
-                        uint32_t v0[32], v1[32];
-                        {
-                            uint32_t s4[4];
-                            scales(j == 0 ? sw[0] : sw[2], s4);
-                            unpack_q6k_chunk(blk, 2 * j, s4, v0);
-                        }
+                        uint32_t slo, v[32];
+                        q6k_expand_hi(blk, c, c == 0 ? scv.x : c == 1 ? scv.y : c == 2 ? scv.z : scv.w, slo, v);
                         signal();
-                        ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
+                        ok = mbar_wait(&a_empty[s], (use & 1) ^ 1, abort_flag, status, 9);
                         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                         tc_fence_after();
-                        tmem_st_32x32b_x32(lane_base + 64 * s, v0);
-                        {
-                            uint32_t s4[4];
-                            scales(j == 0 ? sw[1] : sw[3], s4);
-                            unpack_q6k_chunk(blk, 2 * j + 1, s4, v1);
+                        tmem_st_32x32b_x32(lane_base + 64 * s, v);
+                        const bool need = __any_sync(0xffffffffu, slo != 0u);
+                        const int bit = 1 << (c & 1);
+                        if (need || (lo_dirty & bit)) {
+                            if (need) {
+                                q6k_expand_lo(blk, c, slo, v);
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 32; ++k) v[k] = 0u;
+                            }
+                            tmem_st_32x32b_x32(lane_base + 64 * s + 32, v);
+                            lo_dirty = need ? (lo_dirty | bit) : (lo_dirty & ~bit);
                         }
-                        tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
+                        if (lane == 0) reinterpret_cast<volatile uint8_t*>(lo_flag + s)[quad] = need ? 1 : 0;
                         pend = s;
                     }
                     if (!ok) break;
+                    signal();   // the superblock's last stage now: the other group's superblock comes next
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&raw_empty[r]);
@@ -878,24 +721,12 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                 bool fine = mbar_wait(&raw_full[r], (ts / R) & 1, abort_flag, status, 15);
                 if (!__all_sync(0xffffffffu, fine)) return false;
                 const uint4 hdr = *reinterpret_cast<const uint4*>(raw_slot(r) + row * WTraits<WT>::RAW_BLOCK);
-                const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
-                const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
-                const uint32_t mn03 = hdr.z & 0x3f3f3f3fu;
-                const uint32_t mn47 = ((hdr.w >> 4) & 0x0f0f0f0fu) | ((hdr.z >> 2) & 0x30303030u);
-                const bool main_on = (d != 0.0f);
-                const float e = main_on ? d : dmin;
-                const float ratio = main_on ? -dmin / d : -1.0f;
-                if (!(fabsf(ratio) <= 1000.0f)) atomicOr(status, ST_Q4K_RANGE);
+                // e and the correction operands, on the scale 2^-s the unpack uses
+                // (q4k_side); a row out of even the shifted range gets e = NaN: its
+                // outputs are declined, visibly, rather than computed wrongly
                 uint32_t a1[8], a2[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int mj = ((j < 4 ? mn03 : mn47) >> (8 * (j & 3))) & 0xff;
-                    const float v = static_cast<float>(mj) * ratio;
-                    const __half h1 = __float2half_rn(v);
-                    const __half h2 = __float2half_rn(v - __half2float(h1));
-                    a1[j] = h2dup(h1);
-                    a2[j] = h2dup(h2);
-                }
+                float e;
+                if (!q4k_side(hdr, a1, a2, e)) atomicOr(status, ST_Q4K_RANGE);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&raw_empty[r]);
                 fine = mbar_wait(&sb_empty[ps], ((ts / SBN) & 1) ^ 1, abort_flag, status, 16);

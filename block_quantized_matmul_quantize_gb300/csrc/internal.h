@@ -12,8 +12,8 @@ namespace qg {
 // Device status bits (the word lives in qgemm_api.cu; kernels get its address).
 enum : uint32_t {
     ST_TIMEOUT = 1u << 0,       // an mbarrier wait gave up (pipeline broken)
-    ST_Q4K_RANGE = 1u << 1,     // Q4_K block with |dmin/d| too large for the fp16 correction operand
-    ST_Q6K_SCALE = 1u << 2,     // Q6_K sub-scale with |sc| > 64 (fp16 operand not exact)
+    ST_Q4K_RANGE = 1u << 1,     // Q4_K block row declined: |dmin/d| beyond the shifted fp16 range (NaN output)
+    // (1u << 2 is not used: Q6_K sub-scales of the whole int8 range are computed exactly)
     ST_BAD_EXPERT = 1u << 3,    // routed GEMM: an expert id outside [0, E) (that row is skipped)
 };
 // The status lives in two words: [0] = OR of the bits above, [1] = 1 + the

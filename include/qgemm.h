@@ -152,8 +152,12 @@ QGEMM_API size_t qgemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * contribution of superblock b (fp32 accumulation of exact integer partials).
  * Y is deterministic for a given shape and device: a cut tile's K parts are
  * summed in ascending part order, whichever part finishes last.
- * Value range: |dmin/d| <= 1000 per block (else device status
- * QGEMM_DEV_Q4K_RANGE is set and Y is not to be trusted).
+ * Value range: every Q4_K block is computed except one whose correction
+ * m_j*|dmin/d| exceeds fp16's range even on the largest power-of-two
+ * shifted scale (m_j*|dmin/d| > 65504*2^14, e.g. d = 6e-8 with dmin >= 2):
+ * such a block row is declined -- its output elements become NaN -- and
+ * device status QGEMM_DEV_Q4K_RANGE is set.  (The small-M path computes
+ * every block in fp32.)
  * Errors: EINVAL, EALIGN, EUNSUPPORTED (M, N >= 2^31), ECUDA. */
 QGEMM_API int qgemm_q4k(const void *w, int64_t N, int64_t K, int64_t ldw, const int8_t *xqs, const float *xd,
               const int16_t *xbsums, int64_t M, float *y, int64_t ldy, void *workspace,
@@ -170,7 +174,9 @@ QGEMM_API int qgemm_q6k_prepack(const void *w_aos, int64_t N, int64_t K, int64_t
                       qgemm_stream_t stream);
 
 /* qgemm_q6k: as qgemm_q4k, with Q6_K weights repacked by qgemm_q6k_prepack.
- * Value range: sub-scales |sc| <= 64 (else device status QGEMM_DEV_Q6K_SCALE). */
+ * Every int8 sub-scale (-128..127) is computed exactly: on the tile path
+ * a sub-scale beyond +-64 is split into two parts whose fp16 operands are
+ * both exact, multiplied into the same accumulator. */
 QGEMM_API int qgemm_q6k(const void *w_packed, int64_t N, int64_t K, const int8_t *xqs, const float *xd,
               const int16_t *xbsums, int64_t M, float *y, int64_t ldy, void *workspace,
               size_t workspace_bytes, qgemm_stream_t stream);
@@ -326,6 +332,29 @@ QGEMM_API int qgemm_q4k_noalloc(const void *w, int64_t N, int64_t K, int64_t ldw
                                 const float *xd, const int16_t *xbsums, int64_t M, float *y, int64_t ldy,
                                 qgemm_stream_t stream);
 
+/* ------------------------------------------------- expansion check ----
+ * Diagnostic for tests: the tile GEMM's weight expansion on its own.  For
+ * each of `nblocks` superblock rows it runs the same device functions the
+ * GEMM's unpack warps run and writes one QGEMM_DEBUG_EXPAND_BYTES record of
+ * 32-bit words to `out` (device, 16-B aligned):
+ *   [0, 128)   the fp16 operand pairs of the four K64 chunks (chunk c in words
+ *              32c..32c+31; word j holds weights k and k + 2, k = 64c +
+ *              4*(j/2) + j%2, low half first) -- Q4_K: sc_j*q*2^-s; Q6_K: the
+ *              hi part of sc_j*(q - 32); PTQ1_0: d*(t - 1);
+ *   [128, 256) Q6_K: the lo part (hi + lo = sc_j*(q - 32), both exact);
+ *   [256, 272) Q4_K: the dmin-correction operands m_j*(-dmin/d)*2^-s as fp16
+ *              hi (words 256..263) and lo (264..271) parts, in both halves;
+ *   [272]      the epilogue factor e (fp32): Q4_K d*2^s (dmin when d = 0,
+ *              NaN when declined), Q6_K d, PTQ1_0 1;
+ *   [273]      bit 0: in range (not declined); bits 8..15: the Q4_K shift s.
+ * blocks (device, 16-B aligned): wtype 4 = 144-byte Q4_K blocks; 6 = the
+ * 224-byte blocks of qgemm_q6k_prepack; 1 = superblocks of two 32-byte
+ * blocks from qgemm_ptq1_prepack.  The pages have no such call (llama.cpp
+ * PR #214's review checks its loader by emulating it on 10^4 blocks; this is
+ * that check's device side).  Errors: EINVAL, EALIGN, ECUDA. */
+#define QGEMM_DEBUG_EXPAND_BYTES 1152
+QGEMM_API int qgemm_debug_expand(int wtype, const void *blocks, int64_t nblocks, void *out, qgemm_stream_t stream);
+
 /* ------------------------------------------------------ diagnostics ----
  * Launch counters per path (proof of which kernel ran: the per-variant
  * dispatch counters of PR #3036, commit 4). */
@@ -347,8 +376,8 @@ QGEMM_API int qgemm_reset_counters(void);
 
 /* Device status word of the current device.  Bits: */
 #define QGEMM_DEV_TIMEOUT 0x1u   /* a pipeline wait gave up (bounded waits) */
-#define QGEMM_DEV_Q4K_RANGE 0x2u /* a Q4_K block had |dmin/d| > 1000        */
-#define QGEMM_DEV_Q6K_SCALE 0x4u /* a Q6_K sub-scale had |sc| > 64          */
+#define QGEMM_DEV_Q4K_RANGE 0x2u /* a Q4_K block row was declined (NaN output): m_j*|dmin/d| > 65504*2^14 */
+/* (0x4u is not used: Q6_K sub-scales of the whole int8 range are computed) */
 #define QGEMM_DEV_BAD_EXPERT 0x8u /* a routed GEMM id was outside [0, E)    */
 /* Synchronizes the device, returns the status bits in *bits and the site of
  * the first timed-out wait (0 = none) in *site (may be NULL), then clears

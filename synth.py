@@ -16,7 +16,8 @@ Field distributions (the benchmark workloads):
         bytes give exactly that, whatever the bit packing), d and dmin fp16
         drawn uniform in [1e-4, 1e-3] and rounded to nearest fp16.
   Q6_K  ql 4-bit and qh 2-bit uniform (uniform random bytes), int8 sub-scales
-        uniform in [-32, 31], d fp16 uniform in [1e-4, 1e-3].
+        uniform in [-32, 31] (or, for the full-scale workload, in [-128, 127]),
+        d fp16 uniform in [1e-4, 1e-3].
   X     fp32 sigma * N(0, 1); optionally a seeded 1% of the columns scaled x8
         (the same columns for every row).
 """
@@ -86,12 +87,16 @@ def gen_q4k(N: int, K: int, seed: int) -> np.ndarray:
     return w.reshape(N, nb * Q4K_BYTES)
 
 
-def gen_q6k(N: int, K: int, seed: int) -> np.ndarray:
-    """Q6_K weights, uint8 [N, (K/256)*210]: ql @0, qh @128, scales @192, d @208."""
+def gen_q6k(N: int, K: int, seed: int, full_scales: bool = False) -> np.ndarray:
+    """Q6_K weights, uint8 [N, (K/256)*210]: ql @0, qh @128, scales @192, d @208.
+    Sub-scales uniform in [-32, 31], or with full_scales over the whole int8
+    range [-128, 127] (as quantizers that scale a block's largest sub-block to
+    the int8 limit produce)."""
     assert K % 256 == 0
     nb = K // 256
     w = random_bytes(seed * 4 + 1, N * nb * Q6K_BYTES).reshape(N * nb, Q6K_BYTES)
-    sc = (splitmix64(seed * 4 + 2, N * nb * 16) >> np.uint64(58)).astype(np.int64) - 32
+    bits = 8 if full_scales else 6
+    sc = (splitmix64(seed * 4 + 2, N * nb * 16) >> np.uint64(64 - bits)).astype(np.int64) - (1 << (bits - 1))
     w[:, 192:208] = sc.astype(np.int8).view(np.uint8).reshape(-1, 16)
     d = fp16_uniform_bits(seed * 4 + 3, N * nb)
     w[:, 208:210] = d.view(np.uint8).reshape(-1, 2)
@@ -155,9 +160,12 @@ class Workload:
     x_seed: int
     sigma: float = 1.0
     outlier_frac: float = 0.0
+    full_scales: bool = False   # Q6_K: sub-scales over the whole int8 range
 
     def weights(self) -> np.ndarray:
-        gen = {4: gen_q4k, 6: gen_q6k, 1: gen_ptq1}[self.wtype]
+        if self.wtype == 6:
+            return gen_q6k(self.N, self.K, self.w_seed, self.full_scales)
+        gen = {4: gen_q4k, 1: gen_ptq1}[self.wtype]
         return gen(self.N, self.K, self.w_seed)
 
     def x(self) -> np.ndarray:
@@ -189,6 +197,12 @@ def sweep(M: int) -> Workload:
 
 
 CONFIGS = (C0, C1, C2, C3) + tuple(sweep(m) for m in SWEEP_M)
+
+# The Q6_K shape with sub-scales over the whole int8 range (real Q6_K tensors
+# use it): the cost of the tile path's exact hi/lo split, measured beside C2.
+F2 = Workload("q6k_fullscale_m512_k11008_n2048", 6, 512, 11008, 2048, w_seed=1002, x_seed=100207,
+              full_scales=True)
+FULLSCALE_CONFIGS = (F2,)
 
 # PTQ1_0 ternary weights at the K = 5120 projection shape the pages measure
 # PTQ1_0 prefill on (a 2048-token prompt).

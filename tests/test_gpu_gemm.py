@@ -166,21 +166,99 @@ def test_q6k_scale_edges():
     device_status_clean()
 
 
-def test_out_of_range_blocks_are_flagged():
+Q6K_EXTREMES = np.array([-128, -127, -65, -64, 63, 64, 65, 127])
+
+
+def _q6k_full_range(orc, N, nb, seed):
+    """Q6_K rows whose int8 sub-scales cover the whole range: the extremes
+    (-128, -127, +-65, +-64, 63, 127) in every position, and random int8."""
+    r = np.random.default_rng(seed)
+    rows = []
+    for n in range(N):
+        blks = []
+        for b in range(nb):
+            if (n + b) % 3 == 0:
+                sc = np.roll(Q6K_EXTREMES, n + b)[np.arange(16) % 8]
+            else:
+                sc = r.integers(-128, 128, 16)
+            d_bits = int(r.integers(0x0C00, 0x1400))        # fp16 in [2^-12, 2^-10)
+            blks.append(orc.q6k_pack(d_bits, sc, r.integers(0, 64, 256)))
+        rows.append(np.concatenate(blks))
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("M,N,K,bm,splits", [(100, 300, 2048, 128, 1), (100, 300, 2048, 64, 2), (40, 136, 1024, 32, 3),
+                                             (9, 130, 512, 16, 1), (200, 384, 2560, 0, 0), (1, 256, 768, 0, 0)])
+def test_q6k_full_int8_scales(M, N, K, bm, splits):
+    """Every int8 sub-scale is computed, not flagged: the tile path splits a
+    sub-scale beyond +-64 into two exact fp16 parts."""
+    w = _q6k_full_range(oracle.get(), N, K // 256, seed=M + N + K)
+    x = synth.gen_x(M, K, 11 + M, outlier_frac=0.01)
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, bm)
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_SPLITS, splits)
+    try:
+        qg.qgemm_reset_counters()
+        check(6, w, K, x, what=f"Q6_K full int8 scales M{M} N{N} K{K} bm{bm} splits{splits}")
+        c = qg.qgemm_get_counters()
+        assert c["q6k_tc"] == 1, c
+    finally:
+        qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
+        qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_SPLITS, 0)
+    device_status_clean()
+
+
+def test_q6k_full_int8_scales_cut_last_round():
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    M, K = 200, 2048
+    N = 128 * ((G + 8 + 1) // 2)
+    w = _q6k_full_range(oracle.get(), N, K // 256, seed=77)
+    x = synth.gen_x(M, K, 78)
+    qg.qgemm_reset_counters()
+    rows = np.unique(np.concatenate([sample_rows(M, 24, seed=5), [0, 127, 128, M - 1]]))
+    check(6, w, K, x, rows=rows, what=f"Q6_K full int8 scales, cut last round, N{N}")
+    assert qg.qgemm_get_counters()["split_k"] == 1
+    device_status_clean()
+
+
+def test_q4k_large_dmin_ratio_is_exact():
+    """Blocks with |dmin/d| from 1e3 up to about 1.6e7 run on a power-of-two
+    shifted scale and stay within the tolerance, with no status bit."""
+    orc = oracle.get()
+    r = np.random.default_rng(6)
+    N, K, M = 136, 2048, 24
+    rows = []
+    for n in range(N):
+        blks = []
+        for b in range(K // 256):
+            d_bits = int(r.choice([0x0001, 0x0003, 0x0100, 0x0400, 0x0800, 0x1000, 0x1400]))   # 6e-8 .. 1e-3
+            dmin_bits = int(r.choice([0x3C00, 0x3800, 0x2E00, 0x2400]))                         # 1.0 .. 0.0156
+            blks.append(orc.q4k_pack(d_bits, dmin_bits, r.integers(0, 64, 8), r.integers(0, 64, 8),
+                                     r.integers(0, 16, 256)))
+        rows.append(np.concatenate(blks))
+    w = np.stack(rows)
+    check(4, w, K, synth.gen_x(M, K, 7), what="Q4_K large dmin/d")
+    device_status_clean()
+
+
+def test_q4k_out_of_range_row_is_declined():
+    """A block whose correction leaves fp16's range even on the largest
+    shifted scale is not computed: its row of Y is NaN and the status bit is
+    set; every other row is exact."""
     orc = oracle.get()
     rng = np.random.default_rng(5)
-    # Q4_K: d tiny, dmin large -> |dmin/d| > 1000
-    blk = orc.q4k_pack(0x0001, 0x3C00, rng.integers(0, 64, 8), rng.integers(1, 64, 8), rng.integers(0, 16, 256))
-    w = np.tile(blk, (128, 1))
-    q = gpu_quantize(synth.gen_x(16, 256, 1))
-    gpu_gemm(4, w, 256, q)
+    N, K, M = 128, 512, 16
+    w = synth.gen_q4k(N, K, 9)
+    bad_row = 37
+    mn = np.full(8, 63)
+    w[bad_row, :144] = orc.q4k_pack(0x0001, 0x4400, rng.integers(0, 64, 8), mn, rng.integers(0, 16, 256))  # d 6e-8, dmin 4
+    q = gpu_quantize(synth.gen_x(M, K, 1))
+    y = gpu_gemm(4, w, K, q)
     bits, _ = qg.qgemm_get_device_status()
     assert bits & qg.QGEMM_DEV_Q4K_RANGE
-    # Q6_K: sub-scale -100
-    blk6 = orc.q6k_pack(0x3C00, np.full(16, -100), rng.integers(0, 64, 256))
-    gpu_gemm(6, np.tile(blk6, (128, 1)), 256, q)
-    bits, _ = qg.qgemm_get_device_status()
-    assert bits & qg.QGEMM_DEV_Q6K_SCALE
+    assert np.isnan(y[:, bad_row]).all()
+    keep = np.arange(N) != bad_row
+    yr, absc = oracle_gemm(4, w, K, *q8k_numpy(q))
+    assert_gemm_close(y[:, keep], yr[:, keep], absc[:, keep], "rows beside the declined one")
     device_status_clean()
 
 

@@ -57,6 +57,17 @@ def test_q6k_fields():
     assert d.min() >= float(np.float16(1e-4)) and d.max() <= float(np.float16(1e-3))
 
 
+def test_q6k_full_scale_fields():
+    w = synth.gen_q6k(64, 1024, 5, full_scales=True).reshape(-1, 210)
+    sc = w[:, 192:208].view(np.int8).ravel().astype(np.int64)
+    assert sc.min() == -128 and sc.max() == 127                 # the whole int8 range
+    assert np.bincount(sc + 128, minlength=256).min() > 0        # every value drawn
+    assert abs((np.abs(sc) > 64).mean() - 127 / 256) < 0.03     # about half beyond +-64
+    # the other fields are those of the plain generator
+    w0 = synth.gen_q6k(64, 1024, 5).reshape(-1, 210)
+    assert np.array_equal(np.delete(w, np.s_[192:208], axis=1), np.delete(w0, np.s_[192:208], axis=1))
+
+
 def test_ptq1_fields():
     w = synth.gen_ptq1(32, 1024, 6).reshape(-1, 28)
     assert w[:, :24].max() < 243 and w[:, 24:26].max() < 81
