@@ -4,16 +4,18 @@
 One step = the whole hot path on one batch: quantize fp32 activations to Q8_K
 (qgemm_quantize_q8k_prep, which also writes the tile GEMM's fp16 operand
 planes), then the Q4_K x Q8_K GEMM (qgemm_q4k_prepared: the tcgen05 tile
-GEMM, or for M <= 8 the small-M streaming kernel).  Default workload: Q4_K,
-M = 512 tokens, K = 2048, N = 11008 (FFN up-projection shape), X ~ N(0,1)
-with 1% of the columns scaled x8; synthetic, seeded (synth.py).
+GEMM, or for M <= 8 the small-M streaming kernel).  Default workload: the
+largest configuration, the Q4_K sweep point M = 8192 tokens, K = N = 5120,
+X ~ N(0,1); synthetic, seeded (synth.py).  --workload picks another.
 
 Metric: effective TOPS = 2*M*N*K / step time (the whole job over all ranks);
 weight GB/s and the tile GEMM's roofline fraction are reported beside it.
 
 Timing: W untimed warm-up steps, then exactly K steps, each bracketed by CUDA
 events on the launching stream, with L2 flushed before every step (a 256 MiB
-write, outside the events); barrier + synchronize on both sides; the slowest
+write and then a 256 MiB read of another buffer, outside the events, so that
+the step starts with its inputs in DRAM and no dirty lines of the flush left
+in L2 to write back); barrier + synchronize on both sides; the slowest
 rank's mean is the step time.  A step is replayed as one CUDA graph captured
 from the API calls (--no-graph: the eager calls), which removes the host-side
 gaps between its kernels.  The same K steps then run once more as eager calls,
@@ -28,7 +30,9 @@ around the device step is reported beside it (e2e.copies).  Both count the
 bytes that cross the link each step.
 
 --impl reference times the CPU oracle (the parity authority) on bounded
-samples of the same workload on the host cores: the reference arm.
+samples of the same workload on the host cores (token rows partitioned over
+all of them): the reference arm.  The GPU arm's cpu_baseline is the same
+all-core oracle on a larger sample, with the single-core oracle beside it.
 """
 from __future__ import annotations
 
@@ -51,25 +55,16 @@ import synth  # noqa: E402
 
 METRIC = "k-quant GEMM effective TOPS and weight GB/s vs roofline at prefill M"
 UNIT = "TOPS"
-DEFAULT_WORKLOAD = synth.C1.name
+DEFAULT_WORKLOAD = synth.sweep(8192).name
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
 # kernel, from the ncu capture summarised under profiles/ (absent until
 # measured, and removed whenever the kernel changes).
 NCU_TRAFFIC_BYTES = {
-    "q4k_m512_k2048_n11008_outliers": 15012608,
-    "q4k_m64_k2048_n2048": 2715136,
-    "q6k_m512_k11008_n2048": 31173888,
-    "q4k_m2048_k4096_n14336": 120304640,
+    "q4k_sweep_m8192_k5120_n5120": 262962944,
     "q4k_sweep_m1_k5120_n5120": 14780928,
     "q4k_sweep_m4_k5120_n5120": 14810624,
     "q4k_sweep_m8_k5120_n5120": 14830336,
-    "q4k_sweep_m64_k5120_n5120": 15523584,
-    "q4k_sweep_m512_k5120_n5120": 20443136,
-    "q4k_sweep_m2048_k5120_n5120": 44840448,
-    "q4k_sweep_m8192_k5120_n5120": 1683155968,
-    "q4k_moe_e8_top2_m512_k4096_n14336": 319335424,
-    "ptq1_m2048_k5120_n5120": 34377984,
 }
 
 
@@ -183,27 +178,91 @@ def oracle_sample(wl, rows, x=None, w=None):
     return dt, 2.0 * rows * wl.N * wl.K
 
 
+# The oracle on all host cores: the token rows are partitioned over a pool of
+# single-threaded oracle processes (started with spawn, so that no worker is
+# forked from a process that holds a CUDA context).  Each worker builds the
+# workload's weights once; a task is (X rows, their expert ids or None).
+_POOL_W = None
+_POOL_WL = None
+
+
+def _pool_init(name):
+    global _POOL_W, _POOL_WL
+    _POOL_WL = workloads()[name]
+    _POOL_W = _POOL_WL.weights()
+    import oracle
+    oracle.get()
+
+
+def _pool_rows(task):
+    import oracle
+    orc = oracle.get()
+    xs, ids = task
+    qs, d, bs = orc.quantize_q8k(xs)
+    if ids is not None:
+        orc.gemm_id(_POOL_WL.wtype, _POOL_W, _POOL_WL.E, _POOL_WL.K, qs, d, bs, ids)
+    else:
+        orc.gemm(_POOL_WL.wtype, _POOL_W, _POOL_WL.K, qs, d, bs)
+    return len(xs)
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OraclePool:
+    """`cores` oracle processes; run(rows) times quantize + GEMM of the first
+    `rows` token rows, split evenly over the processes (wall clock)."""
+
+    def __init__(self, wl, x, cores):
+        import multiprocessing as mp
+        self.wl, self.x, self.cores = wl, x, cores
+        self.ids = wl.ids() if routed(wl) else None
+        self.pool = mp.get_context("spawn").Pool(cores, initializer=_pool_init, initargs=(wl.name,))
+
+    def run(self, rows):
+        chunks = [c for c in np.array_split(np.arange(rows), self.cores) if len(c)]
+        tasks = [(np.ascontiguousarray(self.x[c]), None if self.ids is None else np.ascontiguousarray(self.ids[c]))
+                 for c in chunks]
+        t = time.perf_counter()
+        done = sum(self.pool.map(_pool_rows, tasks))
+        dt = time.perf_counter() - t
+        per_row = 2.0 * self.wl.N * self.wl.K * (self.wl.top_k if self.ids is not None else 1)
+        return dt, done * per_row
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
     wl = workloads()[args.workload]
-    w, x = wl.weights(), wl.x()
-    rows = args.ref_rows
+    x = wl.x()
+    cores = host_cores()
+    rows = min(wl.M, args.ref_rows * cores)
+    pool = OraclePool(wl, x, cores)
     for _ in range(args.warmup):
-        oracle_sample(wl, rows, x, w)
+        pool.run(rows)
     ts, ops = [], 0.0
     for _ in range(args.steps):
-        dt, ops = oracle_sample(wl, rows, x, w)
+        dt, ops = pool.run(rows)
         ts.append(dt)
+    pool.close()
     mean = sum(ts) / len(ts)
     value = ops / mean / 1e12
-    sample = f"{rows} of {wl.M} token rows per step (quantize + GEMM over all N={wl.N}, K={wl.K})"
+    sample = (f"{rows} of {wl.M} token rows per step, split over {cores} oracle processes "
+              f"(quantize + GEMM over all N={wl.N}, K={wl.K})")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(wl),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -213,7 +272,8 @@ def run_reference(args, world, rank):
 def config_of(wl):
     c = {"workload": wl.name, "weights": {4: "Q4_K", 6: "Q6_K", 1: "PTQ1_0"}[wl.wtype], "M": wl.M, "K": wl.K,
          "N": wl.N, "x": f"{wl.sigma}*N(0,1)" + (", 1% columns x8" if getattr(wl, "outlier_frac", 0) else ""),
-         "l2": "flushed before every step (256 MiB write outside the timed events)"}
+         "l2": "flushed before every step, outside the timed events: a 256 MiB write, then a 256 MiB read of "
+               "another buffer (L2 left holding clean lines the step never touches)"}
     if routed(wl):
         c.update({"experts": wl.E, "top_k": wl.top_k, "routing": f"synthetic top-{wl.top_k}, skew {wl.skew}",
                   "routed_rows": wl.M * wl.top_k})
@@ -247,9 +307,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads()))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=512, help="token rows in the CPU-baseline sample")
+    ap.add_argument("--cpu-rows", type=int, default=512,
+                    help="token rows of the single-core CPU-baseline sample (the all-core one: this many per core)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline runs until this much time")
-    ap.add_argument("--ref-rows", type=int, default=2, help="token rows per reference-arm step")
+    ap.add_argument("--ref-rows", type=int, default=2, help="token rows per host core in a reference-arm step")
     ap.add_argument("--no-graph", action="store_true", help="time the eager API calls instead of a graph replay")
     ap.add_argument("--settle", type=float, default=0.5,
                     help="seconds of extra untimed steps after warm-up (clock settling); 0 = none")
@@ -295,6 +356,15 @@ def main():
     else:
         ws = torch.empty(max(qg.qgemm_workspace_bytes(M, N, K), 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(64 << 20, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        # Outside the timed region: write a 256 MiB buffer, then read another
+        # 256 MiB one.  L2 (129 MB) then holds only clean lines of a buffer
+        # the step never touches, so the step's inputs come from DRAM and its
+        # kernels do not pay for writing back the flush buffer's dirty lines.
+        flush_l2()
+        flush_r.max()
     stream = torch.cuda.current_stream()
 
     def step_on(xin, yout, ids_in=None):
@@ -323,13 +393,13 @@ def main():
     sampler = ClockSampler(gpu_id_for_smi(local))
     # warm-up, then about half a second more so that clocks settle
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     t_end = time.time() + args.settle
     while time.time() < t_end:
         for _ in range(20):
-            flush.zero_()
+            flush_l2()
             step()
         torch.cuda.synchronize()
 
@@ -366,7 +436,7 @@ def main():
     t0 = time.time()
     # timed steps (graph replay, or the eager calls with --no-graph)
     for i in range(K_steps):
-        flush.zero_()
+        flush_l2()
         ev_s[i].record(stream)
         if graph is not None:
             graph.replay()
@@ -377,7 +447,7 @@ def main():
     # the same steps through the eager API calls, with the GEMM launch timed alone
     c0 = qg.qgemm_get_counters()
     for i in range(K_steps):
-        flush.zero_()
+        flush_l2()
         qg.qgemm_set_profile_events(gb[i], ga[i])
         ex_s[i].record(stream)
         step()
@@ -436,7 +506,7 @@ def main():
         torch.cuda.synchronize()
         barrier()
         for i in range(K_steps):
-            flush.zero_()
+            flush_l2()
             e_s[i].record(stream)
             fn()
             e_e[i].record(stream)
@@ -469,6 +539,10 @@ def main():
             roof = {"kernel": "gemm_tc_kernel (tile GEMM)", "bound": "tensor", "achieved": achieved,
                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                     "peak_source": f"{peak_src} bf16_tflops (burst; fp16 has the bf16 rate)",
+                    "int8_peak": None,
+                    "int8_note": "no int8 tensor-core MMA on sm_103a (ptxas rejects tcgen05 kind::i8 there): "
+                                 "the integer products run exactly as fp16 MMAs, so the fp16/bf16 dense peak "
+                                 "is this kernel's ceiling",
                     "traffic": NCU_TRAFFIC_BYTES.get(wl.name)}
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K_steps,
@@ -490,17 +564,32 @@ def main():
             "device_status": bits,
         }
         if not args.no_cpu_baseline and world == 1:
-            # the oracle on `cpu_rows` token rows, repeated until about 10 s of CPU work
+            # the oracle over all host cores, `cpu_rows` token rows per core, repeated
+            # until about `cpu_seconds` of wall time; then on one core the same way
+            cores = host_cores()
+            pool = OraclePool(wl, x_host, cores)
+            rows = min(args.cpu_rows * cores, M)
+            runs, total, cops = 0, 0.0, 0.0
+            while total < args.cpu_seconds and runs < 1000:
+                dt, cops = pool.run(rows)
+                total += dt
+                runs += 1
+            pool.close()
+            line["cpu_baseline"] = {"value": runs * cops / total / 1e12, "unit": UNIT, "cores": cores,
+                                    "kind": "oracle",
+                                    "sample": f"{rows} of {M} token rows split over {cores} oracle processes "
+                                              f"(quantize + GEMM over all N{', both slots' if is_routed else ''}) "
+                                              f"x {runs} runs, {total:.1f} s wall"}
             rows = min(args.cpu_rows, M)
             runs, total, cops = 0, 0.0, 0.0
             while total < args.cpu_seconds and runs < 1000:
                 dt, cops = oracle_sample(wl, rows, x_host, w_host)
                 total += dt
                 runs += 1
-            line["cpu_baseline"] = {"value": runs * cops / total / 1e12, "unit": UNIT, "cores": 1,
-                                    "kind": "oracle",
-                                    "sample": f"{rows} of {M} token rows (quantize + GEMM over all N"
-                                              f"{', both slots' if is_routed else ''}) x {runs} runs, {total:.1f} s"}
+            line["cpu_baseline_single_core"] = {
+                "value": runs * cops / total / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{rows} of {M} token rows (quantize + GEMM over all N"
+                          f"{', both slots' if is_routed else ''}) x {runs} runs, {total:.1f} s"}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

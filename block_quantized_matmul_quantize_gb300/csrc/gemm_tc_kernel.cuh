@@ -165,7 +165,7 @@ struct Layout {
     static constexpr int RESERVE = 1024 /* base alignment */ + 512 /* barriers, misc */;
     static constexpr int B_STAGES = cmin(12, (SMEM_LIMIT - RESERVE - OFF_B) / B_STAGE) & ~1;
     static constexpr int OFF_BAR = OFF_B + B_STAGES * B_STAGE;
-    static constexpr int NBAR = 2 * RAW_SLOTS + 2 * A_STAGES + 2 * B_STAGES + 2 * SB_SLOTS + 4 + 1;
+    static constexpr int NBAR = 2 * RAW_SLOTS + 2 * A_STAGES + 2 * B_STAGES + 2 * SB_SLOTS + 4 + 1 + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM address, abort and last-part flags
     static constexpr int OFF_LOFLAG = OFF_MISC + 16;        // per weight-operand stage: a lo part was written
     static constexpr int TOTAL = OFF_LOFLAG + 4 * A_STAGES + 1024;
@@ -234,6 +234,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     uint64_t* acc_full = sb_empty + SBN;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* epi_bar = acc_empty + 2;   // the 8 epilogue warps, for cut tiles
+    uint64_t* drain_bar = epi_bar + 1;   // [2]: each MMA thread's last commit, before the CTA ends
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
@@ -253,8 +254,9 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     auto b_stage = [&](int s) { return smem + L::OFF_B + s * L::B_STAGE; };
     auto raw_slot = [&](int r) { return smem + L::OFF_RAW + r * L::RAW; };
     auto sb_slot = [&](int p) { return smem + L::OFF_SB + p * L::SB; };
-    // work item -> (n0, m0, kb0, kb1); token tiles vary fastest, so the CTAs
-    // running at the same time share weight tiles (one DRAM read, L2 hits after)
+    // work item -> (n0, m0, kb0, kb1); token tiles vary fastest (within a group
+    // of token tiles, TcWork::m_group), so the CTAs running at the same time
+    // share weight tiles (one DRAM read, L2 hits after)
     // (cut tiles: cut = index among the cut tiles, part = its K part; -1 for whole tiles)
     auto work_cut = [&](int wi, int& n0, int& m0, int& kb0, int& kb1, int& cut, int& part) {
         int tile;
@@ -290,8 +292,13 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             kb0 = static_cast<int>(static_cast<int64_t>(nb) * part / wk.parts);
             kb1 = static_cast<int>(static_cast<int64_t>(nb) * (part + 1) / wk.parts);
         }
-        n0 = (tile / wk.m_tiles) * BN;
-        m0 = (tile % wk.m_tiles) * BM;
+        // groups of m_group token tiles; within a group, token tiles vary fastest
+        // (the CTAs running at once share the group's activations in L2)
+        const int gsz = wk.m_group * wk.n_tiles;
+        const int grp = tile / gsz, r = tile - grp * gsz;
+        const int gm = min(wk.m_group, wk.m_tiles - grp * wk.m_group);   // token tiles in this group
+        n0 = (r / gm) * BN;
+        m0 = (grp * wk.m_group + r % gm) * BM;
     };
     auto work_of = [&](int wi, int& n0, int& m0, int& kb0, int& kb1) {
         int cut, part;
@@ -328,6 +335,8 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             mbar_init(&acc_empty[p], 8);
         }
         mbar_init(epi_bar, 8);
+        mbar_init(&drain_bar[0], 1);
+        mbar_init(&drain_bar[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -374,6 +383,11 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
         if (lane == 0) {
             int t = 0;
             bool ok = true;
+            // Test only (the status array's skip word): CTA 0 leaves out its
+            // first weight load, so that the waits for it run out and the
+            // kernel's timeout path is exercised without any fault.
+            const bool skip_first =
+                blockIdx.x == 0 && *reinterpret_cast<const volatile uint32_t*>(status + ST_SKIP) == ST_SKIP_TILE_WEIGHTS;
             // L2 prefetch cursor, W_PREFETCH superblocks ahead of the loads
             int pwi = blockIdx.x, pb = 0, pb1 = 0, pn0 = 0, pm0 = 0, pk0 = 0;
             if (pwi < num_work) work_of(pwi, pn0, pm0, pk0, pb1), pb = pk0;
@@ -395,8 +409,10 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                     const int r = t % R;
                     ok = mbar_wait(&raw_empty[r], ((t / R) & 1) ^ 1, abort_flag, status, 3);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(&raw_full[r], L::RAW);
-                    tma_load_2d(&tm_w, &raw_full[r], raw_slot(r), b * WTraits<WT>::RAW_BLOCK, n0);
+                    if (!(skip_first && t == 0)) {
+                        mbar_arrive_expect_tx(&raw_full[r], L::RAW);
+                        tma_load_2d(&tm_w, &raw_full[r], raw_slot(r), b * WTraits<WT>::RAW_BLOCK, n0);
+                    }
                     const int p = t % SBN;
                     ok = mbar_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1, abort_flag, status, 1);
                     if (!ok) break;
@@ -534,6 +550,9 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                     mma_commit(&acc_full[par]);
                 }
             }
+            // every MMA this thread issued has completed before the CTA frees TMEM
+            mma_commit(&drain_bar[par]);
+            mbar_wait_drain(&drain_bar[par], 0, status);
         }
     } else if (warp >= W_UNPACK0 && warp < W_EPI0) {
         // ------------------------------------------------ unpack (thread = weight row)
@@ -948,6 +967,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
         }
     }
 
+    settle_after_abort(abort_flag);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -16,10 +16,18 @@ enum : uint32_t {
     // (1u << 2 is not used: Q6_K sub-scales of the whole int8 range are computed exactly)
     ST_BAD_EXPERT = 1u << 3,    // routed GEMM: an expert id outside [0, E) (that row is skipped)
 };
-// The status lives in two words: [0] = OR of the bits above, [1] = 1 + the
-// site id of the first wait that timed out (0 = none).
+// The status array (one per device, 8 words, 8-byte aligned):
+//   [0]     OR of the bits above;
+//   [1]     1 + the site id of the first wait that timed out (0 = none);
+//   [2..3]  the wait limit in ns (uint64; 0 = QG_WAIT_NS), set by the host;
+//   [4]     test-only: a producer that leaves out one arrival (ST_SKIP_*), so
+//           that the bounded waits behind it run out; 0 = none.
+constexpr int ST_WORDS = 8;
+constexpr int ST_LIMIT = 2;
+constexpr int ST_SKIP = 4;
+enum : uint32_t { ST_SKIP_TILE_WEIGHTS = 1, ST_SKIP_SMALLM_STAGE = 2 };
 
-constexpr uint64_t QG_WAIT_NS = 2000000000ull;  // 2 s of wall time per wait
+constexpr uint64_t QG_WAIT_NS = 2000000000ull;  // 2 s of wall time per wait (default)
 constexpr uint32_t QG_WAIT_ITERS = 1u << 28;    // and at most this many polls
 
 // Output epilogue (the pages' OutT output type, plus an optional fused bias
@@ -86,6 +94,10 @@ cudaError_t launch_xgather(const int8_t* qs, const float* d, const int16_t* bsum
 // Y, and the result does not depend on which part finishes last.
 struct TcWork {
     int n_tiles, m_tiles;
+    // Work order: token tiles in groups of m_group; tile t lies in group
+    // t / (m_group * n_tiles), and within a group the token tiles vary
+    // fastest.  m_group = m_tiles: one group (token tiles fastest overall).
+    int m_group;
     int full_items;       // whole tiles
     int parts;            // K parts of each remaining tile (1: none)
     int items;            // full_items + (tiles - full_items) * parts

@@ -1,10 +1,10 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA (tensor and
 // bulk copies), tcgen05 (TMEM alloc, MMA, commit, loads, fences).
 //
-// Every wait on an mbarrier is bounded: after QG_WAIT_NS of wall time (or
-// QG_WAIT_ITERS polls) it records a timeout in the library's device status
-// word and returns false, so a broken pipeline ends the kernel instead of
-// hanging the GPU.
+// Every wait on an mbarrier is bounded: after the wait limit (the status
+// array's limit word, default QG_WAIT_NS of wall time) or QG_WAIT_ITERS polls
+// it records a timeout in the library's device status word and returns
+// false, so a broken pipeline ends the kernel instead of hanging the GPU.
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -65,14 +65,20 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity.  `abort_flag` (shared
 // memory) lets a CTA whose other role already gave up stop waiting at once.
 // On timeout: status[0] |= ST_TIMEOUT, status[1] = site + 1 (first one wins).
+__device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t* status) {
+    const uint64_t lim = *reinterpret_cast<const volatile uint64_t*>(status + ST_LIMIT);
+    return lim ? lim : QG_WAIT_NS;
+}
+
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                    uint32_t* status, int site) {
     const uint64_t t0 = globaltimer_ns();
+    const uint64_t lim = wait_limit_ns(status);
     for (uint32_t it = 0; it < QG_WAIT_ITERS; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 63u) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > QG_WAIT_NS) break;
+            if (globaltimer_ns() - t0 > lim) break;
         }
     }
     *abort_flag = 1;
@@ -85,6 +91,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
                                           uint32_t* status, int site) {
     if (mbar_try_wait(bar, parity)) return true;
     return mbar_wait_slow(bar, parity, abort_flag, status, site);
+}
+
+// Wait for this thread's own asynchronous work to land before the CTA ends
+// (a bulk copy it armed, a commit of its MMAs): bounded by the wait limit
+// but not cut short by the abort flag.  Returns false if it gave up.
+static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, const uint32_t* status) {
+    const uint64_t t0 = globaltimer_ns();
+    const uint64_t lim = wait_limit_ns(status);
+    for (uint32_t it = 0; it < QG_WAIT_ITERS; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 63u && globaltimer_ns() - t0 > lim) return false;
+    }
+    return false;
+}
+
+// A CTA that gave up (abort flag set) lets the asynchronous copies its
+// threads issued settle before it frees its resources and ends: a few tens
+// of microseconds, far longer than any one copy takes.
+__device__ __forceinline__ void settle_after_abort(volatile int* abort_flag) {
+    if (!*abort_flag) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000ull) __nanosleep(1000);
 }
 
 // ---------------------------------------------------------------- dependent launch

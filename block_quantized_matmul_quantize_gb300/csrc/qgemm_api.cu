@@ -36,13 +36,14 @@ enum { C_QUANT, C_XPREP, C_Q4K_TC, C_Q6K_TC, C_Q4K_SMALL, C_Q6K_SMALL, C_PREPACK
        C_PTQ1_PREPACK };
 // SMALL_M_MAX defaults to the measured crossover: the streaming kernel wins up
 // to 8 tokens at K = N = 5120 and at K = 4096, N = 14336.
-std::atomic<int64_t> g_opt[3] = {{qg::SMALL_M_LIMIT}, {0}, {0}};
+std::atomic<int64_t> g_opt[5] = {{qg::SMALL_M_LIMIT}, {0}, {0}, {0}, {0}};
 std::atomic<cudaEvent_t> g_ev_before{nullptr}, g_ev_after{nullptr};
 
 }  // namespace
 
-// Device status: [0] = bits, [1] = 1 + site of the first timed-out wait.
-__device__ uint32_t g_qgemm_status[2];
+// Device status: [0] = bits, [1] = 1 + site of the first timed-out wait,
+// [2..3] = the wait limit (ns, 0 = default), [4] = the test-only skip switch.
+__device__ __align__(8) uint32_t g_qgemm_status[qg::ST_WORDS];
 
 namespace {
 
@@ -151,6 +152,20 @@ Plan plan_tc(int64_t M, int64_t N, int64_t K, int sm_count) {
     qg::TcWork& w = p.work;
     w.n_tiles = static_cast<int>((N + 127) / 128);
     w.m_tiles = static_cast<int>((M + p.bm - 1) / p.bm);
+    // Work order.  Token tiles vary fastest, so the CTAs running at once share
+    // a few weight tiles and sweep the activations.  Past 32 MiB of fp16
+    // activations a sweep no longer stays in L2 beside the Y being written
+    // (measured on GB300, M=8192 K=5120 N=5120: 1.52 GB of DRAM reads for
+    // ~0.1 GB of operands).  The token tiles are then taken in groups of
+    // about 16 MiB, each group swept by all weight tiles before the next:
+    // every weight tile is read once per group, every activation once.
+    {
+        const int64_t tile_act = static_cast<int64_t>(p.bm) * K * 2;   // fp16 bytes of one token tile
+        int64_t g = w.m_tiles;
+        if (M * K * 2 > (int64_t(32) << 20)) g = (int64_t(16) << 20) / tile_act;
+        if (g < 1) g = 1;
+        w.m_group = static_cast<int>(g < w.m_tiles ? g : w.m_tiles);
+    }
     const int64_t T = static_cast<int64_t>(w.n_tiles) * w.m_tiles;
     const int64_t maxparts = nb / 2 > 1 ? (nb / 2 < 8 ? nb / 2 : 8) : 1;   // >= 2 superblocks per part
     int64_t parts = 1, full = T;
@@ -417,6 +432,7 @@ int run_id(int wtype, const void* w, int64_t E, int64_t N, int64_t K, int64_t ld
     a.K = K;
     a.work.n_tiles = static_cast<int>((N + 127) / 128);
     a.work.m_tiles = 0;
+    a.work.m_group = 1;   // (unused: the routed work list is read on the device)
     a.work.parts = 1;
     // the routed work list is read on the device; the grid is sized for its bound
     const int64_t bound = int64_t(a.work.n_tiles) * ((P + bm - 1) / bm + E);
@@ -830,18 +846,36 @@ int qgemm_get_device_status(uint32_t* bits, uint32_t* site) {
 
 int qgemm_set_option(int option, int64_t value) {
     clear_err();
-    if (option < 0 || option > 2) return fail(QGEMM_EINVAL, "unknown option %d", option);
+    if (option < 0 || option > QGEMM_OPT_TEST_SKIP_ARRIVAL) return fail(QGEMM_EINVAL, "unknown option %d", option);
     if (value < 0) return fail(QGEMM_EINVAL, "option values are >= 0");
     if (option == QGEMM_OPT_FORCE_BM && value != 0 && value != 16 && value != 32 && value != 64 && value != 128)
         return fail(QGEMM_EINVAL, "FORCE_BM must be 0, 16, 32, 64 or 128");
     if (option == QGEMM_OPT_SMALL_M_MAX && value > qg::SMALL_M_LIMIT)
         return fail(QGEMM_EINVAL, "SMALL_M_MAX must be 0..%d", qg::SMALL_M_LIMIT);
+    if (option == QGEMM_OPT_WAIT_LIMIT_US && value > 10000000)
+        return fail(QGEMM_EINVAL, "WAIT_LIMIT_US must be 0..10000000 (10 s)");
+    if (option == QGEMM_OPT_TEST_SKIP_ARRIVAL && value > 2) return fail(QGEMM_EINVAL, "TEST_SKIP_ARRIVAL must be 0..2");
+    if (option == QGEMM_OPT_WAIT_LIMIT_US || option == QGEMM_OPT_TEST_SKIP_ARRIVAL) {
+        // these two live in the current device's status array, read by the kernels
+        DevState* ds = nullptr;
+        int rc = device_state(&ds);
+        if (rc) return rc;
+        cudaError_t e;
+        if (option == QGEMM_OPT_WAIT_LIMIT_US) {
+            const uint64_t ns = static_cast<uint64_t>(value) * 1000u;
+            e = cudaMemcpyToSymbol(g_qgemm_status, &ns, sizeof(ns), qg::ST_LIMIT * sizeof(uint32_t));
+        } else {
+            const uint32_t v = static_cast<uint32_t>(value);
+            e = cudaMemcpyToSymbol(g_qgemm_status, &v, sizeof(v), qg::ST_SKIP * sizeof(uint32_t));
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "writing a device option");
+    }
     g_opt[option] = value;
     return QGEMM_OK;
 }
 
 int64_t qgemm_get_option(int option) {
-    if (option < 0 || option > 2) return -1;
+    if (option < 0 || option > QGEMM_OPT_TEST_SKIP_ARRIVAL) return -1;
     return g_opt[option].load();
 }
 

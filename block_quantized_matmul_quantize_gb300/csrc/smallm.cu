@@ -141,8 +141,12 @@ __global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
         // not depend on the preceding grid: no wait for it here, so with a
         // programmatic dependent launch they stream while it finishes.
         if (lane == 0) {
+            // Test only (the status array's skip word): CTA 0 issues no stage,
+            // so that its consumers' waits run out (and nothing is in flight).
+            const bool skip_all =
+                blockIdx.x == 0 && *reinterpret_cast<const volatile uint32_t*>(status + ST_SKIP) == ST_SKIP_SMALLM_STAGE;
             int issued = 0;
-            for (int g = 0; g < nst; ++g) {
+            for (int g = 0; g < nst && !skip_all; ++g) {
                 const int sl = g % nsb;
                 if (g >= nsb && !mbar_wait(&empty[sl], ((g / nsb) - 1) & 1, &abort_flag, status, 20)) break;
                 const int ra = r0 + g * srw;
@@ -158,9 +162,10 @@ __global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
                 }
                 ++issued;
             }
-            // the copies still in flight land before the CTA may end
+            // the copies still in flight land before the CTA may end (not cut
+            // short by the abort flag)
             for (int g = issued > nsb ? issued - nsb : 0; g < issued; ++g)
-                mbar_wait(&full[g % nsb], (g / nsb) & 1, &abort_flag, status, 21);
+                mbar_wait_drain(&full[g % nsb], (g / nsb) & 1, status);
         }
         return;
     }

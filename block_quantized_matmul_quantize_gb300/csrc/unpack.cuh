@@ -146,9 +146,11 @@ __device__ __forceinline__ bool q4k_side(uint4 hdr, uint32_t (&a1)[8], uint32_t 
 // odd (else 0): hi_j*(q - 32) is then either at most 2048 or even and at most
 // 4096, lo_j*(q - 32) at most 32, both exact, and the tensor core adds the
 // two parts into the same accumulator.  Four int8 scales per word, bytewise.
+// For an odd int8 byte, |sc| > 64 exactly when its bits 7 and 6 differ
+// (65..127 is 01xxxxxx, -127..-65 is 10xxxxxx), so lo is bit 0 of
+// sc & (sc >> 7 ^ sc >> 6) in each byte, and hi = sc - lo clears that bit.
 __device__ __forceinline__ void q6k_split(uint32_t sw, uint32_t& hi, uint32_t& lo) {
-    const uint32_t big = __vcmpgtu4(__vabsss4(sw), 0x40404040u);   // 0xff in each byte with |sc| > 64
-    lo = big & sw & 0x01010101u;
+    lo = sw & ((sw >> 7) ^ (sw >> 6)) & 0x01010101u;
     hi = sw & ~lo;
 }
 // Four int8 scales (one word) -> four fp16 pairs (each scale in both halves).

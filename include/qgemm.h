@@ -392,7 +392,24 @@ QGEMM_API int qgemm_get_device_status(uint32_t *bits, uint32_t *site);
 typedef enum {
     QGEMM_OPT_SMALL_M_MAX = 0,  /* M <= this uses the small-M path: 0 = off, at most 8 (default 8) */
     QGEMM_OPT_FORCE_BM = 1,     /* tokens per CTA for the tile path: 0 = auto, 16/32/64/128 */
-    QGEMM_OPT_FORCE_SPLITS = 2  /* split-K factor: 0 = auto, else 1..K/256       */
+    QGEMM_OPT_FORCE_SPLITS = 2, /* split-K factor: 0 = auto, else 1..K/256       */
+    /* The limit of every pipeline wait in the kernels, in microseconds (0 =
+     * the default of 2 s; at most 10 s).  A wait that runs out records
+     * QGEMM_DEV_TIMEOUT and its site, its CTA stops without writing its
+     * outputs, and qgemm_get_device_status returns QGEMM_ETIMEOUT.  Written
+     * into the current device's copy (a synchronous copy); set it while no
+     * call of this library runs on that device. */
+    QGEMM_OPT_WAIT_LIMIT_US = 3,
+    /* Test only: make the waits run out without any fault.  1: the tile
+     * GEMM's first CTA leaves out its first weight load; 2: the small-M
+     * kernel's first CTA issues no weight stage.  The waits behind the left-
+     * out copy run out after the wait limit, the CTA's other roles give up
+     * at once, and that CTA's output tiles are left unwritten; the other
+     * CTAs finish normally.  0 (default): off.  Current device, as above.
+     * After a timeout, a workspace filled by qgemm_quantize_q8k_prep must be
+     * filled again before another _prepared call (its cut-tile counters may
+     * be left nonzero); the other calls prepare their workspace themselves. */
+    QGEMM_OPT_TEST_SKIP_ARRIVAL = 4
 } qgemm_option;
 QGEMM_API int qgemm_set_option(int option, int64_t value);
 QGEMM_API int64_t qgemm_get_option(int option);

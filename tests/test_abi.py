@@ -217,6 +217,10 @@ def test_options_and_counters(L):
     assert L.qgemm_get_option(qg.QGEMM_OPT_FORCE_BM) == 64
     assert L.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0) == qg.QGEMM_OK
     assert L.qgemm_get_option(99) == -1
+    # the wait limit and the test-only skip switch: range-checked before any device access
+    assert L.qgemm_set_option(qg.QGEMM_OPT_WAIT_LIMIT_US, 10_000_001) == qg.QGEMM_EINVAL
+    assert L.qgemm_set_option(qg.QGEMM_OPT_TEST_SKIP_ARRIVAL, 3) == qg.QGEMM_EINVAL
+    assert L.qgemm_set_option(5, 0) == qg.QGEMM_EINVAL
     L.qgemm_reset_counters()
     c = qg._Counters()
     assert L.qgemm_get_counters(ctypes.byref(c)) == 0

@@ -103,6 +103,20 @@ def test_short_last_round_is_cut(wtype):
     assert c["q4k_tc" if wtype == 4 else "q6k_tc"] == 1 and c["split_k"] == 1, c
 
 
+@pytest.mark.parametrize("wtype", [4, 6])
+@pytest.mark.parametrize("M,N,K", [(1100, 300, 16384), (4096, 1280, 5120)])
+def test_grouped_work_order(wtype, M, N, K):
+    """fp16 activations beyond 32 MiB: token tiles are taken in groups of
+    about 16 MiB (M=1100, K=16384: groups of 4, 4 and 1 token tiles, every
+    tile cut into K parts; M=4096, K=5120: groups of 12, 12 and 8, whole tiles
+    and a cut last round).  Every token tile is checked."""
+    assert M * K * 2 > 32 << 20
+    w = weights(wtype, N, K, 90 + M)
+    x = synth.gen_x(M, K, 91 + M, outlier_frac=0.01)
+    check(wtype, w, K, x, rows=tile_rows(M, 128, seed=M), what=f"grouped order Q{wtype}_K M{M} N{N} K{K}")
+    device_status_clean()
+
+
 @pytest.mark.parametrize("wl", [synth.C0, synth.C1, synth.C2], ids=lambda w: w.name)
 def test_workload_full(wl):
     check(wl.wtype, wl.weights(), wl.K, wl.x(), what=wl.name)
