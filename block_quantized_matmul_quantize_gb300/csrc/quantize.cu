@@ -42,9 +42,35 @@ struct PrepOut {
     int* counters; // TC_MAX_CUT_TILES split-tile counters, zeroed
 };
 
+// round-half-away(x / d) of one element, by the IEEE definition: x / d
+// correctly rounded, then halves away from zero, clamped to +-127.
+__device__ __forceinline__ int q8_exact(float x, float d) {
+    const float r = fminf(fmaxf(roundf(x / d), -127.0f), 127.0f);
+    return static_cast<int>(r);
+}
+
+// The same value for a normal d (d >= 2^-126), cheaper: r = x * RN(1/d) is
+// within 2^-23 * |x/d| <= 1.52e-5 of x/d, and the correctly rounded x / d
+// within 7.6e-6 of it, so they round to the same integer unless r lies
+// within 2.3e-5 of a half-integer.  a = |r| + 0.5 is rounded by at most
+// 2^-18, so if a is more than 2^-14 from an integer, floor(a) is that
+// integer and the result equals q8_exact; otherwise q8_exact decides (about
+// one element in 10^4 of normal data).  |r| <= 127.00002 needs no clamp.
+// (Products and sums with the _rn intrinsics: no contraction into an FMA.)
+__device__ __forceinline__ int q8_fast(float x, float y, float d) {
+    constexpr float TH = 6.103515625e-05f;   // 2^-14
+    const float r = __fmul_rn(x, y);
+    const float a = __fadd_rn(fabsf(r), 0.5f);
+    const int qa = __float2int_rz(a);
+    const float t = __fsub_rn(a, __int2float_rn(qa));
+    if (t < TH || t > 1.0f - TH) return q8_exact(x, d);
+    return r < 0.0f ? -qa : qa;
+}
+
 // One warp per 256-element chunk: each lane owns 8 consecutive elements
-// (two 16-byte loads), so one chunk is one coalesced 1 KiB read.
-template <bool PREP>
+// (two 16-byte loads), so one chunk is one coalesced 1 KiB read.  The chunk
+// index is 32-bit unless M * K/256 reaches 2^31 (WIDE).
+template <bool PREP, bool WIDE>
 __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* __restrict__ x, int64_t M,
                                                                   int64_t K, int64_t ldx, int8_t* __restrict__ qs,
                                                                   float* __restrict__ dout,
@@ -52,10 +78,19 @@ __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* 
     allow_dependent_launch();
     const int lane = threadIdx.x & 31;
     const int64_t nb = K >> 8;
-    const int64_t chunk = static_cast<int64_t>(blockIdx.x) * QWARPS + (threadIdx.x >> 5);
-    if (chunk >= M * nb) return;
-    const int64_t m = chunk / nb;
-    const int64_t b = chunk - m * nb;
+    int64_t m, b;
+    if constexpr (WIDE) {
+        const int64_t chunk = static_cast<int64_t>(blockIdx.x) * QWARPS + (threadIdx.x >> 5);
+        if (chunk >= M * nb) return;
+        m = chunk / nb;
+        b = chunk - m * nb;
+    } else {
+        const uint32_t chunk = blockIdx.x * QWARPS + (threadIdx.x >> 5);
+        if (chunk >= static_cast<uint32_t>(M * nb)) return;
+        const uint32_t m32 = chunk / static_cast<uint32_t>(nb);
+        m = m32;
+        b = chunk - m32 * static_cast<uint32_t>(nb);
+    }
 
     const float4* src = reinterpret_cast<const float4*>(x + m * ldx + b * 256) + lane * 2;
     const float4 v0 = __ldcs(src);
@@ -70,17 +105,19 @@ __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* 
 
     int q[8];
     const float d = amax / 127.0f;
-    if (d == 0.0f) {
+    if (d >= 1.17549435e-38f) {
+        // a normal scale (the usual case): one reciprocal per lane
+        const float y = __frcp_rn(d);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = q8_fast(v[i], y, d);
+    } else if (d == 0.0f) {
         // amax == 0, or amax/127 underflows to zero: the chunk quantizes to zero
 #pragma unroll
         for (int i = 0; i < 8; ++i) q[i] = 0;
     } else {
+        // a subnormal scale: the division itself
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float r = roundf(v[i] / d);
-            r = fminf(fmaxf(r, -127.0f), 127.0f);
-            q[i] = static_cast<int>(r);
-        }
+        for (int i = 0; i < 8; ++i) q[i] = q8_exact(v[i], d);
     }
     uint2 packed;
     packed.x = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) | (static_cast<uint32_t>(q[3] & 0xff) << 24);
@@ -232,12 +269,19 @@ cudaError_t launch_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ld
     const int64_t chunks = M * (K >> 8);
     const int64_t blocks = (chunks + QWARPS - 1) / QWARPS;
     const PrepOut prep{xh, xbs, dxT, Mp, counters};
-    if (xh)
-        quantize_q8k_kernel<true><<<static_cast<unsigned>(blocks), QWARPS * 32, 0, s>>>(x, M, K, ldx, qs, d, bsums,
-                                                                                      prep);
-    else
-        quantize_q8k_kernel<false><<<static_cast<unsigned>(blocks), QWARPS * 32, 0, s>>>(x, M, K, ldx, qs, d,
-                                                                                       bsums, prep);
+    const bool wide = chunks >= (int64_t(1) << 31);
+    const dim3 grid(static_cast<unsigned>(blocks)), block(QWARPS * 32);
+    if (xh) {
+        if (wide)
+            quantize_q8k_kernel<true, true><<<grid, block, 0, s>>>(x, M, K, ldx, qs, d, bsums, prep);
+        else
+            quantize_q8k_kernel<true, false><<<grid, block, 0, s>>>(x, M, K, ldx, qs, d, bsums, prep);
+    } else {
+        if (wide)
+            quantize_q8k_kernel<false, true><<<grid, block, 0, s>>>(x, M, K, ldx, qs, d, bsums, prep);
+        else
+            quantize_q8k_kernel<false, false><<<grid, block, 0, s>>>(x, M, K, ldx, qs, d, bsums, prep);
+    }
     return cudaGetLastError();
 }
 
