@@ -236,8 +236,9 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     uint64_t* epi_bar = acc_empty + 2;   // the 8 epilogue warps, for cut tiles
     uint64_t* drain_bar = epi_bar + 1;   // [2]: each MMA thread's last commit, before the CTA ends
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+    // wait control (ptx.cuh): [0] abort flag, [1] wait limit
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 12);
     // SPLIT: byte q of word s is set by unpack warp q when it wrote a nonzero lo
     // part into stage s (before its a_full arrival; read by the issuer after the wait)
     volatile uint32_t* lo_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_LOFLAG);
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
         mbar_init(epi_bar, 8);
         mbar_init(&drain_bar[0], 1);
         mbar_init(&drain_bar[1], 1);
-        *abort_flag = 0;
+        wait_ctl_init(abort_flag, status);
         fence_mbar_init();
     }
     if (warp == W_PROD_X && lane == 0) tma_prefetch_desc(&tm_xh);
@@ -552,7 +553,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             }
             // every MMA this thread issued has completed before the CTA frees TMEM
             mma_commit(&drain_bar[par]);
-            mbar_wait_drain(&drain_bar[par], 0, status);
+            mbar_wait_drain(&drain_bar[par], 0, abort_flag);
         }
     } else if (warp >= W_UNPACK0 && warp < W_EPI0) {
         // ------------------------------------------------ unpack (thread = weight row)
@@ -598,6 +599,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
 
                 if constexpr (WT == 4) {
                     const Q4kScales qs4 = q4k_scales(*reinterpret_cast<const uint4*>(blk));
+                    if (qs4.declined) atomicOr(status, ST_Q4K_RANGE);   // (its outputs become NaN)
                     // (the dmin correction operands and the scale e of this superblock
                     // are written by the epilogue's side-data warps)
                     // this warp's K128 steps: the second chunk is expanded while the
@@ -609,13 +611,13 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                         // sub-block scales of chunks 2j (bytes 0, 1) and 2j+1 (bytes 2, 3)
                         const uint32_t scw = j == 0 ? qs4.sc03 : qs4.sc47;
                         uint32_t v0[32], v1[32];
-                        q4k_expand<0>(blk, 2 * j, scw, qs4.p2, v0);
+                        q4k_expand<0>(blk, 2 * j, scw, qs4, v0);
                         signal();
                         ok = mbar_wait(&a_empty[s], ((g / A_STAGES) & 1) ^ 1, abort_flag, status, 9);
                         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                         tc_fence_after();
                         tmem_st_32x32b_x32(lane_base + 64 * s, v0);
-                        q4k_expand<1>(blk, 2 * j + 1, scw, qs4.p2, v1);
+                        q4k_expand<1>(blk, 2 * j + 1, scw, qs4, v1);
                         tmem_st_32x32b_x32(lane_base + 64 * s + 32, v1);
                         pend = s;
                     }
@@ -740,25 +742,27 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                 bool fine = mbar_wait(&raw_full[r], (ts / R) & 1, abort_flag, status, 15);
                 if (!__all_sync(0xffffffffu, fine)) return false;
                 const uint4 hdr = *reinterpret_cast<const uint4*>(raw_slot(r) + row * WTraits<WT>::RAW_BLOCK);
-                // e and the correction operands, on the scale 2^-s the unpack uses
-                // (q4k_side); a row out of even the shifted range gets e = NaN: its
-                // outputs are declined, visibly, rather than computed wrongly
-                uint32_t a1[8], a2[8];
-                float e;
-                if (!q4k_side(hdr, a1, a2, e)) atomicOr(status, ST_Q4K_RANGE);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&raw_empty[r]);
                 fine = mbar_wait(&sb_empty[ps], ((ts / SBN) & 1) ^ 1, abort_flag, status, 16);
                 if (!__all_sync(0xffffffffu, fine)) return false;
                 uint8_t* sbw = sb_slot(ps);
-                // correction slabs, 32-byte swizzle: row * 32 + (chunk ^ ((row >> 2) & 1)) * 16
-                uint8_t* s1 = sbw + L::SB_ACORR + row * 32;
-                uint8_t* s2 = s1 + BN * 32;
+                // e and the correction operands, on the scale 2^-s the unpack uses
+                // (q4k_side), each word stored as it is made (few live registers
+                // beside the accumulators); a row out of even the shifted range gets
+                // e = NaN: its outputs are declined, visibly, rather than computed
+                // wrongly (the unpack records the status bit).  Correction slabs,
+                // 32-byte swizzle: word j of a row at
+                // row * 32 + ((j / 4) ^ ((row >> 2) & 1)) * 16 + (j % 4) * 4.
+                uint32_t* s1 = reinterpret_cast<uint32_t*>(sbw + L::SB_ACORR + row * 32);
+                uint32_t* s2 = s1 + BN * 8;
                 const int x = (row >> 2) & 1;
-                *reinterpret_cast<uint4*>(s1 + ((0 ^ x) << 4)) = make_uint4(a1[0], a1[1], a1[2], a1[3]);
-                *reinterpret_cast<uint4*>(s1 + ((1 ^ x) << 4)) = make_uint4(a1[4], a1[5], a1[6], a1[7]);
-                *reinterpret_cast<uint4*>(s2 + ((0 ^ x) << 4)) = make_uint4(a2[0], a2[1], a2[2], a2[3]);
-                *reinterpret_cast<uint4*>(s2 + ((1 ^ x) << 4)) = make_uint4(a2[4], a2[5], a2[6], a2[7]);
+                float e;
+                q4k_side(hdr, e, [&](int j, uint32_t w1, uint32_t w2) {
+                    const int o = (((j >> 2) ^ x) << 2) + (j & 3);
+                    s1[o] = w1;
+                    s2[o] = w2;
+                });
                 reinterpret_cast<float*>(sbw + L::SB_E)[row] = e;
                 fence_proxy_async_smem();
                 __syncwarp();

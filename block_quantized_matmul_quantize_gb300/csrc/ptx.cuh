@@ -65,15 +65,24 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity.  `abort_flag` (shared
 // memory) lets a CTA whose other role already gave up stop waiting at once.
 // On timeout: status[0] |= ST_TIMEOUT, status[1] = site + 1 (first one wins).
-__device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t* status) {
+// A CTA's wait control, in its shared memory: ctl[0] is the abort flag (a
+// role that gave up sets it, so that the others stop waiting at once), ctl[1]
+// the wait limit in microseconds, read once from the status array when the
+// CTA starts (0 = QG_WAIT_NS), so that no wait reads global memory.
+__device__ __forceinline__ void wait_ctl_init(volatile int* ctl, const uint32_t* status) {
     const uint64_t lim = *reinterpret_cast<const volatile uint64_t*>(status + ST_LIMIT);
-    return lim ? lim : QG_WAIT_NS;
+    ctl[0] = 0;
+    ctl[1] = static_cast<int>(lim / 1000u);
+}
+__device__ __forceinline__ uint64_t wait_limit_ns(const volatile int* ctl) {
+    const int us = ctl[1];
+    return us > 0 ? static_cast<uint64_t>(us) * 1000u : QG_WAIT_NS;
 }
 
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                    uint32_t* status, int site) {
     const uint64_t t0 = globaltimer_ns();
-    const uint64_t lim = wait_limit_ns(status);
+    const uint64_t lim = wait_limit_ns(abort_flag);
     for (uint32_t it = 0; it < QG_WAIT_ITERS; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 63u) {
@@ -96,9 +105,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // Wait for this thread's own asynchronous work to land before the CTA ends
 // (a bulk copy it armed, a commit of its MMAs): bounded by the wait limit
 // but not cut short by the abort flag.  Returns false if it gave up.
-static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, const uint32_t* status) {
+static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, const volatile int* ctl) {
     const uint64_t t0 = globaltimer_ns();
-    const uint64_t lim = wait_limit_ns(status);
+    const uint64_t lim = wait_limit_ns(ctl);
     for (uint32_t it = 0; it < QG_WAIT_ITERS; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 63u && globaltimer_ns() - t0 > lim) return false;

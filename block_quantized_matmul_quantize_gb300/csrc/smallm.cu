@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
     static_assert(VALS <= 16, "stage shape");
     __shared__ float red[2][small_max_warps(MT)][VALS];
     __shared__ uint64_t full[SM_MAX_SLOTS], empty[SM_MAX_SLOTS];
-    __shared__ int abort_flag;
+    __shared__ int wait_ctl[2];   // abort flag, wait limit (ptx.cuh)
     extern __shared__ __align__(128) uint8_t ring[];   // [nsb][srw rows of row_bytes]
 
     const int K = nb * 256;
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
             mbar_init(&full[i], 1);          // the producer's expect_tx; completes on the bytes
             mbar_init(&empty[i], ncons);     // one arrival per consumer warp
         }
-        abort_flag = 0;
+        wait_ctl_init(wait_ctl, status);
         fence_mbar_init();
     }
     __syncthreads();
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
             int issued = 0;
             for (int g = 0; g < nst && !skip_all; ++g) {
                 const int sl = g % nsb;
-                if (g >= nsb && !mbar_wait(&empty[sl], ((g / nsb) - 1) & 1, &abort_flag, status, 20)) break;
+                if (g >= nsb && !mbar_wait(&empty[sl], ((g / nsb) - 1) & 1, wait_ctl, status, 20)) break;
                 const int ra = r0 + g * srw;
                 const int nr = min(srw, r1 - ra);
                 uint8_t* dst = ring + static_cast<size_t>(sl) * slot_bytes;
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
             // the copies still in flight land before the CTA may end (not cut
             // short by the abort flag)
             for (int g = issued > nsb ? issued - nsb : 0; g < issued; ++g)
-                mbar_wait_drain(&full[g % nsb], (g / nsb) & 1, status);
+                mbar_wait_drain(&full[g % nsb], (g / nsb) & 1, wait_ctl);
         }
         return;
     }
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
         const int sl = g % nsb;
         const int ra = r0 + g * srw;
         const int nr = min(srw, r1 - ra);
-        if (ok) ok = mbar_wait(&full[sl], (g / nsb) & 1, &abort_flag, status, 22);
+        if (ok) ok = mbar_wait(&full[sl], (g / nsb) & 1, wait_ctl, status, 22);
         float v[VALS];
 #pragma unroll
         for (int t = 0; t < VALS; ++t) v[t] = 0.0f;

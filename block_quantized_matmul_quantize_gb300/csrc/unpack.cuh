@@ -91,16 +91,39 @@ __device__ __forceinline__ void unpack_q4k_chunk(const uint8_t* blk, int c, uint
 // power-of-two shifted scale instead: operands sc_j*q*2^-s and m_j*r*2^-s,
 // epilogue factor e = d*2^s.  The shifted main operand stays exact: sc_j*q
 // is an integer below 2^10 and 2^-s >= 2^-14 keeps it a normal fp16.  The
-// shift s is a function of the exponents of d and dmin alone (so the unpack
-// and the side-data writer agree on it bit for bit):
+// shift is a function of the exponents of d and dmin alone (integer
+// operations on the fp16 fields, so that the unpack and the side-data writer
+// agree on it bit for bit):
 //   s = clamp(E(dmin) - E(d) - 8, 0, 14),  E = floor(log2 |x|),
-// which gives |r|*2^-s < 2^9 whenever the clamp does not bind.
-__device__ __forceinline__ int q4k_shift(float d, float dmin) {
-    if (d == 0.0f) return 0;
-    const int ed = static_cast<int>((__float_as_uint(d) >> 23) & 0xffu);
-    const int em = static_cast<int>((__float_as_uint(dmin) >> 23) & 0xffu);
-    const int s = em - ed - 8;
+// 0 when d or dmin is zero; it gives |r|*2^-s < 2^9 whenever the clamp does
+// not bind.
+__device__ __forceinline__ int h_floor_log2(uint32_t h) {   // fp16 bits, nonzero magnitude
+    const int ex = static_cast<int>((h >> 10) & 0x1fu);
+    return ex != 0 ? ex - 15 : (31 - __clz(static_cast<int>(h & 0x3ffu))) - 24;
+}
+__device__ __forceinline__ int q4k_shift_hdr(uint32_t hx) {   // hx: fp16 d in bits 0..15, dmin in 16..31
+    const uint32_t hd = hx & 0x7fffu, hm = (hx >> 16) & 0x7fffu;
+    if (hd == 0u || hm == 0u) return 0;
+    const int s = h_floor_log2(hm) - h_floor_log2(hd) - 8;
     return s < 0 ? 0 : (s > 14 ? 14 : s);
+}
+// At the largest shift the correction can still leave fp16's range: the row
+// is then declined.  Both the side-data writer (which makes its e NaN) and
+// the unpack (which records the status bit) take this decision from the same
+// fp32 arithmetic: 63 * |r * 2^-14| <= 65504, i.e. |r * 2^-14| <= 1039.
+__device__ __forceinline__ float q4k_ratio(uint32_t hx, int s) {   // r * 2^-s, d != 0
+    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hx & 0xffffu)));
+    const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hx >> 16)));
+    return (-dmin / d) * __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+}
+__device__ __forceinline__ bool q4k_in_range(int s, float ratio) { return s != 14 || fabsf(ratio) <= 1039.0f; }
+// s can be nonzero only for a subnormal d or a dmin whose exponent field is 9
+// or more above d's (d = 0 is caught here too, and gives s = 0): a test of
+// the two exponent fields, so that the usual block pays for nothing
+// more.
+__device__ __forceinline__ bool q4k_maybe_shifted(uint32_t hx) {
+    const uint32_t ed = (hx >> 10) & 0x1fu, em = (hx >> 26) & 0x1fu;
+    return ed == 0u || em >= ed + 9u;
 }
 // fp16 2^-s in both halves (0 <= s <= 14: a normal fp16)
 __device__ __forceinline__ uint32_t h2_pow2m(int s) {
@@ -108,35 +131,49 @@ __device__ __forceinline__ uint32_t h2_pow2m(int s) {
     return b | (b << 16);
 }
 
+// (e, r * 2^-s) of a block that q4k_maybe_shifted flags; (e0, r0) when its
+// shift is 0; e = NaN when the row is declined.
+static __device__ __noinline__ float2 q4k_shifted_side(uint32_t hx, float e0, float r0) {
+    const int s = q4k_shift_hdr(hx);
+    if (s == 0) return make_float2(e0, r0);
+    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hx & 0xffffu)));
+    const float ratio = q4k_ratio(hx, s);
+    const float e = q4k_in_range(s, ratio) ? d * __uint_as_float(static_cast<uint32_t>(127 + s) << 23)
+                                           : __uint_as_float(0x7fc00000u);
+    return make_float2(e, ratio);
+}
+
 // Q4_K side values of one block row, from its 16-byte header (fp16 d, fp16
-// dmin, 12 scale bytes): the epilogue factor e and the correction operands
-// a1[j] + a2[j] = m_j * r * 2^-s (fp16 hi + lo, about 22 significant bits;
-// each duplicated into both halves, one per 16-value group of sub-block j).
-// d = 0: the main operand is zeroed, e = dmin and r = -1 (exact).  Returns
-// false, with e = NaN, when m_j * r * 2^-s leaves the fp16 range even at the
-// largest shift (|dmin/d| above about 1.6e7): that row's output is declined.
-__device__ __forceinline__ bool q4k_side(uint4 hdr, uint32_t (&a1)[8], uint32_t (&a2)[8], float& e) {
+// dmin, 12 scale bytes): the epilogue factor e = d * 2^s and the correction
+// operands a1[j] + a2[j] = m_j * r * 2^-s (fp16 hi + lo, about 22
+// significant bits; each duplicated into both halves, one per 16-value group
+// of sub-block j), handed to put(j, a1[j], a2[j]).  d = 0: the main operand
+// is zeroed, e = dmin and r = -1 (exact).  A declined row (q4k_in_range) gets
+// e = NaN: its outputs become NaN rather than a wrong number.  (No status
+// write here: in the tile GEMM this runs beside 64 live accumulators at the
+// register limit; the unpack records the status bit instead.)
+template <typename Put>
+__device__ __forceinline__ void q4k_side(uint4 hdr, float& e, Put&& put) {
     const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
     const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
     const uint32_t mn03 = hdr.z & 0x3f3f3f3fu;
     const uint32_t mn47 = ((hdr.w >> 4) & 0x0f0f0f0fu) | ((hdr.z >> 2) & 0x30303030u);
     const bool main_on = (d != 0.0f);
-    const int s = q4k_shift(d, dmin);
-    e = main_on ? d * __uint_as_float(static_cast<uint32_t>(127 + s) << 23) : dmin;        // d * 2^s
-    const float ratio = main_on ? (-dmin / d) * __uint_as_float(static_cast<uint32_t>(127 - s) << 23) : -1.0f;
-    bool ok = true;
+    e = main_on ? d : dmin;
+    float ratio = main_on ? -dmin / d : -1.0f;
+    if (q4k_maybe_shifted(hdr.x)) {   // rare: e and r for the row's shift (NaN e if declined)
+        const float2 er = q4k_shifted_side(hdr.x, e, ratio);
+        e = er.x;
+        ratio = er.y;
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int mj = ((j < 4 ? mn03 : mn47) >> (8 * (j & 3))) & 0xff;
         const float v = static_cast<float>(mj) * ratio;
-        ok = ok && (fabsf(v) <= 65504.0f);
         const __half h1 = __float2half_rn(v);
         const __half h2 = __float2half_rn(v - __half2float(h1));
-        a1[j] = h2dup(h1);
-        a2[j] = h2dup(h2);
+        put(j, h2dup(h1), h2dup(h2));
     }
-    if (!ok) e = __uint_as_float(0x7fc00000u);
-    return ok;
 }
 
 // Q6_K sub-scale split.  The operand sc_j*(q - 32) is an integer of up to
@@ -292,25 +329,47 @@ __device__ __forceinline__ void unpack_ptq1_hi(const Ptq1State& st, uint32_t (&v
 // Q4_K: the scale words of chunks 0-1 (sc_0..sc_3) and 2-3 (sc_4..sc_7), zero
 // when d = 0 (the main part vanishes), and the operand scale 2^-s.
 struct Q4kScales {
-    uint32_t sc03, sc47, p2;
+    uint32_t sc03, sc47;
+    uint32_t p2;       // fp16 2^-s in both halves
+    bool shifted;      // s > 0 (rare)
+    bool declined;     // the row is out of range even at the largest shift
 };
+// The rare branches below are out of line (the tile GEMM's role loops stay
+// compact; measured on GB300, inlined they cost 4-5% on every call, not only
+// on the rare blocks).  Bits 0-4: s; bit 5: declined.
+static __device__ __noinline__ uint32_t q4k_shift_info(uint32_t hx) {
+    const int s = q4k_shift_hdr(hx);
+    const bool declined = s == 14 && (hx & 0x7fffu) != 0u && !q4k_in_range(s, q4k_ratio(hx, s));
+    return static_cast<uint32_t>(s) | (declined ? 32u : 0u);
+}
 __device__ __forceinline__ Q4kScales q4k_scales(uint4 hdr) {
-    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
-    const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
-    const bool main_on = (d != 0.0f);
+    const bool main_on = (hdr.x & 0x7fffu) != 0u;   // d != 0
     Q4kScales r;
     r.sc03 = main_on ? (hdr.y & 0x3f3f3f3fu) : 0u;
     r.sc47 = main_on ? ((hdr.w & 0x0f0f0f0fu) | ((hdr.y >> 2) & 0x30303030u)) : 0u;
-    r.p2 = h2_pow2m(q4k_shift(d, dmin));
+    r.p2 = 0x3C003C00u;   // fp16 1
+    r.shifted = false;
+    r.declined = false;
+    if (q4k_maybe_shifted(hdr.x)) {   // rare
+        const uint32_t info = q4k_shift_info(hdr.x);
+        r.p2 = h2_pow2m(static_cast<int>(info & 31u));
+        r.shifted = (info & 31u) != 0u;
+        r.declined = (info & 32u) != 0u;
+    }
     return r;
 }
 // Chunk c (its parity CI = c % 2 picks bytes 2CI, 2CI+1 of the scale word):
 // sc_j * q * 2^-s.  (The low nibbles take sc and -1024 sc, the high ones sc/16
 // and -64 sc; every factor and result is exact in fp16.)
 template <int CI>
-__device__ __forceinline__ void q4k_expand(const uint8_t* blk, int c, uint32_t scw, uint32_t p2, uint32_t (&o)[32]) {
-    const uint32_t sl = hmul2u(byte_h2<2 * CI>(scw, H2_M1024), p2);
-    const uint32_t sh = hmul2u(byte_h2<2 * CI + 1>(scw, H2_M1024), p2);
+__device__ __forceinline__ void q4k_expand(const uint8_t* blk, int c, uint32_t scw, const Q4kScales& qs4,
+                                           uint32_t (&o)[32]) {
+    uint32_t sl = byte_h2<2 * CI>(scw, H2_M1024);
+    uint32_t sh = byte_h2<2 * CI + 1>(scw, H2_M1024);
+    if (qs4.shifted) {
+        sl = hmul2u(sl, qs4.p2);
+        sh = hmul2u(sh, qs4.p2);
+    }
     unpack_q4k_chunk(blk, c, sl, hmul2u(sl, H2_M1024), hmul2u(sh, H2_1_16), hmul2u(sh, H2_M64), o);
 }
 // Q6_K chunk c, scale word scw (the chunk's four int8 sub-scales): the hi

@@ -34,23 +34,20 @@ __global__ void expand_kernel(const uint8_t* __restrict__ blocks, int64_t n, uin
         for (int c = 0; c < 4; ++c) {
             const uint32_t scw = c < 2 ? qs4.sc03 : qs4.sc47;
             if (c & 1)
-                q4k_expand<1>(blk, c, scw, qs4.p2, v);
+                q4k_expand<1>(blk, c, scw, qs4, v);
             else
-                q4k_expand<0>(blk, c, scw, qs4.p2, v);
+                q4k_expand<0>(blk, c, scw, qs4, v);
             for (int k = 0; k < 32; ++k) rec[32 * c + k] = v[k];
         }
         for (int k = 0; k < 128; ++k) rec[128 + k] = 0u;
-        uint32_t a1[8], a2[8];
         float e;
-        const bool ok = q4k_side(hdr, a1, a2, e);
-        for (int j = 0; j < 8; ++j) {
-            rec[256 + j] = a1[j];
-            rec[264 + j] = a2[j];
-        }
-        const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
-        const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
+        q4k_side(hdr, e, [&](int j, uint32_t w1, uint32_t w2) {
+            rec[256 + j] = w1;
+            rec[264 + j] = w2;
+        });
         rec[272] = __float_as_uint(e);
-        rec[273] = (ok ? 1u : 0u) | (static_cast<uint32_t>(q4k_shift(d, dmin)) << 8);
+        const bool ok = !qs4.declined;
+        rec[273] = (ok ? 1u : 0u) | (static_cast<uint32_t>(q4k_shift_hdr(hdr.x)) << 8);
     } else if constexpr (WT == 6) {
         const uint8_t* blk = blocks + i * Q6K_PACKED;
         const uint4 scv = *reinterpret_cast<const uint4*>(blk + 192);

@@ -152,12 +152,12 @@ QGEMM_API size_t qgemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * contribution of superblock b (fp32 accumulation of exact integer partials).
  * Y is deterministic for a given shape and device: a cut tile's K parts are
  * summed in ascending part order, whichever part finishes last.
- * Value range: every Q4_K block is computed except one whose correction
- * m_j*|dmin/d| exceeds fp16's range even on the largest power-of-two
- * shifted scale (m_j*|dmin/d| > 65504*2^14, e.g. d = 6e-8 with dmin >= 2):
- * such a block row is declined -- its output elements become NaN -- and
- * device status QGEMM_DEV_Q4K_RANGE is set.  (The small-M path computes
- * every block in fp32.)
+ * Value range: every Q4_K block is computed except one with |dmin/d| >
+ * 1039 * 2^14 (about 1.7e7, e.g. d = 6e-8 with dmin >= 2), whose dmin
+ * correction leaves fp16's range even on the largest power-of-two shifted
+ * scale: such a block row is declined -- its output elements become NaN --
+ * and device status QGEMM_DEV_Q4K_RANGE is set.  (The small-M path
+ * computes every block in fp32.)
  * Errors: EINVAL, EALIGN, EUNSUPPORTED (M, N >= 2^31), ECUDA. */
 QGEMM_API int qgemm_q4k(const void *w, int64_t N, int64_t K, int64_t ldw, const int8_t *xqs, const float *xd,
               const int16_t *xbsums, int64_t M, float *y, int64_t ldy, void *workspace,
@@ -344,6 +344,7 @@ QGEMM_API int qgemm_q4k_noalloc(const void *w, int64_t N, int64_t K, int64_t ldw
  *   [128, 256) Q6_K: the lo part (hi + lo = sc_j*(q - 32), both exact);
  *   [256, 272) Q4_K: the dmin-correction operands m_j*(-dmin/d)*2^-s as fp16
  *              hi (words 256..263) and lo (264..271) parts, in both halves;
+ *              s = clamp(E(dmin) - E(d) - 8, 0, 14), E = floor(log2 |x|);
  *   [272]      the epilogue factor e (fp32): Q4_K d*2^s (dmin when d = 0,
  *              NaN when declined), Q6_K d, PTQ1_0 1;
  *   [273]      bit 0: in range (not declined); bits 8..15: the Q4_K shift s.
@@ -376,7 +377,7 @@ QGEMM_API int qgemm_reset_counters(void);
 
 /* Device status word of the current device.  Bits: */
 #define QGEMM_DEV_TIMEOUT 0x1u   /* a pipeline wait gave up (bounded waits) */
-#define QGEMM_DEV_Q4K_RANGE 0x2u /* a Q4_K block row was declined (NaN output): m_j*|dmin/d| > 65504*2^14 */
+#define QGEMM_DEV_Q4K_RANGE 0x2u /* a Q4_K block row was declined (NaN output): |dmin/d| > 1039*2^14 */
 /* (0x4u is not used: Q6_K sub-scales of the whole int8 range are computed) */
 #define QGEMM_DEV_BAD_EXPERT 0x8u /* a routed GEMM id was outside [0, E)    */
 /* Synchronizes the device, returns the status bits in *bits and the site of
