@@ -17,16 +17,21 @@
 //     token rows: here TMA stages each tile once into shared memory and the
 //     single MMA-issuing thread feeds the whole tile to the tensor core.
 //   * Operands are fp16 holding exact integers: weights as sc_j*q (Q4_K,
-//     0..945) or sc_j*(q-32) (Q6_K, |.| <= 2048 for |sc_j| <= 64), tokens as
-//     the int8 q (|q| <= 127).  Products and their fp32 sums are exact while
-//     partial sums stay below 2^24, so the tensor core computes the per-
-//     superblock integer form sum_j sc_j * I_j.
+//     0..945) or sc_j*(q-32) (Q6_K), tokens as the int8 q (|q| <= 127).
+//     Q6_K's int8 sub-scales are split sc = hi + lo with lo in {0, 1} and hi
+//     even whenever |sc| > 63, so that both hi*(q-32) (|.| <= 4096, even) and
+//     lo*(q-32) are exact fp16 operands; the lo part is a second operand fed
+//     into the same accumulator, its MMAs issued only for stages where some
+//     row has one.  Products and their fp32 sums are exact while partial sums
+//     stay below 2^24, so the tensor core computes the per-superblock integer
+//     form sum_j sc_j * I_j.
 //   * The Q4_K dmin term rides along as two extra K=16 MMAs per superblock:
 //     A = the sub-mins times r = -dmin/d split into two fp16 parts (a1 + a2,
 //     about 22 significant bits), B = the 16 bsums in fp16.  The TMEM
 //     accumulator then holds  sum_j sc_j I_j - (dmin/d) sum_j m_j B_j  and the
 //     epilogue multiplies by d * dx.  (d = 0: the main part is zeroed and the
-//     multiplier is dmin with r = -1, exact.)
+//     multiplier is dmin with r = -1, exact.  A block with a very large
+//     dmin/d runs on a power-of-two shifted scale: unpack.cuh.)
 //   * Per superblock the accumulator is read once (tcgen05.ld) and folded
 //     into fp32 registers: Y += (S * d) * dx.  Two TMEM accumulators let the
 //     MMA of superblock b+1 run while the epilogue drains superblock b.
@@ -41,7 +46,8 @@
 //     the activation stream fed.
 //
 // TMEM columns: [0, 2*BM) two fp32 accumulators (superblock t uses t & 1);
-// [256, 512) four 64-column K128 stages of the weight operand.  A finished
+// [256, 512) four 64-column stages of the weight operand (K128, or for Q6_K
+// K64 hi + K64 lo).  A finished
 // tile goes out through the slot of its last superblock's accumulator, which
 // is released to the MMA only after that store.
 //
@@ -57,7 +63,8 @@
 //
 // Warp roles (16 warps for Q4_K, 20 for Q6_K and PTQ1_0, whose heavier
 // expansion has a second unpack group; persistent CTAs looping over (n-tile,
-// m-tile, split) work items with token tiles varying fastest):
+// m-tile, split) work items, token tiles varying fastest within a group of
+// token tiles that the host sizes so that its activations stay in L2):
 //   warp 0      TMA producer of the activation stages (K128 or K256 per stage,
 //               one barrier each)
 //   warps 1, 3  MMA issuers (one thread each): even / odd superblocks; warp 1
@@ -66,7 +73,8 @@
 //               per-superblock side data (bsums, dx)
 //   warps 4-7   unpack: thread = weight row; branch-free expand of each K64
 //               chunk into registers, tcgen05.st into TMEM (Q6_K, PTQ1_0:
-//               warps 4-11, group g expanding K128 step g of each superblock)
+//               warps 4-11; PTQ1_0 group g expands K128 step g of each
+//               superblock, Q6_K group g the whole superblocks t % 2 == g)
 //   last 8      epilogue: warp w reads TMEM lanes 32*(w%4).. and half of the
 //               token columns, accumulates Y in registers, stores per tile
 //               through TMEM in a rolled loop; for Q4_K the second half also
@@ -99,7 +107,7 @@ constexpr int A_STAGES = 4;    // weight-operand K128 stages in TMEM (64 columns
 constexpr int A_TMEM_COL = 256;
 constexpr int KCH = 64;        // K elements per stage
 constexpr int SB_SLOTS = 3;    // per-superblock side-data slots
-constexpr int W_PREFETCH = 6;  // raw-weight L2 prefetch distance, in superblocks
+constexpr int W_PREFETCH = 3;  // raw-weight L2 prefetch distance, in superblocks (3: measured best of 3/6/10)
 constexpr int SMEM_LIMIT = 232448;
 
 // warp roles

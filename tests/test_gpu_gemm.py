@@ -107,9 +107,9 @@ def test_short_last_round_is_cut(wtype):
 @pytest.mark.parametrize("M,N,K", [(1100, 300, 16384), (4096, 1280, 5120)])
 def test_grouped_work_order(wtype, M, N, K):
     """fp16 activations beyond 32 MiB: token tiles are taken in groups of
-    about 16 MiB (M=1100, K=16384: groups of 4, 4 and 1 token tiles, every
-    tile cut into K parts; M=4096, K=5120: groups of 12, 12 and 8, whole tiles
-    and a cut last round).  Every token tile is checked."""
+    about 32 MiB (M=1100, K=16384: groups of 8 and 1 token tiles, every tile
+    cut into K parts; M=4096, K=5120: groups of 24 and 8, whole tiles and a
+    cut last round).  Every token tile is checked."""
     assert M * K * 2 > 32 << 20
     w = weights(wtype, N, K, 90 + M)
     x = synth.gen_x(M, K, 91 + M, outlier_frac=0.01)
