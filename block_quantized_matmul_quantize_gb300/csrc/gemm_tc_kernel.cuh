@@ -173,8 +173,8 @@ struct Layout {
     static constexpr int RESERVE = 1024 /* base alignment */ + 512 /* barriers, misc */;
     static constexpr int B_STAGES = cmin(12, (SMEM_LIMIT - RESERVE - OFF_B) / B_STAGE) & ~1;
     static constexpr int OFF_BAR = OFF_B + B_STAGES * B_STAGE;
-    static constexpr int NBAR = 2 * RAW_SLOTS + 2 * A_STAGES + 2 * B_STAGES + 2 * SB_SLOTS + 4 + 1 + 2;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM address, abort and last-part flags
+    static constexpr int NBAR = 2 * RAW_SLOTS + 2 * A_STAGES + 2 * B_STAGES + 2 * SB_SLOTS + 4 + 2;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM address, wait control
     static constexpr int OFF_LOFLAG = OFF_MISC + 16;        // per weight-operand stage: a lo part was written
     static constexpr int TOTAL = OFF_LOFLAG + 4 * A_STAGES + 1024;
     static constexpr int CPT = BM / 2;                   // token columns per epilogue thread
@@ -241,12 +241,10 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     uint64_t* sb_empty = sb_full + SBN;
     uint64_t* acc_full = sb_empty + SBN;
     uint64_t* acc_empty = acc_full + 2;
-    uint64_t* epi_bar = acc_empty + 2;   // the 8 epilogue warps, for cut tiles
-    uint64_t* drain_bar = epi_bar + 1;   // [2]: each MMA thread's last commit, before the CTA ends
+    uint64_t* drain_bar = acc_empty + 2;   // [2]: each MMA thread's last commit, before the CTA ends
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
     // wait control (ptx.cuh): [0] abort flag, [1] wait limit
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 12);
     // SPLIT: byte q of word s is set by unpack warp q when it wrote a nonzero lo
     // part into stage s (before its a_full arrival; read by the issuer after the wait)
     volatile uint32_t* lo_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_LOFLAG);
@@ -343,10 +341,9 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             mbar_init(&acc_full[p], 1);
             mbar_init(&acc_empty[p], 8);
         }
-        mbar_init(epi_bar, 8);
         mbar_init(&drain_bar[0], 1);
         mbar_init(&drain_bar[1], 1);
-        wait_ctl_init(abort_flag, status);
+        wait_ctl_init(abort_flag, wk.wait);
         fence_mbar_init();
     }
     if (warp == W_PROD_X && lane == 0) tma_prefetch_desc(&tm_xh);
@@ -392,35 +389,40 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
         if (lane == 0) {
             int t = 0;
             bool ok = true;
-            // Test only (the status array's skip word): CTA 0 leaves out its
-            // first weight load, so that the waits for it run out and the
-            // kernel's timeout path is exercised without any fault.
-            const bool skip_first =
-                blockIdx.x == 0 && *reinterpret_cast<const volatile uint32_t*>(status + ST_SKIP) == ST_SKIP_TILE_WEIGHTS;
-            // L2 prefetch cursor, W_PREFETCH superblocks ahead of the loads
+            // Test only (WaitCfg): CTA 0 leaves out its first weight load, so
+            // that the waits for it run out and the kernel's timeout path is
+            // exercised without any fault.
+            const bool skip_first = blockIdx.x == 0 && wk.wait.test_skip == ST_SKIP_TILE_WEIGHTS;
+            // L2 prefetch cursor, W_PREFETCH superblocks ahead of the loads.  It
+            // starts after the first load, which nothing else then delays (on a
+            // short launch that load is on the critical path).
             int pwi = blockIdx.x, pb = 0, pb1 = 0, pn0 = 0, pm0 = 0, pk0 = 0;
-            if (pwi < num_work) work_of(pwi, pn0, pm0, pk0, pb1), pb = pk0;
-            auto prefetch_next = [&]() {
+            auto prefetch_next = [&](bool issue) {
                 if (pwi >= num_work) return;
-                tma_prefetch_l2_2d(&tm_w, sb_at(pb, pk0, pb1, pn0) * WTraits<WT>::RAW_BLOCK, pn0);
+                if (issue) tma_prefetch_l2_2d(&tm_w, sb_at(pb, pk0, pb1, pn0) * WTraits<WT>::RAW_BLOCK, pn0);
                 if (++pb >= pb1) {
                     pwi += gridDim.x;
                     if (pwi < num_work) work_of(pwi, pn0, pm0, pk0, pb1), pb = pk0;
                 }
             };
-            for (int i = 0; i < W_PREFETCH; ++i) prefetch_next();
             for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
                 int n0, m0, kb0, kb1;
                 work_of(wi, n0, m0, kb0, kb1);
                 for (int i = kb0; i < kb1; ++i, ++t) {
                     const int b = sb_at(i, kb0, kb1, n0);
-                    prefetch_next();
+                    if (t > 0) prefetch_next(true);
                     const int r = t % R;
                     ok = mbar_wait(&raw_empty[r], ((t / R) & 1) ^ 1, abort_flag, status, 3);
                     if (!ok) break;
                     if (!(skip_first && t == 0)) {
                         mbar_arrive_expect_tx(&raw_full[r], L::RAW);
                         tma_load_2d(&tm_w, &raw_full[r], raw_slot(r), b * WTraits<WT>::RAW_BLOCK, n0);
+                    }
+                    if (t == 0) {   // the cursor: past superblock 0 (loading), then W_PREFETCH ahead
+                        work_of(pwi, pn0, pm0, pk0, pb1);
+                        pb = pk0;
+                        prefetch_next(false);
+                        for (int k = 0; k < W_PREFETCH; ++k) prefetch_next(true);
                     }
                     const int p = t % SBN;
                     ok = mbar_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1, abort_flag, status, 1);
@@ -728,7 +730,6 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
         const int row = 32 * quad + lane;
         const int col0 = half * CPT;
         int t = 0;
-        uint32_t epi_phase = 0;
         bool ok = true;
         // Q4_K: the second half's four warps also write the side data of each
         // superblock (the dmin correction operands and the scale e, from the
@@ -846,43 +847,54 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             };
             if (cut >= 0) {
                 griddep_wait();   // the counters are zeroed by the preceding grid
-                // a part of a cut tile: publish the partial tile, and the part
-                // that completes the tile adds all parts (ascending) into acc
-                // (a part is stored column by column, element (row, col) at col*128 + row,
-                // so that each warp-wide store or load is one contiguous 128-B line)
+                // A part of a cut tile.  Each epilogue warp finishes its own slice
+                // of the tile (TMEM lanes 32*quad.., token columns col0..) with no
+                // other warp: it publishes its partial slice, bumps the slice's
+                // counter, and the warp that completes the slice adds all parts in
+                // ascending part order.  (A part's element (row, col) sits at
+                // col*128 + row: each warp-wide store or load is one 128-B line.)
+                int* ctr = wk.counters + cut * TC_EPI_WARPS + (warp - W_EPI0);
                 float* mine = wk.partials + (static_cast<int64_t>(cut) * wk.parts + part) * (BN * BM) +
                               col0 * BN + row;
 #pragma unroll
                 for (int j = 0; j < CPT; ++j) __stcg(mine + j * BN, acc[j]);
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(epi_bar);
-                ok = mbar_wait(epi_bar, epi_phase, abort_flag, status, 13);   // every warp's partial is out
-                epi_phase ^= 1u;
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                if (warp == W_EPI0 && lane == 0) {
-                    __threadfence();
-                    *last_flag = (atomicAdd(&wk.counters[cut], 1) == wk.parts - 1);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(epi_bar);
-                ok = mbar_wait(epi_bar, epi_phase, abort_flag, status, 14);   // the flag is set
-                epi_phase ^= 1u;
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                if (!*last_flag) {
+                int last = 0;
+                if (lane == 0) last = atomicAdd(ctr, 1) == wk.parts - 1;
+                if (!__shfl_sync(0xffffffffu, last, 0)) {
                     release_held();
                     continue;
                 }
-                // all parts, this one included, from memory in ascending order
                 __threadfence();
                 const float* base = wk.partials + static_cast<int64_t>(cut) * wk.parts * (BN * BM) + col0 * BN + row;
+                if constexpr (CPT <= 32) {
+                    // this part's own values from registers, the others from memory
+                    float sum[CPT];
 #pragma unroll
-                for (int j = 0; j < CPT; ++j) acc[j] = __ldcg(base + j * BN);
-                for (int p2 = 1; p2 < wk.parts; ++p2) {
+                    for (int j = 0; j < CPT; ++j) sum[j] = part == 0 ? acc[j] : __ldcg(base + j * BN);
+                    for (int p2 = 1; p2 < wk.parts; ++p2) {
+                        if (p2 == part) {
 #pragma unroll
-                    for (int j = 0; j < CPT; ++j) acc[j] += __ldcg(base + p2 * (BN * BM) + j * BN);
+                            for (int j = 0; j < CPT; ++j) sum[j] += acc[j];
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < CPT; ++j) sum[j] += __ldcg(base + p2 * (BN * BM) + j * BN);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < CPT; ++j) acc[j] = sum[j];
+                } else {
+                    // all parts, this one included, from memory
+#pragma unroll
+                    for (int j = 0; j < CPT; ++j) acc[j] = __ldcg(base + j * BN);
+                    for (int p2 = 1; p2 < wk.parts; ++p2) {
+#pragma unroll
+                        for (int j = 0; j < CPT; ++j) acc[j] += __ldcg(base + p2 * (BN * BM) + j * BN);
+                    }
                 }
-                if (warp == W_EPI0 && lane == 0) wk.counters[cut] = 0;   // ready for the next call
+                __syncwarp();
+                if (lane == 0) *ctr = 0;   // ready for the next call
             }
             if constexpr (STAGED) {
                 // The finished tile goes out through the TMEM slot of the item's

@@ -19,13 +19,19 @@ enum : uint32_t {
 // The status array (one per device, 8 words, 8-byte aligned):
 //   [0]     OR of the bits above;
 //   [1]     1 + the site id of the first wait that timed out (0 = none);
-//   [2..3]  the wait limit in ns (uint64; 0 = QG_WAIT_NS), set by the host;
-//   [4]     test-only: a producer that leaves out one arrival (ST_SKIP_*), so
-//           that the bounded waits behind it run out; 0 = none.
+//   [2..7]  not used.
 constexpr int ST_WORDS = 8;
-constexpr int ST_LIMIT = 2;
-constexpr int ST_SKIP = 4;
-enum : uint32_t { ST_SKIP_TILE_WEIGHTS = 1, ST_SKIP_SMALLM_STAGE = 2 };
+
+// Wait control, handed by value to every kernel with bounded waits (a kernel
+// parameter: reading it costs no memory access on the way to the first load):
+// the wait limit in microseconds (0 = QG_WAIT_NS), and a test-only switch that
+// makes one producer leave out one arrival (ST_SKIP_*; 0 = none) so that the
+// bounded waits behind it run out.
+struct WaitCfg {
+    int limit_us;
+    int test_skip;
+};
+enum : int { ST_SKIP_TILE_WEIGHTS = 1, ST_SKIP_SMALLM_STAGE = 2 };
 
 constexpr uint64_t QG_WAIT_NS = 2000000000ull;  // 2 s of wall time per wait (default)
 constexpr uint32_t QG_WAIT_ITERS = 1u << 28;    // and at most this many polls
@@ -88,10 +94,12 @@ cudaError_t launch_xgather(const int8_t* qs, const float* d, const int16_t* bsum
 // Work items of the tile GEMM: the first `full_items` tiles (token tiles
 // varying fastest) whole, then each remaining tile cut into `parts` K ranges.
 // A cut tile's parts write fp32 partial tiles to `partials` (slot = (tile -
-// full_items) * parts + part, 128 x bm floats each) and bump `counters[tile -
-// full_items]`; the part that finds all others done adds the parts in
-// ascending part order and stores Y (and resets the counter).  No atomics on
-// Y, and the result does not depend on which part finishes last.
+// full_items) * parts + part, 128 x bm floats each).  Each of the eight
+// epilogue warps owns a fixed slice of the tile and finishes it on its own: it
+// bumps `counters[(tile - full_items) * TC_EPI_WARPS + warp]`, and the warp
+// that finds the other parts' warps done adds the slice's parts in ascending
+// part order, stores Y and resets its counter.  No atomics on Y, and the
+// result does not depend on which part finishes last.
 struct TcWork {
     int n_tiles, m_tiles;
     // Work order: token tiles in groups of m_group; tile t lies in group
@@ -102,7 +110,8 @@ struct TcWork {
     int parts;            // K parts of each remaining tile (1: none)
     int items;            // full_items + (tiles - full_items) * parts
     float* partials;
-    int* counters;
+    int* counters;        // TC_MAX_CUT_TILES * TC_EPI_WARPS, zero between calls
+    WaitCfg wait;
     // Expert-routed GEMM (experts > 0): the token rows are the routed rows,
     // grouped by expert; the work list is read from device memory (written by
     // the routing kernel that precedes the GEMM).  No cut tiles in this mode.
@@ -112,7 +121,9 @@ struct TcWork {
     const int* row_end;   // [E] one past the expert's last routed row
     const int* perm;      // [rows] output row of each routed row
 };
-constexpr int TC_MAX_CUT_TILES = 1024;   // counters in a workspace
+constexpr int TC_MAX_CUT_TILES = 1024;   // cut tiles a workspace has counters for
+constexpr int TC_EPI_WARPS = 8;          // epilogue warps of the tile GEMM (a counter each per cut tile)
+constexpr int TC_COUNTERS = TC_MAX_CUT_TILES * TC_EPI_WARPS;
 
 struct TcLaunch {
     int wtype;            // 4 or 6
@@ -155,6 +166,7 @@ struct SmallLaunch {
     Epi epi;
     int sm_count;
     uint32_t* status;
+    WaitCfg wait;
 };
 bool small_supported(int wtype, int64_t M, int64_t K);
 cudaError_t launch_small(const SmallLaunch& a, cudaStream_t s);

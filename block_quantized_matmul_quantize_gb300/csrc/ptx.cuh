@@ -1,8 +1,8 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA (tensor and
 // bulk copies), tcgen05 (TMEM alloc, MMA, commit, loads, fences).
 //
-// Every wait on an mbarrier is bounded: after the wait limit (the status
-// array's limit word, default QG_WAIT_NS of wall time) or QG_WAIT_ITERS polls
+// Every wait on an mbarrier is bounded: after the wait limit (WaitCfg, a
+// kernel parameter; default QG_WAIT_NS of wall time) or QG_WAIT_ITERS polls
 // it records a timeout in the library's device status word and returns
 // false, so a broken pipeline ends the kernel instead of hanging the GPU.
 #pragma once
@@ -67,12 +67,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // On timeout: status[0] |= ST_TIMEOUT, status[1] = site + 1 (first one wins).
 // A CTA's wait control, in its shared memory: ctl[0] is the abort flag (a
 // role that gave up sets it, so that the others stop waiting at once), ctl[1]
-// the wait limit in microseconds, read once from the status array when the
-// CTA starts (0 = QG_WAIT_NS), so that no wait reads global memory.
-__device__ __forceinline__ void wait_ctl_init(volatile int* ctl, const uint32_t* status) {
-    const uint64_t lim = *reinterpret_cast<const volatile uint64_t*>(status + ST_LIMIT);
+// the wait limit in microseconds, copied from the kernel's WaitCfg parameter
+// when the CTA starts (0 = QG_WAIT_NS), so that no wait reads global memory.
+__device__ __forceinline__ void wait_ctl_init(volatile int* ctl, const WaitCfg& cfg) {
     ctl[0] = 0;
-    ctl[1] = static_cast<int>(lim / 1000u);
+    ctl[1] = cfg.limit_us;
 }
 __device__ __forceinline__ uint64_t wait_limit_ns(const volatile int* ctl) {
     const int us = ctl[1];

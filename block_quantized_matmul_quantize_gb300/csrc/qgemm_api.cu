@@ -37,12 +37,16 @@ enum { C_QUANT, C_XPREP, C_Q4K_TC, C_Q6K_TC, C_Q4K_SMALL, C_Q6K_SMALL, C_PREPACK
 // SMALL_M_MAX defaults to the measured crossover: the streaming kernel wins up
 // to 8 tokens at K = N = 5120 and at K = 4096, N = 14336.
 std::atomic<int64_t> g_opt[5] = {{qg::SMALL_M_LIMIT}, {0}, {0}, {0}, {0}};
+// the wait limit and the test-only skip switch, as the kernels take them
+qg::WaitCfg wait_cfg() {
+    return qg::WaitCfg{static_cast<int>(g_opt[QGEMM_OPT_WAIT_LIMIT_US].load()),
+                       static_cast<int>(g_opt[QGEMM_OPT_TEST_SKIP_ARRIVAL].load())};
+}
 std::atomic<cudaEvent_t> g_ev_before{nullptr}, g_ev_after{nullptr};
 
 }  // namespace
 
-// Device status: [0] = bits, [1] = 1 + site of the first timed-out wait,
-// [2..3] = the wait limit (ns, 0 = default), [4] = the test-only skip switch.
+// Device status: [0] = bits, [1] = 1 + site of the first timed-out wait.
 __device__ __align__(8) uint32_t g_qgemm_status[qg::ST_WORDS];
 
 namespace {
@@ -202,7 +206,7 @@ size_t plane_bytes(int64_t M, int64_t K) {
     const int64_t nb = K / 256, Mp = (M + 3) / 4 * 4;
     return align256(size_t(M) * K * 2) + align256(size_t(M) * (K / 16) * 2) + align256(size_t(nb) * Mp * 4);
 }
-constexpr size_t COUNTER_BYTES = qg::TC_MAX_CUT_TILES * sizeof(int);
+constexpr size_t COUNTER_BYTES = qg::TC_COUNTERS * sizeof(int);
 
 size_t partial_bytes(const Plan& p) {
     const int64_t cut = static_cast<int64_t>(p.work.n_tiles) * p.work.m_tiles - p.work.full_items;
@@ -292,6 +296,7 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
     a.work = pl.work;
     a.work.counters = wp.counters;
     a.work.partials = wp.partials;
+    a.work.wait = wait_cfg();
     a.sm_count = ds->sm_count;
     a.y = y;
     a.ldy = ldy;
@@ -333,6 +338,7 @@ int run_small(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const
     a.epi = epi;
     a.sm_count = ds->sm_count;
     a.status = ds->status;
+    a.wait = wait_cfg();
     cudaEvent_t evb = g_ev_before.load(), eva = g_ev_after.load();
     if (evb) cudaEventRecord(evb, stream);
     cudaError_t e = qg::launch_small(a, stream);
@@ -447,6 +453,7 @@ int run_id(int wtype, const void* w, int64_t E, int64_t N, int64_t K, int64_t ld
     a.work.row_off = iw.row_off;
     a.work.row_end = iw.row_end;
     a.work.perm = iw.perm;
+    a.work.wait = wait_cfg();
     a.sm_count = ds->sm_count;
     a.y = y;
     a.ldy = ldy;
@@ -858,21 +865,6 @@ int qgemm_set_option(int option, int64_t value) {
     if (option == QGEMM_OPT_WAIT_LIMIT_US && value > 10000000)
         return fail(QGEMM_EINVAL, "WAIT_LIMIT_US must be 0..10000000 (10 s)");
     if (option == QGEMM_OPT_TEST_SKIP_ARRIVAL && value > 2) return fail(QGEMM_EINVAL, "TEST_SKIP_ARRIVAL must be 0..2");
-    if (option == QGEMM_OPT_WAIT_LIMIT_US || option == QGEMM_OPT_TEST_SKIP_ARRIVAL) {
-        // these two live in the current device's status array, read by the kernels
-        DevState* ds = nullptr;
-        int rc = device_state(&ds);
-        if (rc) return rc;
-        cudaError_t e;
-        if (option == QGEMM_OPT_WAIT_LIMIT_US) {
-            const uint64_t ns = static_cast<uint64_t>(value) * 1000u;
-            e = cudaMemcpyToSymbol(g_qgemm_status, &ns, sizeof(ns), qg::ST_LIMIT * sizeof(uint32_t));
-        } else {
-            const uint32_t v = static_cast<uint32_t>(value);
-            e = cudaMemcpyToSymbol(g_qgemm_status, &v, sizeof(v), qg::ST_SKIP * sizeof(uint32_t));
-        }
-        if (e != cudaSuccess) return cuda_fail(e, "writing a device option");
-    }
     g_opt[option] = value;
     return QGEMM_OK;
 }

@@ -39,7 +39,7 @@ struct PrepOut {
     __half* xbs;   // [M][K/16] fp16
     float* dxT;    // [K/256][Mp] fp32, rows m >= M zero
     int64_t Mp;
-    int* counters; // TC_MAX_CUT_TILES split-tile counters, zeroed
+    int* counters; // TC_COUNTERS cut-tile counters, zeroed
 };
 
 // round-half-away(x / d) of one element, by the IEEE definition: x / d
@@ -76,6 +76,11 @@ __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* 
                                                                   float* __restrict__ dout,
                                                                   int16_t* __restrict__ bsums, PrepOut prep) {
     allow_dependent_launch();
+    if constexpr (PREP) {
+        // (by every thread of block 0, before any warp without a chunk leaves)
+        if (blockIdx.x == 0)
+            for (int i = threadIdx.x; i < TC_COUNTERS; i += blockDim.x) prep.counters[i] = 0;
+    }
     const int lane = threadIdx.x & 31;
     const int64_t nb = K >> 8;
     int64_t m, b;
@@ -143,8 +148,6 @@ __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* 
         if ((lane & 1) == 0) prep.xbs[m * (K >> 4) + b * 16 + (lane >> 1)] = __int2half_rn(s);
         if (lane == 0) prep.dxT[b * prep.Mp + m] = d;
         if (m == M - 1 && lane >= 1 && lane < 4 && m + lane < prep.Mp) prep.dxT[b * prep.Mp + m + lane] = 0.0f;
-        if (blockIdx.x == 0)
-            for (int i = threadIdx.x; i < TC_MAX_CUT_TILES; i += blockDim.x) prep.counters[i] = 0;
     }
 }
 
@@ -158,7 +161,7 @@ __global__ void xprep_kernel(const int8_t* __restrict__ qs, const float* __restr
                              int* __restrict__ counters) {
     allow_dependent_launch();
     if (blockIdx.x == 0)
-        for (int i = threadIdx.x; i < TC_MAX_CUT_TILES; i += blockDim.x) counters[i] = 0;
+        for (int i = threadIdx.x; i < TC_COUNTERS; i += blockDim.x) counters[i] = 0;
     const int64_t nb = K >> 8;
     const int64_t n16 = M * (K >> 4);                 // 16-element groups of qs (= number of bsums)
     const int64_t ndx = nb * Mp;

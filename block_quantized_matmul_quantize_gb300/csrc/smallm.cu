@@ -105,7 +105,8 @@ template <int WT, int MT>
 __global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
     smallm_kernel(const uint8_t* __restrict__ w, int64_t ldw, int N, int nb, const int8_t* __restrict__ xqs,
                   const float* __restrict__ xd, const int16_t* __restrict__ xbs, void* __restrict__ y,
-                  int64_t ldy, const Epi epi, int wpr, int rl, int rps, int nsb, uint32_t* status) {
+                  int64_t ldy, const Epi epi, int wpr, int rl, int rps, int nsb, uint32_t* status,
+                  const WaitCfg wcfg) {
     constexpr int BLK = SmallTraits<WT>::BLOCK;
     constexpr int P = pow2_at_least(MT);          // token slots per row
     constexpr int R = small_stage_rows(WT, MT);   // rows per row lane and stage, at most
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
             mbar_init(&full[i], 1);          // the producer's expect_tx; completes on the bytes
             mbar_init(&empty[i], ncons);     // one arrival per consumer warp
         }
-        wait_ctl_init(wait_ctl, status);
+        wait_ctl_init(wait_ctl, wcfg);
         fence_mbar_init();
     }
     __syncthreads();
@@ -141,10 +142,9 @@ __global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
         // not depend on the preceding grid: no wait for it here, so with a
         // programmatic dependent launch they stream while it finishes.
         if (lane == 0) {
-            // Test only (the status array's skip word): CTA 0 issues no stage,
-            // so that its consumers' waits run out (and nothing is in flight).
-            const bool skip_all =
-                blockIdx.x == 0 && *reinterpret_cast<const volatile uint32_t*>(status + ST_SKIP) == ST_SKIP_SMALLM_STAGE;
+            // Test only (WaitCfg): CTA 0 issues no stage, so that its
+            // consumers' waits run out (and nothing is in flight).
+            const bool skip_all = blockIdx.x == 0 && wcfg.test_skip == ST_SKIP_SMALLM_STAGE;
             int issued = 0;
             for (int g = 0; g < nst && !skip_all; ++g) {
                 const int sl = g % nsb;
@@ -360,7 +360,7 @@ cudaError_t launch_dependent(void (*kernel)(Params...), int grid, int threads, s
 template <int WT>
 cudaError_t launch_small_wt(const uint8_t* w, int64_t ldw, int N, int nb, const int8_t* xqs, const float* xd,
                             const int16_t* xbs, int M, void* y, int64_t ldy, const Epi& epi, int sm_count,
-                            uint32_t* status, cudaStream_t st) {
+                            uint32_t* status, const WaitCfg& wcfg, cudaStream_t st) {
     const int wpr = (nb + 3) / 4;   // warps per row lane
     if (wpr < 1 || wpr > SM_MAX_WPR || sm_count < 1) return cudaErrorInvalidValue;
     const int grid = sm_count < N ? sm_count : N;   // one CTA per SM
@@ -381,7 +381,7 @@ cudaError_t launch_small_wt(const uint8_t* w, int64_t ldw, int N, int nb, const 
         cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(k), SM_RING_BYTES);             \
         if (e != cudaSuccess) return e;                                                                 \
         return launch_dependent(k, grid, 32 * (rl * wpr + 1), static_cast<size_t>(nsb) * slot, st, w, ldw, N, \
-                                nb, xqs, xd, xbs, y, ldy, epi, wpr, rl, rps, nsb, status);              \
+                                nb, xqs, xd, xbs, y, ldy, epi, wpr, rl, rps, nsb, status, wcfg);        \
     }
     switch (M) {
         QG_SMALL_CASE(1)
@@ -411,9 +411,9 @@ cudaError_t launch_small(const SmallLaunch& a, cudaStream_t st) {
     const uint8_t* w = static_cast<const uint8_t*>(a.w);
     if (a.wtype == 4)
         return launch_small_wt<4>(w, a.ldw, static_cast<int>(a.N), nb, a.xqs, a.xd, a.xbs, static_cast<int>(a.M),
-                                  a.y, a.ldy, a.epi, a.sm_count, a.status, st);
+                                  a.y, a.ldy, a.epi, a.sm_count, a.status, a.wait, st);
     return launch_small_wt<6>(w, a.ldw, static_cast<int>(a.N), nb, a.xqs, a.xd, a.xbs, static_cast<int>(a.M), a.y,
-                              a.ldy, a.epi, a.sm_count, a.status, st);
+                              a.ldy, a.epi, a.sm_count, a.status, a.wait, st);
 }
 
 }  // namespace qg

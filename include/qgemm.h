@@ -397,16 +397,16 @@ typedef enum {
     /* The limit of every pipeline wait in the kernels, in microseconds (0 =
      * the default of 2 s; at most 10 s).  A wait that runs out records
      * QGEMM_DEV_TIMEOUT and its site, its CTA stops without writing its
-     * outputs, and qgemm_get_device_status returns QGEMM_ETIMEOUT.  Written
-     * into the current device's copy (a synchronous copy); set it while no
-     * call of this library runs on that device. */
+     * outputs, and qgemm_get_device_status returns QGEMM_ETIMEOUT.  Read
+     * by each call when it launches its kernels (a kernel parameter): it
+     * applies to the calls made after it is set, on every device. */
     QGEMM_OPT_WAIT_LIMIT_US = 3,
     /* Test only: make the waits run out without any fault.  1: the tile
      * GEMM's first CTA leaves out its first weight load; 2: the small-M
      * kernel's first CTA issues no weight stage.  The waits behind the left-
      * out copy run out after the wait limit, the CTA's other roles give up
      * at once, and that CTA's output tiles are left unwritten; the other
-     * CTAs finish normally.  0 (default): off.  Current device, as above.
+     * CTAs finish normally.  0 (default): off.  Taken at launch, as above.
      * After a timeout, a workspace filled by qgemm_quantize_q8k_prep must be
      * filled again before another _prepared call (its cut-tile counters may
      * be left nonzero); the other calls prepare their workspace themselves. */

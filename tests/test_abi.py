@@ -172,7 +172,7 @@ def test_size_queries(L):
     assert L.qgemm_workspace_bytes(4, 8, 300) == 0
     M, K = 5, 512
     # xh fp16 5*512*2 = 5120; bsums fp16 5*32*2 = 320 -> 512; d^T fp32 2*8*4 = 64 -> 256
-    expect = 5120 + 512 + 256 + 4096   # + the cut-tile counters; one tile: no partial tiles
+    expect = 5120 + 512 + 256 + 1024 * 8 * 4   # + the cut-tile counters (8 per tile); one tile: no partial tiles
     assert L.qgemm_workspace_bytes(M, 8, K) == expect
     assert L.qgemm_q6k_packed_bytes(3, 512) == 3 * 2 * 224
     assert L.qgemm_q6k_packed_bytes(3, 100) == 0
