@@ -1,10 +1,12 @@
 #!/usr/bin/env python
 """Benchmark of the k-quant prefill matmul on one GB300 (or N replicas).
 
-One step = the whole hot path on one batch: quantize fp32 activations to Q8_K
-(qgemm_quantize_q8k_prep, which also writes the tile GEMM's fp16 operand
-planes), then the Q4_K x Q8_K GEMM (qgemm_q4k_prepared: the tcgen05 tile
-GEMM, or for M <= 8 the small-M streaming kernel).  Default workload: the
+One step = the whole hot path on one batch, one call (qgemm_q4k_f32): fp32
+activations quantized to Q8_K, then the Q4_K x Q8_K GEMM.  Above the small-M
+path the quantizer also writes the tile GEMM's fp16 operand planes and the
+tcgen05 tile GEMM starts under it; for M <= 8 the small-M streaming kernel
+runs, and for M <= 2 it quantizes the activations itself (one launch).
+Routed and PTQ1_0 workloads call their own entry points.  Default workload: the
 largest configuration, the Q4_K sweep point M = 8192 tokens, K = N = 5120,
 X ~ N(0,1); synthetic, seeded (synth.py).  --workload picks another.
 
@@ -380,12 +382,13 @@ def main():
             qg.qgemm_quantize_q8k_prep(xin, ws, out=q)
             qg.qgemm_ptq1_prepared(w, N, K, q, ws, y=yout)
             return
-        # quantize, writing the GEMM's operand planes in the same launch, then multiply
-        qg.qgemm_quantize_q8k_prep(xin, ws, out=q)
+        # fp32 X in, Y out, one call: for M <= 2 one launch (the small-M kernel
+        # quantizes X itself), else the quantizer (writing the GEMM's operand
+        # planes in the same launch) and the GEMM started under it
         if wl.wtype == 4:
-            qg.qgemm_q4k_prepared(w, N, K, q, ws, y=yout)
+            qg.qgemm_q4k_f32(w, N, K, xin, out=q, y=yout, workspace=ws)
         else:
-            qg.qgemm_q6k_prepared(w, N, K, q, ws, y=yout)
+            qg.qgemm_q6k_f32(w, N, K, xin, out=q, y=yout, workspace=ws)
 
     def step():
         step_on(x, y, ids if is_routed else None)

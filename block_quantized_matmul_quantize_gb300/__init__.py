@@ -41,7 +41,7 @@ class QgemmError(RuntimeError):
 class _Counters(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
                 ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small", "q6k_prepack", "split_k",
-                 "routed", "ptq1_tc", "ptq1_prepack")]
+                 "routed", "ptq1_tc", "ptq1_prepack", "small_fused")]
 
 
 class _Epilogue(ctypes.Structure):
@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
             "qgemm_q6k": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
             "qgemm_quantize_q8k_prep": ([vp, i64, i64, i64, vp, vp, vp, vp, sz, vp], i32),
             "qgemm_q4k_prepared": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
+            "qgemm_q4k_f32": ([vp, i64, i64, i64, vp, i64, i64, vp, vp, vp, vp, i64, vp, sz, vp], i32),
+            "qgemm_q6k_f32": ([vp, i64, i64, vp, i64, i64, vp, vp, vp, vp, i64, vp, sz, vp], i32),
             "qgemm_q6k_prepared": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
             "qgemm_id_workspace_bytes": ([i64, i64, i64, i64], sz),
             "qgemm_q4k_id": ([vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, i64, vp, sz, vp], i32),
@@ -281,6 +283,43 @@ def qgemm_quantize_q8k_prep(x: torch.Tensor, workspace: torch.Tensor, out: Q8K |
     _check(lib().qgemm_quantize_q8k_prep(_ptr(x, True), M, K, x.stride(0), _ptr(out.qs), _ptr(out.d), _ptr(out.bsums),
                                          _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
+
+
+def qgemm_q4k_f32(w: torch.Tensor, N: int, K: int, x: torch.Tensor, out: Q8K | None = None,
+                  y: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y[M, N] = Q8_K(x) @ W_q4k^T from fp32 x [M, K]; the Q8_K planes of x go
+    to `out` (allocated if None).  The workspace is needed only above the
+    small-M path (allocated if None)."""
+    assert w.dtype == torch.uint8 and w.dim() == 2 and w.stride(1) == 1
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    M = x.shape[0]
+    dev = _device_of(x)
+    if out is None:
+        out = Q8K.empty(M, K, dev)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    workspace = _workspace(M, N, K, workspace, dev)
+    _check(lib().qgemm_q4k_f32(_ptr(w), N, K, w.stride(0), _ptr(x, True), x.stride(0), M, _ptr(out.qs), _ptr(out.d),
+                               _ptr(out.bsums), _ptr(y, True), y.stride(0), _ptr(workspace), workspace.numel(),
+                               _stream(stream)))
+    return y
+
+
+def qgemm_q6k_f32(w_packed: torch.Tensor, N: int, K: int, x: torch.Tensor, out: Q8K | None = None,
+                  y: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """qgemm_q4k_f32 for repacked Q6_K weights."""
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    M = x.shape[0]
+    dev = _device_of(x)
+    if out is None:
+        out = Q8K.empty(M, K, dev)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    workspace = _workspace(M, N, K, workspace, dev)
+    _check(lib().qgemm_q6k_f32(_ptr(w_packed), N, K, _ptr(x, True), x.stride(0), M, _ptr(out.qs), _ptr(out.d),
+                               _ptr(out.bsums), _ptr(y, True), y.stride(0), _ptr(workspace), workspace.numel(),
+                               _stream(stream)))
+    return y
 
 
 def qgemm_q4k_prepared(w: torch.Tensor, N: int, K: int, x: Q8K, workspace: torch.Tensor,

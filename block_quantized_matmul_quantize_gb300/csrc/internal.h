@@ -153,14 +153,26 @@ cudaError_t launch_gemm_tc_routed(const TcLaunch& a, cudaStream_t s);
 // Small-M streaming path (smallm.cu): M <= SMALL_M_LIMIT tokens, reads the
 // Q8_K planes directly (no workspace).
 constexpr int SMALL_M_LIMIT = 8;
+// The small-M kernel's activations: the Q8_K planes, or (fused: x non-null)
+// fp32 X, which the kernel quantizes itself and also stores as Q8_K planes
+// (oqs, od, obs).
+struct SmallAct {
+    const int8_t* xqs;
+    const float* xd;
+    const int16_t* xbs;
+    const float* x;       // fp32 [M][ldx], 16-byte aligned rows (fused)
+    int64_t ldx;
+    int8_t* oqs;
+    float* od;
+    int16_t* obs;
+};
+constexpr int SMALL_FUSED_M_MAX = 2;   // tokens the small-M kernel quantizes itself, at most
 struct SmallLaunch {
     int wtype;            // 4 or 6 (Q6_K: the 224-B repacked blocks)
     int64_t M, N, K;
     const void* w;
     int64_t ldw;          // bytes between weight rows (multiple of 16)
-    const int8_t* xqs;
-    const float* xd;
-    const int16_t* xbs;
+    SmallAct act;
     void* y;              // element type per epi.out
     int64_t ldy;          // in elements
     Epi epi;

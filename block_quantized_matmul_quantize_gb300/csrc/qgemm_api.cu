@@ -31,9 +31,9 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ------------------------------------------------------------ global state
-std::atomic<uint64_t> g_cnt[11];
+std::atomic<uint64_t> g_cnt[12];
 enum { C_QUANT, C_XPREP, C_Q4K_TC, C_Q6K_TC, C_Q4K_SMALL, C_Q6K_SMALL, C_PREPACK, C_SPLITK, C_ROUTED, C_PTQ1_TC,
-       C_PTQ1_PREPACK };
+       C_PTQ1_PREPACK, C_SMALL_FUSED };
 // SMALL_M_MAX defaults to the measured crossover: the streaming kernel wins up
 // to 8 tokens at K = N = 5120 and at K = 4096, N = 14336.
 std::atomic<int64_t> g_opt[5] = {{qg::SMALL_M_LIMIT}, {0}, {0}, {0}, {0}};
@@ -330,9 +330,9 @@ int run_small(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const
     a.K = K;
     a.w = w;
     a.ldw = ldw;
-    a.xqs = xqs;
-    a.xd = xd;
-    a.xbs = xbsums;
+    a.act.xqs = xqs;
+    a.act.xd = xd;
+    a.act.xbs = xbsums;
     a.y = y;
     a.ldy = ldy;
     a.epi = epi;
@@ -352,6 +352,40 @@ int run_small(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const
 // streaming kernel up to QGEMM_OPT_SMALL_M_MAX tokens, the tile GEMM above.
 bool use_small(int wtype, int64_t M, int64_t K) {
     return M <= g_opt[QGEMM_OPT_SMALL_M_MAX].load() && qg::small_supported(wtype, M, K);
+}
+
+// Small-M path with the quantizer fused in: the kernel quantizes fp32 X
+// itself (and stores the Q8_K planes); one launch.
+int run_small_fused(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const float* x, int64_t ldx,
+                    int8_t* qs, float* d, int16_t* bsums, int64_t M, float* y, int64_t ldy, cudaStream_t stream) {
+    DevState* ds = nullptr;
+    int rc = device_state(&ds);
+    if (rc) return rc;
+    qg::SmallLaunch a{};
+    a.wtype = wtype;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.w = w;
+    a.ldw = ldw;
+    a.act.x = x;
+    a.act.ldx = ldx;
+    a.act.oqs = qs;
+    a.act.od = d;
+    a.act.obs = bsums;
+    a.y = y;
+    a.ldy = ldy;
+    a.sm_count = ds->sm_count;
+    a.status = ds->status;
+    a.wait = wait_cfg();
+    cudaEvent_t evb = g_ev_before.load(), eva = g_ev_after.load();
+    if (evb) cudaEventRecord(evb, stream);
+    cudaError_t e = qg::launch_small(a, stream);
+    if (eva) cudaEventRecord(eva, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "small-M (fused quantizer) launch");
+    g_cnt[wtype == 4 ? C_Q4K_SMALL : C_Q6K_SMALL]++;
+    g_cnt[C_SMALL_FUSED]++;
+    return QGEMM_OK;
 }
 
 // ---- routed GEMM (MUL_MAT_ID): workspace = routing arrays, then the operand
@@ -662,6 +696,56 @@ int qgemm_quantize_q8k_prep(const float* x, int64_t M, int64_t K, int64_t ldx, i
     return QGEMM_OK;
 }
 
+// fp32 activations in, Y out: the fused small-M kernel for the fewest tokens,
+// else the quantizer (writing the tile GEMM's operand planes for M above the
+// small-M path) and the GEMM.
+static int run_f32(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const float* x, int64_t ldx,
+                   int8_t* qs, float* d, int16_t* bsums, int64_t M, float* y, int64_t ldy, void* workspace,
+                   size_t workspace_bytes, qgemm_stream_t stream) {
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (use_small(wtype, M, K)) {
+        if (M <= qg::SMALL_FUSED_M_MAX) return run_small_fused(wtype, w, N, K, ldw, x, ldx, qs, d, bsums, M, y, ldy, st);
+        const cudaError_t e = qg::launch_quantize_q8k(x, M, K, ldx, qs, d, bsums, st);
+        if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+        g_cnt[C_QUANT]++;
+        return run_small(wtype, w, N, K, ldw, qs, d, bsums, M, y, ldy, st);
+    }
+    int rc = qgemm_quantize_q8k_prep(x, M, K, ldx, qs, d, bsums, workspace, workspace_bytes, stream);
+    if (rc) return rc;
+    return run_tc(wtype, w, N, K, ldw, qs, d, bsums, M, y, ldy, workspace, workspace_bytes, st, true);
+}
+
+static int f32_checks(const float* x, int64_t ldx, int64_t M, int64_t K) {
+    if (M == 0) return QGEMM_OK;
+    if (!x) return fail(QGEMM_EINVAL, "x is null");
+    if (ldx < K) return fail(QGEMM_EINVAL, "ldx (%lld) < K (%lld)", (long long)ldx, (long long)K);
+    if (!aligned(x, 16) || ldx % 4 != 0) return fail(QGEMM_EALIGN, "x must be 16-byte aligned with ldx % 4 == 0");
+    return QGEMM_OK;
+}
+
+int qgemm_q4k_f32(const void* w, int64_t N, int64_t K, int64_t ldw, const float* x, int64_t ldx, int64_t M,
+                  int8_t* qs, float* d, int16_t* bsums, float* y, int64_t ldy, void* workspace,
+                  size_t workspace_bytes, qgemm_stream_t stream) {
+    clear_err();
+    int rc = gemm_common_checks(w, N, K, qs, d, bsums, M, y, ldy);
+    if (rc || M == 0) return rc;
+    if ((rc = f32_checks(x, ldx, M, K))) return rc;
+    if (ldw < (K / 256) * qg::Q4K_BLOCK) return fail(QGEMM_EINVAL, "ldw smaller than a row of Q4_K blocks");
+    if (ldw % 16 != 0) return fail(QGEMM_EALIGN, "ldw must be a multiple of 16 bytes");
+    return run_f32(4, w, N, K, ldw, x, ldx, qs, d, bsums, M, y, ldy, workspace, workspace_bytes, stream);
+}
+
+int qgemm_q6k_f32(const void* w_packed, int64_t N, int64_t K, const float* x, int64_t ldx, int64_t M, int8_t* qs,
+                  float* d, int16_t* bsums, float* y, int64_t ldy, void* workspace, size_t workspace_bytes,
+                  qgemm_stream_t stream) {
+    clear_err();
+    int rc = gemm_common_checks(w_packed, N, K, qs, d, bsums, M, y, ldy);
+    if (rc || M == 0) return rc;
+    if ((rc = f32_checks(x, ldx, M, K))) return rc;
+    const int64_t ldw = (K / 256) * qg::Q6K_PACKED;
+    return run_f32(6, w_packed, N, K, ldw, x, ldx, qs, d, bsums, M, y, ldy, workspace, workspace_bytes, stream);
+}
+
 int qgemm_q4k_prepared(const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs, const float* xd,
                        const int16_t* xbsums, int64_t M, float* y, int64_t ldy, const void* workspace,
                        size_t workspace_bytes, qgemm_stream_t stream) {
@@ -755,6 +839,7 @@ int qgemm_get_counters(qgemm_counters* out) {
     out->routed = g_cnt[C_ROUTED];
     out->ptq1_tc = g_cnt[C_PTQ1_TC];
     out->ptq1_prepack = g_cnt[C_PTQ1_PREPACK];
+    out->small_fused = g_cnt[C_SMALL_FUSED];
     return QGEMM_OK;
 }
 

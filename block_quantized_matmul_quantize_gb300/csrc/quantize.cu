@@ -1,21 +1,16 @@
 // quantize.cu -- fp32 activations -> Q8_K, plus the small HBM-bound helper
 // kernels around the GEMM (operand preparation, Q6_K repacking).
 //
-// Q8_K, as the library defines it (the block the pages call "BlockQ8_K,
-// 292 B / 256 elements", vllm.cpp PR #3036, commit 4): per 256-element chunk
-// of a row, d = amax/127 (fp32), q = round-half-away-from-zero(x/d) clamped to
-// +-127, and 16 int16 sums of each 16 consecutive q.  d = 0 (amax = 0, or
-// amax/127 underflowing to zero) gives all-zero q and sums.  Stored as three
-// planes (qs [M][K] int8, d [M][K/256] fp32, bsums [M][K/16] int16) so that
-// every plane row is 16-byte aligned.
-//
-// Numerics: x/d and amax/127 are IEEE fp32 divisions, correctly rounded (the
-// library is built without fast-math; -prec-div=true), and roundf rounds
-// halves away from zero, so the int8 values, scales and sums are bit-exact
-// with any IEEE implementation of the same definition.
+// Q8_K (q8k.cuh): per 256-element chunk of a row, d = amax/127 (fp32), q =
+// round-half-away-from-zero(x/d) clamped to +-127, and 16 int16 sums of each
+// 16 consecutive q.  Stored as three planes (qs [M][K] int8, d [M][K/256]
+// fp32, bsums [M][K/16] int16) so that every plane row is 16-byte aligned.
+// The int8 values, scales and sums are bit-exact with any IEEE implementation
+// of the same definition.
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "q8k.cuh"
 
 namespace {
 // The kernel that follows in the stream (the tile GEMM, launched as a
@@ -41,31 +36,6 @@ struct PrepOut {
     int64_t Mp;
     int* counters; // TC_COUNTERS cut-tile counters, zeroed
 };
-
-// round-half-away(x / d) of one element, by the IEEE definition: x / d
-// correctly rounded, then halves away from zero, clamped to +-127.
-__device__ __forceinline__ int q8_exact(float x, float d) {
-    const float r = fminf(fmaxf(roundf(x / d), -127.0f), 127.0f);
-    return static_cast<int>(r);
-}
-
-// The same value for a normal d (d >= 2^-126), cheaper: r = x * RN(1/d) is
-// within 2^-23 * |x/d| <= 1.52e-5 of x/d, and the correctly rounded x / d
-// within 7.6e-6 of it, so they round to the same integer unless r lies
-// within 2.3e-5 of a half-integer.  a = |r| + 0.5 is rounded by at most
-// 2^-18, so if a is more than 2^-14 from an integer, floor(a) is that
-// integer and the result equals q8_exact; otherwise q8_exact decides (about
-// one element in 10^4 of normal data).  |r| <= 127.00002 needs no clamp.
-// (Products and sums with the _rn intrinsics: no contraction into an FMA.)
-__device__ __forceinline__ int q8_fast(float x, float y, float d) {
-    constexpr float TH = 6.103515625e-05f;   // 2^-14
-    const float r = __fmul_rn(x, y);
-    const float a = __fadd_rn(fabsf(r), 0.5f);
-    const int qa = __float2int_rz(a);
-    const float t = __fsub_rn(a, __int2float_rn(qa));
-    if (t < TH || t > 1.0f - TH) return q8_exact(x, d);
-    return r < 0.0f ? -qa : qa;
-}
 
 // One warp per 256-element chunk: each lane owns 8 consecutive elements
 // (two 16-byte loads), so one chunk is one coalesced 1 KiB read.  The chunk
@@ -109,21 +79,7 @@ __global__ void __launch_bounds__(QWARPS * 32) quantize_q8k_kernel(const float* 
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
 
     int q[8];
-    const float d = amax / 127.0f;
-    if (d >= 1.17549435e-38f) {
-        // a normal scale (the usual case): one reciprocal per lane
-        const float y = __frcp_rn(d);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = q8_fast(v[i], y, d);
-    } else if (d == 0.0f) {
-        // amax == 0, or amax/127 underflows to zero: the chunk quantizes to zero
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = 0;
-    } else {
-        // a subnormal scale: the division itself
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = q8_exact(v[i], d);
-    }
+    const float d = q8k_quantize<8>(v, amax, q);
     uint2 packed;
     packed.x = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) | (static_cast<uint32_t>(q[3] & 0xff) << 24);
     packed.y = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) | (static_cast<uint32_t>(q[7] & 0xff) << 24);

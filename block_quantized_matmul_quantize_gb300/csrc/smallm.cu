@@ -44,6 +44,7 @@
 #include "internal.h"
 #include "epilogue.cuh"
 #include "ptx.cuh"
+#include "q8k.cuh"
 
 namespace qg {
 namespace {
@@ -70,6 +71,8 @@ __host__ __device__ constexpr int pow2_at_least(int m) { return m <= 1 ? 1 : m <
 // Consumer warps per CTA at most, by token count: the activations of MT
 // tokens live in registers (8*MT words + 2*MT bsums + MT scales per lane).
 __host__ __device__ constexpr int small_max_warps(int mt) { return mt <= 2 ? 20 : mt <= 4 ? 16 : 15; }
+// shared memory of the fused path's quantized activations: int8 [M][K], then fp32 d [M][K/256]
+__host__ __device__ constexpr int small_act_bytes(int mt, int nb) { return mt * nb * 256 + mt * nb * 4; }
 // Rows per row lane and stage, at most: the stage's R x pow2(MT) outputs of
 // a warp are reduced in one pass (at most 16 values per lane).
 __host__ __device__ constexpr int small_stage_rows(int wt, int mt) {
@@ -101,12 +104,12 @@ __device__ __forceinline__ void row_lane_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-template <int WT, int MT>
+// FUSED: the kernel quantizes its activations itself, from fp32 X (below).
+template <int WT, int MT, bool FUSED>
 __global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
-    smallm_kernel(const uint8_t* __restrict__ w, int64_t ldw, int N, int nb, const int8_t* __restrict__ xqs,
-                  const float* __restrict__ xd, const int16_t* __restrict__ xbs, void* __restrict__ y,
-                  int64_t ldy, const Epi epi, int wpr, int rl, int rps, int nsb, uint32_t* status,
-                  const WaitCfg wcfg) {
+    smallm_kernel(const uint8_t* __restrict__ w, int64_t ldw, int N, int nb, const SmallAct act,
+                  void* __restrict__ y, int64_t ldy, const Epi epi, int wpr, int rl, int rps, int nsb,
+                  uint32_t* status, const WaitCfg wcfg) {
     constexpr int BLK = SmallTraits<WT>::BLOCK;
     constexpr int P = pow2_at_least(MT);          // token slots per row
     constexpr int R = small_stage_rows(WT, MT);   // rows per row lane and stage, at most
@@ -198,24 +201,88 @@ __global__ void __launch_bounds__(32 * (small_max_warps(MT) + 1), 1)
     uint32_t xa[MT][4], xb[MT][4];
     int bsa[MT], bsb[MT];
     float dx[MT];
+    if constexpr (FUSED) {
+        // Quantized here, from fp32 X, once per CTA: the consumer warps take
+        // the M * nb chunks of 256 values in turn (a lane 8 values, as in the
+        // quantizer kernel, with its arithmetic: q8k.cuh, so the values are
+        // those qgemm_quantize_q8k writes) into shared memory after the ring;
+        // CTA 0 also stores them as the Q8_K planes.  Then every lane reads
+        // its slices, and its two group sums are dp4a against ones.
+        int8_t* sq = reinterpret_cast<int8_t*>(ring + static_cast<size_t>(nsb) * slot_bytes);
+        float* sd = reinterpret_cast<float*>(sq + MT * K);
+        const int nchunk = MT * nb;
+        for (int c = warp; c < nchunk; c += ncons) {
+            const int m = c / nb, cb = c - m * nb;
+            const float4* src = reinterpret_cast<const float4*>(act.x + static_cast<int64_t>(m) * act.ldx + 256 * cb) + 2 * lane;
+            const float4 v0 = src[0], v1 = src[1];
+            const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            float amax = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            int q[8];
+            const float d = q8k_quantize<8>(v, amax, q);
+            uint2 packed;
+            packed.x = static_cast<uint32_t>(q[0] & 0xff) | (static_cast<uint32_t>(q[1] & 0xff) << 8) |
+                       (static_cast<uint32_t>(q[2] & 0xff) << 16) | (static_cast<uint32_t>(q[3] & 0xff) << 24);
+            packed.y = static_cast<uint32_t>(q[4] & 0xff) | (static_cast<uint32_t>(q[5] & 0xff) << 8) |
+                       (static_cast<uint32_t>(q[6] & 0xff) << 16) | (static_cast<uint32_t>(q[7] & 0xff) << 24);
+            *reinterpret_cast<uint2*>(sq + m * K + 256 * cb + 8 * lane) = packed;
+            if (lane == 0) sd[m * nb + cb] = d;
+            if (blockIdx.x == 0) {
+                *reinterpret_cast<uint2*>(act.oqs + static_cast<int64_t>(m) * K + 256 * cb + 8 * lane) = packed;
+                int sum = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);   // lanes 2g, 2g+1: group g
+                if ((lane & 1) == 0)
+                    act.obs[static_cast<int64_t>(m) * (K / 16) + 16 * cb + (lane >> 1)] = static_cast<int16_t>(sum);
+                if (lane == 0) act.od[static_cast<int64_t>(m) * nb + cb] = d;
+            }
+        }
+        asm volatile("bar.sync 0, %0;" ::"r"(32 * ncons) : "memory");   // the consumer warps only
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (active) {
+                const uint4 va = *reinterpret_cast<const uint4*>(sq + m * K + 256 * b + ka);
+                const uint4 vb = *reinterpret_cast<const uint4*>(sq + m * K + 256 * b + kb);
+                xa[m][0] = va.x, xa[m][1] = va.y, xa[m][2] = va.z, xa[m][3] = va.w;
+                xb[m][0] = vb.x, xb[m][1] = vb.y, xb[m][2] = vb.z, xb[m][3] = vb.w;
+                int sa = 0, sb = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    sa = __dp4a(static_cast<int>(xa[m][k]), 0x01010101, sa);
+                    sb = __dp4a(static_cast<int>(xb[m][k]), 0x01010101, sb);
+                }
+                bsa[m] = sa;
+                bsb[m] = sb;
+                dx[m] = sd[m * nb + b];
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) xa[m][k] = xb[m][k] = 0u;
+                bsa[m] = bsb[m] = 0;
+                dx[m] = 0.0f;
+            }
+        }
+    } else {
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         if (active) {
-            const int8_t* xr = xqs + static_cast<int64_t>(m) * K + 256 * b;
+            const int8_t* xr = act.xqs + static_cast<int64_t>(m) * K + 256 * b;
             const uint4 va = *reinterpret_cast<const uint4*>(xr + ka);
             const uint4 vb = *reinterpret_cast<const uint4*>(xr + kb);
             xa[m][0] = va.x, xa[m][1] = va.y, xa[m][2] = va.z, xa[m][3] = va.w;
             xb[m][0] = vb.x, xb[m][1] = vb.y, xb[m][2] = vb.z, xb[m][3] = vb.w;
-            const int16_t* br = xbs + static_cast<int64_t>(m) * (K / 16) + 16 * b;
+            const int16_t* br = act.xbs + static_cast<int64_t>(m) * (K / 16) + 16 * b;
             bsa[m] = br[ka / 16];
             bsb[m] = br[kb / 16];
-            dx[m] = xd[static_cast<int64_t>(m) * nb + b];
+            dx[m] = act.xd[static_cast<int64_t>(m) * nb + b];
         } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k) xa[m][k] = xb[m][k] = 0u;
             bsa[m] = bsb[m] = 0;
             dx[m] = 0.0f;
         }
+    }
     }
 
     // A failed wait (timeout, status recorded) does not end the loop: the
@@ -357,17 +424,17 @@ cudaError_t launch_dependent(void (*kernel)(Params...), int grid, int threads, s
     return cudaLaunchKernelEx(&cfg, kernel, args...);   // (arguments converted to the parameter types)
 }
 
-template <int WT>
-cudaError_t launch_small_wt(const uint8_t* w, int64_t ldw, int N, int nb, const int8_t* xqs, const float* xd,
-                            const int16_t* xbs, int M, void* y, int64_t ldy, const Epi& epi, int sm_count,
-                            uint32_t* status, const WaitCfg& wcfg, cudaStream_t st) {
+template <int WT, bool FUSED>
+cudaError_t launch_small_wt(const uint8_t* w, int64_t ldw, int N, int nb, const SmallAct& act, int M, void* y,
+                            int64_t ldy, const Epi& epi, int sm_count, uint32_t* status, const WaitCfg& wcfg,
+                            cudaStream_t st) {
     const int wpr = (nb + 3) / 4;   // warps per row lane
     if (wpr < 1 || wpr > SM_MAX_WPR || sm_count < 1) return cudaErrorInvalidValue;
     const int grid = sm_count < N ? sm_count : N;   // one CTA per SM
     const int row_bytes = nb * SmallTraits<WT>::BLOCK;
 #define QG_SMALL_CASE(MT)                                                                               \
     case MT: {                                                                                          \
-        auto k = smallm_kernel<WT, MT>;                                                                 \
+        auto k = smallm_kernel<WT, MT, FUSED>;                                                          \
         int rl = small_max_warps(MT) / wpr;                                                             \
         if (rl > SM_MAX_ROW_LANES) rl = SM_MAX_ROW_LANES;                                               \
         /* rows per row lane and stage: a stage of at most SM_SLOT_TARGET bytes, one row each at least */ \
@@ -375,25 +442,36 @@ cudaError_t launch_small_wt(const uint8_t* w, int64_t ldw, int N, int nb, const 
         if (rps > small_stage_rows(WT, MT)) rps = small_stage_rows(WT, MT);                             \
         if (rps < 1) rps = 1;                                                                           \
         const int slot = rl * rps * row_bytes;                                                          \
-        int nsb = SM_RING_BYTES / slot;                                                                 \
+        /* (fused: the quantized activations after the ring) */                                       \
+        const int act_bytes = FUSED ? small_act_bytes(MT, nb) : 0;                                       \
+        int nsb = (SM_RING_BYTES - act_bytes) / slot;                                                   \
         if (nsb > SM_MAX_SLOTS) nsb = SM_MAX_SLOTS;                                                     \
         if (nsb < 2) return cudaErrorInvalidValue;                                                      \
         cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(k), SM_RING_BYTES);             \
         if (e != cudaSuccess) return e;                                                                 \
-        return launch_dependent(k, grid, 32 * (rl * wpr + 1), static_cast<size_t>(nsb) * slot, st, w, ldw, N, \
-                                nb, xqs, xd, xbs, y, ldy, epi, wpr, rl, rps, nsb, status, wcfg);        \
+        return launch_dependent(k, grid, 32 * (rl * wpr + 1), static_cast<size_t>(nsb) * slot + act_bytes, st, w, ldw, N, \
+                                nb, act, y, ldy, epi, wpr, rl, rps, nsb, status, wcfg);                 \
     }
-    switch (M) {
-        QG_SMALL_CASE(1)
-        QG_SMALL_CASE(2)
-        QG_SMALL_CASE(3)
-        QG_SMALL_CASE(4)
-        QG_SMALL_CASE(5)
-        QG_SMALL_CASE(6)
-        QG_SMALL_CASE(7)
-        QG_SMALL_CASE(8)
-        default:
-            return cudaErrorInvalidValue;
+    if constexpr (FUSED) {
+        switch (M) {
+            QG_SMALL_CASE(1)
+            QG_SMALL_CASE(2)
+            default:
+                return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (M) {
+            QG_SMALL_CASE(1)
+            QG_SMALL_CASE(2)
+            QG_SMALL_CASE(3)
+            QG_SMALL_CASE(4)
+            QG_SMALL_CASE(5)
+            QG_SMALL_CASE(6)
+            QG_SMALL_CASE(7)
+            QG_SMALL_CASE(8)
+            default:
+                return cudaErrorInvalidValue;
+        }
     }
 #undef QG_SMALL_CASE
 }
@@ -409,11 +487,18 @@ bool small_supported(int wtype, int64_t M, int64_t K) {
 cudaError_t launch_small(const SmallLaunch& a, cudaStream_t st) {
     const int nb = static_cast<int>(a.K / 256);
     const uint8_t* w = static_cast<const uint8_t*>(a.w);
-    if (a.wtype == 4)
-        return launch_small_wt<4>(w, a.ldw, static_cast<int>(a.N), nb, a.xqs, a.xd, a.xbs, static_cast<int>(a.M),
-                                  a.y, a.ldy, a.epi, a.sm_count, a.status, a.wait, st);
-    return launch_small_wt<6>(w, a.ldw, static_cast<int>(a.N), nb, a.xqs, a.xd, a.xbs, static_cast<int>(a.M), a.y,
-                              a.ldy, a.epi, a.sm_count, a.status, a.wait, st);
+    const int M = static_cast<int>(a.M), N = static_cast<int>(a.N);
+    if (a.act.x) {
+        if (M > SMALL_FUSED_M_MAX) return cudaErrorInvalidValue;
+        return a.wtype == 4 ? launch_small_wt<4, true>(w, a.ldw, N, nb, a.act, M, a.y, a.ldy, a.epi, a.sm_count,
+                                                       a.status, a.wait, st)
+                            : launch_small_wt<6, true>(w, a.ldw, N, nb, a.act, M, a.y, a.ldy, a.epi, a.sm_count,
+                                                       a.status, a.wait, st);
+    }
+    return a.wtype == 4 ? launch_small_wt<4, false>(w, a.ldw, N, nb, a.act, M, a.y, a.ldy, a.epi, a.sm_count,
+                                                    a.status, a.wait, st)
+                        : launch_small_wt<6, false>(w, a.ldw, N, nb, a.act, M, a.y, a.ldy, a.epi, a.sm_count,
+                                                    a.status, a.wait, st);
 }
 
 }  // namespace qg

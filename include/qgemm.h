@@ -209,6 +209,31 @@ QGEMM_API int qgemm_q6k_prepared(const void *w_packed, int64_t N, int64_t K, con
                                  const int16_t *xbsums, int64_t M, float *y, int64_t ldy, const void *workspace,
                                  size_t workspace_bytes, qgemm_stream_t stream);
 
+/* ------------------------------------------ fp32 activations in ----
+ * The whole path behind one call: X (fp32) is quantized to Q8_K and
+ * multiplied, Y[M][N] = Q8_K(X) . W^T, as qgemm_quantize_q8k followed by
+ * qgemm_q4k / qgemm_q6k (the same Y and Q8_K values, bit for bit; the pages
+ * quantize the activations as the step before the GEMM, vllm.cpp PR #3036,
+ * commit 5, and suggest doing it inside the GEMM's load stage).
+ *   x, ldx          fp32 [M][ldx], device or pinned host memory; 16-B aligned,
+ *                   ldx >= K, ldx % 4 == 0 (as qgemm_quantize_q8k).
+ *   qs, d, bsums    the Q8_K planes of X, written in every case.
+ *   workspace       >= qgemm_workspace_bytes(M, N, K), 256-B aligned; used
+ *                   only above the small-M path (may be NULL at or below it).
+ *   w, ldw, N, K, y, ldy   as qgemm_q4k (Q6_K: the repacked blocks).
+ * For M <= 2 within the small-M path (QGEMM_OPT_SMALL_M_MAX, K <= 15360) it
+ * is one launch: the weight-streaming kernel quantizes the activations
+ * itself, each lane the values it multiplies, while the first weights are
+ * in flight (counted in small_fused).  Otherwise the quantizer runs first
+ * (for the tile GEMM it also fills the workspace's operand planes) and the
+ * GEMM starts under it.  Errors: as qgemm_quantize_q8k and qgemm_q4k. */
+QGEMM_API int qgemm_q4k_f32(const void *w, int64_t N, int64_t K, int64_t ldw, const float *x, int64_t ldx,
+                            int64_t M, int8_t *qs, float *d, int16_t *bsums, float *y, int64_t ldy, void *workspace,
+                            size_t workspace_bytes, qgemm_stream_t stream);
+QGEMM_API int qgemm_q6k_f32(const void *w_packed, int64_t N, int64_t K, const float *x, int64_t ldx, int64_t M,
+                            int8_t *qs, float *d, int16_t *bsums, float *y, int64_t ldy, void *workspace,
+                            size_t workspace_bytes, qgemm_stream_t stream);
+
 /* ------------------------------------ expert-routed GEMM (MUL_MAT_ID) ----
  * The routed form of the GEMM that the pages test beside MUL_MAT (llama.cpp
  * PR #214 "cuda: branch-free PTQ1_0 MMQ tile loader ...", test-backend-ops
@@ -371,6 +396,7 @@ typedef struct {
     uint64_t routed;       /* expert-routed GEMM launches (_id)     */
     uint64_t ptq1_tc;      /* PTQ1_0 tile GEMM launches             */
     uint64_t ptq1_prepack; /* PTQ1_0 repack launches                */
+    uint64_t small_fused;  /* small-M launches that quantized X themselves (also counted in q4k/q6k_small) */
 } qgemm_counters;
 QGEMM_API int qgemm_get_counters(qgemm_counters *out);
 QGEMM_API int qgemm_reset_counters(void);
