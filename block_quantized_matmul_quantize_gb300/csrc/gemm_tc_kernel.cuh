@@ -217,12 +217,12 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     constexpr int R = L::RAW_SLOTS;
     constexpr int BS = L::B_STAGES;
     constexpr int SBN = SB_SLOTS;
-    // Weight-operand stages: K128 (8 MMAs) per stage, or for SPLIT (Q6_K) K64
-    // with the hi part in the stage's first 32 columns and the lo part in the
-    // other 32 (4 + 4 MMAs; the lo MMAs only when some row wrote a lo part).
+    // Weight-operand stages: K128 (8 MMAs) per stage.  SPLIT (Q6_K): a K128
+    // step's hi part in one stage use and, where some row of the superblock
+    // has one, its lo part in the next use, against the same activations.
     constexpr bool SPLIT = WTraits<WT>::SPLIT;
-    constexpr int KSTEP = SPLIT ? 64 : 128;
-    constexpr int STEPS = 256 / KSTEP;   // weight-operand stages per superblock
+    constexpr int KSTEP = 128;
+    constexpr int STEPS = 256 / KSTEP;   // K128 steps per superblock
     // With two-box stages and as many activation stages as weight-operand
     // stages, every K128 step consumes exactly one stage of each ring, so one
     // commit (on a_empty) releases both and the activation producers wait on it.
@@ -245,8 +245,9 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
     // wait control (ptx.cuh): [0] abort flag, [1] wait limit
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
-    // SPLIT: byte q of word s is set by unpack warp q when it wrote a nonzero lo
-    // part into stage s (before its a_full arrival; read by the issuer after the wait)
+    // SPLIT: word s is nonzero when the stage's current (hi) use is followed by
+    // a lo use of the same step (written by the expansion group before its
+    // a_full arrivals; read by the issuer after its wait)
     volatile uint32_t* lo_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_LOFLAG);
 
     const int warp = threadIdx.x >> 5;
@@ -441,11 +442,11 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
         // accumulator `par`, weight-operand stages 2*par and 2*par+1 and (two-
         // box activation stages) the same two activation stages: every stage
         // barrier is waited on by one thread, phase after phase.  Per
-        // superblock: STEPS weight-operand steps (two K128 steps of 8 MMAs, or
-        // for SPLIT four K64 steps of 4 hi MMAs plus 4 lo MMAs where a lo part
-        // was written), +2 correction MMAs for Q4_K, and the commits; readiness
-        // of the next step, the side slot and the next accumulator is probed
-        // without blocking between the MMAs of the current step.
+        // superblock: two K128 steps of 8 MMAs (for SPLIT each followed by a lo
+        // use of 8 more where the expansion group flagged one), +2 correction
+        // MMAs for Q4_K, and the commits; readiness of the next step, the side
+        // slot and the next accumulator is probed without blocking between the
+        // MMAs of the current step.
         if (lane == 0) {
             const int par = (warp == W_MMA) ? 0 : 1;
             constexpr uint32_t IDESC = idesc_f16_f32(BN, BM);
@@ -456,19 +457,13 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             const uint64_t acorr0 = smem_desc(sb0 + L::SB_ACORR, 16, 256, SWZ_32B);
             const uint64_t bcorr0 = smem_desc(sb0 + L::SB_BCORR, 16, 256, SWZ_32B);
             const uint32_t d_tmem = tmem_base + par * BM;
-            // weight-operand stage and phase parity of step h of superblock t.
-            // K128: g = 2t + h over the four stages (superblocks of parity par
-            // use stages 2par, 2par+1).  SPLIT: the superblocks of parity par use
-            // stage 2par + (h & 1), twice each (steps h and h + 2).
+            // weight-operand stage and phase parity of step h of superblock t:
+            // g = 2t + h over the four stages (superblocks of parity par use
+            // stages 2par, 2par+1)
             auto a_at = [&](int t, int h, int& s, uint32_t& ph) {
-                if constexpr (SPLIT) {
-                    s = 2 * (t & 1) + (h & 1);
-                    ph = static_cast<uint32_t>(2 * (t >> 1) + (h >> 1)) & 1u;
-                } else {
-                    const int g = 2 * t + h;
-                    s = g % A_STAGES;
-                    ph = static_cast<uint32_t>(g / A_STAGES) & 1u;
-                }
+                const int g = 2 * t + h;
+                s = g % A_STAGES;
+                ph = static_cast<uint32_t>(g / A_STAGES) & 1u;
             };
             // activation stage of step h of superblock t, and the step's first box in it
             auto b_at = [&](int t, int h, int& s, uint32_t& ph, int& q0) {
@@ -482,6 +477,57 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             bool step_ok = false;   // next step's A (and B) stage seen complete
             bool acc_ok = false;    // next superblock's accumulator seen free
             bool ok = true;
+            if constexpr (SPLIT) {
+                // Q6_K: this thread's superblocks use stages 2par and 2par+1 in
+                // turn, one use after another: use u is stage 2par + (u & 1) with
+                // phase parity (u >> 1) & 1, and expansion group par counts its
+                // uses the same way.  A step's hi use says (lo_flag) whether a lo
+                // use follows.
+                int u = 0;
+                for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
+                    int n0, m0, kb0, kb1;
+                    work_of(wi, n0, m0, kb0, kb1);
+                    for (int b = kb0; b < kb1 && ok; ++b, ++t) {
+                        if ((t & 1) != par) continue;
+                        ok = mbar_wait(&acc_empty[par], ((t >> 1) & 1) ^ 1, abort_flag, status, 4);
+                        if (!ok) break;
+                        for (int h = 0; h < STEPS && ok; ++h) {
+                            int sx, q0;
+                            uint32_t px;
+                            b_at(t, h, sx, px, q0);
+                            if (q0 == 0) {
+                                ok = mbar_wait(&b_full[sx], px, abort_flag, status, 5);
+                                if (!ok) break;
+                            }
+                            const uint64_t bd = bdesc0 + static_cast<uint64_t>((sx * L::B_STAGE + q0 * L::BOX) >> 4);
+                            const uint64_t bd1 = bd + (L::BOX >> 4);
+                            bool more = true;   // the hi use, then the lo use if flagged
+                            for (int part = 0; more; ++part) {
+                                const int sa = 2 * par + (u & 1);
+                                ok = mbar_wait(&a_full[sa], static_cast<uint32_t>(u >> 1) & 1u, abort_flag, status, 12);
+                                if (!ok) break;
+                                tc_fence_after();
+                                more = part == 0 && lo_flag[sa] != 0u;
+                                const uint32_t a0 = tmem_base + A_TMEM_COL + 64 * sa;
+                                mma_f16_ta(d_tmem, a0, bd, IDESC, (h | part) != 0);
+                                mma_f16_ta(d_tmem, a0 + 8, bd + 2, IDESC, 1u);
+                                mma_f16_ta(d_tmem, a0 + 16, bd + 4, IDESC, 1u);
+                                mma_f16_ta(d_tmem, a0 + 24, bd + 6, IDESC, 1u);
+                                mma_f16_ta(d_tmem, a0 + 32, bd1, IDESC, 1u);
+                                mma_f16_ta(d_tmem, a0 + 40, bd1 + 2, IDESC, 1u);
+                                mma_f16_ta(d_tmem, a0 + 48, bd1 + 4, IDESC, 1u);
+                                mma_f16_ta(d_tmem, a0 + 56, bd1 + 6, IDESC, 1u);
+                                mma_commit(&a_empty[sa]);
+                                ++u;
+                            }
+                            if (!ok) break;
+                            if (q0 + KSTEP / 64 == L::SCH) mma_commit(&b_empty[sx]);   // the step ends its B stage
+                        }
+                        if (!ok) break;
+                        mma_commit(&acc_full[par]);   // the epilogue then also frees the side slot
+                    }
+                }
+            } else
             for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
                 int n0, m0, kb0, kb1;
                 work_of(wi, n0, m0, kb0, kb1);
@@ -507,8 +553,6 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                         tc_fence_after();
                         const uint32_t a0 = tmem_base + A_TMEM_COL + 64 * sa;
                         const uint64_t bd = bdesc0 + static_cast<uint64_t>((sx * L::B_STAGE + q0 * L::BOX) >> 4);
-                        bool lo = false;   // (SPLIT) some row of this stage has a lo part
-                        if constexpr (SPLIT) lo = (lo_flag[sa] != 0u);
                         mma_f16_ta(d_tmem, a0, bd, IDESC, h != 0);
                         mma_f16_ta(d_tmem, a0 + 8, bd + 2, IDESC, 1u);
                         mma_f16_ta(d_tmem, a0 + 16, bd + 4, IDESC, 1u);
@@ -528,14 +572,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                             if (h == STEPS - 1) acc_ok = mbar_test_wait(&acc_empty[par], (((t + 2) >> 1) & 1) ^ 1);
                             step_ok = ta && tb;
                         }
-                        if constexpr (SPLIT) {
-                            if (lo) {   // the lo part, against the same activation box
-                                mma_f16_ta(d_tmem, a0 + 32, bd, IDESC, 1u);
-                                mma_f16_ta(d_tmem, a0 + 40, bd + 2, IDESC, 1u);
-                                mma_f16_ta(d_tmem, a0 + 48, bd + 4, IDESC, 1u);
-                                mma_f16_ta(d_tmem, a0 + 56, bd + 6, IDESC, 1u);
-                            }
-                        } else {
+                        {
                             const uint64_t bd1 = bd + (L::BOX >> 4);
                             mma_f16_ta(d_tmem, a0 + 32, bd1, IDESC, 1u);
                             mma_f16_ta(d_tmem, a0 + 40, bd1 + 2, IDESC, 1u);
@@ -571,8 +608,9 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
         // warp must).  Q4_K: one group.  PTQ1_0: group g expands K128 step g
         // of every superblock; group 0 also writes the superblock's side data.
         // Q6_K (SPLIT): group g owns the superblocks t with t % 2 == g -- the
-        // same ones as MMA thread g -- and expands all four K64 steps of each
-        // into weight-operand stages 2g and 2g+1, writing its side data too.
+        // same ones as MMA thread g -- and expands both K128 steps of each, hi
+        // parts and (where needed) lo parts, into stages 2g and 2g+1 in turn,
+        // writing its side data too.
         const int grp = (warp - W_UNPACK0) >> 2;
         const int j0 = UG == 2 ? grp : 0, j1 = UG == 2 ? grp + 1 : 2;   // this warp's K128 steps
         const int quad = warp & 3;
@@ -591,9 +629,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                 pend = -1;
             }
         };
-        // (SPLIT) bit i: this warp's lo columns of stage 2*grp + i may be nonzero
-        // (TMEM starts with unknown contents)
-        int lo_dirty = 3;
+        int u = 0;   // (SPLIT) this group's stage uses, as MMA thread grp counts them
         int t = 0;
         bool ok = true;
         for (int wi = blockIdx.x; wi < num_work && ok; wi += gridDim.x) {
@@ -670,6 +706,27 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                     }
                     // sub-block scales split into exact hi and lo parts (q6k_split)
                     const uint4 scv = *reinterpret_cast<const uint4*>(blk + 192);
+                    // Does step j need a lo use?  Yes if any of the CTA's 128 rows has a
+                    // lo part among the step's eight sub-block scales (every warp of the
+                    // group reads them all and decides alike).
+                    bool lo_step[2];
+                    {
+                        uint32_t need0 = 0u, need1 = 0u;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint4 sv = *reinterpret_cast<const uint4*>(raw_slot(r) + (lane + 32 * k) *
+                                                                             WTraits<WT>::RAW_BLOCK + 192);
+                            uint32_t h0, l0, l1, l2, l3;
+                            q6k_split(sv.x, h0, l0);
+                            q6k_split(sv.y, h0, l1);
+                            q6k_split(sv.z, h0, l2);
+                            q6k_split(sv.w, h0, l3);
+                            need0 |= l0 | l1;
+                            need1 |= l2 | l3;
+                        }
+                        lo_step[0] = __any_sync(0xffffffffu, need0 != 0u);
+                        lo_step[1] = __any_sync(0xffffffffu, need1 != 0u);
+                    }
                     {
                         const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
                         if (!mbar_test_wait(&sb_empty[p], ((t / SBN) & 1) ^ 1)) signal();
@@ -679,35 +736,33 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&sb_full[p]);
                     }
-                    // K64 step c into stage 2*grp + (c & 1): hi part in its first 32
-                    // columns; the lo part in the other 32 where some row of the warp has
-                    // one (else zeros, written only if the columns may hold old values)
+                    // step j: chunks 2j and 2j+1, the hi parts in one stage use, then the
+                    // lo parts (zero for rows without one) in the next if lo_step[j]
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        const int s = 2 * grp + (c & 1);
-                        const int use = 2 * (t >> 1) + (c >> 1);   // the stage's phase
-                        // the chunk's four sub-block scales: bytes 4c..4c+3 of the scale array
-                        uint32_t slo, v[32];
-                        q6k_expand_hi(blk, c, c == 0 ? scv.x : c == 1 ? scv.y : c == 2 ? scv.z : scv.w, slo, v);
-                        signal();
-                        ok = mbar_wait(&a_empty[s], (use & 1) ^ 1, abort_flag, status, 9);
-                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                        tc_fence_after();
-                        tmem_st_32x32b_x32(lane_base + 64 * s, v);
-                        const bool need = __any_sync(0xffffffffu, slo != 0u);
-                        const int bit = 1 << (c & 1);
-                        if (need || (lo_dirty & bit)) {
-                            if (need) {
-                                q6k_expand_lo(blk, c, slo, v);
-                            } else {
-#pragma unroll
-                                for (int k = 0; k < 32; ++k) v[k] = 0u;
-                            }
+                    for (int j = 0; j < 2 && ok; ++j) {
+                        const uint32_t sw0 = j == 0 ? scv.x : scv.z, sw1 = j == 0 ? scv.y : scv.w;
+                        uint32_t slo0, slo1, v[32];
+                        const int nuse = lo_step[j] ? 2 : 1;
+                        for (int use = 0; use < nuse; ++use) {
+                            if (use == 0)
+                                q6k_expand_hi(blk, 2 * j, sw0, slo0, v);
+                            else
+                                q6k_expand_lo(blk, 2 * j, slo0, v);
+                            signal();
+                            const int s = 2 * grp + (u & 1);
+                            ok = mbar_wait(&a_empty[s], ((u >> 1) & 1) ^ 1, abort_flag, status, 9);
+                            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                            tc_fence_after();
+                            tmem_st_32x32b_x32(lane_base + 64 * s, v);
+                            if (use == 0)
+                                q6k_expand_hi(blk, 2 * j + 1, sw1, slo1, v);
+                            else
+                                q6k_expand_lo(blk, 2 * j + 1, slo1, v);
                             tmem_st_32x32b_x32(lane_base + 64 * s + 32, v);
-                            lo_dirty = need ? (lo_dirty | bit) : (lo_dirty & ~bit);
+                            if (quad == 0 && lane == 0) lo_flag[s] = (use == 0 && nuse == 2) ? 1u : 0u;
+                            pend = s;
+                            ++u;
                         }
-                        if (lane == 0) reinterpret_cast<volatile uint8_t*>(lo_flag + s)[quad] = need ? 1 : 0;
-                        pend = s;
                     }
                     if (!ok) break;
                     signal();   // the superblock's last stage now: the other group's superblock comes next
