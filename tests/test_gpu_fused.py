@@ -132,6 +132,26 @@ def test_fused_adversarial_rows(wtype):
         run_f32(wtype, w_np, 1024, to_dev(xs), f"Q{wtype}_K adversarial rows {i}, {i + 1}")
 
 
+@pytest.mark.parametrize("M", [1, 2, 5, 40])
+def test_q6k_full_int8_scales(M):
+    """Q6_K sub-scales over the whole int8 range (real quantizers use it),
+    on the fused, small-M and tile paths."""
+    N, K = 150, 2560
+    w_np = synth.gen_q6k(N, K, 61 + M, full_scales=True)
+    x = to_dev(synth.gen_x(M, K, 62 + M, outlier_frac=0.01))
+    what = f"Q6_K full int8 scales M{M}"
+    expect_path(run_f32(6, w_np, K, x, what), 6, M, what)
+
+
+def test_tile_path_ragged():
+    """The tile path through the fp32 entry point on ragged M and N (several
+    token and weight tiles, cut tiles)."""
+    M, N, K = 300, 1000, 4096
+    x = to_dev(synth.gen_x(M, K, 71, outlier_frac=0.01))
+    what = "Q4_K M300 N1000 K4096 fp32 in"
+    expect_path(run_f32(4, weights(4, N, K, 72), K, x, what, ldy_pad=5), 4, M, what)
+
+
 def test_fused_near_ties():
     """Values on or one or two ulps beside rounding boundaries: the fused
     kernel's reciprocal shortcut must hand them to the exact division."""
