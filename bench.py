@@ -81,6 +81,20 @@ NCU_TRAFFIC_BYTES = {
 }
 
 
+def quantize_report(M, K, us, with_planes, hbm_gbs):
+    """The quantizer's own line: algorithmic bytes (fp32 X read, Q8_K written:
+    (4 + 292/256) bytes per element) over its event time, against HBM."""
+    if us is None:
+        return {"kernel": "none: the small-M kernel quantizes X itself (one launch per step)"}
+    algo = (4.0 + 292.0 / 256.0) * M * K
+    planes = (2.0 + 2.0 / 16.0) * M * K + (K // 256) * ((M + 3) // 4 * 4) * 4.0 if with_planes else 0.0
+    gbs = algo / (us * 1e-6) / 1e9
+    return {"kernel": "quantize_q8k_kernel" + (" (also writes the tile GEMM's operand planes)" if with_planes else ""),
+            "us": us, "algorithmic_bytes": algo, "achieved_gbs": gbs, "frac_hbm": gbs / float(hbm_gbs),
+            "bytes_moved_incl_operand_planes": algo + planes,
+            "gbs_incl_operand_planes": (algo + planes) / (us * 1e-6) / 1e9}
+
+
 def workloads():
     return {w.name: w for w in synth.CONFIGS + synth.FULLSCALE_CONFIGS + synth.ROUTED_CONFIGS + synth.PTQ1_CONFIGS}
 
@@ -534,6 +548,32 @@ def main():
     e2e_value = job_tops(world, ops, e2e_ms)
     e2e_copies_value = job_tops(world, ops, e2e_copies_ms)
 
+    # ---- the quantizer alone, reported against HBM: the launch the step's call
+    # makes for this workload (with the tile GEMM's operand planes when the
+    # tile GEMM follows; none when the small-M kernel quantizes X itself)
+    fused_small = c1["small_fused"] > c0["small_fused"]
+    tile_next = not is_routed and any(c1[k] > c0[k] for k in ("q4k_tc", "q6k_tc", "ptq1_tc"))
+    quant_us = None
+    if not fused_small:
+        def quant_only():
+            if tile_next:
+                qg.qgemm_quantize_q8k_prep(x, ws, out=q)
+            else:
+                qg.qgemm_quantize_q8k(x, out=q)
+        for _ in range(3):
+            quant_only()
+        q_s = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+        q_e = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+        torch.cuda.synchronize()
+        for i in range(K_steps):
+            flush_l2()
+            q_s[i].record(stream)
+            quant_only()
+            q_e[i].record(stream)
+        torch.cuda.synchronize()
+        quant_us = max_over_ranks([sum(q_s[i].elapsed_time(q_e[i]) for i in range(K_steps)) / K_steps],
+                                  world, dev)[0] * 1e3
+
     bits, site = qg.qgemm_get_device_status()
 
     if rank == 0:
@@ -573,6 +613,7 @@ def main():
                     "path": "zero-copy: X read and Y written in pinned host memory by the library's kernels",
                     "copies": {"value": e2e_copies_value, "ms_per_step": e2e_copies_ms,
                                "path": "cudaMemcpyAsync of X and Y around the device step"}},
+            "quantize": quantize_report(M, K, quant_us, tile_next, measured_peaks()[0]["hbm_gbs"]),
             "gpu_launches": int(launches),
             "clocks": sampler.summary(t0, t1),
             "device_status": bits,
