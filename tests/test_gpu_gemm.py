@@ -117,9 +117,33 @@ def test_grouped_work_order(wtype, M, N, K):
     device_status_clean()
 
 
-@pytest.mark.parametrize("wl", [synth.C0, synth.C1, synth.C2], ids=lambda w: w.name)
+def check_bench_path(wl, rows=None):
+    """The workload through the call the benchmark times (fp32 X in, one call:
+    qgemm_q4k_f32 / qgemm_q6k_f32 with a caller workspace), with its Q8_K
+    planes bit-exact and Y (all rows, or the sampled ones) within tolerance."""
+    x = wl.x()
+    M, N, K = wl.M, wl.N, wl.K
+    w_np = wl.weights()
+    w = to_dev(w_np)
+    q = qg.Q8K.empty(M, K, "cuda")
+    ws = torch.empty(max(qg.qgemm_workspace_bytes(M, N, K), 256), dtype=torch.uint8, device="cuda")
+    xd = to_dev(x)
+    if wl.wtype == 4:
+        y = qg.qgemm_q4k_f32(w, N, K, xd, out=q, workspace=ws)
+    else:
+        y = qg.qgemm_q6k_f32(qg.qgemm_q6k_prepack(w, N, K), N, K, xd, out=q, workspace=ws)
+    torch.cuda.synchronize()
+    q8 = q8k_numpy(q)
+    assert_q8k_equal(q8, oracle.get().quantize_q8k(x), wl.name)
+    yr, absc = oracle_gemm(wl.wtype, w_np, K, *q8, rows=rows)
+    yg = y.cpu().numpy()
+    assert_gemm_close(yg if rows is None else yg[rows], yr, absc, wl.name)
+    device_status_clean()
+
+
+@pytest.mark.parametrize("wl", [synth.C0, synth.C1, synth.C2, synth.F2], ids=lambda w: w.name)
 def test_workload_full(wl):
-    check(wl.wtype, wl.weights(), wl.K, wl.x(), what=wl.name)
+    check_bench_path(wl)
 
 
 @pytest.mark.parametrize("wl", [synth.C3] + [synth.sweep(m) for m in synth.SWEEP_M],
@@ -127,7 +151,7 @@ def test_workload_full(wl):
 def test_workload_sampled(wl):
     # at least 256 rows, one in every 128-token tile, and the tail rows
     rows = None if wl.M <= 256 else tile_rows(wl.M, 256, seed=wl.M)
-    check(wl.wtype, wl.weights(), wl.K, wl.x(), rows=rows, what=wl.name)
+    check_bench_path(wl, rows)
 
 
 def _q4k_blocks(orc, N, nb, rng, d_bits=None, dmin_bits=None, q_zero=False):
