@@ -6,7 +6,8 @@ activations quantized to Q8_K, then the Q4_K x Q8_K GEMM.  Above the small-M
 path the quantizer also writes the tile GEMM's fp16 operand planes and the
 tcgen05 tile GEMM starts under it; for M <= 8 the small-M streaming kernel
 runs, and for M <= 2 it quantizes the activations itself (one launch).
-Routed and PTQ1_0 workloads call their own entry points.  Default workload: the
+PTQ1_0 workloads call qgemm_ptq1_f32, routed ones quantize and then call the
+routed GEMM.  Default workload: the
 largest configuration, the Q4_K sweep point M = 8192 tokens, K = N = 5120,
 X ~ N(0,1); synthetic, seeded (synth.py).  --workload picks another.
 
@@ -404,8 +405,7 @@ def main():
                 qg.qgemm_q6k_id(w, wl.E, N, K, q, ids_in, y=yout, workspace=ws)
             return
         if wl.wtype == 1:
-            qg.qgemm_quantize_q8k_prep(xin, ws, out=q)
-            qg.qgemm_ptq1_prepared(w, N, K, q, ws, y=yout)
+            qg.qgemm_ptq1_f32(w, N, K, xin, out=q, y=yout, workspace=ws)
             return
         # fp32 X in, Y out, one call: for M <= 2 one launch (the small-M kernel
         # quantizes X itself), else the quantizer (writing the GEMM's operand

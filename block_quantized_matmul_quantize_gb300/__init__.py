@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
             "qgemm_q4k_prepared": ([vp, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
             "qgemm_q4k_f32": ([vp, i64, i64, i64, vp, i64, i64, vp, vp, vp, vp, i64, vp, sz, vp], i32),
             "qgemm_q6k_f32": ([vp, i64, i64, vp, i64, i64, vp, vp, vp, vp, i64, vp, sz, vp], i32),
+            "qgemm_ptq1_f32": ([vp, i64, i64, vp, i64, i64, vp, vp, vp, vp, i64, vp, sz, vp], i32),
             "qgemm_q6k_prepared": ([vp, i64, i64, vp, vp, vp, i64, vp, i64, vp, sz, vp], i32),
             "qgemm_id_workspace_bytes": ([i64, i64, i64, i64], sz),
             "qgemm_q4k_id": ([vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, i64, vp, sz, vp], i32),
@@ -319,6 +320,23 @@ def qgemm_q6k_f32(w_packed: torch.Tensor, N: int, K: int, x: torch.Tensor, out: 
     _check(lib().qgemm_q6k_f32(_ptr(w_packed), N, K, _ptr(x, True), x.stride(0), M, _ptr(out.qs), _ptr(out.d),
                                _ptr(out.bsums), _ptr(y, True), y.stride(0), _ptr(workspace), workspace.numel(),
                                _stream(stream)))
+    return y
+
+
+def qgemm_ptq1_f32(w_packed: torch.Tensor, N: int, K: int, x: torch.Tensor, out: Q8K | None = None,
+                   y: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """qgemm_q4k_f32 for repacked PTQ1_0 weights (always the tile GEMM)."""
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    M = x.shape[0]
+    dev = _device_of(x)
+    if out is None:
+        out = Q8K.empty(M, K, dev)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    workspace = _workspace(M, N, K, workspace, dev)
+    _check(lib().qgemm_ptq1_f32(_ptr(w_packed), N, K, _ptr(x, True), x.stride(0), M, _ptr(out.qs), _ptr(out.d),
+                                _ptr(out.bsums), _ptr(y, True), y.stride(0), _ptr(workspace), workspace.numel(),
+                                _stream(stream)))
     return y
 
 

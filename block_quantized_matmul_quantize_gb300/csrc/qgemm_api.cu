@@ -884,6 +884,21 @@ int qgemm_ptq1_prepared(const void* w_packed, int64_t N, int64_t K, const int8_t
                   reinterpret_cast<cudaStream_t>(stream), true);
 }
 
+int qgemm_ptq1_f32(const void* w_packed, int64_t N, int64_t K, const float* x, int64_t ldx, int64_t M, int8_t* qs,
+                   float* d, int16_t* bsums, float* y, int64_t ldy, void* workspace, size_t workspace_bytes,
+                   qgemm_stream_t stream) {
+    clear_err();
+    int rc = gemm_common_checks(w_packed, N, K, qs, d, bsums, M, y, ldy);
+    if (rc || M == 0) return rc;
+    if ((rc = f32_checks(x, ldx, M, K))) return rc;
+    const int64_t ldw = (K / 128) * qg::PTQ1_PACKED;
+    // (every M on the tile GEMM: the small-M streaming kernel has no PTQ1_0 decode)
+    rc = qgemm_quantize_q8k_prep(x, M, K, ldx, qs, d, bsums, workspace, workspace_bytes, stream);
+    if (rc) return rc;
+    return run_tc(1, w_packed, N, K, ldw, qs, d, bsums, M, y, ldy, workspace, workspace_bytes,
+                  reinterpret_cast<cudaStream_t>(stream), true);
+}
+
 size_t qgemm_id_workspace_bytes(int64_t M, int64_t top_k, int64_t experts, int64_t K) {
     if (M <= 0 || top_k < 1 || experts < 1 || K <= 0 || K % 256) return 0;
     const int64_t P = M * top_k;

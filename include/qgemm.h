@@ -288,6 +288,12 @@ QGEMM_API int qgemm_ptq1_prepack(const void *w, int64_t N, int64_t K, int64_t ld
 QGEMM_API int qgemm_ptq1(const void *w_packed, int64_t N, int64_t K, const int8_t *xqs, const float *xd,
                          const int16_t *xbsums, int64_t M, float *y, int64_t ldy, void *workspace,
                          size_t workspace_bytes, qgemm_stream_t stream);
+/* qgemm_ptq1_f32: fp32 X in, Y out, as qgemm_q4k_f32 (the quantizer with the
+ * operand planes, then the tile GEMM started under it; every M runs on the tile
+ * GEMM, and the workspace is always needed). */
+QGEMM_API int qgemm_ptq1_f32(const void *w_packed, int64_t N, int64_t K, const float *x, int64_t ldx, int64_t M,
+                             int8_t *qs, float *d, int16_t *bsums, float *y, int64_t ldy, void *workspace,
+                             size_t workspace_bytes, qgemm_stream_t stream);
 /* qgemm_ptq1_prepared: as qgemm_ptq1 from a workspace that
  * qgemm_quantize_q8k_prep filled for the same X (see the prepared calls). */
 QGEMM_API int qgemm_ptq1_prepared(const void *w_packed, int64_t N, int64_t K, const int8_t *xqs, const float *xd,

@@ -12,7 +12,7 @@ import torch
 import oracle
 import synth
 import block_quantized_matmul_quantize_gb300 as qg
-from gpu_common import device_status_clean, ensure_built, gpu_quantize, q8k_numpy, to_dev
+from gpu_common import assert_q8k_equal, device_status_clean, ensure_built, gpu_quantize, q8k_numpy, to_dev
 from parity_util import assert_gemm_close, oracle_gemm, tile_rows
 
 pytestmark = pytest.mark.gpu
@@ -101,6 +101,28 @@ def test_prepared_workspace():
     torch.cuda.synchronize()
     yr, absc = oracle_gemm(1, w, K, *q8k_numpy(q))
     assert_gemm_close(y.cpu().numpy(), yr, absc, "PTQ1_0 prepared")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 130, 512), (70, 260, 1024), (2048, 5120, 5120)])
+def test_fp32_in(M, N, K):
+    """qgemm_ptq1_f32 (fp32 X in, one call, the call the benchmark times):
+    the Q8_K planes bit-exact, Y within tolerance (sampled rows at the
+    benchmark's 2048 x 5120 x 5120)."""
+    w = synth.gen_ptq1(N, K, 51 + M)
+    x = synth.gen_x(M, K, 52 + M, outlier_frac=0.01)
+    wp = qg.qgemm_ptq1_prepack(to_dev(w), N, K)
+    q = qg.Q8K.empty(M, K, "cuda")
+    qg.qgemm_reset_counters()
+    y = qg.qgemm_ptq1_f32(wp, N, K, to_dev(x), out=q)
+    torch.cuda.synchronize()
+    c = qg.qgemm_get_counters()
+    assert (c["quantize"], c["ptq1_tc"], c["xprep"]) == (1, 1, 0), c
+    q8 = q8k_numpy(q)
+    assert_q8k_equal(q8, oracle.get().quantize_q8k(x), f"PTQ1_0 fp32 in M{M}")
+    rows = None if M <= 256 else tile_rows(M, 256, seed=M)
+    yr, absc = oracle_gemm(1, w, K, *q8, rows=rows)
+    yg = y.cpu().numpy()
+    assert_gemm_close(yg if rows is None else yg[rows], yr, absc, f"PTQ1_0 fp32 in M{M} N{N} K{K}")
 
 
 def test_device_status_clean_at_end():
