@@ -352,8 +352,7 @@ QGEMM_API int qgemm_q6k_ex(const void *w_packed, int64_t N, int64_t K, const int
  *     N = 11008 needs 9.7 MiB on a 152-SM GB300, 2.1 MiB of it the copy).  Larger calls return
  *     QGEMM_EUNSUPPORTED with a message and launch nothing.
  *   - The first call on each device looks up the scratch array's device
- *     address (cudaGetSymbolAddress) with that device current; make that
- *     first call before any stream capture.
+ *     address (cudaGetSymbolAddress) with that device current.
  *   - All calls on a device share the one array and it keeps the last call's
  *     contents; every byte the GEMM reads is rewritten by the same call, so
  *     nothing needs clearing.  Calls that overlap on the GPU (e.g. on two
