@@ -500,7 +500,7 @@ def main():
     # library kernels per step, counted on the eager pass; the graph replays the same ones
     # (a routed GEMM call is three: routing, operand gather, tile GEMM)
     per_step = sum(c1[k] - c0[k] for k in ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small",
-                                            "ptq1_tc"))
+                                            "ptq1_tc", "q4k_side"))
     per_step += 2 * (c1["routed"] - c0["routed"])
     launches = per_step  # == K_steps x kernels per step, the count in each of the two timed loops
 

@@ -41,7 +41,7 @@ class QgemmError(RuntimeError):
 class _Counters(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
                 ("quantize", "xprep", "q4k_tc", "q6k_tc", "q4k_small", "q6k_small", "q6k_prepack", "split_k",
-                 "routed", "ptq1_tc", "ptq1_prepack", "small_fused")]
+                 "routed", "ptq1_tc", "ptq1_prepack", "small_fused", "q4k_side")]
 
 
 class _Epilogue(ctypes.Structure):

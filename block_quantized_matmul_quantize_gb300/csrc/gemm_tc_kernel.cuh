@@ -209,6 +209,7 @@ template <int WT, int BM, int VAR>
 __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
                    const __grid_constant__ CUtensorMap tm_xbs, const __grid_constant__ CUtensorMap tm_dx,
+                   const __grid_constant__ CUtensorMap tm_side, const __grid_constant__ CUtensorMap tm_e,
                    void* __restrict__ y, int64_t ldy, const Epi epi, int M, int N, int nb, const TcWork wk,
                    uint32_t* __restrict__ status) {
     using L = Layout<WT, BM>;
@@ -227,6 +228,14 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     // stages, every K128 step consumes exactly one stage of each ring, so one
     // commit (on a_empty) releases both and the activation producers wait on it.
     constexpr bool MERGED_RELEASE = !SPLIT && (L::SCH == 2) && (BS == A_STAGES);
+    // Q4_K, plain variant: the side data (dmin-correction operands and the
+    // scale e of each row and superblock) depend on the weights alone, so they
+    // are made once per call (launch_q4k_side) and loaded by TMA beside the raw
+    // block, instead of being recomputed for every token tile (measured on
+    // GB300: recomputing them in four epilogue warps cost 2-3% of the GEMM at
+    // M=8192 K=N=5120, on the sub-partitions the expansion warps need).  The
+    // epilogue and routed variants keep the side-data warps.
+    constexpr bool PRE = L::CORR && VAR == VAR_PLAIN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -324,7 +333,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int r = 0; r < R; ++r) {
             mbar_init(&raw_full[r], 1);
-            mbar_init(&raw_empty[r], 4 * UG + (L::CORR ? 4 : 0));   // unpack warps (+ side-data warps)
+            mbar_init(&raw_empty[r], 4 * UG + (L::CORR && !PRE ? 4 : 0));   // unpack warps (+ side-data warps)
         }
         for (int s = 0; s < A_STAGES; ++s) {
             mbar_init(&a_full[s], 4);
@@ -335,7 +344,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
             mbar_init(&b_empty[s], 1);
         }
         for (int p = 0; p < SBN; ++p) {
-            mbar_init(&sb_full[p], 1 + 4);   // producer's bytes + the four warps writing the slot
+            mbar_init(&sb_full[p], PRE ? 1 : 1 + 4);   // producer's bytes (+ the four warps writing the slot)
             mbar_init(&sb_empty[p], 8);   // the epilogue warps, after acc_full covered the MMAs reading it
         }
         for (int p = 0; p < 2; ++p) {
@@ -352,6 +361,10 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
         tma_prefetch_desc(&tm_w);
         tma_prefetch_desc(&tm_dx);
         if (L::CORR) tma_prefetch_desc(&tm_xbs);
+        if (PRE) {
+            tma_prefetch_desc(&tm_side);
+            tma_prefetch_desc(&tm_e);
+        }
     }
     if (warp == W_MMA) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
@@ -430,9 +443,13 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                     if (!ok) break;
                     if (t == 0) griddep_wait();   // bsums and scales come from the preceding grid
                     uint8_t* sb = sb_slot(p);
-                    mbar_arrive_expect_tx(&sb_full[p], (L::CORR ? BM * 32 : 0) + BM * 4);
+                    mbar_arrive_expect_tx(&sb_full[p], (L::CORR ? BM * 32 : 0) + BM * 4 + (PRE ? 2 * BN * 32 + BN * 4 : 0));
                     if (L::CORR) tma_load_2d(&tm_xbs, &sb_full[p], sb + L::SB_BCORR, b * 16, m0);
                     tma_load_2d(&tm_dx, &sb_full[p], sb + L::SB_DX, m0, b);
+                    if constexpr (PRE) {   // both correction slabs, then the scales e
+                        tma_load_3d(&tm_side, &sb_full[p], sb + L::SB_ACORR, 0, n0, 2 * b);
+                        tma_load_2d(&tm_e, &sb_full[p], sb + L::SB_E, n0, b);
+                    }
                 }
             }
         }
@@ -790,7 +807,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
         // superblock (the dmin correction operands and the scale e, from the
         // block header in the raw ring), SBN - 1 superblocks ahead of the
         // accumulator they wait for, while the unpack warps only expand.
-        const bool side_writer = L::CORR && half == 1;
+        const bool side_writer = L::CORR && !PRE && half == 1;
         int ts = 0;         // next superblock whose side data is due
         int total_sb = 0;   // this CTA's superblocks
         if (side_writer) {
@@ -1074,7 +1091,11 @@ cudaError_t launch_t(const TcLaunch& a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const CUtensorMap tm_xbs = a.tm_xbs ? *a.tm_xbs : *a.tm_xh;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<WT, BM, VAR>, *a.tm_w, *a.tm_xh, tm_xbs, *a.tm_dx, a.y, a.ldy, a.epi,
+    const CUtensorMap tm_side = a.tm_side ? *a.tm_side : *a.tm_xh;   // (read only by the plain Q4_K variant)
+    const CUtensorMap tm_e = a.tm_e ? *a.tm_e : *a.tm_xh;
+    if (L::CORR && VAR == VAR_PLAIN && (!a.tm_side || !a.tm_e)) return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<WT, BM, VAR>, *a.tm_w, *a.tm_xh, tm_xbs, *a.tm_dx, tm_side, tm_e,
+                              a.y, a.ldy, a.epi,
                               static_cast<int>(a.M), static_cast<int>(a.N), static_cast<int>(a.K / 256), a.work,
                               a.status);
 }

@@ -56,16 +56,19 @@ constexpr int PTQ1_PACKED = 32;                 // 28 B + 4 B of zero padding (1
 // ---- kernels' host launchers (each returns cudaError_t of the launch) ----
 // With xh != nullptr the same launch also writes the tile GEMM's operand
 // planes (as launch_xprep would from its output) and zeroes the split-tile
-// counters (TC_MAX_CUT_TILES ints).
+// counters (TC_COUNTERS ints).  `dependent`: launched as a programmatic
+// dependent of the preceding kernel (the Q4_K side-data kernel), which it
+// joins before it ends.
 cudaError_t launch_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d,
                                 int16_t* bsums, cudaStream_t s, __half* xh = nullptr, __half* xbs = nullptr,
-                                float* dxT = nullptr, int64_t Mp = 0, int* counters = nullptr);
+                                float* dxT = nullptr, int64_t Mp = 0, int* counters = nullptr, bool dependent = false);
 
 // Q8_K planes -> tensor-core operand planes in the workspace:
 //   xh  [M][K] fp16 (the int8 values), xbs [M][K/16] fp16 (bsums),
 //   dxT [nb][Mp] fp32 (d transposed, Mp = M rounded up to 4, tail zeroed).
 cudaError_t launch_xprep(const int8_t* qs, const float* d, const int16_t* bsums, int64_t M, int64_t K,
-                         __half* xh, __half* xbs, float* dxT, int64_t Mp, int* counters, cudaStream_t s);
+                         __half* xh, __half* xbs, float* dxT, int64_t Mp, int* counters, cudaStream_t s,
+                         bool dependent = false);
 
 // Expert routing (route.cu) for the routed GEMM (MUL_MAT_ID): the P = M *
 // top_k (token, slot) pairs are grouped by expert id.  Each expert's rows
@@ -139,7 +142,16 @@ struct TcLaunch {
     const CUtensorMap* tm_xh;   // fp16 [M][K], box {64, bm}, 128B swizzle
     const CUtensorMap* tm_xbs;  // fp16 [M][K/16], box {16, bm}, 32B swizzle (Q4_K only)
     const CUtensorMap* tm_dx;   // fp32 [nb][Mp], box {bm, 1}
+    // Q4_K, plain variant: the side words of every (row, superblock), made by
+    // launch_q4k_side before the GEMM (q4k_side's values: the dmin-correction
+    // operands and the scale e), loaded beside the raw blocks
+    const CUtensorMap* tm_side; // uint32 [2 nb][N][8] (superblock b: slabs 2b, 2b+1), box {8, 128, 2}, 32B swizzle
+    const CUtensorMap* tm_e;    // fp32 [nb][Np], box {128, 1}
 };
+// The side words: a1 (slab 2b) and a2 (slab 2b+1) of row n at [slab][n][0..7],
+// e at e[b][n] (row stride Np = N rounded up to 4).
+cudaError_t launch_q4k_side(const void* w, int64_t N, int64_t nb, int64_t ldw, uint32_t* side, float* e,
+                            int64_t Np, cudaStream_t s);
 size_t tc_smem_bytes(int wtype, int bm);
 cudaError_t tc_prepare(int wtype, int bm);   // sets the dynamic smem attribute (per device)
 cudaError_t launch_gemm_tc(const TcLaunch& a, cudaStream_t s);

@@ -142,6 +142,12 @@ __device__ __forceinline__ void tma_load_2d(const void* tmap, uint64_t* bar, voi
         ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(const void* tmap, uint64_t* bar, void* dst, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
 // Same, with an L2 cache policy (from createpolicy) for the loaded lines.
 __device__ __forceinline__ void tma_load_2d_hint(const void* tmap, uint64_t* bar, void* dst, int x, int y,
                                                  uint64_t policy) {

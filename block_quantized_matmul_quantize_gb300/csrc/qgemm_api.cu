@@ -31,9 +31,9 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ------------------------------------------------------------ global state
-std::atomic<uint64_t> g_cnt[12];
+std::atomic<uint64_t> g_cnt[13];
 enum { C_QUANT, C_XPREP, C_Q4K_TC, C_Q6K_TC, C_Q4K_SMALL, C_Q6K_SMALL, C_PREPACK, C_SPLITK, C_ROUTED, C_PTQ1_TC,
-       C_PTQ1_PREPACK, C_SMALL_FUSED };
+       C_PTQ1_PREPACK, C_SMALL_FUSED, C_SIDE };
 // SMALL_M_MAX defaults to the measured crossover: the streaming kernel wins up
 // to 8 tokens at K = N = 5120 and at K = 4096, N = 14336.
 std::atomic<int64_t> g_opt[5] = {{qg::SMALL_M_LIMIT}, {0}, {0}, {0}, {0}};
@@ -113,6 +113,22 @@ int make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t 
     CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(QGEMM_ECUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return QGEMM_OK;
+}
+
+// A 3D map: dims {inner, mid, outer} elements, byte strides of mid and outer.
+int make_map3(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
+              uint64_t mid_bytes, uint64_t outer_bytes, uint32_t box_inner, uint32_t box_mid, uint32_t box_outer,
+              CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(QGEMM_ECUDA, "cuTensorMapEncodeTiled not available from the driver");
+    const cuuint64_t dims[3] = {inner, mid, outer};
+    const cuuint64_t strides[2] = {mid_bytes, outer_bytes};
+    const cuuint32_t box[3] = {box_inner, box_mid, box_outer};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QGEMM_ECUDA, "cuTensorMapEncodeTiled (3D) failed (%d)", static_cast<int>(r));
     return QGEMM_OK;
 }
 
@@ -208,6 +224,14 @@ size_t plane_bytes(int64_t M, int64_t K) {
 }
 constexpr size_t COUNTER_BYTES = qg::TC_COUNTERS * sizeof(int);
 
+// The Q4_K side words (qg::launch_q4k_side) of an N x K weight matrix: two
+// 32-byte slabs per row and superblock, then the fp32 scales e [nb][Np].
+int64_t side_np(int64_t N) { return (N + 3) / 4 * 4; }
+size_t side_slab_bytes(int64_t N, int64_t K) { return align256(size_t(K / 256) * 2 * size_t(N) * 32); }
+size_t side_bytes(int64_t N, int64_t K) {
+    return N > 0 ? side_slab_bytes(N, K) + align256(size_t(K / 256) * size_t(side_np(N)) * 4) : 0;
+}
+
 size_t partial_bytes(const Plan& p) {
     const int64_t cut = static_cast<int64_t>(p.work.n_tiles) * p.work.m_tiles - p.work.full_items;
     return cut > 0 ? size_t(cut) * p.work.parts * 128 * p.bm * sizeof(float) : 0;
@@ -224,16 +248,18 @@ int sizing_sm_count() {
 }
 
 // The workspace of the tile GEMM: the operand planes, the cut-tile counters,
-// then the partial tiles of the cut tiles.
+// the Q4_K side words (sized by N), then the partial tiles of the cut tiles.
 struct WsPlanes {
     __half* xh;
     __half* xbs;
     float* dxT;
     int64_t Mp;
     int* counters;
+    uint32_t* side;
+    float* side_e;
     float* partials;
 };
-WsPlanes ws_planes(void* ws, int64_t M, int64_t K) {
+WsPlanes ws_planes(void* ws, int64_t M, int64_t K, int64_t N = 0) {
     uint8_t* base = static_cast<uint8_t*>(ws);
     WsPlanes p{};
     p.Mp = (M + 3) / 4 * 4;
@@ -241,13 +267,16 @@ WsPlanes ws_planes(void* ws, int64_t M, int64_t K) {
     p.xbs = reinterpret_cast<__half*>(base + align256(size_t(M) * K * 2));
     p.dxT = reinterpret_cast<float*>(base + align256(size_t(M) * K * 2) + align256(size_t(M) * (K / 16) * 2));
     p.counters = reinterpret_cast<int*>(base + plane_bytes(M, K));
-    p.partials = reinterpret_cast<float*>(base + plane_bytes(M, K) + COUNTER_BYTES);
+    uint8_t* side = base + plane_bytes(M, K) + COUNTER_BYTES;
+    p.side = reinterpret_cast<uint32_t*>(side);
+    p.side_e = reinterpret_cast<float*>(side + side_slab_bytes(N, K));
+    p.partials = reinterpret_cast<float*>(side + side_bytes(N, K));
     return p;
 }
 
 int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs, const float* xd,
            const int16_t* xbsums, int64_t M, void* y, int64_t ldy, void* ws, size_t ws_bytes,
-           cudaStream_t stream, bool prepared, const qg::Epi& epi = qg::Epi{}) {
+           cudaStream_t stream, bool prepared, const qg::Epi& epi = qg::Epi{}, bool side_ready = false) {
     DevState* ds = nullptr;
     int rc = device_state(&ds);
     if (rc) return rc;
@@ -258,16 +287,26 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
 
     const Plan pl = plan_tc(M, N, K, ds->sm_count);
     const int64_t nb = K / 256;
-    const WsPlanes wp = ws_planes(ws, M, K);
+    const WsPlanes wp = ws_planes(ws, M, K, N);
     const int64_t Mp = wp.Mp;
     __half* xh = wp.xh;
     __half* xbs = wp.xbs;
     float* dxT = wp.dxT;
 
     cudaError_t e = cudaSuccess;
+    // Q4_K without an output epilogue: the side words come precomputed (see
+    // gemm_tc_kernel.cuh), made here unless the caller made them already
+    const bool pre = wtype == 4 && epi.out == qg::OUT_F32 && epi.act == qg::ACT_NONE && epi.bias == nullptr;
+    const bool side_now = pre && !side_ready;
+    if (side_now) {
+        e = qg::launch_q4k_side(w, N, nb, ldw, wp.side, wp.side_e, side_np(N), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "side-data launch");
+        g_cnt[C_SIDE]++;
+    }
     if (!prepared) {
-        // (a prepared workspace already holds these planes: qgemm_quantize_q8k_prep)
-        e = qg::launch_xprep(xqs, xd, xbsums, M, K, xh, xbs, dxT, Mp, wp.counters, stream);
+        // (a prepared workspace already holds these planes: qgemm_quantize_q8k_prep;
+        // after the side-data kernel this one runs beside it)
+        e = qg::launch_xprep(xqs, xd, xbsums, M, K, xh, xbs, dxT, Mp, wp.counters, stream, side_now);
         if (e != cudaSuccess) return cuda_fail(e, "operand preparation launch");
         g_cnt[C_XPREP]++;
     }
@@ -286,6 +325,17 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
     if ((rc = make_map(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dxT, Mp, nb, uint64_t(Mp) * 4, pl.bm, 1,
                        CU_TENSOR_MAP_SWIZZLE_NONE)))
         return rc;
+    CUtensorMap tm_side, tm_e;
+    if (pre) {
+        // slabs [2 nb][N][8 words]: a 128-row box of both slabs of superblock b lands as the
+        // two 32-byte-swizzled correction operands the MMA reads
+        if ((rc = make_map3(&tm_side, CU_TENSOR_MAP_DATA_TYPE_UINT32, wp.side, 8, N, uint64_t(2) * nb, 32,
+                            uint64_t(N) * 32, 8, 128, 2, CU_TENSOR_MAP_SWIZZLE_32B)))
+            return rc;
+        if ((rc = make_map(&tm_e, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, wp.side_e, N, nb, uint64_t(side_np(N)) * 4, 128, 1,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)))
+            return rc;
+    }
 
     qg::TcLaunch a{};
     a.wtype = wtype;
@@ -306,6 +356,8 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
     a.tm_xh = &tm_xh;
     a.tm_xbs = wtype == 4 ? &tm_xbs : nullptr;
     a.tm_dx = &tm_dx;
+    a.tm_side = pre ? &tm_side : nullptr;
+    a.tm_e = pre ? &tm_e : nullptr;
     cudaEvent_t evb = g_ev_before.load(), eva = g_ev_after.load();
     if (evb) cudaEventRecord(evb, stream);
     e = qg::launch_gemm_tc(a, stream);
@@ -593,7 +645,7 @@ size_t qgemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || K <= 0 || K % 256) return 0;
     const size_t base = plane_bytes(M, K) + COUNTER_BYTES;
     if (N <= 0) return base;
-    return base + partial_bytes(plan_tc(M, N, K, sizing_sm_count()));
+    return base + side_bytes(N, K) + partial_bytes(plan_tc(M, N, K, sizing_sm_count()));
 }
 
 static int gemm_common_checks(const void* w, int64_t N, int64_t K, const int8_t* xqs, const float* xd,
@@ -673,8 +725,8 @@ int qgemm_q6k(const void* w_packed, int64_t N, int64_t K, const int8_t* xqs, con
                   reinterpret_cast<cudaStream_t>(stream), false);
 }
 
-int qgemm_quantize_q8k_prep(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d,
-                            int16_t* bsums, void* workspace, size_t workspace_bytes, qgemm_stream_t stream) {
+static int quantize_prep_impl(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d, int16_t* bsums,
+                              void* workspace, size_t workspace_bytes, qgemm_stream_t stream, bool dependent) {
     clear_err();
     int rc = check_mk(M, K);
     if (rc) return rc;
@@ -690,10 +742,15 @@ int qgemm_quantize_q8k_prep(const float* x, int64_t M, int64_t K, int64_t ldx, i
     if (!aligned(workspace, 256)) return fail(QGEMM_EALIGN, "workspace must be 256-byte aligned");
     const WsPlanes wp = ws_planes(workspace, M, K);
     cudaError_t e = qg::launch_quantize_q8k(x, M, K, ldx, qs, d, bsums, reinterpret_cast<cudaStream_t>(stream), wp.xh,
-                                            wp.xbs, wp.dxT, wp.Mp, wp.counters);
+                                            wp.xbs, wp.dxT, wp.Mp, wp.counters, dependent);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     g_cnt[C_QUANT]++;
     return QGEMM_OK;
+}
+
+int qgemm_quantize_q8k_prep(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d,
+                            int16_t* bsums, void* workspace, size_t workspace_bytes, qgemm_stream_t stream) {
+    return quantize_prep_impl(x, M, K, ldx, qs, d, bsums, workspace, workspace_bytes, stream, false);
 }
 
 // fp32 activations in, Y out: the fused small-M kernel for the fewest tokens,
@@ -710,9 +767,25 @@ static int run_f32(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, 
         g_cnt[C_QUANT]++;
         return run_small(wtype, w, N, K, ldw, qs, d, bsums, M, y, ldy, st);
     }
-    int rc = qgemm_quantize_q8k_prep(x, M, K, ldx, qs, d, bsums, workspace, workspace_bytes, stream);
+    // Q4_K: the side words first (they need only the weights), so that the GEMM
+    // still starts under the quantizer
+    bool side_ready = false;
+    if (wtype == 4) {
+        const size_t need = qgemm_workspace_bytes(M, N, K);
+        if (!workspace || workspace_bytes < need)
+            return fail(QGEMM_EINVAL, "workspace of %zu bytes needed (got %zu)", need,
+                        workspace ? workspace_bytes : size_t(0));
+        if (!aligned(workspace, 256)) return fail(QGEMM_EALIGN, "workspace must be 256-byte aligned");
+        const WsPlanes wp = ws_planes(workspace, M, K, N);
+        const cudaError_t e = qg::launch_q4k_side(w, N, K / 256, ldw, wp.side, wp.side_e, side_np(N), st);
+        if (e != cudaSuccess) return cuda_fail(e, "side-data launch");
+        g_cnt[C_SIDE]++;
+        side_ready = true;
+    }
+    int rc = quantize_prep_impl(x, M, K, ldx, qs, d, bsums, workspace, workspace_bytes, stream, side_ready);
     if (rc) return rc;
-    return run_tc(wtype, w, N, K, ldw, qs, d, bsums, M, y, ldy, workspace, workspace_bytes, st, true);
+    return run_tc(wtype, w, N, K, ldw, qs, d, bsums, M, y, ldy, workspace, workspace_bytes, st, true, qg::Epi{},
+                  side_ready);
 }
 
 static int f32_checks(const float* x, int64_t ldx, int64_t M, int64_t K) {
@@ -840,6 +913,7 @@ int qgemm_get_counters(qgemm_counters* out) {
     out->ptq1_tc = g_cnt[C_PTQ1_TC];
     out->ptq1_prepack = g_cnt[C_PTQ1_PREPACK];
     out->small_fused = g_cnt[C_SMALL_FUSED];
+    out->q4k_side = g_cnt[C_SIDE];
     return QGEMM_OK;
 }
 

@@ -19,6 +19,29 @@ namespace {
 __device__ __forceinline__ void allow_dependent_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Launched as a programmatic dependent of the Q4_K side-data kernel (whose
+// output this kernel does not read), this kernel ends only after that one
+// has: the GEMM that depends on this kernel then sees both outputs.  (A
+// no-op without such a predecessor.)
+__device__ __forceinline__ void join_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// A launch of `kernel` that may start while the preceding kernel in the
+// stream runs (programmatic stream serialization), or a plain launch.
+template <typename... Params, typename... Args>
+cudaError_t launch_maybe_dependent(bool dependent, void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t st,
+                                   Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 }  // namespace
 
 namespace qg {
@@ -108,6 +131,7 @@ __global__ void __launch_bounds__(QWARPS * 32, 8) quantize_q8k_kernel(const floa
         if (lane == 0) prep.dxT[b * prep.Mp + m] = d;
         if (m == M - 1 && lane >= 1 && lane < 4 && m + lane < prep.Mp) prep.dxT[b * prep.Mp + m + lane] = 0.0f;
     }
+    join_predecessor();
 }
 
 // Q8_K -> fp16 operand planes.  Every int8 value and every bsum (|bsum| <=
@@ -152,6 +176,7 @@ __global__ void xprep_kernel(const int8_t* __restrict__ qs, const float* __restr
             dxT[j] = (m < M) ? d[m * nb + b] : 0.0f;
         }
     }
+    join_predecessor();
 }
 
 // SRC-byte blocks -> DST-byte blocks (the same bytes, zeros after), so that
@@ -227,31 +252,32 @@ int grid_for(int64_t work, int threads) {
 
 cudaError_t launch_quantize_q8k(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, float* d,
                                 int16_t* bsums, cudaStream_t s, __half* xh, __half* xbs, float* dxT, int64_t Mp,
-                                int* counters) {
+                                int* counters, bool dependent) {
     const int64_t chunks = M * (K >> 8);
     const int64_t blocks = (chunks + QWARPS - 1) / QWARPS;
     const PrepOut prep{xh, xbs, dxT, Mp, counters};
     const bool wide = chunks >= (int64_t(1) << 31);
     const dim3 grid(static_cast<unsigned>(blocks)), block(QWARPS * 32);
-    if (xh) {
-        if (wide)
-            quantize_q8k_kernel<true, true><<<grid, block, 0, s>>>(x, M, K, ldx, qs, d, bsums, prep);
-        else
-            quantize_q8k_kernel<true, false><<<grid, block, 0, s>>>(x, M, K, ldx, qs, d, bsums, prep);
-    } else {
-        if (wide)
-            quantize_q8k_kernel<false, true><<<grid, block, 0, s>>>(x, M, K, ldx, qs, d, bsums, prep);
-        else
-            quantize_q8k_kernel<false, false><<<grid, block, 0, s>>>(x, M, K, ldx, qs, d, bsums, prep);
-    }
-    return cudaGetLastError();
+    cudaError_t e;
+    if (xh)
+        e = wide ? launch_maybe_dependent(dependent, quantize_q8k_kernel<true, true>, grid, block, s, x, M, K, ldx, qs,
+                                          d, bsums, prep)
+                 : launch_maybe_dependent(dependent, quantize_q8k_kernel<true, false>, grid, block, s, x, M, K, ldx,
+                                          qs, d, bsums, prep);
+    else
+        e = wide ? launch_maybe_dependent(dependent, quantize_q8k_kernel<false, true>, grid, block, s, x, M, K, ldx,
+                                          qs, d, bsums, prep)
+                 : launch_maybe_dependent(dependent, quantize_q8k_kernel<false, false>, grid, block, s, x, M, K, ldx,
+                                          qs, d, bsums, prep);
+    return e;
 }
 
 cudaError_t launch_xprep(const int8_t* qs, const float* d, const int16_t* bsums, int64_t M, int64_t K,
-                         __half* xh, __half* xbs, float* dxT, int64_t Mp, int* counters, cudaStream_t s) {
+                         __half* xh, __half* xbs, float* dxT, int64_t Mp, int* counters, cudaStream_t s,
+                         bool dependent) {
     const int64_t work = M * (K >> 4) + (K >> 8) * Mp;
-    xprep_kernel<<<grid_for(work, 256), 256, 0, s>>>(qs, d, bsums, M, K, xh, xbs, dxT, Mp, counters);
-    return cudaGetLastError();
+    return launch_maybe_dependent(dependent, xprep_kernel, dim3(grid_for(work, 256)), dim3(256), s, qs, d, bsums, M, K,
+                                  xh, xbs, dxT, Mp, counters);
 }
 
 cudaError_t launch_q8k_aos(int8_t* qs, float* d, int16_t* bsums, int64_t M, int64_t K, void* aos, bool to_aos,

@@ -402,6 +402,7 @@ typedef struct {
     uint64_t ptq1_tc;      /* PTQ1_0 tile GEMM launches             */
     uint64_t ptq1_prepack; /* PTQ1_0 repack launches                */
     uint64_t small_fused;  /* small-M launches that quantized X themselves (also counted in q4k/q6k_small) */
+    uint64_t q4k_side;     /* Q4_K side-data launches (before the tile GEMM without an output epilogue) */
 } qgemm_counters;
 QGEMM_API int qgemm_get_counters(qgemm_counters *out);
 QGEMM_API int qgemm_reset_counters(void);

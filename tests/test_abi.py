@@ -72,7 +72,7 @@ def test_prepared_validation(L):
     assert P(FAKE, 1, 100, 100, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == qg.QGEMM_EINVAL
     assert P(FAKE, 0, 256, 256, FAKE, FAKE, FAKE, None, 0, None) == qg.QGEMM_OK       # empty
     assert P(MISALIGNED, 2, 256, 256, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == qg.QGEMM_EALIGN
-    need = L.qgemm_workspace_bytes(2, 1, 256)
+    need = L.qgemm_workspace_bytes(2, 0, 256)   # N = 0: the planes and counters the quantizer writes
     assert P(FAKE, 2, 256, 256, FAKE, FAKE, FAKE, None, need, None) == qg.QGEMM_EINVAL
     assert P(FAKE, 2, 256, 256, FAKE, FAKE, FAKE, FAKE, need - 1, None) == qg.QGEMM_EINVAL
     assert P(FAKE, 2, 256, 256, FAKE, FAKE, FAKE, ctypes.c_void_p(0x100010), need, None) == qg.QGEMM_EALIGN
@@ -172,7 +172,9 @@ def test_size_queries(L):
     assert L.qgemm_workspace_bytes(4, 8, 300) == 0
     M, K = 5, 512
     # xh fp16 5*512*2 = 5120; bsums fp16 5*32*2 = 320 -> 512; d^T fp32 2*8*4 = 64 -> 256
-    expect = 5120 + 512 + 256 + 1024 * 8 * 4   # + the cut-tile counters (8 per tile); one tile: no partial tiles
+    # + the cut-tile counters (8 per tile) + the Q4_K side words (2 superblocks x 2 slabs x 8 rows x 32 B,
+    # and the scales e 2 x 8 fp32 -> 256); one tile: no partial tiles
+    expect = 5120 + 512 + 256 + 1024 * 8 * 4 + 1024 + 256
     assert L.qgemm_workspace_bytes(M, 8, K) == expect
     assert L.qgemm_q6k_packed_bytes(3, 512) == 3 * 2 * 224
     assert L.qgemm_q6k_packed_bytes(3, 100) == 0
