@@ -23,6 +23,7 @@ QGEMM_DEV_TIMEOUT, QGEMM_DEV_Q4K_RANGE, QGEMM_DEV_BAD_EXPERT = 0x1, 0x2, 0x8
 QGEMM_DEBUG_EXPAND_BYTES = 1152
 QGEMM_OPT_SMALL_M_MAX, QGEMM_OPT_FORCE_BM, QGEMM_OPT_FORCE_SPLITS = 0, 1, 2
 QGEMM_OPT_WAIT_LIMIT_US, QGEMM_OPT_TEST_SKIP_ARRIVAL = 3, 4
+QGEMM_OPT_Q4K_SIDE_MIN_TILES = 5
 QGEMM_SMALL_M_DEFAULT = 8   # the library's default for QGEMM_OPT_SMALL_M_MAX
 
 QGEMM_OUT_F32, QGEMM_OUT_F16, QGEMM_OUT_BF16 = 0, 1, 2

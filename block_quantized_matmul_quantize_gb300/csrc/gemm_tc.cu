@@ -1,7 +1,7 @@
 // gemm_tc.cu -- the tile GEMM's plain instantiations (fp32 output, no
 // epilogue, host work list) and its host dispatch; the kernel is in
-// gemm_tc_kernel.cuh, the epilogue and routed instantiations in
-// gemm_tc_epi.cu and gemm_tc_routed.cu (built in parallel).
+// gemm_tc_kernel.cuh, the epilogue, routed and Q4_K self-side instantiations
+// in gemm_tc_epi.cu, gemm_tc_routed.cu and gemm_tc_self.cu (built in parallel).
 #include "gemm_tc_kernel.cuh"
 
 namespace qg {
@@ -20,6 +20,7 @@ cudaError_t tc_prepare(int wtype, int bm) {
     if (wtype == 4 || wtype == 6) {   // (the epilogue and routed variants: Q4_K and Q6_K)
         cudaError_t e = tc_prepare_epi(wtype, bm);
         if (e == cudaSuccess) e = tc_prepare_routed(wtype, bm);
+        if (e == cudaSuccess && wtype == 4) e = tc_prepare_self(bm);
         if (e != cudaSuccess) return e;
     }
 #define QG_CASE(W, B) \
@@ -68,6 +69,7 @@ cudaError_t launch_q4k_side(const void* w, int64_t N, int64_t nb, int64_t ldw, u
 cudaError_t launch_gemm_tc(const TcLaunch& a, cudaStream_t s) {
     if (a.work.experts > 0) return launch_gemm_tc_routed(a, s);
     if (a.epi.out != OUT_F32 || a.epi.act != ACT_NONE || a.epi.bias != nullptr) return launch_gemm_tc_epi(a, s);
+    if (a.wtype == 4 && !a.tm_side) return launch_gemm_tc_self(a, s);
 #define QG_CASE(W, B) \
     if (a.wtype == W && a.bm == B) return launch_t<W, B, VAR_PLAIN>(a, s);
     QG_CASE(4, 16) QG_CASE(4, 32) QG_CASE(4, 64) QG_CASE(4, 128)

@@ -203,8 +203,11 @@ __device__ __forceinline__ void fold4(float* a, const uint32_t* S, float2 ee, fl
 // spills and slowed the plain GEMM by 5-8%):
 //   VAR_PLAIN   fp32 output, the work list from the host plan;
 //   VAR_EPI     plus the output epilogue (bias, activation, fp16/bf16 output);
-//   VAR_ROUTED  the routed GEMM (work list and output rows from the routing).
-enum : int { VAR_PLAIN = 0, VAR_EPI = 1, VAR_ROUTED = 2 };
+//   VAR_ROUTED  the routed GEMM (work list and output rows from the routing);
+//   VAR_SELF    VAR_PLAIN for Q4_K with the side words computed in the kernel
+//               rather than loaded (for one token tile per weight tile, where
+//               each tile's side words are made once either way).
+enum : int { VAR_PLAIN = 0, VAR_EPI = 1, VAR_ROUTED = 2, VAR_SELF = 3 };
 template <int WT, int BM, int VAR>
 __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,

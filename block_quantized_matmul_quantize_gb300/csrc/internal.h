@@ -158,6 +158,10 @@ cudaError_t launch_gemm_tc(const TcLaunch& a, cudaStream_t s);
 // (the epilogue instantiations, gemm_tc_epi.cu; launch_gemm_tc dispatches to them)
 cudaError_t tc_prepare_epi(int wtype, int bm);
 cudaError_t launch_gemm_tc_epi(const TcLaunch& a, cudaStream_t s);
+// (Q4_K with the side words made in the kernel, gemm_tc_self.cu: a plain
+// launch without tm_side)
+cudaError_t tc_prepare_self(int bm);
+cudaError_t launch_gemm_tc_self(const TcLaunch& a, cudaStream_t s);
 // (the routed instantiations, gemm_tc_routed.cu: work.experts > 0)
 cudaError_t tc_prepare_routed(int wtype, int bm);
 cudaError_t launch_gemm_tc_routed(const TcLaunch& a, cudaStream_t s);

@@ -36,7 +36,14 @@ enum { C_QUANT, C_XPREP, C_Q4K_TC, C_Q6K_TC, C_Q4K_SMALL, C_Q6K_SMALL, C_PREPACK
        C_PTQ1_PREPACK, C_SMALL_FUSED, C_SIDE };
 // SMALL_M_MAX defaults to the measured crossover: the streaming kernel wins up
 // to 8 tokens at K = N = 5120 and at K = 4096, N = 14336.
-std::atomic<int64_t> g_opt[5] = {{qg::SMALL_M_LIMIT}, {0}, {0}, {0}, {0}};
+// Q4K_SIDE_MIN_TILES defaults to the measured crossover (Q4_K fp32 entry,
+// CUDA-graph steps on one GB300, side-data kernel against side words made in
+// the GEMM): with one to three token tiles per weight tile the kernel adds
+// more than it saves (K = N = 5120: M = 64 26.7 against 24.6 us, M = 256 39.9
+// against 38.7, M = 384 41.4 against 39.4); at four the two are even (M = 512
+// 57.8 and 57.8; K = 2048, N = 11008: 47.6 and 47.6); beyond, it saves (M =
+// 2048: 135.5 against 140.6 us).
+std::atomic<int64_t> g_opt[6] = {{qg::SMALL_M_LIMIT}, {0}, {0}, {0}, {0}, {4}};
 // the wait limit and the test-only skip switch, as the kernels take them
 qg::WaitCfg wait_cfg() {
     return qg::WaitCfg{static_cast<int>(g_opt[QGEMM_OPT_WAIT_LIMIT_US].load()),
@@ -274,6 +281,11 @@ WsPlanes ws_planes(void* ws, int64_t M, int64_t K, int64_t N = 0) {
     return p;
 }
 
+// Q4_K without an output epilogue: the side words come precomputed (their
+// own kernel, loaded by the GEMM) when a weight tile meets at least
+// QGEMM_OPT_Q4K_SIDE_MIN_TILES token tiles, else the GEMM makes them itself.
+bool q4k_side_precomputed(const Plan& pl) { return pl.work.m_tiles >= g_opt[QGEMM_OPT_Q4K_SIDE_MIN_TILES].load(); }
+
 int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const int8_t* xqs, const float* xd,
            const int16_t* xbsums, int64_t M, void* y, int64_t ldy, void* ws, size_t ws_bytes,
            cudaStream_t stream, bool prepared, const qg::Epi& epi = qg::Epi{}, bool side_ready = false) {
@@ -295,8 +307,10 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
 
     cudaError_t e = cudaSuccess;
     // Q4_K without an output epilogue: the side words come precomputed (see
-    // gemm_tc_kernel.cuh), made here unless the caller made them already
-    const bool pre = wtype == 4 && epi.out == qg::OUT_F32 && epi.act == qg::ACT_NONE && epi.bias == nullptr;
+    // gemm_tc_kernel.cuh) for enough token tiles, made here unless the caller
+    // made them already
+    const bool pre = wtype == 4 && epi.out == qg::OUT_F32 && epi.act == qg::ACT_NONE && epi.bias == nullptr &&
+                     q4k_side_precomputed(pl);
     const bool side_now = pre && !side_ready;
     if (side_now) {
         e = qg::launch_q4k_side(w, N, nb, ldw, wp.side, wp.side_e, side_np(N), stream);
@@ -770,7 +784,11 @@ static int run_f32(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, 
     // Q4_K: the side words first (they need only the weights), so that the GEMM
     // still starts under the quantizer
     bool side_ready = false;
+    DevState* ds = nullptr;
     if (wtype == 4) {
+        if (int rc = device_state(&ds)) return rc;
+    }
+    if (wtype == 4 && q4k_side_precomputed(plan_tc(M, N, K, ds->sm_count))) {
         const size_t need = qgemm_workspace_bytes(M, N, K);
         if (!workspace || workspace_bytes < need)
             return fail(QGEMM_EINVAL, "workspace of %zu bytes needed (got %zu)", need,
@@ -1030,7 +1048,7 @@ int qgemm_get_device_status(uint32_t* bits, uint32_t* site) {
 
 int qgemm_set_option(int option, int64_t value) {
     clear_err();
-    if (option < 0 || option > QGEMM_OPT_TEST_SKIP_ARRIVAL) return fail(QGEMM_EINVAL, "unknown option %d", option);
+    if (option < 0 || option > QGEMM_OPT_Q4K_SIDE_MIN_TILES) return fail(QGEMM_EINVAL, "unknown option %d", option);
     if (value < 0) return fail(QGEMM_EINVAL, "option values are >= 0");
     if (option == QGEMM_OPT_FORCE_BM && value != 0 && value != 16 && value != 32 && value != 64 && value != 128)
         return fail(QGEMM_EINVAL, "FORCE_BM must be 0, 16, 32, 64 or 128");
@@ -1039,12 +1057,14 @@ int qgemm_set_option(int option, int64_t value) {
     if (option == QGEMM_OPT_WAIT_LIMIT_US && value > 10000000)
         return fail(QGEMM_EINVAL, "WAIT_LIMIT_US must be 0..10000000 (10 s)");
     if (option == QGEMM_OPT_TEST_SKIP_ARRIVAL && value > 2) return fail(QGEMM_EINVAL, "TEST_SKIP_ARRIVAL must be 0..2");
+    if (option == QGEMM_OPT_Q4K_SIDE_MIN_TILES && value > (int64_t(1) << 30))
+        return fail(QGEMM_EINVAL, "Q4K_SIDE_MIN_TILES must be 0..2^30");
     g_opt[option] = value;
     return QGEMM_OK;
 }
 
 int64_t qgemm_get_option(int option) {
-    if (option < 0 || option > QGEMM_OPT_TEST_SKIP_ARRIVAL) return -1;
+    if (option < 0 || option > QGEMM_OPT_Q4K_SIDE_MIN_TILES) return -1;
     return g_opt[option].load();
 }
 

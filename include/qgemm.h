@@ -133,10 +133,14 @@ QGEMM_API int qgemm_unpack_q8k_aos(const void *aos, int64_t M, int64_t K, int8_t
  * Workspace bytes the GEMM calls need for M tokens, N weight rows and depth K
  * on the current device: the fp16 tensor-core operand copy of the Q8_K
  * activations (about 2.1 B per element of M*K), the cut-tile counters
- * (4 KiB), and the partial tiles of the cut tiles (128 x BM fp32 per K part;
- * tiles are cut when there are fewer of them than SMs, or when a last round
- * would leave at least half of the SMs idle).  0 when the small-M path runs.
- * The workspace must be 256-B aligned. */
+ * (32 KiB), the Q4_K side words (68 B per weight block: the dmin-correction
+ * operands and scales that the Q4_K calls without an output epilogue make
+ * from the weights before the GEMM; counted for every weight type), and the
+ * partial tiles of the cut tiles (128 x BM fp32 per K part; tiles are cut
+ * when there are fewer of them than SMs, or when a last round would leave at
+ * least half of the SMs idle).  With N = 0: the activation part alone (what
+ * qgemm_quantize_q8k_prep writes).  0 for M = 0 or an invalid K.  The
+ * workspace must be 256-B aligned. */
 QGEMM_API size_t qgemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* qgemm_q4k: Y[M][N] = X_q8k[M][K] * W_q4k[N][K]^T.
@@ -442,7 +446,14 @@ typedef enum {
      * After a timeout, a workspace filled by qgemm_quantize_q8k_prep must be
      * filled again before another _prepared call (its cut-tile counters may
      * be left nonzero); the other calls prepare their workspace themselves. */
-    QGEMM_OPT_TEST_SKIP_ARRIVAL = 4
+    QGEMM_OPT_TEST_SKIP_ARRIVAL = 4,
+    /* Q4_K tile GEMM without an output epilogue: the side words of the
+     * weight blocks (the dmin-correction operands and scales, which depend
+     * on the weights alone) are made by a kernel of their own and loaded by
+     * the GEMM when a weight tile meets at least this many token tiles;
+     * below that, the GEMM makes them itself.  Y is the same either way.
+     * 0 = always the separate kernel; default 4. */
+    QGEMM_OPT_Q4K_SIDE_MIN_TILES = 5
 } qgemm_option;
 QGEMM_API int qgemm_set_option(int option, int64_t value);
 QGEMM_API int64_t qgemm_get_option(int option);

@@ -222,7 +222,13 @@ def test_options_and_counters(L):
     # the wait limit and the test-only skip switch: range-checked before any device access
     assert L.qgemm_set_option(qg.QGEMM_OPT_WAIT_LIMIT_US, 10_000_001) == qg.QGEMM_EINVAL
     assert L.qgemm_set_option(qg.QGEMM_OPT_TEST_SKIP_ARRIVAL, 3) == qg.QGEMM_EINVAL
-    assert L.qgemm_set_option(5, 0) == qg.QGEMM_EINVAL
+    assert L.qgemm_set_option(6, 0) == qg.QGEMM_EINVAL
+    # the Q4_K side-data threshold: default 4 token tiles, any count up to 2^30
+    assert L.qgemm_get_option(qg.QGEMM_OPT_Q4K_SIDE_MIN_TILES) == 4
+    assert L.qgemm_set_option(qg.QGEMM_OPT_Q4K_SIDE_MIN_TILES, (1 << 30) + 1) == qg.QGEMM_EINVAL
+    assert L.qgemm_set_option(qg.QGEMM_OPT_Q4K_SIDE_MIN_TILES, 0) == qg.QGEMM_OK
+    assert L.qgemm_get_option(qg.QGEMM_OPT_Q4K_SIDE_MIN_TILES) == 0
+    assert L.qgemm_set_option(qg.QGEMM_OPT_Q4K_SIDE_MIN_TILES, 4) == qg.QGEMM_OK
     L.qgemm_reset_counters()
     c = qg._Counters()
     assert L.qgemm_get_counters(ctypes.byref(c)) == 0

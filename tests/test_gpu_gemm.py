@@ -10,6 +10,8 @@ M / N edges around every tile size, every tile width and split-K factor,
 degenerate blocks (d = 0, dmin = 0, all-zero quants, extreme sub-scales),
 guard canaries around Y, the launch counters and the device status word.
 """
+import contextlib
+
 import numpy as np
 import pytest
 import torch
@@ -37,6 +39,21 @@ def _built():
     qg.qgemm_set_option(qg.QGEMM_OPT_SMALL_M_MAX, small)
     qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
     qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_SPLITS, 0)
+
+
+# Q4_K side words: made by their own kernel and loaded (threshold 0 token
+# tiles), or made inside the GEMM (threshold above any tile count)
+SIDE_MODES = {"side_kernel": 0, "side_in_gemm": 1 << 30}
+
+
+@contextlib.contextmanager
+def side_mode(mode):
+    old = qg.qgemm_get_option(qg.QGEMM_OPT_Q4K_SIDE_MIN_TILES)
+    qg.qgemm_set_option(qg.QGEMM_OPT_Q4K_SIDE_MIN_TILES, SIDE_MODES[mode])
+    try:
+        yield
+    finally:
+        qg.qgemm_set_option(qg.QGEMM_OPT_Q4K_SIDE_MIN_TILES, old)
 
 
 def weights(wtype, N, K, seed):
@@ -167,8 +184,9 @@ def _q4k_blocks(orc, N, nb, rng, d_bits=None, dmin_bits=None, q_zero=False):
     return np.stack(rows)
 
 
+@pytest.mark.parametrize("mode", list(SIDE_MODES))
 @pytest.mark.parametrize("case", ["d_zero", "dmin_zero", "both_zero", "q_zero", "max_fields"])
-def test_q4k_degenerate_blocks(case):
+def test_q4k_degenerate_blocks(case, mode):
     orc = oracle.get()
     rng = np.random.default_rng(3)
     N, K, M = 130, 512, 20
@@ -186,7 +204,8 @@ def test_q4k_degenerate_blocks(case):
     x = synth.gen_x(M, K, 8)
     x[3] = 0.0                                        # an all-zero token row
     x[4, :256] = 127.0                                # saturated superblock
-    check(4, w, K, x, what=case)
+    with side_mode(mode):
+        check(4, w, K, x, what=f"{case}, {mode}")
     device_status_clean()
 
 
@@ -258,7 +277,8 @@ def test_q6k_full_int8_scales_cut_last_round():
     device_status_clean()
 
 
-def test_q4k_large_dmin_ratio_is_exact():
+@pytest.mark.parametrize("mode", list(SIDE_MODES))
+def test_q4k_large_dmin_ratio_is_exact(mode):
     """Blocks with |dmin/d| from 1e3 up to about 1.6e7 run on a power-of-two
     shifted scale and stay within the tolerance, with no status bit."""
     orc = oracle.get()
@@ -274,11 +294,13 @@ def test_q4k_large_dmin_ratio_is_exact():
                                      r.integers(0, 16, 256)))
         rows.append(np.concatenate(blks))
     w = np.stack(rows)
-    check(4, w, K, synth.gen_x(M, K, 7), what="Q4_K large dmin/d")
+    with side_mode(mode):
+        check(4, w, K, synth.gen_x(M, K, 7), what=f"Q4_K large dmin/d, {mode}")
     device_status_clean()
 
 
-def test_q4k_out_of_range_row_is_declined():
+@pytest.mark.parametrize("mode", list(SIDE_MODES))
+def test_q4k_out_of_range_row_is_declined(mode):
     """A block whose correction leaves fp16's range even on the largest
     shifted scale is not computed: its row of Y is NaN and the status bit is
     set; every other row is exact."""
@@ -290,13 +312,67 @@ def test_q4k_out_of_range_row_is_declined():
     mn = np.full(8, 63)
     w[bad_row, :144] = orc.q4k_pack(0x0001, 0x4400, rng.integers(0, 64, 8), mn, rng.integers(0, 16, 256))  # d 6e-8, dmin 4
     q = gpu_quantize(synth.gen_x(M, K, 1))
-    y = gpu_gemm(4, w, K, q)
+    with side_mode(mode):
+        y = gpu_gemm(4, w, K, q)
     bits, _ = qg.qgemm_get_device_status()
     assert bits & qg.QGEMM_DEV_Q4K_RANGE
     assert np.isnan(y[:, bad_row]).all()
     keep = np.arange(N) != bad_row
     yr, absc = oracle_gemm(4, w, K, *q8k_numpy(q))
     assert_gemm_close(y[:, keep], yr[:, keep], absc[:, keep], "rows beside the declined one")
+    device_status_clean()
+
+
+@pytest.mark.parametrize("M,N,K,bm,splits", [(64, 300, 2048, 0, 0), (100, 136, 1024, 32, 3), (128, 260, 768, 128, 1),
+                                             (129, 1000, 2048, 0, 0), (300, 200, 4096, 64, 2), (520, 384, 512, 0, 0)])
+def test_q4k_side_paths_agree(M, N, K, bm, splits):
+    """The side words made by their own kernel and loaded, or made inside the
+    GEMM: bit-equal Y, both within the oracle's tolerance, and the launch
+    counters show which ran."""
+    w = weights(4, N, K, 3 * M + N)
+    x = synth.gen_x(M, K, 5 * M + K, outlier_frac=0.01)
+    q = gpu_quantize(x)
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, bm)
+    qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_SPLITS, splits)
+    ys = {}
+    try:
+        for mode in SIDE_MODES:
+            with side_mode(mode):
+                qg.qgemm_reset_counters()
+                ys[mode] = gpu_gemm(4, w, K, q)
+                c = qg.qgemm_get_counters()
+            assert c["q4k_tc"] == 1 and c["q4k_side"] == (1 if mode == "side_kernel" else 0), (mode, c)
+    finally:
+        qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_BM, 0)
+        qg.qgemm_set_option(qg.QGEMM_OPT_FORCE_SPLITS, 0)
+    assert np.array_equal(ys["side_kernel"], ys["side_in_gemm"], equal_nan=True)
+    yr, absc = oracle_gemm(4, w, K, *q8k_numpy(q))
+    assert_gemm_close(ys["side_in_gemm"], yr, absc, f"M{M} N{N} K{K} bm{bm} splits{splits}")
+    device_status_clean()
+
+
+def test_q4k_side_default_threshold():
+    """Default: up to three token tiles per weight tile make the side words in
+    the GEMM, four or more load them from their own kernel (fp32 entry point
+    and Q8_K entry point alike)."""
+    assert qg.qgemm_get_option(qg.QGEMM_OPT_Q4K_SIDE_MIN_TILES) == 4
+    N, K = 256, 1024
+    w_np = weights(4, N, K, 90)
+    w = to_dev(w_np)
+    for M, expect in [(100, 0), (129, 0), (384, 0), (385, 1), (700, 1)]:
+        x = synth.gen_x(M, K, 91 + M)
+        q = gpu_quantize(x)
+        qg.qgemm_reset_counters()
+        y1 = gpu_gemm(4, w_np, K, q)
+        c = qg.qgemm_get_counters()
+        assert c["q4k_side"] == expect, (M, c)
+        ws = torch.empty(qg.qgemm_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+        qg.qgemm_reset_counters()
+        y2 = qg.qgemm_q4k_f32(w, N, K, to_dev(x), workspace=ws)
+        torch.cuda.synchronize()
+        c = qg.qgemm_get_counters()
+        assert c["q4k_side"] == expect and c["quantize"] == 1 and c["q4k_tc"] == 1, (M, c)
+        assert np.array_equal(y1, y2.cpu().numpy(), equal_nan=True), M
     device_status_clean()
 
 
