@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqgemm.so")
 
-SOURCES = ["quantize.cu", "gemm_tc.cu", "gemm_tc_epi.cu", "gemm_tc_routed.cu", "gemm_tc_self.cu", "smallm.cu", "route.cu", "qgemm_api.cu", "qgemm_noalloc.cu", "unpack_check.cu"]
+SOURCES = ["quantize.cu", "gemm_tc.cu", "gemm_tc_epi.cu", "gemm_tc_routed.cu", "gemm_tc_self.cu", "gemm_tc_epi_self.cu", "smallm.cu", "route.cu", "qgemm_api.cu", "qgemm_noalloc.cu", "unpack_check.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-Xptxas", "-v"]

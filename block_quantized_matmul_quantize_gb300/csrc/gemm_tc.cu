@@ -1,7 +1,8 @@
 // gemm_tc.cu -- the tile GEMM's plain instantiations (fp32 output, no
 // epilogue, host work list) and its host dispatch; the kernel is in
 // gemm_tc_kernel.cuh, the epilogue, routed and Q4_K self-side instantiations
-// in gemm_tc_epi.cu, gemm_tc_routed.cu and gemm_tc_self.cu (built in parallel).
+// in gemm_tc_epi.cu, gemm_tc_routed.cu, gemm_tc_self.cu and
+// gemm_tc_epi_self.cu (built in parallel).
 #include "gemm_tc_kernel.cuh"
 
 namespace qg {
@@ -21,6 +22,7 @@ cudaError_t tc_prepare(int wtype, int bm) {
         cudaError_t e = tc_prepare_epi(wtype, bm);
         if (e == cudaSuccess) e = tc_prepare_routed(wtype, bm);
         if (e == cudaSuccess && wtype == 4) e = tc_prepare_self(bm);
+        if (e == cudaSuccess && wtype == 4) e = tc_prepare_epi_self(bm);
         if (e != cudaSuccess) return e;
     }
 #define QG_CASE(W, B) \
@@ -33,8 +35,8 @@ cudaError_t tc_prepare(int wtype, int bm) {
 }
 
 // The Q4_K side words of every (row, superblock), computed as the side-data
-// warps of the other variants compute them (q4k_side), for the plain variant
-// to load by TMA.  One thread per (superblock, row), rows fastest: each warp
+// warps of the other variants compute them (q4k_side), for the plain and
+// epilogue variants to load by TMA.  One thread per (superblock, row), rows fastest: each warp
 // writes 32 consecutive 32-byte rows of a slab.
 __global__ void q4k_side_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t nb, int64_t ldw,
                                 uint32_t* __restrict__ side, float* __restrict__ eout, int64_t Np) {
@@ -68,8 +70,9 @@ cudaError_t launch_q4k_side(const void* w, int64_t N, int64_t nb, int64_t ldw, u
 
 cudaError_t launch_gemm_tc(const TcLaunch& a, cudaStream_t s) {
     if (a.work.experts > 0) return launch_gemm_tc_routed(a, s);
-    if (a.epi.out != OUT_F32 || a.epi.act != ACT_NONE || a.epi.bias != nullptr) return launch_gemm_tc_epi(a, s);
-    if (a.wtype == 4 && !a.tm_side) return launch_gemm_tc_self(a, s);
+    const bool epi = a.epi.out != OUT_F32 || a.epi.act != ACT_NONE || a.epi.bias != nullptr;
+    if (a.wtype == 4 && !a.tm_side) return epi ? launch_gemm_tc_epi_self(a, s) : launch_gemm_tc_self(a, s);
+    if (epi) return launch_gemm_tc_epi(a, s);
 #define QG_CASE(W, B) \
     if (a.wtype == W && a.bm == B) return launch_t<W, B, VAR_PLAIN>(a, s);
     QG_CASE(4, 16) QG_CASE(4, 32) QG_CASE(4, 64) QG_CASE(4, 128)

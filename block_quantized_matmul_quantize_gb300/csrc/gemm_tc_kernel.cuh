@@ -201,13 +201,15 @@ __device__ __forceinline__ void fold4(float* a, const uint32_t* S, float2 ee, fl
 // Kernel variants, each compiled only with the code it needs (measured on
 // GB300: routing and epilogue code in one kernel doubled the register
 // spills and slowed the plain GEMM by 5-8%):
-//   VAR_PLAIN   fp32 output, the work list from the host plan;
-//   VAR_EPI     plus the output epilogue (bias, activation, fp16/bf16 output);
-//   VAR_ROUTED  the routed GEMM (work list and output rows from the routing);
-//   VAR_SELF    VAR_PLAIN for Q4_K with the side words computed in the kernel
-//               rather than loaded (for one token tile per weight tile, where
-//               each tile's side words are made once either way).
-enum : int { VAR_PLAIN = 0, VAR_EPI = 1, VAR_ROUTED = 2, VAR_SELF = 3 };
+//   VAR_PLAIN     fp32 output, the work list from the host plan;
+//   VAR_EPI       plus the output epilogue (bias, activation, fp16/bf16 output);
+//   VAR_ROUTED    the routed GEMM (work list and output rows from the routing);
+//   VAR_SELF      VAR_PLAIN for Q4_K with the side words computed in the
+//                 kernel rather than loaded (for few token tiles per weight
+//                 tile, where each tile's side words are made few times);
+//   VAR_EPI_SELF  VAR_EPI for Q4_K with the side words computed in the kernel.
+// Q4_K's plain and epilogue variants load the side words (PRE).
+enum : int { VAR_PLAIN = 0, VAR_EPI = 1, VAR_ROUTED = 2, VAR_SELF = 3, VAR_EPI_SELF = 4 };
 template <int WT, int BM, int VAR>
 __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
@@ -231,14 +233,15 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     // stages, every K128 step consumes exactly one stage of each ring, so one
     // commit (on a_empty) releases both and the activation producers wait on it.
     constexpr bool MERGED_RELEASE = !SPLIT && (L::SCH == 2) && (BS == A_STAGES);
-    // Q4_K, plain variant: the side data (dmin-correction operands and the
-    // scale e of each row and superblock) depend on the weights alone, so they
-    // are made once per call (launch_q4k_side) and loaded by TMA beside the raw
-    // block, instead of being recomputed for every token tile (measured on
-    // GB300: recomputing them in four epilogue warps cost 2-3% of the GEMM at
-    // M=8192 K=N=5120, on the sub-partitions the expansion warps need).  The
-    // epilogue and routed variants keep the side-data warps.
-    constexpr bool PRE = L::CORR && VAR == VAR_PLAIN;
+    // Q4_K, plain and epilogue variants: the side data (dmin-correction
+    // operands and the scale e of each row and superblock) depend on the
+    // weights alone, so they are made once per call (launch_q4k_side) and
+    // loaded by TMA beside the raw block, instead of being recomputed for every
+    // token tile (measured on GB300: recomputing them in four epilogue warps
+    // cost 2-3% of the plain GEMM at M=8192 K=N=5120, on the sub-partitions the
+    // expansion warps need, and 6% of the epilogue GEMM at M=2048 K=4096
+    // N=14336).  The self-side and routed variants keep the side-data warps.
+    constexpr bool PRE = L::CORR && (VAR == VAR_PLAIN || VAR == VAR_EPI);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // routed mode: the work list comes from the preceding (routing) grid
-    constexpr bool EPI = VAR == VAR_EPI;
+    constexpr bool EPI = VAR == VAR_EPI || VAR == VAR_EPI_SELF;
     constexpr bool ROUTED = VAR == VAR_ROUTED;
     if constexpr (ROUTED) griddep_wait();
     int num_work = wk.items;
@@ -990,33 +993,68 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                 const bool live = !*abort_flag && n < N;
                 float bn = 0.0f;
                 if constexpr (EPI) bn = bias_n;
-                // chunks of 32 columns for the plain store, 8 where the epilogue's
-                // activation would be unrolled over the chunk (measured on GB300:
-                // 32-column chunks took 2% off the plain GEMM, 16 nothing)
-                constexpr int CH = EPI ? 8 : (CPT < 32 ? CPT : 32);
+                // Without an activation (the plain variant, and the epilogue
+                // variant's bias and output-type forms) in chunks of 32 columns,
+                // each element at most one add and one converting store; with an
+                // activation in chunks of 8, the activation unrolled over the
+                // chunk.  This code runs once per tile, cold in the instruction
+                // cache, so its size is much of its cost: measured on GB300 (M=2048
+                // K=4096 N=14336, bias and bf16 output), every form on the 8-column
+                // path took 292.9 us, the no-activation forms on this one 256.0 us
+                // (plain fp32: 241.7 us); 32-column chunks also took 2% off the
+                // plain GEMM against 8.
+                constexpr int CH = CPT < 32 ? CPT : 32;
+                const bool add_bias = EPI && epi.bias != nullptr;
+                if (!EPI || epi.act == ACT_NONE) {
 #pragma unroll 1
-                for (int c = 0; c < CPT; c += CH) {
-                    uint32_t v[CH];
-                    __syncwarp();   // (the TMEM load is warp-collective: every lane, converged)
-                    if constexpr (CH == 32)
-                        tmem_ld_32x32b_x32(taddr + c, v);
-                    else
-                        tmem_ld_32x32b_x8(taddr + c, v);
-                    tmem_ld_wait();
-                    const int mc = m0 + col0 + c;
-                    if (live) {
-                        if constexpr (!EPI) {
-                            float* yp = static_cast<float*>(y) + static_cast<int64_t>(mc) * ldy + n;
+                    for (int c = 0; c < CPT; c += CH) {
+                        uint32_t v[CH];
+                        __syncwarp();   // (the TMEM load is warp-collective: every lane, converged)
+                        if constexpr (CH == 32)
+                            tmem_ld_32x32b_x32(taddr + c, v);
+                        else
+                            tmem_ld_32x32b_x8(taddr + c, v);
+                        tmem_ld_wait();
+                        const int mc = m0 + col0 + c;
+                        if (live) {
+                            if (!EPI || epi.out == OUT_F32) {
+                                float* yp = static_cast<float*>(y) + static_cast<int64_t>(mc) * ldy + n;
 #pragma unroll
-                            for (int u = 0; u < CH; ++u) {
-                                if (mc + u < M) *yp = __uint_as_float(v[u]);
-                                yp += ldy;
+                                for (int u = 0; u < CH; ++u) {
+                                    const float a = __uint_as_float(v[u]);
+                                    if (mc + u < M) *yp = add_bias ? a + bn : a;
+                                    yp += ldy;
+                                }
+                            } else {
+                                // fp16 or bf16, stored as their 16-bit patterns
+                                const bool f16 = epi.out == OUT_F16;
+                                unsigned short* yp =
+                                    static_cast<unsigned short*>(y) + static_cast<int64_t>(mc) * ldy + n;
+#pragma unroll
+                                for (int u = 0; u < CH; ++u) {
+                                    const float a = add_bias ? __uint_as_float(v[u]) + bn : __uint_as_float(v[u]);
+                                    const unsigned short h = f16 ? __half_as_ushort(__float2half_rn(a))
+                                                                 : __bfloat16_as_ushort(__float2bfloat16_rn(a));
+                                    if (mc + u < M) *yp = h;
+                                    yp += ldy;
+                                }
                             }
-                        } else {
-                            float vv[CH];
+                        }
+                    }
+                } else if constexpr (EPI) {
+                    constexpr int CA = 8;
+#pragma unroll 1
+                    for (int c = 0; c < CPT; c += CA) {
+                        uint32_t v[CA];
+                        __syncwarp();
+                        tmem_ld_32x32b_x8(taddr + c, v);
+                        tmem_ld_wait();
+                        const int mc = m0 + col0 + c;
+                        if (live) {
+                            float vv[CA];
 #pragma unroll
-                            for (int u = 0; u < CH; ++u) vv[u] = __uint_as_float(v[u]);
-                            epi_tile<CH>(vv, epi, bn, y, ldy, n, mc, M);
+                            for (int u = 0; u < CA; ++u) vv[u] = __uint_as_float(v[u]);
+                            epi_tile<CA>(vv, epi, bn, y, ldy, n, mc, M);
                         }
                     }
                 }
@@ -1094,9 +1132,9 @@ cudaError_t launch_t(const TcLaunch& a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const CUtensorMap tm_xbs = a.tm_xbs ? *a.tm_xbs : *a.tm_xh;
-    const CUtensorMap tm_side = a.tm_side ? *a.tm_side : *a.tm_xh;   // (read only by the plain Q4_K variant)
+    const CUtensorMap tm_side = a.tm_side ? *a.tm_side : *a.tm_xh;   // (read only where the side words are loaded)
     const CUtensorMap tm_e = a.tm_e ? *a.tm_e : *a.tm_xh;
-    if (L::CORR && VAR == VAR_PLAIN && (!a.tm_side || !a.tm_e)) return cudaErrorInvalidValue;
+    if (L::CORR && (VAR == VAR_PLAIN || VAR == VAR_EPI) && (!a.tm_side || !a.tm_e)) return cudaErrorInvalidValue;
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<WT, BM, VAR>, *a.tm_w, *a.tm_xh, tm_xbs, *a.tm_dx, tm_side, tm_e,
                               a.y, a.ldy, a.epi,
                               static_cast<int>(a.M), static_cast<int>(a.N), static_cast<int>(a.K / 256), a.work,

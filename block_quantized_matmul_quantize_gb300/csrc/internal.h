@@ -142,9 +142,10 @@ struct TcLaunch {
     const CUtensorMap* tm_xh;   // fp16 [M][K], box {64, bm}, 128B swizzle
     const CUtensorMap* tm_xbs;  // fp16 [M][K/16], box {16, bm}, 32B swizzle (Q4_K only)
     const CUtensorMap* tm_dx;   // fp32 [nb][Mp], box {bm, 1}
-    // Q4_K, plain variant: the side words of every (row, superblock), made by
-    // launch_q4k_side before the GEMM (q4k_side's values: the dmin-correction
-    // operands and the scale e), loaded beside the raw blocks
+    // Q4_K, plain and epilogue variants: the side words of every (row,
+    // superblock), made by launch_q4k_side before the GEMM (q4k_side's values:
+    // the dmin-correction operands and the scale e), loaded beside the raw
+    // blocks; null where the GEMM makes them itself
     const CUtensorMap* tm_side; // uint32 [2 nb][N][8] (superblock b: slabs 2b, 2b+1), box {8, 128, 2}, 32B swizzle
     const CUtensorMap* tm_e;    // fp32 [nb][Np], box {128, 1}
 };
@@ -158,10 +159,12 @@ cudaError_t launch_gemm_tc(const TcLaunch& a, cudaStream_t s);
 // (the epilogue instantiations, gemm_tc_epi.cu; launch_gemm_tc dispatches to them)
 cudaError_t tc_prepare_epi(int wtype, int bm);
 cudaError_t launch_gemm_tc_epi(const TcLaunch& a, cudaStream_t s);
-// (Q4_K with the side words made in the kernel, gemm_tc_self.cu: a plain
-// launch without tm_side)
+// (Q4_K with the side words made in the kernel, gemm_tc_self.cu and
+// gemm_tc_epi_self.cu: a launch without tm_side)
 cudaError_t tc_prepare_self(int bm);
 cudaError_t launch_gemm_tc_self(const TcLaunch& a, cudaStream_t s);
+cudaError_t tc_prepare_epi_self(int bm);
+cudaError_t launch_gemm_tc_epi_self(const TcLaunch& a, cudaStream_t s);
 // (the routed instantiations, gemm_tc_routed.cu: work.experts > 0)
 cudaError_t tc_prepare_routed(int wtype, int bm);
 cudaError_t launch_gemm_tc_routed(const TcLaunch& a, cudaStream_t s);

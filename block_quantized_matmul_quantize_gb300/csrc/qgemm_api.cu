@@ -281,8 +281,8 @@ WsPlanes ws_planes(void* ws, int64_t M, int64_t K, int64_t N = 0) {
     return p;
 }
 
-// Q4_K without an output epilogue: the side words come precomputed (their
-// own kernel, loaded by the GEMM) when a weight tile meets at least
+// Q4_K tile GEMM (not routed): the side words come precomputed (their own
+// kernel, loaded by the GEMM) when a weight tile meets at least
 // QGEMM_OPT_Q4K_SIDE_MIN_TILES token tiles, else the GEMM makes them itself.
 bool q4k_side_precomputed(const Plan& pl) { return pl.work.m_tiles >= g_opt[QGEMM_OPT_Q4K_SIDE_MIN_TILES].load(); }
 
@@ -306,11 +306,9 @@ int run_tc(int wtype, const void* w, int64_t N, int64_t K, int64_t ldw, const in
     float* dxT = wp.dxT;
 
     cudaError_t e = cudaSuccess;
-    // Q4_K without an output epilogue: the side words come precomputed (see
-    // gemm_tc_kernel.cuh) for enough token tiles, made here unless the caller
-    // made them already
-    const bool pre = wtype == 4 && epi.out == qg::OUT_F32 && epi.act == qg::ACT_NONE && epi.bias == nullptr &&
-                     q4k_side_precomputed(pl);
+    // Q4_K: the side words come precomputed (see gemm_tc_kernel.cuh) for
+    // enough token tiles, made here unless the caller made them already
+    const bool pre = wtype == 4 && q4k_side_precomputed(pl);
     const bool side_now = pre && !side_ready;
     if (side_now) {
         e = qg::launch_q4k_side(w, N, nb, ldw, wp.side, wp.side_e, side_np(N), stream);

@@ -134,8 +134,8 @@ QGEMM_API int qgemm_unpack_q8k_aos(const void *aos, int64_t M, int64_t K, int8_t
  * on the current device: the fp16 tensor-core operand copy of the Q8_K
  * activations (about 2.1 B per element of M*K), the cut-tile counters
  * (32 KiB), the Q4_K side words (68 B per weight block: the dmin-correction
- * operands and scales that the Q4_K calls without an output epilogue make
- * from the weights before the GEMM; counted for every weight type), and the
+ * operands and scales that the Q4_K tile GEMM calls make from the weights
+ * before the GEMM; counted for every weight type), and the
  * partial tiles of the cut tiles (128 x BM fp32 per K part; tiles are cut
  * when there are fewer of them than SMs, or when a last round would leave at
  * least half of the SMs idle).  With N = 0: the activation part alone (what
@@ -406,7 +406,7 @@ typedef struct {
     uint64_t ptq1_tc;      /* PTQ1_0 tile GEMM launches             */
     uint64_t ptq1_prepack; /* PTQ1_0 repack launches                */
     uint64_t small_fused;  /* small-M launches that quantized X themselves (also counted in q4k/q6k_small) */
-    uint64_t q4k_side;     /* Q4_K side-data launches (before the tile GEMM without an output epilogue) */
+    uint64_t q4k_side;     /* Q4_K side-data launches (before the tile GEMM, QGEMM_OPT_Q4K_SIDE_MIN_TILES) */
 } qgemm_counters;
 QGEMM_API int qgemm_get_counters(qgemm_counters *out);
 QGEMM_API int qgemm_reset_counters(void);
@@ -447,7 +447,7 @@ typedef enum {
      * filled again before another _prepared call (its cut-tile counters may
      * be left nonzero); the other calls prepare their workspace themselves. */
     QGEMM_OPT_TEST_SKIP_ARRIVAL = 4,
-    /* Q4_K tile GEMM without an output epilogue: the side words of the
+    /* Q4_K tile GEMM (not the routed one): the side words of the
      * weight blocks (the dmin-correction operands and scales, which depend
      * on the weights alone) are made by a kernel of their own and loaded by
      * the GEMM when a weight tile meets at least this many token tiles;

@@ -65,6 +65,49 @@ def test_tile_path(wtype, out_name, act_name):
 
 @pytest.mark.parametrize("wtype", [4, 6])
 @pytest.mark.parametrize("out_name", sorted(OUT))
+@pytest.mark.parametrize("act_name", ["none", "gelu"])
+def test_tile_path_many_token_tiles(wtype, out_name, act_name):
+    # five token tiles per weight tile: Q4_K loads the side words made by
+    # their own kernel (QGEMM_OPT_Q4K_SIDE_MIN_TILES, default 4)
+    check(wtype, 520, 260, 1024, out_name, act_name, True, seed=51 + wtype)
+
+
+@pytest.mark.parametrize("out_name", sorted(OUT))
+@pytest.mark.parametrize("act_name", ["none", "relu"])
+def test_tile_path_narrow_token_tile(out_name, act_name):
+    # M = 20: 32-token tiles, whose store goes from registers (not through TMEM)
+    check(4, 20, 260, 1024, out_name, act_name, True, seed=61)
+
+
+@pytest.mark.parametrize("M", [70, 520])
+@pytest.mark.parametrize("out_name,act_name,with_bias", [("f32", "none", True), ("bf16", "none", False),
+                                                         ("f16", "silu", True), ("bf16", "gelu", True)])
+def test_q4k_side_forms_agree(M, out_name, act_name, with_bias):
+    """The epilogue GEMM with the Q4_K side words from their own kernel or made
+    in the GEMM: bit-equal output, and the launch counters show which ran."""
+    K, N = 1024, 260
+    w = to_dev(synth.gen_q4k(N, K, 71 + M))
+    q = gpu_quantize(synth.gen_x(M, K, 72 + M, outlier_frac=0.01))
+    b = to_dev((synth.normal(73, N) * 0.5).astype(np.float32)) if with_bias else None
+    out = OUT[out_name][0]
+    old = qg.qgemm_get_option(qg.QGEMM_OPT_Q4K_SIDE_MIN_TILES)
+    ys = []
+    try:
+        for mode in (0, 1 << 30):
+            qg.qgemm_set_option(qg.QGEMM_OPT_Q4K_SIDE_MIN_TILES, mode)
+            qg.qgemm_reset_counters()
+            ys.append(qg.qgemm_q4k_ex(w, N, K, q, out_dtype=out, bias=b, activation=ACT[act_name]))
+            torch.cuda.synchronize()
+            c = qg.qgemm_get_counters()
+            assert c["q4k_tc"] == 1 and c["q4k_side"] == (1 if mode == 0 else 0), (mode, c)
+    finally:
+        qg.qgemm_set_option(qg.QGEMM_OPT_Q4K_SIDE_MIN_TILES, old)
+    assert torch.equal(ys[0], ys[1])
+    device_status_clean()
+
+
+@pytest.mark.parametrize("wtype", [4, 6])
+@pytest.mark.parametrize("out_name", sorted(OUT))
 @pytest.mark.parametrize("act_name", ["none", "silu"])
 def test_small_m_path(wtype, out_name, act_name):
     check(wtype, 5, 200, 1024, out_name, act_name, True, seed=21 + wtype)
