@@ -218,6 +218,7 @@ Plan plan_tc(int64_t M, int64_t N, int64_t K, int sm_count) {
         }
     }
     if (T - full > qg::TC_MAX_CUT_TILES) parts = 1, full = T;   // counters are finite
+    if (parts > 1 && nb * parts >= (int64_t(1) << 31)) parts = (int64_t(1) << 31) / nb - 1;   // 32-bit part bounds
     if (parts <= 1) parts = 1, full = T;
     w.full_items = static_cast<int>(full);
     w.parts = static_cast<int>(parts);
