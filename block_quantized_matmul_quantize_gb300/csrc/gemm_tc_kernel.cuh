@@ -320,11 +320,16 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
         }
         // groups of m_group token tiles; within a group, token tiles vary fastest
         // (the CTAs running at once share the group's activations in L2)
+        // (the divisions by multiply and shift, TcWork::dv_*)
         const int gsz = wk.m_group * wk.n_tiles;
-        const int grp = tile / gsz, r = tile - grp * gsz;
-        const int gm = min(wk.m_group, wk.m_tiles - grp * wk.m_group);   // token tiles in this group
-        n0 = (r / gm) * BN;
-        m0 = (grp * wk.m_group + r % gm) * BM;
+        const int grp = static_cast<int>((static_cast<uint64_t>(tile) * wk.dv_gsz_mul) >> wk.dv_gsz_shr);
+        const int r = tile - grp * gsz;
+        const bool full_group = (grp + 1) * wk.m_group <= wk.m_tiles;
+        const int gm = full_group ? wk.m_group : wk.m_tiles - grp * wk.m_group;   // token tiles in this group
+        const int rq = static_cast<int>((static_cast<uint64_t>(r) * (full_group ? wk.dv_mg_mul : wk.dv_ml_mul)) >>
+                                        (full_group ? wk.dv_mg_shr : wk.dv_ml_shr));
+        n0 = rq * BN;
+        m0 = (grp * wk.m_group + (r - rq * gm)) * BM;
     };
     auto work_of = [&](int wi, int& n0, int& m0, int& kb0, int& kb1) {
         int cut, part;

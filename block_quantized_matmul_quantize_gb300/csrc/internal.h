@@ -109,6 +109,13 @@ struct TcWork {
     // t / (m_group * n_tiles), and within a group the token tiles vary
     // fastest.  m_group = m_tiles: one group (token tiles fastest overall).
     int m_group;
+    // The work decode's divisions, by m_group * n_tiles, by m_group and by the
+    // last group's token-tile count, as a multiply and a shift: q = (n * mul)
+    // >> shr with mul = ceil(2^shr / d), shr = 32 + ceil(log2 d), exact for
+    // 0 <= n < 2^32 (division by invariant integers, Granlund and Montgomery,
+    // PLDI 1994).
+    uint64_t dv_gsz_mul, dv_mg_mul, dv_ml_mul;
+    int dv_gsz_shr, dv_mg_shr, dv_ml_shr;
     int full_items;       // whole tiles
     int parts;            // K parts of each remaining tile (1: none)
     int items;            // full_items + (tiles - full_items) * parts
