@@ -889,7 +889,7 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                 const float2 ee = make_float2(e, e);
                 const float4* dx4 = reinterpret_cast<const float4*>(sb + L::SB_DX) + col0 / 4;
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + buf * BM + col0;
-                if constexpr (CPT >= 16) {
+                if constexpr (CPT >= 16 && UG == 1 && (PRE || !L::CORR) && !ROUTED) {
                     // one 16-column load per wait (measured on GB300: two in flight per
                     // wait cost 32 more live registers and 3.6% on M=2048 K=4096 N=14336)
                     constexpr int PAIR = 1;
@@ -907,11 +907,22 @@ __global__ void __launch_bounds__(Warps<WT>::THREADS, 1)
                         }
                     }
                 } else {
-                    uint32_t v[8];
-                    tmem_ld_32x32b_x8(taddr, v);
-                    tmem_ld_wait();
+                    // 8-column loads where registers are short: the kernels with two
+                    // expansion groups run at 96 registers, and the Q4_K variants with
+                    // the side-data writer or the routed decode hold more beside the 64
+                    // accumulators; 16 columns in flight spilled there (measured on
+                    // GB300, Y bit-identical: Q6_K M=512 K=11008 N=2048 136 B of spill
+                    // stores -> 40 B, 50.8 -> 47.0 us; PTQ1_0 M=2048 K=N=5120 149.3 ->
+                    // 140.0 us; routed Q4_K 36 B -> 0, MoE 8 experts 225.7 -> 220.1 us)
 #pragma unroll
-                    for (int q4 = 0; q4 < 2; ++q4) fold4(acc + 4 * q4, v + 4 * q4, ee, dx4[q4]);
+                    for (int ch = 0; ch < CPT / 8; ++ch) {
+                        uint32_t v[8];
+                        tmem_ld_32x32b_x8(taddr + 8 * ch, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q4 = 0; q4 < 2; ++q4)
+                            fold4(acc + 8 * ch + 4 * q4, v + 4 * q4, ee, dx4[2 * ch + q4]);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
