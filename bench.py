@@ -65,20 +65,20 @@ DEFAULT_WORKLOAD = synth.sweep(8192).name
 # captures summarised in profiles/dram_traffic_by_workload.md (absent until
 # measured, and removed whenever the kernel changes).
 NCU_TRAFFIC_BYTES = {
-    "q4k_sweep_m8192_k5120_n5120": 301665536,
-    "q4k_sweep_m2048_k5120_n5120": 54525440,
-    "q4k_sweep_m512_k5120_n5120": 27387392,
-    "q4k_sweep_m64_k5120_n5120": 15517184,
+    "q4k_sweep_m8192_k5120_n5120": 302274048,
+    "q4k_sweep_m2048_k5120_n5120": 54499840,
+    "q4k_sweep_m512_k5120_n5120": 27387904,
+    "q4k_sweep_m64_k5120_n5120": 15517440,
     "q4k_sweep_m8_k5120_n5120": 14830080,
     "q4k_sweep_m4_k5120_n5120": 14810880,
     "q4k_sweep_m1_k5120_n5120": 14807552,
-    "q4k_m64_k2048_n2048": 2709504,
+    "q4k_m64_k2048_n2048": 2709760,
     "q4k_m512_k2048_n11008_outliers": 20983040,
-    "q6k_m512_k11008_n2048": 31312128,
-    "q6k_fullscale_m512_k11008_n2048": 31316480,
-    "q4k_m2048_k4096_n14336": 139397888,
-    "q4k_moe_e8_top2_m512_k4096_n14336": 320257792,
-    "ptq1_m2048_k5120_n5120": 34543872,
+    "q6k_m512_k11008_n2048": 31299072,
+    "q6k_fullscale_m512_k11008_n2048": 31300608,
+    "q4k_m2048_k4096_n14336": 139535872,
+    "q4k_moe_e8_top2_m512_k4096_n14336": 318473728,
+    "ptq1_m2048_k5120_n5120": 32066560,
 }
 
 
