@@ -6,8 +6,8 @@ cudaMalloc is not allowed); it takes its scratch from a fixed device array in
 the library instead of a caller workspace.  This file is collected last so a
 run that stops at the first failure has already run every other test.
 
-Checked here, through the C ABI: two calls in a row (of different shapes, so
-the second one runs over the first one's leftover scratch) each match the CPU
+Checked here, through the C ABI: three calls in a row (of different shapes, so
+each runs over the previous one's leftover scratch) each match the CPU
 oracle's Y within the GEMM tolerance, and give the same bits as the workspace
 entry point qgemm_q4k on the same inputs; a call too large for the built-in
 scratch is refused without launching anything.
@@ -37,7 +37,9 @@ def _noalloc(L, w, N, K, q, y):
 def test_noalloc_matches_oracle_twice():
     ensure_built()
     L = qg.lib()
-    for call, (M, N, K) in enumerate(((300, 520, 2048), (37, 256, 1024))):
+    # (the third shape has five token tiles per weight tile: the Q4_K side words
+    # are then made by their own kernel into the built-in scratch)
+    for call, (M, N, K) in enumerate(((300, 520, 2048), (37, 256, 1024), (520, 384, 1024))):
         w_np = synth.gen_q4k(N, K, 61 + call)
         x_np = synth.gen_x(M, K, 62 + call, outlier_frac=0.01)
         w = to_dev(w_np)
@@ -49,9 +51,11 @@ def test_noalloc_matches_oracle_twice():
         y_or, absc = oracle_gemm(4, w_np, K, *q8k_numpy(q))
         assert_gemm_close(y.cpu().numpy(), y_or, absc, f"noalloc call {call + 1} vs the oracle")
         # the same kernels as the workspace entry point: the same bits
+        qg.qgemm_reset_counters()
         y_ws = qg.qgemm_q4k(w, N, K, q)
         torch.cuda.synchronize()
         assert torch.equal(y, y_ws), f"noalloc call {call + 1}: Y differs from qgemm_q4k's"
+        assert qg.qgemm_get_counters()["q4k_side"] == (1 if M > 3 * 128 else 0)
     bits, site = qg.qgemm_get_device_status()
     assert bits == 0, f"device status {bits:#x} site {site}"
 
